@@ -1,0 +1,521 @@
+#!/usr/bin/env python3
+"""Benchmark: sparse decode queries/s and achieved HBM GB/s on one GB300 (or N replicas).
+
+One step = one pass of the hot path over one batch of decode queries:
+select (score every block from its metadata + top-k + window) and decode (exact
+softmax attention over the selected blocks), plus the diff/LRU step for the
+multi-step workload.  Inputs are resident in HBM when the timed region starts;
+the L2 is flushed (a 2x-L2 write) before every timed step, outside the step's
+events.  Each kernel is bracketed by CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (the path has no exchange
+step); `value` is the sum over ranks of the queries processed divided by the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode queries/s and achieved HBM GB/s (% of peak) at 128K ctx, 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "gqa_128k"
+
+
+# --------------------------------------------------------------- helpers --
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over the process group (identity without one)."""
+    if world <= 1 or not torch.distributed.is_initialized():
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "select": ["query_guided_block_gb300/csrc/sa_select.cu", "query_guided_block_gb300/csrc/sa_common.cuh"],
+    "decode": ["query_guided_block_gb300/csrc/sa_decode.cu", "query_guided_block_gb300/csrc/sa_common.cuh"],
+}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source_sha:\s*([0-9a-f]+)", text)
+    if not m:
+        return None
+    if m.group(2) != source_digest(KERNEL_SOURCES[kernel]):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed region runs."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.rows = []
+        self.proc = None
+        self.err = None
+        self.thread = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception as e:  # no nvidia-smi
+            self.err = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        if self.err or not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": self.err or "no samples"}
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside:
+            # region shorter than the sampling interval: nearest samples around it
+            near = sorted(self.rows, key=lambda tr: min(abs(tr[0] - t0), abs(tr[0] - t1)))[:3]
+            inside = [r for _, r in near]
+            note = "timed region shorter than the sampling interval; nearest samples"
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in inside if num(r[0]) is not None]
+        mx = [num(r[1]) for r in inside if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4)
+                          if len(r) > 4 + i and r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note,
+                "power_w_max": max((num(r[2]) or 0.0) for r in inside)}
+
+
+# ------------------------------------------------------ algorithmic bytes --
+
+def algorithmic_bytes(w, sel_count: torch.Tensor, sel_ids: torch.Tensor):
+    """Bytes the method must move per launch (see the design notes):
+    select: q + candidate metadata (min/max at the KV width; fp32 means) + ids out;
+    decode: q + K/V of the selected tokens + their page-table entries + ids + out."""
+    import numpy as np
+    esz = 2 if w.kv_dtype == torch.bfloat16 else 4
+    qsz = 2 if w.q_dtype == torch.bfloat16 else 4
+    B, Hq, Hkv, D, bs, N = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.n_tokens
+    nb = w.num_blocks
+    units = B * Hkv
+    q_bytes = B * Hq * D * qsz
+    win_first = (max(0, N - w.window_tokens) // bs) if w.window_tokens > 0 else nb
+    cnt = sel_count.detach().cpu().numpy().reshape(-1).astype(np.int64)
+    ids_bytes = int(cnt.sum()) * 4 + units * 4
+    if w.two_level:
+        n_coarse = -(-N // w.coarse_block)
+        per = w.coarse_block // bs
+        meta = units * n_coarse * D * 4 + units * min(w.topk_coarse * per, win_first) * 2 * D * esz
+    elif w.score == "mean":
+        meta = units * win_first * D * 4
+    else:
+        meta = units * win_first * 2 * D * esz
+    select_bytes = q_bytes + meta + ids_bytes
+    # selected tokens (the last block may be partial)
+    tokens = int(cnt.sum()) * bs
+    tail = N - (nb - 1) * bs if nb else bs
+    if tail != bs:
+        ids = sel_ids.detach().cpu().numpy().reshape(units, -1)
+        holds_last = sum(int((ids[u, : cnt[u]] == nb - 1).any()) for u in range(units))
+        tokens -= holds_last * (bs - tail)
+    decode_bytes = q_bytes + tokens * 2 * D * esz + int(cnt.sum()) * 4 * 2 + units * 4 + B * Hq * D * 4
+    return {"select": select_bytes, "decode": decode_bytes}
+
+
+# ------------------------------------------------------------- GPU arm --
+
+def run_gpu_arm(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from query_guided_block_gb300 import binding as Bn
+    from query_guided_block_gb300.build import build
+    from query_guided_block_gb300.decoder import SlotCache, SparseDecoder
+    from query_guided_block_gb300.workloads import WORKLOADS, make_inputs
+
+    if rank == 0 or world == 1:
+        build()
+    barrier(world)
+    build()
+    Bn.lib()
+
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, dev)
+    p = Bn.params_for(w)
+    dec = SparseDecoder(p, dev)
+    q_all = inp["q"] if inp["q"].dim() == 4 else inp["q"].unsqueeze(0)
+    q_static = q_all[0].clone()
+    kp, vp, bt = inp["k_pages"], inp["v_pages"], inp["block_table"]
+    cache = SlotCache(dec, w.cache_slots) if w.cache_slots else None
+    stream = torch.cuda.current_stream()
+
+    # metadata (prefill-time), timed on its own
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dec.build_meta(kp, bt)
+    torch.cuda.synchronize()
+    e0.record()
+    dec.build_meta(kp, bt)
+    e1.record()
+    torch.cuda.synchronize()
+    meta_ms = e0.elapsed_time(e1)
+    esz = 2 if w.kv_dtype == torch.bfloat16 else 4
+    meta_bytes = kp.numel() * esz + dec.metadata_bytes() + bt.numel() * 4
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    launches_per_step = (3 if w.two_level else 2) + (1 if cache else 0)
+    step_counter = [0]
+
+    def one_step(q):
+        dec.select(q)
+        dec.decode(q, kp, vp, bt)
+        if cache:
+            cache.diff(step_counter[0])
+            cache.advance()
+            step_counter[0] += 1
+
+    for i in range(args.warmup):
+        q = q_all[i % q_all.shape[0]] if cache else q_static
+        one_step(q)
+    torch.cuda.synchronize()
+    if dec.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(dev.index) if (rank == 0 or world == 1) else None
+    time.sleep(0.2 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = time.time()
+    for i in range(K):
+        flush.zero_()
+        q = q_all[(args.warmup + i) % q_all.shape[0]] if cache else q_static
+        a, b, c, d = ev[i]
+        a.record(stream)
+        dec.select(q)
+        b.record(stream)
+        dec.decode(q, kp, vp, bt)
+        c.record(stream)
+        if cache:
+            cache.diff(step_counter[0])
+            cache.advance()
+            step_counter[0] += 1
+        d.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_end = time.time()
+    clocks = sampler.summary(t_start, t_end) if sampler else None
+    if sampler:
+        sampler.stop()
+    flags = dec.device_error()
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x}")
+
+    sel_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    total_ms_local = sum(step_ms)
+    total_ms = aggregate_max(total_ms_local, world, dev)
+    queries = w.batch * w.num_q_heads
+    value = world * queries * K / (total_ms / 1e3)
+    ms_per_step = total_ms / K
+
+    nbytes = algorithmic_bytes(w, dec.sel_count, dec.sel_ids)
+    peak, peak_kind = hbm_peak()
+    sel_avg, dec_avg = statistics.mean(sel_ms), statistics.mean(dec_ms)
+    kern = {
+        "select": {"ms": sel_avg, "bytes": nbytes["select"], "gbs": nbytes["select"] / sel_avg / 1e6,
+                   "launches_per_step": 2 if w.two_level else 1},
+        "decode": {"ms": dec_avg, "bytes": nbytes["decode"], "gbs": nbytes["decode"] / dec_avg / 1e6,
+                   "launches_per_step": 1},
+    }
+    if cache:
+        kern["diff"] = {"ms": statistics.mean([e[2].elapsed_time(e[3]) for e in ev]),
+                        "launches_per_step": 1}
+    dominant = "select" if sel_avg >= dec_avg else "decode"
+    dk = kern[dominant]
+    step_bytes = nbytes["select"] + nbytes["decode"]
+    step_gbs = step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9
+    traffic = recorded_traffic(dominant, w.name)
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak,
+                "unit": "GB/s", "frac": dk["gbs"] / peak, "traffic": traffic,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s"}
+
+    # end to end: pinned host q in, fp32 out back to pinned host, every step
+    q_host = q_static.cpu().pin_memory()
+    out_host = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    q_dev = torch.empty_like(q_static)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        a, b = e2e_ev[i]
+        a.record(stream)
+        q_dev.copy_(q_host, non_blocking=True)
+        dec.select(q_dev)
+        dec.decode(q_dev, kp, vp, bt)
+        out_host.copy_(dec.out, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = aggregate_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
+    e2e = {"value": world * queries * K / (e2e_ms / 1e3), "unit": "queries/s",
+           "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+           "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
+           "ms_per_step": e2e_ms / K}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, dev, args.cpu_seconds)
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "queries/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded; planted relevant blocks)",
+        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "context": w.n_tokens,
+                   "block_size": w.block_size, "topk_blocks": w.topk,
+                   "window_tokens": w.window_tokens, "two_level": w.two_level,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"flushed before every step ({flush.numel() >> 20} MB write, outside the step events)",
+                   "timing": "CUDA events per kernel on the launching stream"},
+        "hbm_gbs": step_gbs,
+        "hbm_frac_of_measured": step_gbs / peak,
+        "hbm_frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS,
+        "step_bytes": step_bytes,
+        "roofline": roofline,
+        "kernels": kern,
+        "build_meta": {"ms": meta_ms, "gbs": meta_bytes / meta_ms / 1e6, "bytes": meta_bytes},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# -------------------------------------------------------------- CPU arms --
+
+def oracle_sample(w, inp, seqs):
+    """Host copies of the sequences `seqs` with their metadata built by the oracle
+    (not timed)."""
+    import dataclasses
+    import oracle
+    from query_guided_block_gb300.workloads import gather_sequences
+    host = gather_sequences(inp, seqs, "cpu")
+    ws = dataclasses.replace(w, batch=len(seqs))
+    p = oracle.problem(batch=ws.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                       head_dim=w.head_dim, n_tokens=w.n_tokens, block_size=w.block_size,
+                       num_pages=host["k_pages"].shape[0], window_tokens=w.window_tokens,
+                       topk=w.topk, two_level=w.two_level, coarse_block=w.coarse_block,
+                       topk_coarse=w.topk_coarse, score_kind=w.score,
+                       kv_bf16=w.kv_dtype == torch.bfloat16, q_bf16=w.q_dtype == torch.bfloat16)
+    need_mean = w.two_level or w.score == "mean"
+    kmin, kmax, kmean = oracle.build_meta(p, host["k_pages"], host["block_table"], with_mean=need_mean)
+    q = host["q"] if host["q"].dim() == 3 else host["q"][0]
+    arrays = {k: oracle.host_array(v) for k, v in host.items()}
+    arrays["q"] = oracle.host_array(q)
+    return p, arrays, kmin, kmax, kmean
+
+
+def oracle_unit_step(p, a, kmin, kmax, kmean, u):
+    """The oracle's select + decode for one unit."""
+    import oracle
+    rng = (u, u + 1)
+    if p.two_level:
+        r = oracle.select_two_level(p, a["q"], kmin, kmax, kmean, units=rng)
+        ids, cnt = r["sel_ids"], r["sel_count"]
+    else:
+        if p.score_kind == 1:
+            sc = oracle.mean_scores(p, a["q"], kmean, units=rng)
+        else:
+            sc = oracle.quest_scores(p, a["q"], kmin, kmax, units=rng)
+        ids, cnt = oracle.select(p, sc, units=rng)
+    oracle.decode(p, a["q"], a["k_pages"], a["v_pages"], a["block_table"], ids, cnt, units=rng)
+
+
+def cpu_baseline(w, inp, dev, seconds):
+    seqs = sorted({0, w.batch - 1})
+    p, a, kmin, kmax, kmean = oracle_sample(w, inp, seqs)
+    units = list(range(p.units))
+    threads = min(len(units), os.cpu_count() or 1)
+    done, t0 = 0, time.time()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        while True:
+            list(ex.map(lambda u: oracle_unit_step(p, a, kmin, kmax, kmean, u), units))
+            done += len(units)
+            if time.time() - t0 >= seconds:
+                break
+    dt = time.time() - t0
+    return {"value": done * w.group / dt, "unit": "queries/s", "cores": threads, "kind": "oracle",
+            "sample": f"select+decode of {len(units)} units (sequences {seqs} of {w.batch}, all KV "
+                      f"heads) repeated {done // len(units)}x over {dt:.1f} s; fp64 C oracle, "
+                      f"one unit per thread"}
+
+
+def run_reference_arm(args):
+    """The fp64 oracle timed on the host cores, same workload / metric / unit."""
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    from query_guided_block_gb300.workloads import WORKLOADS, make_inputs
+    oracle.build()
+    from query_guided_block_gb300.workloads import scaled
+    w = WORKLOADS[args.workload]
+    # the same workload drawn on the host for two sequences (the oracle never needs more)
+    ws = scaled(w, name=w.name, batch=min(2, w.batch))
+    inp = make_inputs(ws, "cpu")
+    seqs = list(range(ws.batch))
+    p, a, kmin, kmax, kmean = oracle_sample(ws, inp, seqs)
+    del inp
+    threads = min(p.units, os.cpu_count() or 1)
+    per_step_units = list(range(threads))           # one unit per thread per step
+
+    def step():
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda u: oracle_unit_step(p, a, kmin, kmax, kmean, u), per_step_units))
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = len(per_step_units) * w.group * args.steps / total
+    sample = (f"each step: oracle select+decode of {len(per_step_units)} units (one per thread) "
+              f"of sequences {seqs}")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; planted relevant blocks)",
+        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "context": w.n_tokens},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference_arm(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * sparse_attn.h -- C ABI of the GB300 (sm_103a) query-guided block-sparse decode
+ * attention library (libsparse_attn.so).
+ *
+ * One decode step ("select-then-compute", SGLang分层稀疏注意力技术解析与优化实践 §1.2, §2.2):
+ *
+ *   sparse_attn_build_meta   once per context: per-block key bounding box (min/max per
+ *                            channel) and, when asked for, per-block key means.
+ *   sparse_attn_select       per step: score every block of each (sequence, KV head) from
+ *                            the metadata, keep the local window, take the top-k blocks
+ *                            (optionally in two levels), emit ascending block ids.
+ *   sparse_attn_decode       per step: exact softmax attention over the union of the
+ *                            selected blocks' tokens.
+ *   sparse_attn_diff         per step: diff against the previous step and an LRU slot
+ *                            cache; reports hits, misses (with their slots), evictions.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  * All tensor pointers are DEVICE pointers into memory the caller owns.  The library
+ *    never allocates or frees device memory and keeps no pointer after a call returns.
+ *  * Calls are asynchronous on the given stream (a cudaStream_t; NULL = legacy default
+ *    stream).  Only sparse_attn_get_device_error synchronises.
+ *  * "unit" = one (sequence b, KV head kvh) pair, index u = b * Hkv + kvh.
+ *  * Query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
+ *  * Layouts (row-major, contiguous):
+ *      q           [B, Hq, D]                      q_dtype
+ *      k_pages,
+ *      v_pages     [num_pages, Hkv, block_size, D] kv_dtype  (one page = one block)
+ *      block_table [B, nb] int32   logical block j of sequence b -> physical page
+ *      kmin, kmax  [B, Hkv, nb, D] kv_dtype  (min/max of stored values: exact)
+ *      kmean       [B, Hkv, n_mean, D] float  (mean over mean_block tokens)
+ *      sel_ids     [B, Hkv, sel_stride] int32 ascending; sel_count [B, Hkv] int32
+ *      out         [B, Hq, D] float
+ *    with nb = ceil(n_tokens / block_size), sel_stride = sparse_attn_sel_stride(p),
+ *    mean_block = two_level ? coarse_block : block_size, n_mean = ceil(n_tokens/mean_block).
+ *    The last block may be partial (n_tokens not a multiple of block_size); its
+ *    missing tokens are never read into any result.
+ *  * Inputs must be finite.  Every pointer must be 16-byte aligned.
+ *  * The workspace (`ws`, `ws_bytes` >= sparse_attn_workspace_size) holds scores,
+ *    split-K partials, per-unit completion counters and a device error word.  Run
+ *    sparse_attn_workspace_init once after allocating it.  Calls that share one
+ *    workspace must be ordered on one stream.
+ *
+ * Status codes: 0 OK, 1 INVALID_ARG (null/misaligned pointer, bad size), 2 UNSUPPORTED
+ * (a dtype / head_dim / block_size / group combination without a kernel), 3 CUDA_ERROR
+ * (a launch failed), 4 DEVICE_BOUNDS (reported only by sparse_attn_get_device_error).
+ * Argument checks happen on the host before any launch; an entry that fails them
+ * launches nothing.  No call traps, asserts on the device or spins without a bound.
+ */
+#ifndef SPARSE_ATTN_H
+#define SPARSE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sparse_attn_stream; /* same type as cudaStream_t */
+
+enum {
+    SPARSE_ATTN_OK = 0,
+    SPARSE_ATTN_INVALID_ARG = 1,
+    SPARSE_ATTN_UNSUPPORTED = 2,
+    SPARSE_ATTN_CUDA_ERROR = 3,
+    SPARSE_ATTN_DEVICE_BOUNDS = 4
+};
+
+enum { SPARSE_ATTN_F32 = 0, SPARSE_ATTN_BF16 = 1 };
+enum { SPARSE_ATTN_SCORE_QUEST = 0, SPARSE_ATTN_SCORE_MEAN = 1 };
+
+/* Device error word bits (sparse_attn_get_device_error). */
+enum {
+    SPARSE_ATTN_ERR_PAGE = 1u << 0,      /* block_table entry outside [0, num_pages) */
+    SPARSE_ATTN_ERR_SEL_ID = 1u << 1,    /* sel_ids / prev_ids entry outside [0, nb) */
+    SPARSE_ATTN_ERR_SEL_COUNT = 1u << 2, /* sel_count outside [0, sel_stride] */
+    SPARSE_ATTN_ERR_TIMEOUT = 1u << 3,   /* a bounded wait on an async copy gave up */
+    SPARSE_ATTN_ERR_SLOT = 1u << 4       /* LRU state holds an id outside [-1, nb) */
+};
+
+/* Problem description.  Passed by pointer, read during the call, never retained.
+ * Field names follow the sparse-attention config of 从HiSparse到QSA的移植实战 §3.1
+ * (window size, coarse block, fine block, top_k_coarse, top_k_fine). */
+typedef struct sparse_attn_params {
+    int32_t batch;          /* B >= 0 (0: nothing to do) */
+    int32_t num_q_heads;    /* Hq, a multiple of Hkv; Hq / Hkv in {1, 2, 4, 8} */
+    int32_t num_kv_heads;   /* Hkv >= 1 */
+    int32_t head_dim;       /* D in {64, 128} */
+    int32_t n_tokens;       /* N >= 0 tokens cached per sequence */
+    int32_t block_size;     /* tokens per page = per selection block: 8, 16, 32, 64 or 128 */
+    int32_t num_pages;      /* pages in k_pages / v_pages (bounds for block_table) */
+    int32_t window_tokens;  /* W >= 0: blocks holding any of the last W tokens are always kept */
+    int32_t topk;           /* k >= 0 blocks (single level) or level-2 slices (two level) */
+    int32_t two_level;      /* 0: single level; 1: coarse blocks, then slices */
+    int32_t coarse_block;   /* tokens per coarse block (two level), a multiple of block_size */
+    int32_t topk_coarse;    /* K1 >= 0 coarse blocks surviving level 1 */
+    int32_t score_kind;     /* single level: SPARSE_ATTN_SCORE_QUEST or SPARSE_ATTN_SCORE_MEAN */
+    int32_t kv_dtype;       /* SPARSE_ATTN_F32 or SPARSE_ATTN_BF16 for K/V pages and kmin/kmax */
+    int32_t q_dtype;        /* SPARSE_ATTN_F32 or SPARSE_ATTN_BF16 */
+    float softmax_scale;    /* <= 0: 1/sqrt(D) */
+} sparse_attn_params;
+
+/* Human-readable name of a status code (static storage). */
+const char* sparse_attn_status_string(int status);
+
+/* Blocks per sequence, nb = ceil(n_tokens / block_size); -1 on bad params. */
+int32_t sparse_attn_num_blocks(const sparse_attn_params* p);
+
+/* int32 entries per unit row of sel_ids (and of every diff list): the largest
+ * selection possible, min(topk, candidates) + window blocks; -1 on bad params. */
+int32_t sparse_attn_sel_stride(const sparse_attn_params* p);
+
+/* Bytes of workspace the calls below need for this problem. */
+int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes);
+
+/* Zero the workspace's counters and error word (stream-ordered).  Call once after
+ * allocating a workspace, before its first use. */
+int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
+/* Per-block metadata from the paged keys.
+ * Defines: Quest key bounding box -- for each unit, block j and channel d,
+ *   kmin[j][d] = min_t K[t][d], kmax[j][d] = max_t K[t][d] over the block's tokens
+ *   (SGLang分层稀疏注意力技术解析与优化实践 §3.1.2, "Key Bounding Box");
+ * and, when kmean != NULL, kmean[r][d] = mean of K[t][d] over the tokens of mean row r
+ *   (SparDA page www.2kiu.com/news/4656707 §3.1, mean pooling; 从HiSparse到QSA的移植实战
+ *   §2.2, the coarse-block summary).  kmean is required when two_level or score_kind ==
+ *   MEAN, and may be NULL otherwise.
+ * Reads k_pages through block_table; writes kmin, kmax (kv_dtype) and kmean (float). */
+int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
+                           const int32_t* block_table, void* kmin, void* kmax, float* kmean,
+                           void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
+/* Block selection for one decode query per query head.
+ * Single level (SGLang page §3.1.2; SparDA page §3.2 fixed top-k):
+ *   score[u][j] = sum over the group's heads h and channels d of
+ *                 max(q_h[d] * kmin[j][d], q_h[d] * kmax[j][d])           (QUEST), or
+ *               = sum over h of q_h . kmean[j]                           (MEAN);
+ *   candidates are the blocks outside the window; the top k by (score desc, block id
+ *   asc) are united with the window blocks (从HiSparse到QSA的移植实战 §2.2, third level).
+ * Two level (从HiSparse到QSA的移植实战 §2.2, §3.1):
+ *   level 1 ranks every coarse block by sum_h q_h . kmean[c] and keeps topk_coarse;
+ *   level 2 ranks the non-window slices (blocks) inside the survivors by the Quest bound
+ *   and keeps topk; the window blocks are added.
+ * Scores are kept in fp32 (the HiSparse->QSA page's §5.1 shows fp16 block scores
+ * mis-ranking the top-k boundary).
+ * Writes sel_ids (ascending, sel_count[u] valid entries per row) and sel_count. */
+int sparse_attn_select(const sparse_attn_params* p, const void* q, const void* kmin,
+                       const void* kmax, const float* kmean, int32_t* sel_ids,
+                       int32_t* sel_count, void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
+/* Sparse decode attention (从HiSparse到QSA的移植实战 §3.3: iterate only the selected
+ * blocks given as a compact index array; SGLang page §2.2, "finally the sparse attention").
+ *   out[b][h] = sum over tokens t of the selected blocks of unit (b, h / G) of
+ *               softmax_t(softmax_scale * q_h . k_t) * v_t,
+ * exactly, over those tokens only; an empty selection gives a zero row.
+ * Out-of-range sel_ids / block_table entries set a device error bit and are skipped. */
+int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k_pages,
+                       const void* v_pages, const int32_t* block_table, const int32_t* sel_ids,
+                       const int32_t* sel_count, float* out, void* ws, size_t ws_bytes,
+                       sparse_attn_stream stream);
+
+/* Step-to-step diff and LRU slot cache (SGLang page §3.2: cache 2-4x top-k, LRU
+ * eviction; steps a-d: diff against the previous step, find what is resident, load
+ * the misses, update the index).  For each unit, with S = sel_ids row (ascending,
+ * sel_count entries) and P = prev_ids row:
+ *   new = S \ P, dropped = P \ S, hits = S blocks resident, misses = the others
+ *   (all ascending).  Miss i (ascending) takes the lowest free slot (slot_block == -1)
+ *   if any, else evicts the resident block NOT in S with the smallest
+ *   (slot_last_use, block id); evict_ids[i'] / evict_slot[i'] list evictions in miss
+ *   order.  Then slot_last_use = step for every block of S.
+ * In/out state: slot_block, slot_last_use [B*Hkv, cache_slots] int32 (start: all -1).
+ * Outputs: every list [B*Hkv, sel_stride] int32; counts [B*Hkv, 5] int32 =
+ *   {hits, misses, evictions, new, dropped}.
+ * Requires sel_stride <= cache_slots <= 1024. */
+int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
+                     const int32_t* sel_count, const int32_t* prev_ids,
+                     const int32_t* prev_count, int32_t cache_slots, int32_t* slot_block,
+                     int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
+                     int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
+                     int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, void* ws,
+                     size_t ws_bytes, sparse_attn_stream stream);
+
+/* Synchronise `stream`, copy the device error word to *flags (SPARSE_ATTN_ERR_* bits)
+ * and clear it.  Returns SPARSE_ATTN_DEVICE_BOUNDS when any bit was set. */
+int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream stream,
+                                 uint32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPARSE_ATTN_H */

@@ -1,0 +1,281 @@
+// extern "C" entry points of libsparse_attn: argument checks, problem geometry,
+// workspace carve-up and kernel launches.  No entry allocates device memory.
+#include <math.h>
+#include <string.h>
+
+#include "sa_internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int kMaxCandidates = 16384;   // per-unit selection keys staged in shared memory
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 0 on success, else a status code; fills g.
+int make_geometry(const sparse_attn_params* p, Geometry* g)
+{
+    if (!p || !g) return SPARSE_ATTN_INVALID_ARG;
+    memset(g, 0, sizeof *g);
+    if (p->batch < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->head_dim < 1 ||
+        p->n_tokens < 0 || p->block_size < 1 || p->num_pages < 0 || p->window_tokens < 0 ||
+        p->topk < 0 || p->topk_coarse < 0)
+        return SPARSE_ATTN_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return SPARSE_ATTN_INVALID_ARG;
+    if (p->two_level != 0 && p->two_level != 1) return SPARSE_ATTN_INVALID_ARG;
+    if (p->score_kind != SPARSE_ATTN_SCORE_QUEST && p->score_kind != SPARSE_ATTN_SCORE_MEAN)
+        return SPARSE_ATTN_INVALID_ARG;
+    if ((p->kv_dtype != SPARSE_ATTN_F32 && p->kv_dtype != SPARSE_ATTN_BF16) ||
+        (p->q_dtype != SPARSE_ATTN_F32 && p->q_dtype != SPARSE_ATTN_BF16))
+        return SPARSE_ATTN_INVALID_ARG;
+    if (!(p->softmax_scale == p->softmax_scale) || isinf(p->softmax_scale)) return SPARSE_ATTN_INVALID_ARG;
+
+    const int G = p->num_q_heads / p->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return SPARSE_ATTN_UNSUPPORTED;
+    if (p->head_dim != 64 && p->head_dim != 128) return SPARSE_ATTN_UNSUPPORTED;
+    const int bs = p->block_size;
+    if (bs != 8 && bs != 16 && bs != 32 && bs != 64 && bs != 128) return SPARSE_ATTN_UNSUPPORTED;
+    const bool kv_bf16 = p->kv_dtype == SPARSE_ATTN_BF16;
+    if (bs > decode_tokens_per_split(p->head_dim, kv_bf16)) return SPARSE_ATTN_UNSUPPORTED;
+
+    g->B = p->batch;
+    g->Hq = p->num_q_heads;
+    g->Hkv = p->num_kv_heads;
+    g->G = G;
+    g->D = p->head_dim;
+    g->N = p->n_tokens;
+    g->bs = bs;
+    g->nb = (p->n_tokens + bs - 1) / bs;
+    g->num_pages = p->num_pages;
+    if (g->nb > kMaxCandidates) return SPARSE_ATTN_UNSUPPORTED;
+    if (g->B > 0 && g->nb > 0 && g->num_pages < 1) return SPARSE_ATTN_INVALID_ARG;
+    if (p->window_tokens > 0) {
+        int first_tok = p->n_tokens - p->window_tokens;
+        if (first_tok < 0) first_tok = 0;
+        g->win_first = first_tok / bs;
+    } else {
+        g->win_first = g->nb;
+    }
+    g->win_count = g->nb - g->win_first;
+    g->n_cand = g->win_first;
+    g->topk = p->topk;
+    const int k_max = p->topk < g->n_cand ? p->topk : g->n_cand;
+    g->sel_stride = k_max + g->win_count > 0 ? k_max + g->win_count : 1;
+    g->kv_bf16 = kv_bf16;
+    g->q_bf16 = p->q_dtype == SPARSE_ATTN_BF16;
+    g->two_level = p->two_level != 0;
+    g->score_kind = p->score_kind;
+    if (g->two_level) {
+        if (p->coarse_block < bs || p->coarse_block % bs != 0) return SPARSE_ATTN_INVALID_ARG;
+        g->coarse_block = p->coarse_block;
+        g->per_coarse = p->coarse_block / bs;
+        g->n_coarse = (p->n_tokens + p->coarse_block - 1) / p->coarse_block;
+        g->topk_coarse = p->topk_coarse;
+        if (g->n_coarse > kMaxCandidates) return SPARSE_ATTN_UNSUPPORTED;
+        if ((long long)g->topk_coarse * g->per_coarse > kMaxCandidates) return SPARSE_ATTN_UNSUPPORTED;
+        g->mean_block = p->coarse_block;
+    } else {
+        g->mean_block = bs;
+    }
+    g->n_mean = (p->n_tokens + g->mean_block - 1) / g->mean_block;
+    const float scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf(float(p->head_dim));
+    g->scale_log2 = scale * 1.4426950408889634f;
+    return SPARSE_ATTN_OK;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? SPARSE_ATTN_OK : SPARSE_ATTN_CUDA_ERROR; }
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(const Geometry& g)
+{
+    WorkspaceLayout L{};
+    const size_t units = size_t(g.units());
+    int cols = g.n_cand;
+    if (g.two_level) {
+        cols = g.n_coarse;
+        if (g.topk_coarse * g.per_coarse > cols) cols = g.topk_coarse * g.per_coarse;
+    }
+    L.score_cols = cols > 0 ? cols : 1;
+    const int tps = decode_tokens_per_split(g.D, g.kv_bf16);
+    L.blocks_per_split = tps / g.bs;
+    L.max_splits = (g.sel_stride + L.blocks_per_split - 1) / L.blocks_per_split;
+    if (L.max_splits < 1) L.max_splits = 1;
+    const size_t heads = size_t(g.B) * g.Hq;
+
+    size_t off = 0;
+    L.err = off;              off = align256(off + sizeof(uint32_t));
+    L.sel_counters = off;     off = align256(off + units * sizeof(uint32_t));
+    L.dec_counters = off;     off = align256(off + units * sizeof(uint32_t));
+    L.l1_counters = off;      off = align256(off + units * sizeof(uint32_t));
+    L.scores = off;           off = align256(off + units * L.score_cols * sizeof(float));
+    L.survivors = off;        off = align256(off + units * size_t(g.topk_coarse > 0 ? g.topk_coarse : 1) * sizeof(int32_t));
+    L.n_survivors = off;      off = align256(off + units * sizeof(int32_t));
+    L.part_m = off;           off = align256(off + heads * L.max_splits * sizeof(float));
+    L.part_l = off;           off = align256(off + heads * L.max_splits * sizeof(float));
+    L.part_o = off;           off = align256(off + heads * L.max_splits * size_t(g.D) * sizeof(float));
+    L.total = off;
+    return L;
+}
+
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" {
+
+const char* sparse_attn_status_string(int status)
+{
+    switch (status) {
+        case SPARSE_ATTN_OK: return "ok";
+        case SPARSE_ATTN_INVALID_ARG: return "invalid argument";
+        case SPARSE_ATTN_UNSUPPORTED: return "unsupported configuration";
+        case SPARSE_ATTN_CUDA_ERROR: return "CUDA launch error";
+        case SPARSE_ATTN_DEVICE_BOUNDS: return "device-side bounds error";
+        default: return "unknown status";
+    }
+}
+
+int32_t sparse_attn_num_blocks(const sparse_attn_params* p)
+{
+    Geometry g;
+    return make_geometry(p, &g) == SPARSE_ATTN_OK ? g.nb : -1;
+}
+
+int32_t sparse_attn_sel_stride(const sparse_attn_params* p)
+{
+    Geometry g;
+    return make_geometry(p, &g) == SPARSE_ATTN_OK ? g.sel_stride : -1;
+}
+
+int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes)
+{
+    if (!bytes) return SPARSE_ATTN_INVALID_ARG;
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    *bytes = workspace_layout(g).total;
+    return SPARSE_ATTN_OK;
+}
+
+int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream stream)
+{
+    if (!ws || !aligned(ws, 256) || ws_bytes < 256) return SPARSE_ATTN_INVALID_ARG;
+    return status_of(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
+                           const int32_t* block_table, void* kmin, void* kmax, float* kmean,
+                           void* ws, size_t ws_bytes, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    const bool need_mean = g.two_level || g.score_kind == SPARSE_ATTN_SCORE_MEAN;
+    if (need_mean && !kmean) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() > 0 && g.nb > 0) {
+        if (!k_pages || !block_table || !kmin || !kmax) return SPARSE_ATTN_INVALID_ARG;
+        if (!aligned(k_pages, 16) || !aligned(kmin, 16) || !aligned(kmax, 16) ||
+            !aligned(block_table, 4) || (kmean && !aligned(kmean, 16)))
+            return SPARSE_ATTN_INVALID_ARG;
+    }
+    char* w = static_cast<char*>(ws);
+    return status_of(launch_build_meta(g, k_pages, block_table, kmin, kmax, need_mean ? kmean : nullptr,
+                                       reinterpret_cast<uint32_t*>(w + L.err),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_select(const sparse_attn_params* p, const void* q, const void* kmin,
+                       const void* kmax, const float* kmean, int32_t* sel_ids,
+                       int32_t* sel_count, void* ws, size_t ws_bytes, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() > 0) {
+        if (!q || !sel_ids || !sel_count || !aligned(q, 16) || !aligned(sel_ids, 4) ||
+            !aligned(sel_count, 4))
+            return SPARSE_ATTN_INVALID_ARG;
+        const bool need_mean = g.two_level || g.score_kind == SPARSE_ATTN_SCORE_MEAN;
+        const bool need_box = g.two_level || g.score_kind == SPARSE_ATTN_SCORE_QUEST;
+        if (g.nb > 0) {
+            if (need_mean && (!kmean || !aligned(kmean, 16))) return SPARSE_ATTN_INVALID_ARG;
+            if (need_box && (!kmin || !kmax || !aligned(kmin, 16) || !aligned(kmax, 16)))
+                return SPARSE_ATTN_INVALID_ARG;
+        }
+    }
+    return status_of(launch_select(g, L, static_cast<char*>(ws), q, kmin, kmax, kmean, sel_ids,
+                                   sel_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k_pages,
+                       const void* v_pages, const int32_t* block_table, const int32_t* sel_ids,
+                       const int32_t* sel_count, float* out, void* ws, size_t ws_bytes,
+                       sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() > 0) {
+        if (!q || !out || !sel_ids || !sel_count || !aligned(q, 16) || !aligned(out, 16) ||
+            !aligned(sel_ids, 4) || !aligned(sel_count, 4))
+            return SPARSE_ATTN_INVALID_ARG;
+        if (g.nb > 0 && (!k_pages || !v_pages || !block_table || !aligned(k_pages, 16) ||
+                         !aligned(v_pages, 16) || !aligned(block_table, 4)))
+            return SPARSE_ATTN_INVALID_ARG;
+    }
+    return status_of(launch_decode(g, L, static_cast<char*>(ws), q, k_pages, v_pages, block_table,
+                                   sel_ids, sel_count, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
+                     const int32_t* sel_count, const int32_t* prev_ids,
+                     const int32_t* prev_count, int32_t cache_slots, int32_t* slot_block,
+                     int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
+                     int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
+                     int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, void* ws,
+                     size_t ws_bytes, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (cache_slots < 1 || cache_slots > 1024 || g.sel_stride > cache_slots) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() > 0) {
+        const void* ptrs[] = {sel_ids, sel_count, prev_ids, prev_count, slot_block, slot_last_use,
+                              hit_ids, miss_ids, miss_slot, evict_ids, evict_slot, new_ids,
+                              dropped_ids, counts};
+        for (const void* ptr : ptrs)
+            if (!ptr || !aligned(ptr, 4)) return SPARSE_ATTN_INVALID_ARG;
+    }
+    char* w = static_cast<char*>(ws);
+    return status_of(launch_diff(g, step, sel_ids, sel_count, prev_ids, prev_count, cache_slots,
+                                 slot_block, slot_last_use, hit_ids, miss_ids, miss_slot, evict_ids,
+                                 evict_slot, new_ids, dropped_ids, counts,
+                                 reinterpret_cast<uint32_t*>(w + L.err),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream stream, uint32_t* flags)
+{
+    if (!ws || !flags || !aligned(ws, 256) || ws_bytes < 256) return SPARSE_ATTN_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof word, s);
+    if (e != cudaSuccess) return SPARSE_ATTN_CUDA_ERROR;
+    *flags = word;
+    return word ? SPARSE_ATTN_DEVICE_BOUNDS : SPARSE_ATTN_OK;
+}
+
+}  // extern "C"

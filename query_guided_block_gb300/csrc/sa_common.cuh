@@ -1,0 +1,192 @@
+// Device-side helpers shared by the sm_103a kernels of libsparse_attn.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sparse_attn.h"
+
+namespace sa {
+
+constexpr uint32_t kFullMask = 0xffffffffu;
+constexpr int kWarp = 32;
+
+// ------------------------------------------------------------ error word --
+__device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
+
+// --------------------------------------------------------- element loads --
+// bfloat16 is the upper half of an IEEE-754 binary32, so widening is a shift.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 16 bytes -> 8 floats (bf16) or 4 floats (fp32).
+template <bool BF16>
+__device__ __forceinline__ void unpack16(const uint4& v, float* f)
+{
+    if constexpr (BF16) {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+        f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    } else {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+}
+
+// Streaming 16-byte load that does not allocate in L1 (data read exactly once).
+__device__ __forceinline__ uint4 ld_stream16(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Load one element of a q vector stored as bf16 or fp32 (runtime dtype).
+__device__ __forceinline__ float load_q(const void* q, size_t idx, bool bf16)
+{
+    if (bf16) {
+        uint16_t h = reinterpret_cast<const uint16_t*>(q)[idx];
+        return __uint_as_float(uint32_t(h) << 16);
+    }
+    return reinterpret_cast<const float*>(q)[idx];
+}
+
+// Round-trip of a float that holds a bf16 value back to its 16-bit pattern (exact).
+__device__ __forceinline__ uint32_t f32_to_bf16_bits_exact(float x) { return __float_as_uint(x) >> 16; }
+
+// ------------------------------------------------------ ordering of keys --
+// Monotone map float -> uint32: a > b  <=>  key(a) > key(b) for non-NaN values.
+// Finite scores never map to 0, which marks "not a candidate".
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------- warp utilities --
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ int warp_inclusive_scan(int v, int lane)
+{
+#pragma unroll
+    for (int off = 1; off < kWarp; off <<= 1) {
+        int t = __shfl_up_sync(kFullMask, v, off);
+        if (lane >= off) v += t;
+    }
+    return v;
+}
+
+// Sum each of V values held by a lane over the groups of L consecutive lanes
+// (L a power of two <= 32, xor-aligned).  "Transposed" halving: at every step a lane
+// keeps half of its values and trades the other half with its partner, so reducing
+// V values costs V - V/L shuffles instead of V * log2(L).  Afterwards lane
+// (lane % L) holds, in v[0 .. max(1, V/L) - 1], the totals of value indices
+//   (lane % L) * (V / L) + r            when V >= L, or
+//   (lane % L) / (L / V)                when V <  L (one value, replicated).
+template <int V, int L>
+__device__ __forceinline__ void group_reduce_transposed(float (&v)[V], int lane)
+{
+    int n = V;
+#pragma unroll
+    for (int m = L / 2; m >= 1; m >>= 1) {
+        if (n > 1) {
+            const bool upper = (lane & m) != 0;
+            const int half = n / 2;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                if (i < half) {
+                    float send = upper ? v[i] : v[i + half];
+                    float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(kFullMask, send, m);
+                }
+            }
+            n = half;
+        } else {
+            v[0] += __shfl_xor_sync(kFullMask, v[0], m);
+        }
+    }
+}
+
+// --------------------------------------------------- mbarrier / bulk copy --
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk async copy global -> this CTA's shared memory, completion counted in bytes
+// on `bar`.  Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after about `max_cycles`
+// SM clocks.  Returns false on time-out (the caller records an error).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long max_cycles)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > max_cycles) return false;
+    }
+    return true;
+}
+
+// About one second at GB300 clocks: far beyond any legitimate copy latency.
+constexpr long long kWaitCycles = 2000000000LL;
+
+// exp2 on the special-function unit (PTX ex2.approx.ftz.f32; about 2 ulp).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace sa

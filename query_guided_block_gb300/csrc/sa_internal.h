@@ -1,0 +1,74 @@
+// Host-side launcher interface between the C ABI (sa_api.cu) and the kernel files.
+// Every launcher assumes its arguments were validated by the ABI layer and returns a
+// cudaError_t from the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sparse_attn.h"
+
+namespace sa {
+
+// Derived, validated problem geometry.
+struct Geometry {
+    int B, Hq, Hkv, G, D, N, bs, nb, num_pages;
+    int win_first, win_count;      // window blocks [win_first, nb)
+    int n_cand;                    // single-level candidates = win_first
+    int sel_stride;                // ids per unit row
+    bool kv_bf16, q_bf16;
+    bool two_level;
+    int coarse_block, per_coarse, n_coarse, topk_coarse;
+    int mean_block, n_mean;        // kmean rows per unit
+    int topk;
+    int score_kind;
+    float scale_log2;              // softmax_scale * log2(e)
+    int units() const { return B * Hkv; }
+};
+
+// Workspace carve-up (byte offsets from the workspace base, each 256-byte aligned).
+struct WorkspaceLayout {
+    size_t err;            // uint32 error word
+    size_t sel_counters;   // uint32 [units]
+    size_t dec_counters;   // uint32 [units]
+    size_t l1_counters;    // uint32 [units] (two-level, level 1)
+    size_t scores;         // float [units, score_cols]
+    size_t survivors;      // int32 [units, topk_coarse] (two-level)
+    size_t n_survivors;    // int32 [units]
+    size_t part_m;         // float [B*Hq, max_splits]
+    size_t part_l;         // float [B*Hq, max_splits]
+    size_t part_o;         // float [B*Hq, max_splits, D]
+    size_t total;
+    int score_cols;        // candidates per unit row of the score buffer
+    int max_splits;        // decode split-K slices per unit
+    int blocks_per_split;  // selected blocks per decode CTA
+};
+
+WorkspaceLayout workspace_layout(const Geometry& g);
+
+// Tokens one decode CTA stages (K and V tiles of this many tokens fit in 64 KB).
+int decode_tokens_per_split(int D, bool kv_bf16);
+
+cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int32_t* block_table,
+                              void* kmin, void* kmax, float* kmean, uint32_t* err,
+                              cudaStream_t s);
+
+cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
+                          const void* kmin, const void* kmax, const float* kmean,
+                          int32_t* sel_ids, int32_t* sel_count, cudaStream_t s);
+
+cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
+                          const void* k_pages, const void* v_pages, const int32_t* block_table,
+                          const int32_t* sel_ids, const int32_t* sel_count, float* out,
+                          cudaStream_t s);
+
+cudaError_t launch_diff(const Geometry& g, int step, const int32_t* sel_ids,
+                        const int32_t* sel_count, const int32_t* prev_ids,
+                        const int32_t* prev_count, int cache_slots, int32_t* slot_block,
+                        int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
+                        int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
+                        int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, uint32_t* err,
+                        cudaStream_t s);
+
+}  // namespace sa

@@ -1,0 +1,111 @@
+"""Device-buffer plumbing around the C ABI: allocates, with torch, the tensors one
+decode problem needs and calls the entry points in order.  No arithmetic of the method
+happens here."""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class SparseDecoder:
+    """Owns metadata, selection, output and workspace buffers for one problem.
+
+    The KV page pools, block table and queries belong to the caller.
+    """
+
+    def __init__(self, params: B.sparse_attn_params, device="cuda"):
+        self.p = params
+        self.device = torch.device(device)
+        p = params
+        self.nb = B.sparse_attn_num_blocks(p)
+        self.sel_stride = B.sparse_attn_sel_stride(p)
+        self.units = p.batch * p.num_kv_heads
+        kv = torch.bfloat16 if p.kv_dtype == B.BF16 else torch.float32
+        self.kv_dtype = kv
+        dev = self.device
+        self.kmin = torch.empty(p.batch, p.num_kv_heads, self.nb, p.head_dim, dtype=kv, device=dev)
+        self.kmax = torch.empty_like(self.kmin)
+        self.needs_mean = bool(p.two_level) or p.score_kind == B.SCORE_MEAN
+        self.kmean = None
+        if self.needs_mean:
+            mb = p.coarse_block if p.two_level else p.block_size
+            rows = -(-p.n_tokens // mb)
+            self.kmean = torch.empty(p.batch, p.num_kv_heads, rows, p.head_dim, dtype=torch.float32,
+                                     device=dev)
+        self.ws_bytes = B.sparse_attn_workspace_size(p)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        B.sparse_attn_workspace_init(self.ws)
+        self.sel_ids = torch.empty(p.batch, p.num_kv_heads, self.sel_stride, dtype=torch.int32,
+                                   device=dev)
+        self.sel_count = torch.empty(p.batch, p.num_kv_heads, dtype=torch.int32, device=dev)
+        self.out = torch.empty(p.batch, p.num_q_heads, p.head_dim, dtype=torch.float32, device=dev)
+
+    def metadata_bytes(self) -> int:
+        n = self.kmin.numel() * self.kmin.element_size() * 2
+        if self.kmean is not None:
+            n += self.kmean.numel() * 4
+        return n
+
+    def build_meta(self, k_pages, block_table, stream=None):
+        B.sparse_attn_build_meta(self.p, k_pages, block_table, self.kmin, self.kmax, self.kmean,
+                                 self.ws, stream)
+
+    def select(self, q, stream=None):
+        B.sparse_attn_select(self.p, q, self.kmin, self.kmax, self.kmean, self.sel_ids,
+                             self.sel_count, self.ws, stream)
+
+    def decode(self, q, k_pages, v_pages, block_table, sel_ids=None, sel_count=None, out=None,
+               stream=None):
+        B.sparse_attn_decode(self.p, q, k_pages, v_pages, block_table,
+                             self.sel_ids if sel_ids is None else sel_ids,
+                             self.sel_count if sel_count is None else sel_count,
+                             self.out if out is None else out, self.ws, stream)
+
+    def step(self, q, k_pages, v_pages, block_table, stream=None):
+        """select + decode for one query batch; returns the output tensor."""
+        self.select(q, stream)
+        self.decode(q, k_pages, v_pages, block_table, stream=stream)
+        return self.out
+
+    def device_error(self, stream=None) -> int:
+        return B.sparse_attn_get_device_error(self.ws, stream)
+
+
+class SlotCache:
+    """LRU slot-cache state and per-step diff outputs for ``sparse_attn_diff``."""
+
+    def __init__(self, decoder: SparseDecoder, cache_slots: int):
+        d = decoder
+        dev = d.device
+        u, w = d.units, d.sel_stride
+        self.decoder = d
+        self.cache_slots = cache_slots
+        self.slot_block = torch.full((u, cache_slots), -1, dtype=torch.int32, device=dev)
+        self.slot_last_use = torch.full((u, cache_slots), -1, dtype=torch.int32, device=dev)
+        self.prev_ids = torch.full((u, w), -1, dtype=torch.int32, device=dev)
+        self.prev_count = torch.zeros(u, dtype=torch.int32, device=dev)
+        names = ("hit_ids", "miss_ids", "miss_slot", "evict_ids", "evict_slot", "new_ids",
+                 "dropped_ids")
+        self.lists = {n: torch.full((u, w), -1, dtype=torch.int32, device=dev) for n in names}
+        self.counts = torch.zeros(u, 5, dtype=torch.int32, device=dev)
+
+    def diff(self, step: int, sel_ids: Optional[torch.Tensor] = None,
+             sel_count: Optional[torch.Tensor] = None, stream=None):
+        d = self.decoder
+        ids = d.sel_ids if sel_ids is None else sel_ids
+        cnt = d.sel_count if sel_count is None else sel_count
+        L = self.lists
+        B.sparse_attn_diff(d.p, step, ids, cnt, self.prev_ids, self.prev_count, self.cache_slots,
+                           self.slot_block, self.slot_last_use, L["hit_ids"], L["miss_ids"],
+                           L["miss_slot"], L["evict_ids"], L["evict_slot"], L["new_ids"],
+                           L["dropped_ids"], self.counts, d.ws, stream)
+
+    def advance(self, sel_ids: Optional[torch.Tensor] = None,
+                sel_count: Optional[torch.Tensor] = None):
+        """Remember this step's request set as the next step's previous set."""
+        d = self.decoder
+        self.prev_ids.copy_((d.sel_ids if sel_ids is None else sel_ids).view(self.prev_ids.shape))
+        self.prev_count.copy_((d.sel_count if sel_count is None else sel_count).view(-1))

@@ -33,7 +33,7 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "derive_seed", "scaled"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "derive_seed", "scaled", "gather_sequences"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -215,3 +215,19 @@ def make_inputs(w: Workload, device="cpu", planted_blocks: Optional[torch.Tensor
 
     return {"q": q, "k_pages": k_pages, "v_pages": v_pages,
             "block_table": block_table, "planted": planted}
+
+
+def gather_sequences(inp: dict, seqs, device="cpu") -> dict:
+    """The sequences ``seqs`` of a drawn instance with their pages copied into a private
+    pool in logical order (page table = identity), on ``device``.  Pure data movement:
+    used to hand a sample of a large instance to a host-side checker."""
+    seqs = list(seqs)
+    bt = inp["block_table"][seqs].long()
+    pages = bt.reshape(-1)
+    q = inp["q"]
+    q = q[:, seqs] if q.dim() == 4 else q[seqs]
+    return {"k_pages": inp["k_pages"][pages].to(device),
+            "v_pages": inp["v_pages"][pages].to(device),
+            "block_table": torch.arange(pages.numel(), dtype=torch.int32,
+                                        device=device).view(len(seqs), -1),
+            "q": q.to(device)}

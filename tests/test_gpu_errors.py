@@ -1,0 +1,85 @@
+"""Bad inputs that only the device can see are caught by the kernels' own bounds
+checks: the access is skipped, a bit is set in the workspace error word, and the
+context stays usable.  Every input here is one the kernels check before use; nothing
+is expected to fault."""
+import numpy as np
+import pytest
+import torch
+
+from query_guided_block_gb300 import binding as B
+from query_guided_block_gb300.build import build
+from query_guided_block_gb300.decoder import SlotCache, SparseDecoder
+from query_guided_block_gb300.workloads import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available()
+    build()
+    B.lib()
+
+
+def _case():
+    w = Workload(name="err", batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                 n_tokens=4096, block_size=64, window_tokens=256, topk=6)
+    inp = make_inputs(w, "cuda")
+    dec = SparseDecoder(B.params_for(w))
+    dec.build_meta(inp["k_pages"], inp["block_table"])
+    dec.select(inp["q"])
+    assert dec.device_error() == 0
+    return w, inp, dec
+
+
+def test_out_of_range_page_in_block_table():
+    w, inp, dec = _case()
+    bt = inp["block_table"].clone()
+    j = int(dec.sel_ids[0, 0, 0])
+    bt[0, j] = w.num_pages + 5
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], bt)
+    assert dec.device_error() & B.ERR_PAGE
+    bt[0, 3] = -7
+    dec.build_meta(inp["k_pages"], bt)
+    assert dec.device_error() & B.ERR_PAGE
+    # the error word was cleared by the read; a clean call reports nothing
+    dec.build_meta(inp["k_pages"], inp["block_table"])
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"])
+    assert dec.device_error() == 0
+
+
+def test_out_of_range_selection():
+    w, inp, dec = _case()
+    ids = dec.sel_ids.clone()
+    ids[1, 1, 2] = w.num_blocks + 3
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], sel_ids=ids)
+    assert dec.device_error() & B.ERR_SEL_ID
+    cnt = dec.sel_count.clone()
+    cnt[0, 1] = dec.sel_stride + 9
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], sel_count=cnt)
+    assert dec.device_error() & B.ERR_SEL_COUNT
+    cnt[0, 1] = -1
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], sel_count=cnt)
+    assert dec.device_error() & B.ERR_SEL_COUNT
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"])
+    assert dec.device_error() == 0
+    assert torch.isfinite(dec.out).all()
+
+
+def test_diff_rejects_corrupt_state_and_leaves_it_untouched():
+    w, inp, dec = _case()
+    cache = SlotCache(dec, 32)
+    cache.slot_block[1, 4] = w.num_blocks + 1
+    before = cache.slot_block.clone()
+    cache.diff(0)
+    assert dec.device_error() & B.ERR_SLOT
+    assert torch.equal(cache.slot_block[1], before[1])
+    assert int(cache.counts[1].abs().sum()) == 0
+    # non-ascending request set
+    cache.slot_block.fill_(-1)
+    ids = dec.sel_ids.clone()
+    ids[0, 0, 0], ids[0, 0, 1] = ids[0, 0, 1].item(), ids[0, 0, 0].item()
+    cache.diff(0, sel_ids=ids)
+    assert dec.device_error() & B.ERR_SEL_ID
+    cache.diff(0)
+    assert dec.device_error() == 0

@@ -1,0 +1,218 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Tolerances (from the problem statement): selected ids, diff / LRU outputs and the
+min/max bounding box are bit-exact (selection up to swaps among candidates whose
+oracle scores lie within 1e-5 relative of the k-th score); attention output within
+2e-3 max-abs for bf16 KV and 1e-5 for fp32 KV; block means (fp32 accumulation vs fp64)
+within 1e-4.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from query_guided_block_gb300 import binding as B
+from query_guided_block_gb300.build import build
+from query_guided_block_gb300.decoder import SparseDecoder
+from query_guided_block_gb300.workloads import WORKLOADS, Workload, make_inputs, scaled
+from tests.conftest import oracle_problem_for
+from tests.parity import (ATOL, as_np, bf16_bits_to_f64, check_selection, check_two_level,
+                          oracle_meta, sub_problem, sub_workload)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build()
+    B.lib()
+
+
+def run_gpu(w, inp, params=None):
+    p = params or B.params_for(w)
+    dec = SparseDecoder(p)
+    dec.build_meta(inp["k_pages"], inp["block_table"])
+    q = inp["q"] if inp["q"].dim() == 3 else inp["q"][0]
+    dec.select(q)
+    dec.decode(q, inp["k_pages"], inp["v_pages"], inp["block_table"])
+    flags = dec.device_error()
+    assert flags == 0, f"device error flags 0x{flags:x}"
+    return dec
+
+
+def compare_all(w, inp, dec, seqs=None):
+    """Full comparison of metadata, selection and output on sequences `seqs`."""
+    seqs = list(range(w.batch)) if seqs is None else list(seqs)
+    host = sub_problem(w, inp, seqs)
+    ws = sub_workload(w, len(seqs))
+    p, (kmin, kmax, kmean) = oracle_meta(ws, host)
+    Hkv = w.num_kv_heads
+    rows = [s * Hkv + h for s in seqs for h in range(Hkv)]
+    # metadata: exact box, close means
+    gmin = bf16_bits_to_f64(dec.kmin[seqs])
+    gmax = bf16_bits_to_f64(dec.kmax[seqs])
+    assert np.array_equal(gmin, kmin) and np.array_equal(gmax, kmax)
+    if kmean is not None:
+        np.testing.assert_allclose(as_np(dec.kmean[seqs]).astype(np.float64), kmean, rtol=0, atol=1e-4)
+    gids = as_np(dec.sel_ids).reshape(w.units, -1)[rows]
+    gcnt = as_np(dec.sel_count).reshape(-1)[rows]
+    hq = host["q"] if host["q"].dim() == 3 else host["q"][0]
+    if w.two_level:
+        check_two_level(ws, p, hq, kmin, kmax, kmean, gids, gcnt, units=range(ws.units))
+    else:
+        if w.score == "mean":
+            scores = oracle.mean_scores(p, hq, kmean)
+        else:
+            scores = oracle.quest_scores(p, hq, kmin, kmax)
+        oid, ocnt = oracle.select(p, scores)
+        check_selection(gids, gcnt, oid, ocnt, scores, w.topk, p.first_window_block())
+    # attention on the GPU's own selection
+    out = oracle.decode(p, hq, host["k_pages"], host["v_pages"], host["block_table"], gids, gcnt)
+    got = as_np(dec.out[seqs]).astype(np.float64)
+    err = np.abs(got - out).max() if out.size else 0.0
+    assert err <= ATOL[w.kv_dtype], f"max abs error {err}"
+    return err
+
+
+def _w(**kw):
+    base = dict(name="gpu_small", batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                n_tokens=5000, block_size=64, window_tokens=300, topk=9)
+    base.update(kw)
+    return Workload(**base)
+
+
+# ------------------------------------------------------------- small cases --
+
+def test_tiny_config_exact():
+    w = WORKLOADS["tiny_fp32_4k"]
+    inp = make_inputs(w, "cuda")
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+
+
+SMALL = [
+    dict(head_dim=128, num_q_heads=8, kv_dtype=torch.bfloat16, block_size=64),
+    dict(head_dim=128, num_q_heads=8, kv_dtype=torch.bfloat16, block_size=32, planted_per_unit=5),
+    dict(head_dim=64, num_q_heads=16, kv_dtype=torch.bfloat16, block_size=16),
+    dict(head_dim=128, num_q_heads=2, kv_dtype=torch.float32, q_dtype=torch.float32, block_size=32),
+    dict(head_dim=64, num_q_heads=4, kv_dtype=torch.float32, q_dtype=torch.bfloat16, block_size=8,
+         n_tokens=3001),
+    dict(head_dim=128, num_q_heads=2, kv_dtype=torch.bfloat16, block_size=128, n_tokens=9000,
+         window_tokens=0),
+    dict(head_dim=128, num_q_heads=8, kv_dtype=torch.bfloat16, score="mean", block_size=64),
+    dict(head_dim=64, num_q_heads=8, kv_dtype=torch.float32, q_dtype=torch.float32, score="mean",
+         block_size=32, n_tokens=4097),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=[str(i) for i in range(len(SMALL))])
+def test_small_matrix(cfg):
+    w = _w(**cfg)
+    inp = make_inputs(w, "cuda")
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+
+
+@pytest.mark.parametrize("n_tokens,topk,window", [(40000, 12, 512), (33000, 5, 1000), (70001, 20, 0)])
+def test_two_level_small(n_tokens, topk, window):
+    w = _w(n_tokens=n_tokens, block_size=64, window_tokens=window, topk=topk, two_level=True,
+           coarse_block=1024, topk_coarse=6, planted_per_unit=10)
+    inp = make_inputs(w, "cuda")
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+
+
+def test_ties_go_to_the_lower_block_id():
+    """Logical blocks that share one physical page have identical scores."""
+    w = _w(n_tokens=64 * 64, block_size=64, window_tokens=128, topk=7, num_q_heads=4,
+           num_kv_heads=2)
+    inp = make_inputs(w, "cuda")
+    bt = inp["block_table"]
+    # blocks 3, 10, 17, ... all point at one page; 5 more at another
+    bt[:, 3::7] = bt[:, 3:4]
+    bt[:, 5:40:9] = bt[:, 5:6]
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+    # and the exact-tie members picked are the lowest ids of their tie group
+    host = sub_problem(w, inp, range(w.batch))
+    p, (kmin, kmax, _) = oracle_meta(w, host)
+    sc = oracle.quest_scores(p, host["q"], kmin, kmax)
+    ids = as_np(dec.sel_ids).reshape(w.units, -1)
+    cnt = as_np(dec.sel_count).reshape(-1)
+    for u in range(w.units):
+        sel = set(ids[u, : cnt[u]].tolist())
+        for j in sel:
+            if j >= p.first_window_block():
+                continue
+            for i in range(j):
+                if sc[u, i] == sc[u, j]:
+                    assert i in sel, f"unit {u}: tie {i} < {j} not taken first"
+
+
+@pytest.mark.parametrize("case", ["dense", "k_zero", "window_only_all", "no_window", "short"])
+def test_degenerate_selections(case):
+    kw = {"dense": dict(topk=10 ** 6), "k_zero": dict(topk=0),
+          "window_only_all": dict(window_tokens=10 ** 6, topk=3),
+          "no_window": dict(window_tokens=0, topk=4),
+          "short": dict(n_tokens=37, block_size=16, window_tokens=20, topk=1)}[case]
+    w = _w(**kw)
+    inp = make_inputs(w, "cuda")
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+    if case in ("dense", "window_only_all"):
+        assert np.all(as_np(dec.sel_count) == w.num_blocks)
+
+
+def test_empty_inputs():
+    # zero context: nothing to select, zero output
+    w = _w(n_tokens=0)
+    p = B.params_for(w)
+    dec = SparseDecoder(p)
+    q = torch.randn(w.batch, w.num_q_heads, w.head_dim, device="cuda").to(w.q_dtype)
+    dec.out.fill_(7.0)
+    dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dec.select(q)
+    dec.decode(q, dummy, dummy, bt)
+    assert dec.device_error() == 0
+    assert np.all(as_np(dec.sel_count) == 0)
+    assert np.all(as_np(dec.out) == 0)
+    # zero batch: every entry point is a no-op
+    p0 = B.params_for(dataclasses.replace(w, batch=0, n_tokens=100))
+    dec0 = SparseDecoder(p0)
+    dec0.select(q)
+    dec0.decode(q, dummy, dummy, bt)
+    assert dec0.device_error() == 0
+
+
+def test_largest_block_count():
+    """16384 blocks per unit: the largest selection the top-k stage holds on chip."""
+    w = _w(batch=1, num_q_heads=2, num_kv_heads=1, n_tokens=16384 * 8, block_size=8,
+           window_tokens=64, topk=100, planted_per_unit=20)
+    inp = make_inputs(w, "cuda")
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+
+
+# ----------------------------------------------------------- full sizes ----
+
+@pytest.mark.parametrize("name", ["mha_32k", "gqa_128k", "two_level_256k"])
+def test_full_size_sampled(name):
+    """The full configuration in the launch configuration the benchmark times; the
+    first and last sequences are checked against the oracle in full."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w, "cuda")
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec, seqs=[0, w.batch - 1])
+    # workload sanity: planted blocks are found (the query points at them)
+    if w.planted_per_unit and not w.two_level:
+        ids = as_np(dec.sel_ids).reshape(w.units, -1)
+        cnt = as_np(dec.sel_count).reshape(-1)
+        planted = as_np(inp["planted"]).reshape(w.units, -1)
+        hit = np.mean([np.isin(planted[u], ids[u, : cnt[u]]).mean() for u in range(w.units)])
+        assert hit > 0.95, f"planted-block recall {hit:.3f}"
+    del inp
+    torch.cuda.empty_cache()
