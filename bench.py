@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import dataclasses
 import hashlib
 import json
 import math
@@ -226,6 +227,8 @@ def run_gpu_arm(args):
     Bn.lib()
 
     w = WORKLOADS[args.workload]
+    if args.batch:
+        w = dataclasses.replace(w, batch=args.batch)
     inp = make_inputs(w, dev)
     p = Bn.params_for(w)
     dec = SparseDecoder(p, dev)
@@ -505,6 +508,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
