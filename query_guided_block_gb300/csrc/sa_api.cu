@@ -89,6 +89,19 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? SPARSE_ATTN_OK : SPARSE
 
 }  // namespace
 
+int num_sms()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 WorkspaceLayout workspace_layout(const Geometry& g)
 {
     WorkspaceLayout L{};
@@ -106,7 +119,13 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     const size_t heads = size_t(g.B) * g.Hq;
 
     size_t off = 0;
-    L.err = off;              off = align256(off + sizeof(uint32_t));
+    // one 256-byte header: error word and the persistent kernels' work counters
+    L.err = 0;
+    L.sel_work = 4;
+    L.sel_done = 8;
+    L.dec_work = 12;
+    L.dec_done = 16;
+    off = 256;
     L.sel_counters = off;     off = align256(off + units * sizeof(uint32_t));
     L.dec_counters = off;     off = align256(off + units * sizeof(uint32_t));
     L.l1_counters = off;      off = align256(off + units * sizeof(uint32_t));

@@ -30,6 +30,10 @@ struct Geometry {
 // Workspace carve-up (byte offsets from the workspace base, each 256-byte aligned).
 struct WorkspaceLayout {
     size_t err;            // uint32 error word
+    size_t sel_work;       // uint32 next chunk id (select kernels)
+    size_t sel_done;       // uint32 finished CTAs (select kernels)
+    size_t dec_work;       // uint32 next work item (decode)
+    size_t dec_done;       // uint32 finished CTAs (decode)
     size_t sel_counters;   // uint32 [units]
     size_t dec_counters;   // uint32 [units]
     size_t l1_counters;    // uint32 [units] (two-level, level 1)
@@ -46,6 +50,10 @@ struct WorkspaceLayout {
 };
 
 WorkspaceLayout workspace_layout(const Geometry& g);
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
+constexpr int kSmemPerSm = 228 * 1024;
 
 // Tokens one decode CTA stages (K and V tiles of this many tokens fit in 64 KB).
 int decode_tokens_per_split(int D, bool kv_bf16);

@@ -15,14 +15,14 @@
 // Selection (SparDA page §3.2 fixed top-k; HiSparse->QSA §2.2 window level): the k
 // largest scores by (score desc, block id asc), plus the window blocks, ascending.
 //
-// Work split: the candidates of a unit are cut into `splits` slices, one CTA each.  A
-// half-warp (D = 128, bf16) covers one metadata row with 16-byte loads; four rows per
-// half-warp are in flight.  Scores go to an L2-resident workspace row.  The CTA that
-// completes a unit last (device-scope counter, no waiting) runs a radix select over
-// the unit's order-preserving uint32 keys in shared memory: four 8-bit digit passes
-// with warp-aggregated shared-memory histograms, early exit once a digit bin holds
-// exactly the remaining count, then a stable tie rule (lower id first) and an ordered
-// compaction by warp ballots.
+// Work split: a persistent grid streams chunks of metadata rows through a multi-stage
+// bulk-copy pipeline (see the kernel below); a half-warp (D = 128, bf16) scores one
+// row from shared memory.  Scores go to an L2-resident workspace row.  The CTA that
+// scores a unit's last chunk (device-scope counter, no waiting) runs a radix select
+// over the unit's order-preserving uint32 keys in shared memory: four 8-bit digit
+// passes with warp-aggregated shared-memory histograms, early exit once a digit bin
+// holds exactly the remaining count, then a stable tie rule (lower id first) and an
+// ordered compaction by warp ballots.
 #include "sa_common.cuh"
 #include "sa_internal.h"
 
@@ -31,8 +31,9 @@ namespace {
 
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kScoreUnroll = 4;
-constexpr int kMaxSelectKeys = 16384;   // candidates per unit held in shared memory
+constexpr int kStages = 4;                // chunks in flight per CTA
+constexpr int kStageBytes = 16 * 1024;    // metadata bytes per chunk
+constexpr int kMaxSelectKeys = 16384;     // candidates per unit held in shared memory
 
 enum { KIND_QUEST = 0, KIND_MEAN = 1 };
 
@@ -52,9 +53,9 @@ struct SelectArgs {
     int surv_stride;
     int per_coarse;          // rows per coarse block
     int row_limit;           // rows >= row_limit are not candidates (window / past end)
-    int n_cand;
-    int cand_per_cta;
-    int splits;
+    int n_cand;              // candidate slots per unit = groups * group_rows
+    int groups, group_rows;  // candidate slots come in groups of contiguous rows
+    int chunks_per_group, chunks_per_unit, total_chunks;
     // selection
     int k;
     int win_first, win_count;
@@ -63,7 +64,9 @@ struct SelectArgs {
     int32_t* out_count;
     // workspace
     float* scores;           // [units, n_cand]
-    uint32_t* counters;      // [units]
+    uint32_t* counters;      // [units] scored slots
+    uint32_t* work;          // next chunk id
+    uint32_t* done;          // CTAs finished
     uint32_t* err;
 };
 
@@ -71,7 +74,7 @@ struct SelectArgs {
 __device__ __forceinline__ int candidate_row(const SelectArgs& a, int u, int c)
 {
     if (c >= a.n_cand) return -1;
-    if (!a.via_survivors) return c;
+    if (!a.via_survivors) return c < a.row_limit ? c : -1;
     const int i = c / a.per_coarse;
     if (i >= a.n_surv[u]) return -1;
     const int row = a.surv[size_t(u) * a.surv_stride + i] * a.per_coarse + (c - i * a.per_coarse);
@@ -207,129 +210,211 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
 }
 
 // ------------------------------------------------------------- kernel ---
+// Persistent streaming kernel.  The candidates of every unit are cut into chunks of
+// contiguous metadata rows (<= kStageBytes per chunk); CTAs take chunk ids from a
+// device-wide counter in unit-major order, so units complete one after another and a
+// unit's top-k overlaps the streaming of later units.  Thread 0 keeps kStages chunks
+// in flight with 1-D bulk async copies (complete_tx on one mbarrier per stage); all
+// threads score from shared memory.  A per-unit counter of scored candidate slots
+// (release / acquire) tells the CTA that finishes a unit to run its top-k.
 template <int KIND, bool MBF16, int D>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
+struct SelectShape {
+    static constexpr int ESZ = (KIND == KIND_QUEST && MBF16) ? 2 : 4;
+    static constexpr int EPL = 16 / ESZ;
+    static constexpr int LPR = D / EPL;
+    static constexpr int RPW = 32 / LPR;
+    static constexpr int ROW_BYTES = D * ESZ;
+    static constexpr int ARRAYS = KIND == KIND_QUEST ? 2 : 1;
+    static constexpr int ROWS = kStageBytes / (ARRAYS * ROW_BYTES);   // rows per chunk
+    static constexpr int ROWS_PER_PASS = kSelWarps * RPW;
+    static_assert(ROWS % ROWS_PER_PASS == 0, "chunk rows must split over the warps");
+};
+
+struct ChunkInfo {
+    int u, cand0, row0, nrows, nslots;
+};
+
+__device__ __forceinline__ ChunkInfo chunk_info(const SelectArgs& a, int cid, int rows_per_chunk)
 {
-    extern __shared__ uint32_t keys[];
-    __shared__ bool s_last;
-
-    constexpr int ESZ = (KIND == KIND_QUEST && MBF16) ? 2 : 4;
-    constexpr int EPL = 16 / ESZ;
-    constexpr int LPR = D / EPL;
-    constexpr int RPW = 32 / LPR;
-    constexpr int ROWS_PER_PASS = kSelWarps * RPW;
-
-    const int u = blockIdx.x / a.splits;
-    const int split = blockIdx.x - u * a.splits;
-    const int b = u / a.Hkv, kvh = u - b * a.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sub = lane % LPR, rsub = lane / LPR;
-    const int d0 = sub * EPL;
-
-    // query coefficients for this lane's channels
-    float cp[EPL], cn[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) { cp[e] = 0.f; cn[e] = 0.f; }
-    for (int g = 0; g < a.G; ++g) {
-        const size_t qrow = (size_t(b) * a.Hq + size_t(kvh) * a.G + g) * D + d0;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const float x = load_q(a.q, qrow + e, a.q_bf16 != 0);
-            if constexpr (KIND == KIND_QUEST) {
-                cp[e] += fmaxf(x, 0.f);
-                cn[e] += fminf(x, 0.f);
-            } else {
-                cp[e] += x;
-            }
+    ChunkInfo c;
+    c.u = cid / a.chunks_per_unit;
+    const int rem = cid - c.u * a.chunks_per_unit;
+    const int grp = rem / a.chunks_per_group;
+    const int slot0 = (rem - grp * a.chunks_per_group) * rows_per_chunk;
+    c.nslots = min(rows_per_chunk, a.group_rows - slot0);
+    c.cand0 = grp * a.group_rows + slot0;
+    if (a.via_survivors) {
+        if (grp >= a.n_surv[c.u]) {
+            c.row0 = 0;
+            c.nrows = 0;
+            return c;
         }
-    }
-
-    // score this CTA's candidates
-    const int cbeg = split * a.cand_per_cta;
-    const int cend = min(a.n_cand, cbeg + a.cand_per_cta);
-    float* srow = a.scores + size_t(u) * a.n_cand;
-    const char* hi_base;
-    const char* lo_base;
-    if constexpr (KIND == KIND_QUEST) {
-        hi_base = reinterpret_cast<const char*>(a.kmax) + size_t(u) * a.rows * D * ESZ + d0 * ESZ;
-        lo_base = reinterpret_cast<const char*>(a.kmin) + size_t(u) * a.rows * D * ESZ + d0 * ESZ;
+        c.row0 = a.surv[size_t(c.u) * a.surv_stride + grp] * a.per_coarse + slot0;
     } else {
-        hi_base = reinterpret_cast<const char*>(a.kmean) + size_t(u) * a.rows * D * 4 + d0 * 4;
-        lo_base = hi_base;
+        c.row0 = slot0;
     }
-    for (int base = cbeg + warp * RPW; base < cend; base += ROWS_PER_PASS * kScoreUnroll) {
-        uint4 vh[kScoreUnroll], vl[kScoreUnroll];
-        int row[kScoreUnroll];
-#pragma unroll
-        for (int i = 0; i < kScoreUnroll; ++i) {
-            const int c = base + i * ROWS_PER_PASS + rsub;
-            row[i] = c < cend ? candidate_row(a, u, c) : -1;
-            if (row[i] >= 0) {
-                vh[i] = ld_stream16(hi_base + size_t(row[i]) * D * ESZ);
-                if constexpr (KIND == KIND_QUEST) vl[i] = ld_stream16(lo_base + size_t(row[i]) * D * ESZ);
-            } else {
-                vh[i] = make_uint4(0, 0, 0, 0);
-                vl[i] = make_uint4(0, 0, 0, 0);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kScoreUnroll; ++i) {
-            float fh[EPL], s = 0.f;
-            unpack16<ESZ == 2>(vh[i], fh);
-            if constexpr (KIND == KIND_QUEST) {
-                float fl[EPL];
-                unpack16<ESZ == 2>(vl[i], fl);
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) s = fmaf(cp[e], fh[e], fmaf(cn[e], fl[e], s));
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) s = fmaf(cp[e], fh[e], s);
-            }
-#pragma unroll
-            for (int m = LPR / 2; m >= 1; m >>= 1) s += __shfl_xor_sync(kFullMask, s, m);
-            const int c = base + i * ROWS_PER_PASS + rsub;
-            if (sub == 0 && c < cend) srow[c] = row[i] >= 0 ? s : -INFINITY;
-        }
-    }
+    c.nrows = max(0, min(c.nslots, a.row_limit - c.row0));
+    return c;
+}
 
-    // the last CTA of this unit selects
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t done = atomicAdd(&a.counters[u], 1u);
-        s_last = (done == uint32_t(a.splits - 1));
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (tid == 0) a.counters[u] = 0u;   // every split of this launch has arrived
-
-    int n_valid = 0;
-    for (int base = 0; base < a.n_cand; base += kSelThreads) {
-        const int c = base + tid;
-        bool valid = false;
-        if (c < a.n_cand) {
-            valid = candidate_row(a, u, c) >= 0;
-            keys[c] = valid ? order_key(__ldcg(srow + c)) : 0u;
-        }
-        n_valid += __syncthreads_count(valid);
-    }
-    topk_and_emit(a, u, keys, a.n_cand, n_valid);
+__device__ __forceinline__ int grab_chunk(const SelectArgs& a)
+{
+    const int id = int(atomicAdd(a.work, 1u));
+    return id < a.total_chunks ? id : -1;
 }
 
 template <int KIND, bool MBF16, int D>
-cudaError_t launch_select_t(const SelectArgs& a, int units, cudaStream_t s)
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
 {
-    const size_t smem = size_t(a.n_cand) * sizeof(uint32_t);
+    using SS = SelectShape<KIND, MBF16, D>;
+    constexpr int EPL = SS::EPL, LPR = SS::LPR, RPW = SS::RPW, ROWS = SS::ROWS;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);
+    __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ int s_chunk[kStages];
+    __shared__ int s_topk_unit;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sub = lane % LPR, rsub = lane / LPR;
+    const int d0 = sub * EPL;
+    const char* hi_src = reinterpret_cast<const char*>(KIND == KIND_QUEST ? a.kmax : (const void*)a.kmean);
+    const char* lo_src = reinterpret_cast<const char*>(a.kmin);
+
+    auto issue = [&](int s, int cid) {   // thread 0 only
+        s_chunk[s] = cid;
+        uint32_t bytes = 0;
+        ChunkInfo c{};
+        if (cid >= 0) {
+            c = chunk_info(a, cid, ROWS);
+            bytes = uint32_t(c.nrows) * SS::ROW_BYTES;
+        }
+        mbar_arrive_expect_tx(&full[s], bytes * SS::ARRAYS);
+        if (bytes) {
+            const size_t off = (size_t(c.u) * a.rows + c.row0) * SS::ROW_BYTES;
+            unsigned char* dst = smem + s * kStageBytes;
+            bulk_copy_g2s(dst, hi_src + off, bytes, &full[s]);
+            if constexpr (KIND == KIND_QUEST)
+                bulk_copy_g2s(dst + ROWS * SS::ROW_BYTES, lo_src + off, bytes, &full[s]);
+        }
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+        for (int s = 0; s < kStages; ++s) issue(s, grab_chunk(a));
+    }
+    __syncthreads();
+
+    int cur_u = -1;
+    float cp[EPL], cn[EPL];
+    for (int it = 0;; ++it) {
+        const int s = it % kStages;
+        const uint32_t parity = uint32_t(it / kStages) & 1u;
+        const int cid = s_chunk[s];
+        if (cid < 0) break;
+        const ChunkInfo c = chunk_info(a, cid, ROWS);
+        if (c.u != cur_u) {   // query coefficients of this unit (uniform across the CTA)
+            cur_u = c.u;
+            const int b = c.u / a.Hkv, kvh = c.u - (c.u / a.Hkv) * a.Hkv;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) { cp[e] = 0.f; cn[e] = 0.f; }
+            for (int g = 0; g < a.G; ++g) {
+                const size_t qrow = (size_t(b) * a.Hq + size_t(kvh) * a.G + g) * D + d0;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    const float x = load_q(a.q, qrow + e, a.q_bf16 != 0);
+                    if constexpr (KIND == KIND_QUEST) {
+                        cp[e] += fmaxf(x, 0.f);
+                        cn[e] += fminf(x, 0.f);
+                    } else {
+                        cp[e] += x;
+                    }
+                }
+            }
+        }
+        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+
+        const unsigned char* hi = smem + s * kStageBytes + d0 * SS::ESZ;
+        const unsigned char* lo = hi + ROWS * SS::ROW_BYTES;
+        float* srow = a.scores + size_t(c.u) * a.n_cand + c.cand0;
+#pragma unroll
+        for (int pass = 0; pass < ROWS / SS::ROWS_PER_PASS; ++pass) {
+            const int r = pass * SS::ROWS_PER_PASS + warp * RPW + rsub;
+            float fh[EPL], sc = 0.f;
+            unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(hi + r * SS::ROW_BYTES), fh);
+            if constexpr (KIND == KIND_QUEST) {
+                float fl[EPL];
+                unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(lo + r * SS::ROW_BYTES), fl);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) sc = fmaf(cp[e], fh[e], fmaf(cn[e], fl[e], sc));
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) sc = fmaf(cp[e], fh[e], sc);
+            }
+#pragma unroll
+            for (int m = LPR / 2; m >= 1; m >>= 1) sc += __shfl_xor_sync(kFullMask, sc, m);
+            if (sub == 0 && r < c.nrows) srow[r] = sc;
+        }
+        __syncthreads();   // stage s fully read; this chunk's scores written
+        if (tid == 0) {
+            issue(s, grab_chunk(a));
+            __threadfence();
+            const uint32_t before = atomicAdd(&a.counters[c.u], uint32_t(c.nslots));
+            s_topk_unit = (before + uint32_t(c.nslots) == uint32_t(a.n_cand)) ? c.u : -1;
+        }
+        __syncthreads();
+        const int tu = s_topk_unit;
+        if (tu >= 0) {
+            __threadfence();
+            if (tid == 0) a.counters[tu] = 0u;   // every slot of this unit is scored
+            const float* row = a.scores + size_t(tu) * a.n_cand;
+            int n_valid = 0;
+            for (int base = 0; base < a.n_cand; base += kSelThreads) {
+                const int cc = base + tid;
+                bool valid = false;
+                if (cc < a.n_cand) {
+                    valid = candidate_row(a, tu, cc) >= 0;
+                    keys[cc] = valid ? order_key(__ldcg(row + cc)) : 0u;
+                }
+                n_valid += __syncthreads_count(valid);
+            }
+            topk_and_emit(a, tu, keys, a.n_cand, n_valid);
+            __syncthreads();
+        }
+    }
+
+    // the last CTA out resets the work counters for the next launch
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(a.done, 1u) == gridDim.x - 1) {
+            *a.work = 0u;
+            *a.done = 0u;
+        }
+    }
+}
+
+template <int KIND, bool MBF16, int D>
+cudaError_t launch_select_t(const SelectArgs& a0, int units, cudaStream_t s)
+{
+    using SS = SelectShape<KIND, MBF16, D>;
+    SelectArgs a = a0;
+    a.chunks_per_group = (a.group_rows + SS::ROWS - 1) / SS::ROWS;
+    a.chunks_per_unit = a.groups * a.chunks_per_group;
+    a.total_chunks = units * a.chunks_per_unit;
+    const size_t smem = size_t(kStages) * kStageBytes + size_t(a.n_cand) * sizeof(uint32_t);
     static bool configured = false;   // once per instantiation, before any graph capture
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(select_kernel<KIND, MBF16, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(kMaxSelectKeys * sizeof(uint32_t)));
+                                             int(kStages * kStageBytes + kMaxSelectKeys * sizeof(uint32_t)));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    select_kernel<KIND, MBF16, D><<<dim3(unsigned(units * a.splits)), kSelThreads, smem, s>>>(a);
+    const int per_sm = smem + 4096 <= (kSmemPerSm / 2) ? 2 : 1;
+    int ctas = num_sms() * per_sm;
+    if (ctas > a.total_chunks) ctas = a.total_chunks > 0 ? a.total_chunks : 1;
+    select_kernel<KIND, MBF16, D><<<dim3(unsigned(ctas)), kSelThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -348,20 +433,6 @@ cudaError_t dispatch_select(const SelectArgs& a, int kind, bool mbf16, int D, in
                  : launch_select_t<KIND_QUEST, false, 64>(a, units, s);
 }
 
-// Candidates per CTA: enough CTAs to cover the GPU several times over, each streaming
-// between 16 KB and 256 KB of metadata.
-int pick_cand_per_cta(long long units, int n_cand, int row_bytes)
-{
-    const long long total = units * (long long)n_cand * row_bytes;
-    long long target = total / (4 * 152);
-    if (target < 16 * 1024) target = 16 * 1024;
-    if (target > 256 * 1024) target = 256 * 1024;
-    long long per = target / row_bytes;
-    if (per < 32) per = 32;
-    if (per > n_cand) per = n_cand;
-    return int(per > 0 ? per : 1);
-}
-
 }  // namespace
 
 cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
@@ -370,9 +441,6 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
 {
     const int units = g.units();
     if (units == 0) return cudaSuccess;
-    uint32_t* err = reinterpret_cast<uint32_t*>(ws + L.err);
-    const int meta_esz = g.kv_bf16 ? 2 : 4;
-
     SelectArgs a{};
     a.q = q;
     a.q_bf16 = g.q_bf16;
@@ -382,33 +450,30 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.Hkv = g.Hkv;
     a.G = g.G;
     a.Hq = g.Hq;
-    a.err = err;
+    a.err = reinterpret_cast<uint32_t*>(ws + L.err);
     a.scores = reinterpret_cast<float*>(ws + L.scores);
+    a.work = reinterpret_cast<uint32_t*>(ws + L.sel_work);
+    a.done = reinterpret_cast<uint32_t*>(ws + L.sel_done);
+    a.counters = reinterpret_cast<uint32_t*>(ws + L.sel_counters);
 
     if (!g.two_level) {
         a.rows = g.nb;
         a.via_survivors = 0;
         a.row_limit = g.win_first;
         a.n_cand = g.n_cand;
+        a.groups = 1;
+        a.group_rows = g.n_cand;
         a.k = g.topk;
         a.win_first = g.win_first;
         a.win_count = g.win_count;
         a.out_ids = sel_ids;
         a.out_stride = g.sel_stride;
         a.out_count = sel_count;
-        a.counters = reinterpret_cast<uint32_t*>(ws + L.sel_counters);
-        if (g.score_kind == SPARSE_ATTN_SCORE_MEAN) {
-            a.kmean = kmean;
-            a.cand_per_cta = pick_cand_per_cta(units, a.n_cand, g.D * 4);
-        } else {
-            a.cand_per_cta = pick_cand_per_cta(units, a.n_cand, 2 * g.D * meta_esz);
-        }
         if (a.n_cand == 0) {
-            // no candidates: a single pass that only emits the window
-            a.cand_per_cta = 1;
-            a.splits = 1;
-        } else {
-            a.splits = (a.n_cand + a.cand_per_cta - 1) / a.cand_per_cta;
+            // no candidates: one slot-free pass that only emits the window
+            a.group_rows = 1;
+            a.n_cand = 1;
+            a.row_limit = 0;
         }
         const int kind = g.score_kind == SPARSE_ATTN_SCORE_MEAN ? KIND_MEAN : KIND_QUEST;
         return dispatch_select(a, kind, g.kv_bf16, g.D, units, s);
@@ -422,6 +487,8 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     l1.via_survivors = 0;
     l1.row_limit = g.n_coarse;
     l1.n_cand = g.n_coarse;
+    l1.groups = 1;
+    l1.group_rows = g.n_coarse;
     l1.k = g.topk_coarse;
     l1.win_first = 0;
     l1.win_count = 0;
@@ -429,9 +496,7 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     l1.out_stride = g.topk_coarse > 0 ? g.topk_coarse : 1;
     l1.out_count = n_surv;
     l1.counters = reinterpret_cast<uint32_t*>(ws + L.l1_counters);
-    l1.cand_per_cta = pick_cand_per_cta(units, l1.n_cand, g.D * 4);
-    if (l1.n_cand == 0) { l1.cand_per_cta = 1; l1.splits = 1; }
-    else l1.splits = (l1.n_cand + l1.cand_per_cta - 1) / l1.cand_per_cta;
+    if (l1.n_cand == 0) { l1.n_cand = 1; l1.group_rows = 1; l1.row_limit = 0; }
     cudaError_t e = dispatch_select(l1, KIND_MEAN, false, g.D, units, s);
     if (e != cudaSuccess) return e;
 
@@ -444,6 +509,8 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     l2.surv_stride = l1.out_stride;
     l2.per_coarse = g.per_coarse;
     l2.row_limit = g.win_first;
+    l2.groups = g.topk_coarse;
+    l2.group_rows = g.per_coarse;
     l2.n_cand = g.topk_coarse * g.per_coarse;
     l2.k = g.topk;
     l2.win_first = g.win_first;
@@ -451,10 +518,9 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     l2.out_ids = sel_ids;
     l2.out_stride = g.sel_stride;
     l2.out_count = sel_count;
-    l2.counters = reinterpret_cast<uint32_t*>(ws + L.sel_counters);
-    l2.cand_per_cta = pick_cand_per_cta(units, l2.n_cand, 2 * g.D * meta_esz);
-    if (l2.n_cand == 0) { l2.cand_per_cta = 1; l2.splits = 1; }
-    else l2.splits = (l2.n_cand + l2.cand_per_cta - 1) / l2.cand_per_cta;
+    if (l2.n_cand == 0) {
+        l2.groups = 1; l2.group_rows = 1; l2.n_cand = 1; l2.row_limit = 0; l2.via_survivors = 0;
+    }
     return dispatch_select(l2, KIND_QUEST, g.kv_bf16, g.D, units, s);
 }
 
