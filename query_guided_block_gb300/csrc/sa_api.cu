@@ -38,7 +38,7 @@ int make_geometry(const sparse_attn_params* p, Geometry* g)
     const int bs = p->block_size;
     if (bs != 8 && bs != 16 && bs != 32 && bs != 64 && bs != 128) return SPARSE_ATTN_UNSUPPORTED;
     const bool kv_bf16 = p->kv_dtype == SPARSE_ATTN_BF16;
-    if (bs > decode_tokens_per_split(p->head_dim, kv_bf16)) return SPARSE_ATTN_UNSUPPORTED;
+    if (!decode_supported(p->head_dim, kv_bf16, bs, G)) return SPARSE_ATTN_UNSUPPORTED;
 
     g->B = p->batch;
     g->Hq = p->num_q_heads;
@@ -112,8 +112,7 @@ WorkspaceLayout workspace_layout(const Geometry& g)
         if (g.topk_coarse * g.per_coarse > cols) cols = g.topk_coarse * g.per_coarse;
     }
     L.score_cols = cols > 0 ? cols : 1;
-    const int tps = decode_tokens_per_split(g.D, g.kv_bf16);
-    L.blocks_per_split = tps / g.bs;
+    L.blocks_per_split = decode_blocks_per_item(g.D, g.kv_bf16, g.bs);
     L.max_splits = (g.sel_stride + L.blocks_per_split - 1) / L.blocks_per_split;
     if (L.max_splits < 1) L.max_splits = 1;
     const size_t heads = size_t(g.B) * g.Hq;

@@ -6,20 +6,27 @@
 // gathering them into a temporary buffer first.  The softmax is exact over the union of
 // the selected tokens (SGLang page §1.2 "select-then-compute").
 //
-// Design (one CTA = one split of one (sequence, KV head) unit, all G query heads):
-//   1. read this split's slice of sel_ids, map block -> page through block_table;
-//   2. one thread issues 1-D bulk async copies (cp.async.bulk) of each selected
-//      (page, KV head) K tile and V tile -- each tile is block_size x D contiguous -- into
-//      shared memory, completing on two mbarriers (K first, so QK^T overlaps the V copy);
-//   3. QK^T in fp32: a key row is covered by LPR lanes with one 16-byte shared load each;
-//      per-row partial dots of all G heads are summed across the row's lanes with the
-//      transposed halving reduction;
-//   4. per-head max / exp2 / sum for the split (scores pre-scaled by scale*log2 e);
-//   5. PV in fp32: lanes own D-slices, warps own tokens, reduced through shared memory;
-//   6. write the split's (m, l, o) partial; the CTA finishing a unit last merges the
-//      unit's partials (log-sum-exp) and writes fp32 outputs.  No CTA waits on another.
-// GQA tiles are G x tokens: far too narrow for a tensor-core tile to pay (>= 64 rows), and
-// the kernel is HBM-bound at ~2 FMA per byte, so the contraction stays on FMA units.
+// Design: a persistent grid streams "items" (a few selected blocks, ~64 tokens, of one
+// (sequence, KV head) unit) through a kStages-deep shared-memory pipeline.
+//   * Items are numbered unit-major; CTA i owns an equal contiguous range, so it sees
+//     one or two unit boundaries and no CTA ever waits on another.
+//   * At start the CTA resolves, for its whole range, selected id -> page through the
+//     page table into shared memory (bounds-checked), so the producer thread issues
+//     copies without touching global memory.
+//   * Thread 0 keeps kStages items in flight: per item, 1-D bulk async copies
+//     (cp.async.bulk) of each (page, KV head) K tile and V tile -- block_size x D
+//     contiguous -- complete on the stage's `full` mbarrier; warps release the stage on
+//     its `empty` mbarrier.
+//   * QK^T in fp32: a key row is covered by LPR lanes with one 16-byte shared load
+//     each; the G heads' partial dots are summed across the row's lanes with the
+//     transposed halving reduction.  Per head, warps keep the running max / sum of an
+//     online softmax (exp2, scores pre-scaled by scale * log2 e); PV accumulates in
+//     registers, rescaled when the max moves.
+//   * At the end of its segment of a unit, the CTA reduces its accumulators across
+//     warps and writes one (m, l, o) partial; the CTA that completes a unit's item
+//     count merges the unit's partials (log-sum-exp) into fp32 outputs.
+// GQA tiles are G x tokens: far too narrow for a tensor-core tile to pay (>= 64 rows),
+// and the kernel is HBM-bound at ~2 FMA per byte, so the contraction stays on FMA units.
 #include "sa_common.cuh"
 #include "sa_internal.h"
 
@@ -28,8 +35,9 @@ namespace {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kStageBytes = 64 * 1024;   // K + V tiles staged per CTA
-constexpr int kMaxBlocksPerSplit = 32;   // 256 tokens / 8-token blocks
+constexpr int kItemKBytes = 16 * 1024;     // K bytes per item (V the same)
+constexpr int kMaxRangeBlocks = 1024;      // page lookups a CTA caches in shared memory
+constexpr int kDecSmemLimit = 200 * 1024;  // dynamic shared memory a decode CTA may use
 
 struct DecodeArgs {
     const void* q;
@@ -41,80 +49,90 @@ struct DecodeArgs {
     const int32_t* sel_count;
     float* out;
     int Hq, Hkv, nb, bs, N, num_pages, sel_stride;
-    int blocks_per_split, max_splits;
+    int blocks_per_item, items_per_unit, total_items, units;
+    int stages;
     float scale_log2;
-    float* part_m;   // [B*Hq, max_splits]
+    float* part_m;   // [B*Hq, items_per_unit]
     float* part_l;
-    float* part_o;   // [B*Hq, max_splits, D]
+    float* part_o;   // [B*Hq, items_per_unit, D]
     uint32_t* counters;
     uint32_t* err;
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, int G>
 struct DecodeShape {
     static constexpr int ESZ = BF16 ? 2 : 4;
     static constexpr int EPL = 16 / ESZ;
     static constexpr int LPR = D / EPL;
     static constexpr int RPW = 32 / LPR;
-    static constexpr int TPS = kStageBytes / (2 * D * ESZ);   // tokens per split
     static constexpr int ROW_BYTES = D * ESZ;
+    static constexpr int ITEM_TOKENS = kItemKBytes / ROW_BYTES;       // at block_size <= this
+    static constexpr int R0 = 16 / G;
+    static constexpr int R1 = ITEM_TOKENS / (kDecWarps * RPW);
+    static constexpr int R = R0 < R1 ? R0 : R1;                      // rows per lane group
+    static constexpr int V = R * G;                                  // partial dots per lane
+    static constexpr int ROWS_PER_BATCH = kDecWarps * RPW * R;
+    static_assert(ITEM_TOKENS % ROWS_PER_BATCH == 0, "item must split evenly over the warps");
+    // the cross-warp reduction at a segment end reuses the item's stage buffer
+    static_assert(kDecWarps * G * D * 4 <= 2 * ITEM_TOKENS * ROW_BYTES, "reduction must fit a stage");
 };
+
+size_t decode_fixed_smem(int G, int item_tokens)
+{
+    return size_t(2) * G * item_tokens * sizeof(float) + size_t(2) * kMaxRangeBlocks * sizeof(int);
+}
 
 template <int D, bool BF16, int G>
 __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
 {
-    using S = DecodeShape<D, BF16>;
-    constexpr int EPL = S::EPL, LPR = S::LPR, RPW = S::RPW, TPS = S::TPS;
-    constexpr int R = (16 / G) < (TPS / (kDecWarps * RPW)) ? (16 / G) : (TPS / (kDecWarps * RPW));
-    constexpr int V = R * G;                        // partial dots per lane per batch
-    constexpr int ROWS_PER_BATCH = kDecWarps * RPW * R;
-    static_assert(TPS % ROWS_PER_BATCH == 0, "token tile must split evenly");
-    static_assert(8 * G * D * 4 <= TPS * S::ROW_BYTES, "reduction buffer must fit the K region");
-
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char* k_s = smem;
-    unsigned char* v_s = smem + TPS * S::ROW_BYTES;
-    float* s_s = reinterpret_cast<float*>(v_s + TPS * S::ROW_BYTES);   // [G][TPS]
-    float* p_s = s_s + G * TPS;                                       // [TPS][G]
-    __shared__ __align__(8) uint64_t bar_k, bar_v;
-    __shared__ int blk_page[kMaxBlocksPerSplit];
-    __shared__ int blk_valid[kMaxBlocksPerSplit];     // valid tokens per staged block
-    __shared__ int s_nblk, s_count;
-    __shared__ float s_m[G], s_l[G];
-    __shared__ bool s_last;
+    using S = DecodeShape<D, BF16, G>;
+    constexpr int EPL = S::EPL, LPR = S::LPR, RPW = S::RPW, R = S::R, V = S::V;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int splits = a.max_splits;
-    const int u = blockIdx.x / splits;
-    const int split = blockIdx.x - u * splits;
-    const int b = u / a.Hkv, kvh = u - b * a.Hkv;
-    const int bps = a.blocks_per_split;
+    const int sub = lane % LPR, rsub = lane / LPR;
+    const int bpi = a.blocks_per_item;
+    const int item_tokens = bpi * a.bs;
+    const uint32_t tile_bytes = uint32_t(a.bs) * S::ROW_BYTES;
+    const size_t stage_bytes = size_t(2) * item_tokens * S::ROW_BYTES;
 
-    // ---- 1. this split's blocks ---------------------------------------
-    if (tid == 0) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* s_s = reinterpret_cast<float*>(smem + a.stages * stage_bytes);   // [G][item_tokens]
+    float* p_s = s_s + G * item_tokens;                                     // [item_tokens][G]
+    int* blk_page = reinterpret_cast<int*>(p_s + G * item_tokens);          // [range blocks]
+    int* blk_valid = blk_page + kMaxRangeBlocks;
+    __shared__ __align__(8) uint64_t full[4], empty[4];
+    __shared__ float s_alpha[G], s_m[G], s_l[G];
+    __shared__ int s_counts[64];
+    __shared__ int s_merge_unit;
+
+    const int i_begin = int((long long)a.total_items * blockIdx.x / gridDim.x);
+    const int i_end = int((long long)a.total_items * (blockIdx.x + 1) / gridDim.x);
+    if (i_begin >= i_end) return;
+    const int u_lo = i_begin / a.items_per_unit;
+    const int u_hi = (i_end - 1) / a.items_per_unit;
+
+    // ---- resolve the range: counts, selected ids -> pages ---------------------
+    for (int u = u_lo + tid; u <= u_hi; u += kDecThreads) {
         int count = a.sel_count[u];
         if (count < 0 || count > a.sel_stride) {
             raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
             count = count < 0 ? 0 : a.sel_stride;
         }
-        s_count = count;
-        const int first = split * bps;
-        int n = min(bps, count - first);
-        if (n < 0) n = 0;
-        s_nblk = n;
-        mbar_init(&bar_k, 1);
-        mbar_init(&bar_v, 1);
-        fence_mbar_init();
+        s_counts[u - u_lo] = count;
     }
     __syncthreads();
-    const int nblk = s_nblk;
-    if (tid < bps) {
+    const int n_range_blocks = (i_end - i_begin) * bpi;
+    for (int e = tid; e < n_range_blocks; e += kDecThreads) {
+        const int item = i_begin + e / bpi;
+        const int u = item / a.items_per_unit;
+        const int slot = (item - u * a.items_per_unit) * bpi + e % bpi;
         int page = -1, valid = 0;
-        if (tid < nblk) {
-            const int j = a.sel_ids[size_t(u) * a.sel_stride + split * bps + tid];
+        if (slot < s_counts[u - u_lo]) {
+            const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
             if (j < 0 || j >= a.nb) {
                 raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
             } else {
+                const int b = u / a.Hkv;
                 const int p = a.block_table[size_t(b) * a.nb + j];
                 if (p < 0 || p >= a.num_pages) {
                     raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
@@ -124,117 +142,141 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
                 }
             }
         }
-        blk_page[tid] = page;
-        blk_valid[tid] = valid;
+        blk_page[e] = page;
+        blk_valid[e] = valid;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kDecWarps);
+        }
+        fence_mbar_init();
     }
     __syncthreads();
 
-    if (nblk > 0) {
-        // ---- 2. stage K and V tiles --------------------------------------
-        const uint32_t tile_bytes = uint32_t(a.bs) * S::ROW_BYTES;
-        if (tid == 0) {
-            uint32_t nbytes = 0;
-            for (int i = 0; i < nblk; ++i) nbytes += blk_page[i] >= 0 ? tile_bytes : 0u;
-            const size_t head_off = size_t(kvh) * tile_bytes;
-            const size_t page_stride = size_t(a.Hkv) * tile_bytes;
-            mbar_arrive_expect_tx(&bar_k, nbytes);
-            for (int i = 0; i < nblk; ++i)
-                if (blk_page[i] >= 0)
-                    bulk_copy_g2s(k_s + size_t(i) * tile_bytes,
-                                  reinterpret_cast<const char*>(a.k_pages) + blk_page[i] * page_stride + head_off,
-                                  tile_bytes, &bar_k);
-            mbar_arrive_expect_tx(&bar_v, nbytes);
-            for (int i = 0; i < nblk; ++i)
-                if (blk_page[i] >= 0)
-                    bulk_copy_g2s(v_s + size_t(i) * tile_bytes,
-                                  reinterpret_cast<const char*>(a.v_pages) + blk_page[i] * page_stride + head_off,
-                                  tile_bytes, &bar_v);
+    const char* kbase = reinterpret_cast<const char*>(a.k_pages);
+    const char* vbase = reinterpret_cast<const char*>(a.v_pages);
+    auto issue = [&](int item) {   // thread 0 only
+        const int k = item - i_begin;
+        const int s = k % a.stages;
+        unsigned char* kd = smem + s * stage_bytes;
+        unsigned char* vd = kd + size_t(item_tokens) * S::ROW_BYTES;
+        const int u = item / a.items_per_unit;
+        const size_t head_off = size_t(u % a.Hkv) * tile_bytes;
+        const size_t page_stride = size_t(a.Hkv) * tile_bytes;
+        uint32_t nbytes = 0;
+        for (int i = 0; i < bpi; ++i) nbytes += blk_page[k * bpi + i] >= 0 ? tile_bytes : 0u;
+        mbar_arrive_expect_tx(&full[s], 2 * nbytes);
+        for (int i = 0; i < bpi; ++i) {
+            const int page = blk_page[k * bpi + i];
+            if (page < 0) continue;
+            bulk_copy_g2s(kd + size_t(i) * tile_bytes, kbase + page * page_stride + head_off, tile_bytes, &full[s]);
+            bulk_copy_g2s(vd + size_t(i) * tile_bytes, vbase + page * page_stride + head_off, tile_bytes, &full[s]);
         }
+    };
+    if (tid == 0)
+        for (int item = i_begin; item < i_end && item < i_begin + a.stages; ++item) issue(item);
 
-        // q for this lane's channels, pre-scaled into the log2 domain
-        const int sub = lane % LPR, rsub = lane / LPR;
-        float qr[G][EPL];
+    // running state of the current unit segment
+    float qr[G][EPL];
+    float acc[G][EPL];
+    float m_run = -INFINITY, l_run = 0.f;      // per head, kept by warp g (replicated in its lanes)
+    int cur_u = -1, seg_first = 0;
+
+    for (int item = i_begin; item < i_end; ++item) {
+        const int k = item - i_begin;
+        const int s = k % a.stages;
+        const uint32_t parity = uint32_t(k / a.stages) & 1u;
+        const int u = item / a.items_per_unit;
+        if (u != cur_u) {
+            cur_u = u;
+            seg_first = item;
+            const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const size_t qrow = (size_t(b) * a.Hq + size_t(kvh) * G + g) * D + sub * EPL;
+            for (int g = 0; g < G; ++g) {
+                const size_t qrow = (size_t(b) * a.Hq + size_t(kvh) * G + g) * D + sub * EPL;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) qr[g][e] = load_q(a.q, qrow + e, a.q_bf16 != 0) * a.scale_log2;
+                for (int e = 0; e < EPL; ++e) {
+                    qr[g][e] = load_q(a.q, qrow + e, a.q_bf16 != 0) * a.scale_log2;
+                    acc[g][e] = 0.f;
+                }
+            }
+            m_run = -INFINITY;
+            l_run = 0.f;
         }
+        const unsigned char* ks = smem + s * stage_bytes;
+        const unsigned char* vs = ks + size_t(item_tokens) * S::ROW_BYTES;
+        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
 
-        if (!mbar_wait_bounded(&bar_k, 0, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
-
-        // ---- 3. S = q K^T for the staged tokens ----------------------------
-        const int ntok = nblk * a.bs;
-        for (int t_base = 0; t_base < ntok; t_base += ROWS_PER_BATCH) {
+        // ---- S = q K^T over the item's tokens -------------------------------
+        for (int t_base = 0; t_base < item_tokens; t_base += S::ROWS_PER_BATCH) {
             const int t0 = t_base + ((warp * RPW) + rsub) * R;
             float v[V];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 float kf[EPL];
-                unpack16<BF16>(*reinterpret_cast<const uint4*>(k_s + size_t(t0 + r) * S::ROW_BYTES + sub * 16), kf);
+                unpack16<BF16>(*reinterpret_cast<const uint4*>(ks + size_t(t0 + r) * S::ROW_BYTES + sub * 16), kf);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    float acc = 0.f;
+                    float d = 0.f;
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc = fmaf(qr[g][e], kf[e], acc);
-                    v[r * G + g] = acc;
+                    for (int e = 0; e < EPL; ++e) d = fmaf(qr[g][e], kf[e], d);
+                    v[r * G + g] = d;
                 }
             }
             group_reduce_transposed<V, LPR>(v, lane);
-            if constexpr (V >= LPR) {
+            constexpr int OUT = V >= LPR ? V / LPR : 1;
+            constexpr int SPREAD = V >= LPR ? 1 : LPR / V;
+            if (sub % SPREAD == 0) {
 #pragma unroll
-                for (int i = 0; i < V / LPR; ++i) {
-                    const int idx = sub * (V / LPR) + i;
+                for (int i = 0; i < OUT; ++i) {
+                    const int idx = V >= LPR ? sub * (V / LPR) + i : sub / SPREAD;
                     const int r = idx / G, g = idx - (idx / G) * G;
                     const int t = t0 + r;
                     const int blk = t / a.bs;
-                    const bool ok = t < ntok && (t - blk * a.bs) < blk_valid[blk];
-                    s_s[g * TPS + t] = ok ? v[i] : -INFINITY;
-                }
-            } else {
-                if (sub % (LPR / V) == 0) {
-                    const int idx = sub / (LPR / V);
-                    const int r = idx / G, g = idx - (idx / G) * G;
-                    const int t = t0 + r;
-                    const int blk = t / a.bs;
-                    const bool ok = t < ntok && (t - blk * a.bs) < blk_valid[blk];
-                    s_s[g * TPS + t] = ok ? v[0] : -INFINITY;
+                    const bool ok = (t - blk * a.bs) < blk_valid[k * bpi + blk];
+                    s_s[g * item_tokens + t] = ok ? v[i] : -INFINITY;
                 }
             }
         }
         __syncthreads();
 
-        // ---- 4. per-head split softmax statistics ---------------------------
-        for (int g = warp; g < G; g += kDecWarps) {
-            float m = -INFINITY;
-            for (int t = lane; t < ntok; t += 32) m = fmaxf(m, s_s[g * TPS + t]);
+        // ---- online softmax statistics: warp g owns head g ---------------------
+        if (warp < G) {
+            const int g = warp;
+            float mi = -INFINITY;
+            for (int t = lane; t < item_tokens; t += 32) mi = fmaxf(mi, s_s[g * item_tokens + t]);
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
-            float l = 0.f;
-            for (int t = lane; t < ntok; t += 32) {
-                const float x = s_s[g * TPS + t];
-                const float p = (m == -INFINITY || x == -INFINITY) ? 0.f : fast_exp2(x - m);
+            for (int off = 16; off >= 1; off >>= 1) mi = fmaxf(mi, __shfl_xor_sync(kFullMask, mi, off));
+            const float m_new = fmaxf(m_run, mi);
+            const float alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+            float li = 0.f;
+            for (int t = lane; t < item_tokens; t += 32) {
+                const float x = s_s[g * item_tokens + t];
+                const float p = (x == -INFINITY) ? 0.f : fast_exp2(x - m_new);
                 p_s[t * G + g] = p;
-                l += p;
+                li += p;
             }
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(kFullMask, l, off);
-            if (lane == 0) { s_m[g] = m; s_l[g] = l; }
+            for (int off = 16; off >= 1; off >>= 1) li += __shfl_xor_sync(kFullMask, li, off);
+            l_run = l_run * alpha + li;
+            m_run = m_new;
+            if (lane == 0) s_alpha[g] = alpha;
         }
-        if (!mbar_wait_bounded(&bar_v, 0, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
         __syncthreads();
 
-        // ---- 5. O = P V ------------------------------------------------------
-        float acc[G][EPL];
+        // ---- O += P V ----------------------------------------------------------
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g) {
+            const float al = s_alpha[g];
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
-        for (int t = warp * RPW + rsub; t < ntok; t += kDecWarps * RPW) {
+            for (int e = 0; e < EPL; ++e) acc[g][e] *= al;
+        }
+        for (int t = warp * RPW + rsub; t < item_tokens; t += kDecWarps * RPW) {
             const int blk = t / a.bs;
-            if ((t - blk * a.bs) >= blk_valid[blk]) continue;
+            if ((t - blk * a.bs) >= blk_valid[k * bpi + blk]) continue;
             float vf[EPL];
-            unpack16<BF16>(*reinterpret_cast<const uint4*>(v_s + size_t(t) * S::ROW_BYTES + sub * 16), vf);
+            unpack16<BF16>(*reinterpret_cast<const uint4*>(vs + size_t(t) * S::ROW_BYTES + sub * 16), vf);
             float p[G];
             if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -251,98 +293,142 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(p[g], vf[e], acc[g][e]);
         }
+        const bool seg_end = item + 1 == i_end || (item + 1) / a.items_per_unit != u;
+        if (seg_end) {
+            // ---- end of this CTA's segment of unit u: one partial ---------------
 #pragma unroll
-        for (int m = LPR; m < 32; m <<= 1)
+            for (int m = LPR; m < 32; m <<= 1)
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+                for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[g][e] += __shfl_xor_sync(kFullMask, acc[g][e], m);
-        float* red = reinterpret_cast<float*>(k_s);   // K tiles are no longer needed
-        if (rsub == 0) {
+                    for (int e = 0; e < EPL; ++e) acc[g][e] += __shfl_xor_sync(kFullMask, acc[g][e], m);
+            __syncthreads();   // every warp is done with this stage: reduce through it
+            float* red = reinterpret_cast<float*>(smem + s * stage_bytes);   // [warps][G][D]
+            if (rsub == 0) {
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+                for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) red[(warp * G + g) * D + sub * EPL + e] = acc[g][e];
-        }
-        __syncthreads();
-
-        // ---- 6. split partial -------------------------------------------------
-        const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
-        for (int i = tid; i < G * D; i += kDecThreads) {
-            const int g = i / D, d = i - g * D;
-            float o = 0.f;
+                    for (int e = 0; e < EPL; ++e) red[(warp * G + g) * D + sub * EPL + e] = acc[g][e];
+            }
+            if (warp < G && lane == 0) { s_m[warp] = m_run; s_l[warp] = l_run; }
+            __syncthreads();
+            const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+            const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
+            const int slot = seg_first - u * a.items_per_unit;
+            const int ipu = a.items_per_unit;
+            for (int i = tid; i < G * D; i += kDecThreads) {
+                const int g = i / D, d = i - g * D;
+                float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) o += red[(w * G + g) * D + d];
-            a.part_o[((head0 + g) * splits + split) * D + d] = o;
-        }
-        if (tid < G) {
-            a.part_m[(head0 + tid) * splits + split] = s_m[tid];
-            a.part_l[(head0 + tid) * splits + split] = s_l[tid];
-        }
-    }
-
-    // ---- merge, by whichever CTA completes this unit last ----------------------
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&a.counters[u], 1u) == uint32_t(splits - 1);
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (tid == 0) a.counters[u] = 0u;
-    const int used = (s_count + bps - 1) / bps;
-    const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
-    for (int i = tid; i < G * D; i += kDecThreads) {
-        const int g = i / D, d = i - g * D;
-        const size_t h = head0 + g;
-        float mx = -INFINITY;
-        for (int sp = 0; sp < used; ++sp) mx = fmaxf(mx, __ldcg(a.part_m + h * splits + sp));
-        float num = 0.f, den = 0.f;
-        if (mx != -INFINITY) {
-            for (int sp = 0; sp < used; ++sp) {
-                const float ms = __ldcg(a.part_m + h * splits + sp);
-                if (ms == -INFINITY) continue;
-                const float w = fast_exp2(ms - mx);
-                den = fmaf(w, __ldcg(a.part_l + h * splits + sp), den);
-                num = fmaf(w, __ldcg(a.part_o + (h * splits + sp) * D + d), num);
+                for (int w = 0; w < kDecWarps; ++w) sum += red[(w * G + g) * D + d];
+                a.part_o[((head0 + g) * ipu + slot) * D + d] = sum;
+            }
+            // this segment's first slot carries its partial; its other slots carry none
+            for (int i = tid; i < G * (item - seg_first + 1); i += kDecThreads) {
+                const int g = i % G, sl = slot + i / G;
+                a.part_m[(head0 + g) * ipu + sl] = sl == slot ? s_m[g] : -INFINITY;
+                if (sl == slot) a.part_l[(head0 + g) * ipu + sl] = s_l[g];
+            }
+            __syncthreads();   // the stage buffer is free again
+            if (tid == 0) {
+                __threadfence();
+                const uint32_t n = uint32_t(item - seg_first + 1);
+                const uint32_t before = atomicAdd(&a.counters[u], n);
+                s_merge_unit = before + n == uint32_t(ipu) ? u : -1;
             }
         }
-        a.out[h * D + d] = den > 0.f ? num / den : 0.f;
+        // release the stage; the producer refills it with the item kStages ahead
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (tid == 0 && item + a.stages < i_end) {
+            if (!mbar_wait_bounded(&empty[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+            issue(item + a.stages);
+        }
+        if (!seg_end) continue;
+        __syncthreads();
+        if (s_merge_unit < 0) continue;
+
+        // ---- this CTA completed unit u: merge its partials ------------------------
+        __threadfence();
+        if (tid == 0) a.counters[u] = 0u;
+        const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+        const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
+        const int ipu = a.items_per_unit;
+        for (int i = tid; i < G * D; i += kDecThreads) {
+            const int g = i / D, d = i - g * D;
+            const size_t h = head0 + g;
+            float mx = -INFINITY;
+            for (int sp = 0; sp < ipu; ++sp) mx = fmaxf(mx, __ldcg(a.part_m + h * ipu + sp));
+            float num = 0.f, den = 0.f;
+            if (mx != -INFINITY) {
+                for (int sp = 0; sp < ipu; ++sp) {
+                    const float ms = __ldcg(a.part_m + h * ipu + sp);
+                    if (ms == -INFINITY) continue;
+                    const float wgt = fast_exp2(ms - mx);
+                    den = fmaf(wgt, __ldcg(a.part_l + h * ipu + sp), den);
+                    num = fmaf(wgt, __ldcg(a.part_o + (h * ipu + sp) * D + d), num);
+                }
+            }
+            a.out[h * D + d] = den > 0.f ? num / den : 0.f;
+        }
     }
 }
 
 template <int D, bool BF16, int G>
-cudaError_t launch_decode_t(const DecodeArgs& a, int units, cudaStream_t s)
+cudaError_t launch_decode_t(DecodeArgs a, cudaStream_t s)
 {
-    using S = DecodeShape<D, BF16>;
-    const size_t smem = size_t(2) * S::TPS * S::ROW_BYTES + size_t(2) * G * S::TPS * sizeof(float);
+    using S = DecodeShape<D, BF16, G>;
+    const int item_tokens = a.blocks_per_item * a.bs;
+    const size_t stage = size_t(2) * item_tokens * S::ROW_BYTES;
+    const size_t fixed = decode_fixed_smem(G, item_tokens);
+    a.stages = (2 * (3 * stage + fixed + 1024) <= size_t(kSmemPerSm)) ? 3 : 2;
+    const size_t smem = a.stages * stage + fixed;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemLimit);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    decode_kernel<D, BF16, G><<<dim3(unsigned(units * a.max_splits)), kDecThreads, smem, s>>>(a);
+    const int per_sm = (2 * (smem + 1024) <= size_t(kSmemPerSm)) ? 2 : 1;
+    long long ctas = (long long)num_sms() * per_sm;
+    // every CTA's range must fit its shared-memory page cache
+    const long long min_ctas = ((long long)a.total_items * a.blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
+    if (ctas < min_ctas) ctas = min_ctas;
+    // ... and touch at most 64 units
+    const long long min_ctas_units = (a.units + 61) / 62;
+    if (ctas < min_ctas_units) ctas = min_ctas_units;
+    if (ctas > a.total_items) ctas = a.total_items;
+    decode_kernel<D, BF16, G><<<dim3(unsigned(ctas)), kDecThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 template <int D, bool BF16>
-cudaError_t dispatch_group(const DecodeArgs& a, int G, int units, cudaStream_t s)
+cudaError_t dispatch_group(const DecodeArgs& a, int G, cudaStream_t s)
 {
     switch (G) {
-        case 1: return launch_decode_t<D, BF16, 1>(a, units, s);
-        case 2: return launch_decode_t<D, BF16, 2>(a, units, s);
-        case 4: return launch_decode_t<D, BF16, 4>(a, units, s);
-        case 8: return launch_decode_t<D, BF16, 8>(a, units, s);
+        case 1: return launch_decode_t<D, BF16, 1>(a, s);
+        case 2: return launch_decode_t<D, BF16, 2>(a, s);
+        case 4: return launch_decode_t<D, BF16, 4>(a, s);
+        case 8: return launch_decode_t<D, BF16, 8>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-int decode_tokens_per_split(int D, bool kv_bf16)
+int decode_blocks_per_item(int D, bool kv_bf16, int block_size)
 {
-    return kStageBytes / (2 * D * (kv_bf16 ? 2 : 4));
+    const int item_tokens = kItemKBytes / (D * (kv_bf16 ? 2 : 4));
+    return item_tokens >= block_size ? item_tokens / block_size : 1;
+}
+
+bool decode_supported(int D, bool kv_bf16, int block_size, int G)
+{
+    const int bpi = decode_blocks_per_item(D, kv_bf16, block_size);
+    const int item_tokens = bpi * block_size;
+    const size_t stage = size_t(2) * item_tokens * D * (kv_bf16 ? 2 : 4);
+    return 2 * stage + decode_fixed_smem(G, item_tokens) <= size_t(kDecSmemLimit);
 }
 
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
@@ -368,8 +454,10 @@ cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.N = g.N;
     a.num_pages = g.num_pages;
     a.sel_stride = g.sel_stride;
-    a.blocks_per_split = L.blocks_per_split;
-    a.max_splits = L.max_splits;
+    a.blocks_per_item = L.blocks_per_split;
+    a.items_per_unit = L.max_splits;
+    a.units = units;
+    a.total_items = units * L.max_splits;
     a.scale_log2 = g.scale_log2;
     a.part_m = reinterpret_cast<float*>(ws + L.part_m);
     a.part_l = reinterpret_cast<float*>(ws + L.part_l);
@@ -377,10 +465,8 @@ cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.counters = reinterpret_cast<uint32_t*>(ws + L.dec_counters);
     a.err = reinterpret_cast<uint32_t*>(ws + L.err);
     if (g.D == 128)
-        return g.kv_bf16 ? dispatch_group<128, true>(a, g.G, units, s)
-                         : dispatch_group<128, false>(a, g.G, units, s);
-    return g.kv_bf16 ? dispatch_group<64, true>(a, g.G, units, s)
-                     : dispatch_group<64, false>(a, g.G, units, s);
+        return g.kv_bf16 ? dispatch_group<128, true>(a, g.G, s) : dispatch_group<128, false>(a, g.G, s);
+    return g.kv_bf16 ? dispatch_group<64, true>(a, g.G, s) : dispatch_group<64, false>(a, g.G, s);
 }
 
 }  // namespace sa

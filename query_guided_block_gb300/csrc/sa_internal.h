@@ -45,8 +45,8 @@ struct WorkspaceLayout {
     size_t part_o;         // float [B*Hq, max_splits, D]
     size_t total;
     int score_cols;        // candidates per unit row of the score buffer
-    int max_splits;        // decode split-K slices per unit
-    int blocks_per_split;  // selected blocks per decode CTA
+    int max_splits;        // decode work items (split-K slices) per unit
+    int blocks_per_split;  // selected blocks per decode work item
 };
 
 WorkspaceLayout workspace_layout(const Geometry& g);
@@ -55,8 +55,10 @@ WorkspaceLayout workspace_layout(const Geometry& g);
 int num_sms();
 constexpr int kSmemPerSm = 228 * 1024;
 
-// Tokens one decode CTA stages (K and V tiles of this many tokens fit in 64 KB).
-int decode_tokens_per_split(int D, bool kv_bf16);
+// Selected blocks per decode work item, and whether a (D, dtype, block, group)
+// combination fits the decode kernel's shared-memory pipeline.
+int decode_blocks_per_item(int D, bool kv_bf16, int block_size);
+bool decode_supported(int D, bool kv_bf16, int block_size, int G);
 
 cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int32_t* block_table,
                               void* kmin, void* kmax, float* kmean, uint32_t* err,

@@ -65,8 +65,6 @@ struct SelectArgs {
     // workspace
     float* scores;           // [units, n_cand]
     uint32_t* counters;      // [units] scored slots
-    uint32_t* work;          // next chunk id
-    uint32_t* done;          // CTAs finished
     uint32_t* err;
 };
 
@@ -211,12 +209,13 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
 
 // ------------------------------------------------------------- kernel ---
 // Persistent streaming kernel.  The candidates of every unit are cut into chunks of
-// contiguous metadata rows (<= kStageBytes per chunk); CTAs take chunk ids from a
-// device-wide counter in unit-major order, so units complete one after another and a
-// unit's top-k overlaps the streaming of later units.  Thread 0 keeps kStages chunks
-// in flight with 1-D bulk async copies (complete_tx on one mbarrier per stage); all
-// threads score from shared memory.  A per-unit counter of scored candidate slots
-// (release / acquire) tells the CTA that finishes a unit to run its top-k.
+// contiguous metadata rows (<= kStageBytes per chunk), numbered unit-major; CTA i
+// owns an equal contiguous range of chunk ids, so it crosses a unit boundary once or
+// twice and needs no per-chunk synchronisation with other CTAs.  Thread 0 keeps
+// kStages chunks in flight with 1-D bulk async copies (complete_tx on one mbarrier per
+// stage); all threads score from shared memory.  When a CTA finishes its segment of a
+// unit it adds the segment's slot count to the unit's counter; the CTA that completes
+// the count runs the unit's top-k.  Nothing waits on another CTA.
 template <int KIND, bool MBF16, int D>
 struct SelectShape {
     static constexpr int ESZ = (KIND == KIND_QUEST && MBF16) ? 2 : 4;
@@ -257,12 +256,6 @@ __device__ __forceinline__ ChunkInfo chunk_info(const SelectArgs& a, int cid, in
     return c;
 }
 
-__device__ __forceinline__ int grab_chunk(const SelectArgs& a)
-{
-    const int id = int(atomicAdd(a.work, 1u));
-    return id < a.total_chunks ? id : -1;
-}
-
 template <int KIND, bool MBF16, int D>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
 {
@@ -271,7 +264,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);
     __shared__ __align__(8) uint64_t full[kStages];
-    __shared__ int s_chunk[kStages];
     __shared__ int s_topk_unit;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -279,15 +271,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
     const int d0 = sub * EPL;
     const char* hi_src = reinterpret_cast<const char*>(KIND == KIND_QUEST ? a.kmax : (const void*)a.kmean);
     const char* lo_src = reinterpret_cast<const char*>(a.kmin);
+    const int c_begin = int((long long)a.total_chunks * blockIdx.x / gridDim.x);
+    const int c_end = int((long long)a.total_chunks * (blockIdx.x + 1) / gridDim.x);
 
-    auto issue = [&](int s, int cid) {   // thread 0 only
-        s_chunk[s] = cid;
-        uint32_t bytes = 0;
-        ChunkInfo c{};
-        if (cid >= 0) {
-            c = chunk_info(a, cid, ROWS);
-            bytes = uint32_t(c.nrows) * SS::ROW_BYTES;
-        }
+    auto issue = [&](int cid) {   // thread 0 only
+        const int s = (cid - c_begin) % kStages;
+        const ChunkInfo c = chunk_info(a, cid, ROWS);
+        const uint32_t bytes = uint32_t(c.nrows) * SS::ROW_BYTES;
         mbar_arrive_expect_tx(&full[s], bytes * SS::ARRAYS);
         if (bytes) {
             const size_t off = (size_t(c.u) * a.rows + c.row0) * SS::ROW_BYTES;
@@ -301,17 +291,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
-        for (int s = 0; s < kStages; ++s) issue(s, grab_chunk(a));
+        for (int cid = c_begin; cid < c_end && cid < c_begin + kStages; ++cid) issue(cid);
     }
     __syncthreads();
 
     int cur_u = -1;
+    uint32_t seg_slots = 0;
     float cp[EPL], cn[EPL];
-    for (int it = 0;; ++it) {
-        const int s = it % kStages;
-        const uint32_t parity = uint32_t(it / kStages) & 1u;
-        const int cid = s_chunk[s];
-        if (cid < 0) break;
+    for (int cid = c_begin; cid < c_end; ++cid) {
+        const int s = (cid - c_begin) % kStages;
+        const uint32_t parity = uint32_t((cid - c_begin) / kStages) & 1u;
         const ChunkInfo c = chunk_info(a, cid, ROWS);
         if (c.u != cur_u) {   // query coefficients of this unit (uniform across the CTA)
             cur_u = c.u;
@@ -355,41 +344,38 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
             for (int m = LPR / 2; m >= 1; m >>= 1) sc += __shfl_xor_sync(kFullMask, sc, m);
             if (sub == 0 && r < c.nrows) srow[r] = sc;
         }
+        seg_slots += uint32_t(c.nslots);
         __syncthreads();   // stage s fully read; this chunk's scores written
-        if (tid == 0) {
-            issue(s, grab_chunk(a));
-            __threadfence();
-            const uint32_t before = atomicAdd(&a.counters[c.u], uint32_t(c.nslots));
-            s_topk_unit = (before + uint32_t(c.nslots) == uint32_t(a.n_cand)) ? c.u : -1;
-        }
-        __syncthreads();
-        const int tu = s_topk_unit;
-        if (tu >= 0) {
-            __threadfence();
-            if (tid == 0) a.counters[tu] = 0u;   // every slot of this unit is scored
-            const float* row = a.scores + size_t(tu) * a.n_cand;
-            int n_valid = 0;
-            for (int base = 0; base < a.n_cand; base += kSelThreads) {
-                const int cc = base + tid;
-                bool valid = false;
-                if (cc < a.n_cand) {
-                    valid = candidate_row(a, tu, cc) >= 0;
-                    keys[cc] = valid ? order_key(__ldcg(row + cc)) : 0u;
-                }
-                n_valid += __syncthreads_count(valid);
-            }
-            topk_and_emit(a, tu, keys, a.n_cand, n_valid);
-            __syncthreads();
-        }
-    }
+        if (tid == 0 && cid + kStages < c_end) issue(cid + kStages);
 
-    // the last CTA out resets the work counters for the next launch
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        if (atomicAdd(a.done, 1u) == gridDim.x - 1) {
-            *a.work = 0u;
-            *a.done = 0u;
+        // end of this CTA's segment of unit c.u: report it; the completing CTA selects
+        const bool seg_end = cid + 1 == c_end || (cid + 1) / a.chunks_per_unit != c.u;
+        if (seg_end) {
+            if (tid == 0) {
+                __threadfence();
+                const uint32_t before = atomicAdd(&a.counters[c.u], seg_slots);
+                s_topk_unit = (before + seg_slots == uint32_t(a.n_cand)) ? c.u : -1;
+            }
+            seg_slots = 0;
+            __syncthreads();
+            const int tu = s_topk_unit;
+            if (tu >= 0) {
+                __threadfence();
+                if (tid == 0) a.counters[tu] = 0u;   // every slot of this unit is scored
+                const float* row = a.scores + size_t(tu) * a.n_cand;
+                int n_valid = 0;
+                for (int base = 0; base < a.n_cand; base += kSelThreads) {
+                    const int cc = base + tid;
+                    bool valid = false;
+                    if (cc < a.n_cand) {
+                        valid = candidate_row(a, tu, cc) >= 0;
+                        keys[cc] = valid ? order_key(__ldcg(row + cc)) : 0u;
+                    }
+                    n_valid += __syncthreads_count(valid);
+                }
+                topk_and_emit(a, tu, keys, a.n_cand, n_valid);
+                __syncthreads();
+            }
         }
     }
 }
@@ -413,7 +399,7 @@ cudaError_t launch_select_t(const SelectArgs& a0, int units, cudaStream_t s)
     }
     const int per_sm = smem + 4096 <= (kSmemPerSm / 2) ? 2 : 1;
     int ctas = num_sms() * per_sm;
-    if (ctas > a.total_chunks) ctas = a.total_chunks > 0 ? a.total_chunks : 1;
+    if (ctas > a.total_chunks) ctas = a.total_chunks;
     select_kernel<KIND, MBF16, D><<<dim3(unsigned(ctas)), kSelThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
@@ -452,8 +438,6 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.Hq = g.Hq;
     a.err = reinterpret_cast<uint32_t*>(ws + L.err);
     a.scores = reinterpret_cast<float*>(ws + L.scores);
-    a.work = reinterpret_cast<uint32_t*>(ws + L.sel_work);
-    a.done = reinterpret_cast<uint32_t*>(ws + L.sel_done);
     a.counters = reinterpret_cast<uint32_t*>(ws + L.sel_counters);
 
     if (!g.two_level) {
