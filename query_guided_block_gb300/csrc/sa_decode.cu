@@ -323,11 +323,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
                 for (int w = 0; w < kDecWarps; ++w) sum += red[(w * G + g) * D + d];
                 a.part_o[((head0 + g) * ipu + slot) * D + d] = sum;
             }
-            // this segment's first slot carries its partial; its other slots carry none
-            for (int i = tid; i < G * (item - seg_first + 1); i += kDecThreads) {
-                const int g = i % G, sl = slot + i / G;
-                a.part_m[(head0 + g) * ipu + sl] = sl == slot ? s_m[g] : -INFINITY;
-                if (sl == slot) a.part_l[(head0 + g) * ipu + sl] = s_l[g];
+            // the segment's partial lives at the slot of its first item
+            if (tid < G) {
+                a.part_m[(head0 + tid) * ipu + slot] = s_m[tid];
+                a.part_l[(head0 + tid) * ipu + slot] = s_l[tid];
             }
             __syncthreads();   // the stage buffer is free again
             if (tid == 0) {
@@ -349,28 +348,40 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
         if (s_merge_unit < 0) continue;
 
         // ---- this CTA completed unit u: merge its partials ------------------------
+        // A unit's segments start at its first item and at every CTA range start inside
+        // it; each segment wrote one partial at its first item's slot.
         __threadfence();
         if (tid == 0) a.counters[u] = 0u;
         const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
         const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
         const int ipu = a.items_per_unit;
+        const int x0 = u * ipu, x1 = x0 + ipu;
+        const long long T = a.total_items, C = gridDim.x;
+        int c0 = int((long long)x0 * C / T);                         // CTA holding item x0
+        while (c0 + 1 < C && (T * (c0 + 1)) / C <= x0) ++c0;
+        while (c0 > 0 && (T * c0) / C > x0) --c0;
         for (int i = tid; i < G * D; i += kDecThreads) {
             const int g = i / D, d = i - g * D;
             const size_t h = head0 + g;
             float mx = -INFINITY;
-            for (int sp = 0; sp < ipu; ++sp) mx = fmaxf(mx, __ldcg(a.part_m + h * ipu + sp));
+            for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
+                const int slot = int(max((T * c) / C, (long long)x0) - x0);
+                mx = fmaxf(mx, __ldcg(a.part_m + h * ipu + slot));
+            }
             float num = 0.f, den = 0.f;
             if (mx != -INFINITY) {
-                for (int sp = 0; sp < ipu; ++sp) {
-                    const float ms = __ldcg(a.part_m + h * ipu + sp);
+                for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
+                    const int slot = int(max((T * c) / C, (long long)x0) - x0);
+                    const float ms = __ldcg(a.part_m + h * ipu + slot);
                     if (ms == -INFINITY) continue;
                     const float wgt = fast_exp2(ms - mx);
-                    den = fmaf(wgt, __ldcg(a.part_l + h * ipu + sp), den);
-                    num = fmaf(wgt, __ldcg(a.part_o + (h * ipu + sp) * D + d), num);
+                    den = fmaf(wgt, __ldcg(a.part_l + h * ipu + slot), den);
+                    num = fmaf(wgt, __ldcg(a.part_o + (h * ipu + slot) * D + d), num);
                 }
             }
             a.out[h * D + d] = den > 0.f ? num / den : 0.f;
         }
+        __syncthreads();
     }
 }
 

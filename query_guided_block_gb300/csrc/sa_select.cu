@@ -207,6 +207,37 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
     if (tid == 0) a.out_count[u] = k_eff + a.win_count;
 }
 
+// Unit u's scores -> order keys in shared memory (0 for slots that are not
+// candidates); returns the number of candidates.  Loads are issued in batches of
+// independent requests so the L2 latency is paid once per batch, not per element.
+__device__ int load_keys(const SelectArgs& a, int u, uint32_t* keys, int* s_count)
+{
+    constexpr int kBatch = 8;
+    const float* row = a.scores + size_t(u) * a.n_cand;
+    int mine = 0;
+    for (int base = threadIdx.x; base < a.n_cand; base += kSelThreads * kBatch) {
+        float x[kBatch];
+        bool ok[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int c = base + i * kSelThreads;
+            ok[i] = c < a.n_cand && candidate_row(a, u, c) >= 0;
+            x[i] = ok[i] ? __ldcg(row + c) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int c = base + i * kSelThreads;
+            if (c < a.n_cand) keys[c] = ok[i] ? order_key(x[i]) : 0u;
+            mine += ok[i];
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mine += __shfl_xor_sync(kFullMask, mine, off);
+    if ((threadIdx.x & 31) == 0) atomicAdd(s_count, mine);
+    __syncthreads();
+    return *s_count;
+}
+
 // ------------------------------------------------------------- kernel ---
 // Persistent streaming kernel.  The candidates of every unit are cut into chunks of
 // contiguous metadata rows (<= kStageBytes per chunk), numbered unit-major; CTA i
@@ -264,7 +295,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);
     __shared__ __align__(8) uint64_t full[kStages];
-    __shared__ int s_topk_unit;
+    __shared__ int s_topk_unit, s_nvalid;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sub = lane % LPR, rsub = lane / LPR;
@@ -361,18 +392,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
             const int tu = s_topk_unit;
             if (tu >= 0) {
                 __threadfence();
-                if (tid == 0) a.counters[tu] = 0u;   // every slot of this unit is scored
-                const float* row = a.scores + size_t(tu) * a.n_cand;
-                int n_valid = 0;
-                for (int base = 0; base < a.n_cand; base += kSelThreads) {
-                    const int cc = base + tid;
-                    bool valid = false;
-                    if (cc < a.n_cand) {
-                        valid = candidate_row(a, tu, cc) >= 0;
-                        keys[cc] = valid ? order_key(__ldcg(row + cc)) : 0u;
-                    }
-                    n_valid += __syncthreads_count(valid);
+                if (tid == 0) {
+                    a.counters[tu] = 0u;   // every slot of this unit is scored
+                    s_nvalid = 0;
                 }
+                __syncthreads();
+                const int n_valid = load_keys(a, tu, keys, &s_nvalid);
                 topk_and_emit(a, tu, keys, a.n_cand, n_valid);
                 __syncthreads();
             }
