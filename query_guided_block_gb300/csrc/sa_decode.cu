@@ -13,10 +13,11 @@
 //   * At start the CTA resolves, for its whole range, selected id -> page through the
 //     page table into shared memory (bounds-checked), so the producer thread issues
 //     copies without touching global memory.
-//   * Thread 0 keeps kStages items in flight: per item, 1-D bulk async copies
-//     (cp.async.bulk) of each (page, KV head) K tile and V tile -- block_size x D
-//     contiguous -- complete on the stage's `full` mbarrier; warps release the stage on
-//     its `empty` mbarrier.
+//   * kStages items stay in flight: per item, 1-D bulk async copies (cp.async.bulk) of
+//     each (page, KV head) K tile and V tile -- block_size x D contiguous -- complete
+//     on the stage's `full` mbarrier; warps release the stage on its `empty` mbarrier.
+//     Copies from one issuing thread complete one after another, so each item's copies
+//     are issued by different warps.
 //   * QK^T in fp32: a key row is covered by LPR lanes with one 16-byte shared load
 //     each; the G heads' partial dots are summed across the row's lanes with the
 //     transposed halving reduction.  Per head, warps keep the running max / sum of an
@@ -156,7 +157,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
 
     const char* kbase = reinterpret_cast<const char*>(a.k_pages);
     const char* vbase = reinterpret_cast<const char*>(a.v_pages);
-    auto issue = [&](int item) {   // thread 0 only
+    // Copies issued by one thread complete one after another, so an item's 2 * bpi
+    // copies (K and V tile of each block) are spread over the warps: copy i of the item
+    // in stage s is issued by warp (s * 2 bpi + i) mod 8; the owner of copy 0 also posts
+    // the stage's expected byte count.
+    auto issue_mine = [&](int item) {   // every warp's lane 0
         const int k = item - i_begin;
         const int s = k % a.stages;
         unsigned char* kd = smem + s * stage_bytes;
@@ -164,18 +169,24 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
         const int u = item / a.items_per_unit;
         const size_t head_off = size_t(u % a.Hkv) * tile_bytes;
         const size_t page_stride = size_t(a.Hkv) * tile_bytes;
-        uint32_t nbytes = 0;
-        for (int i = 0; i < bpi; ++i) nbytes += blk_page[k * bpi + i] >= 0 ? tile_bytes : 0u;
-        mbar_arrive_expect_tx(&full[s], 2 * nbytes);
-        for (int i = 0; i < bpi; ++i) {
-            const int page = blk_page[k * bpi + i];
+        for (int i = 0; i < 2 * bpi; ++i) {
+            if ((s * 2 * bpi + i) % kDecWarps != warp) continue;
+            if (i == 0) {
+                uint32_t nbytes = 0;
+                for (int j = 0; j < bpi; ++j) nbytes += blk_page[k * bpi + j] >= 0 ? tile_bytes : 0u;
+                mbar_arrive_expect_tx(&full[s], 2 * nbytes);
+            }
+            const int j = i >> 1;
+            const int page = blk_page[k * bpi + j];
             if (page < 0) continue;
-            bulk_copy_g2s(kd + size_t(i) * tile_bytes, kbase + page * page_stride + head_off, tile_bytes, &full[s]);
-            bulk_copy_g2s(vd + size_t(i) * tile_bytes, vbase + page * page_stride + head_off, tile_bytes, &full[s]);
+            if ((i & 1) == 0)
+                bulk_copy_g2s(kd + size_t(j) * tile_bytes, kbase + page * page_stride + head_off, tile_bytes, &full[s]);
+            else
+                bulk_copy_g2s(vd + size_t(j) * tile_bytes, vbase + page * page_stride + head_off, tile_bytes, &full[s]);
         }
     };
-    if (tid == 0)
-        for (int item = i_begin; item < i_end && item < i_begin + a.stages; ++item) issue(item);
+    if (lane == 0)
+        for (int item = i_begin; item < i_end && item < i_begin + a.stages; ++item) issue_mine(item);
 
     // running state of the current unit segment
     float qr[G][EPL];
@@ -336,12 +347,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
                 s_merge_unit = before + n == uint32_t(ipu) ? u : -1;
             }
         }
-        // release the stage; the producer refills it with the item kStages ahead
+        // release the stage; its issuing warps refill it with the item kStages ahead
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (tid == 0 && item + a.stages < i_end) {
-            if (!mbar_wait_bounded(&empty[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
-            issue(item + a.stages);
+        if (lane == 0) {
+            mbar_arrive(&empty[s]);
+            const int nxt = item + a.stages;
+            bool mine = false;
+            for (int i = 0; i < 2 * bpi; ++i) mine |= (s * 2 * bpi + i) % kDecWarps == warp;
+            if (nxt < i_end && mine) {
+                if (!mbar_wait_bounded(&empty[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+                issue_mine(nxt);
+            }
         }
         if (!seg_end) continue;
         __syncthreads();

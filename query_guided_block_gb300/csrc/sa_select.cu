@@ -242,9 +242,10 @@ __device__ int load_keys(const SelectArgs& a, int u, uint32_t* keys, int* s_coun
 // Persistent streaming kernel.  The candidates of every unit are cut into chunks of
 // contiguous metadata rows (<= kStageBytes per chunk), numbered unit-major; CTA i
 // owns an equal contiguous range of chunk ids, so it crosses a unit boundary once or
-// twice and needs no per-chunk synchronisation with other CTAs.  Thread 0 keeps
+// twice and needs no per-chunk synchronisation with other CTAs.  The CTA keeps
 // kStages chunks in flight with 1-D bulk async copies (complete_tx on one mbarrier per
-// stage); all threads score from shared memory.  When a CTA finishes its segment of a
+// stage; a stage's copies are issued by different warps); all threads score from
+// shared memory.  When a CTA finishes its segment of a
 // unit it adds the segment's slot count to the unit's counter; the CTA that completes
 // the count runs the unit's top-k.  Nothing waits on another CTA.
 template <int KIND, bool MBF16, int D>
@@ -305,26 +306,33 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
     const int c_begin = int((long long)a.total_chunks * blockIdx.x / gridDim.x);
     const int c_end = int((long long)a.total_chunks * (blockIdx.x + 1) / gridDim.x);
 
-    auto issue = [&](int cid) {   // thread 0 only
+    // Copies issued by one thread complete one after another, so each stage's copies
+    // come from different warps (lane 0): stage s, array a -> warp (2 s + a) mod 8.
+    auto issue = [&](int cid, int array) {
         const int s = (cid - c_begin) % kStages;
         const ChunkInfo c = chunk_info(a, cid, ROWS);
         const uint32_t bytes = uint32_t(c.nrows) * SS::ROW_BYTES;
-        mbar_arrive_expect_tx(&full[s], bytes * SS::ARRAYS);
+        if (array == 0) mbar_arrive_expect_tx(&full[s], bytes * SS::ARRAYS);
         if (bytes) {
             const size_t off = (size_t(c.u) * a.rows + c.row0) * SS::ROW_BYTES;
             unsigned char* dst = smem + s * kStageBytes;
-            bulk_copy_g2s(dst, hi_src + off, bytes, &full[s]);
-            if constexpr (KIND == KIND_QUEST)
-                bulk_copy_g2s(dst + ROWS * SS::ROW_BYTES, lo_src + off, bytes, &full[s]);
+            if (array == 0) bulk_copy_g2s(dst, hi_src + off, bytes, &full[s]);
+            else bulk_copy_g2s(dst + ROWS * SS::ROW_BYTES, lo_src + off, bytes, &full[s]);
         }
+    };
+    auto issue_mine = [&](int cid) {   // every warp's lane 0
+        const int s = (cid - c_begin) % kStages;
+        for (int arr = 0; arr < SS::ARRAYS; ++arr)
+            if ((s * SS::ARRAYS + arr) % kSelWarps == warp) issue(cid, arr);
     };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
-        for (int cid = c_begin; cid < c_end && cid < c_begin + kStages; ++cid) issue(cid);
     }
     __syncthreads();
+    if (lane == 0)
+        for (int cid = c_begin; cid < c_end && cid < c_begin + kStages; ++cid) issue_mine(cid);
 
     int cur_u = -1;
     uint32_t seg_slots = 0;
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
         }
         seg_slots += uint32_t(c.nslots);
         __syncthreads();   // stage s fully read; this chunk's scores written
-        if (tid == 0 && cid + kStages < c_end) issue(cid + kStages);
+        if (lane == 0 && cid + kStages < c_end) issue_mine(cid + kStages);
 
         // end of this CTA's segment of unit c.u: report it; the completing CTA selects
         const bool seg_end = cid + 1 == c_end || (cid + 1) / a.chunks_per_unit != c.u;
