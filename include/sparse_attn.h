@@ -186,6 +186,38 @@ int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* s
 int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream stream,
                                  uint32_t* flags);
 
+/* Block selection without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory: code that runs where cudaMalloc is forbidden or
+ * unsafe (inside another framework's allocator or stream-ordered memory pool,
+ * inside a host callback, in a plugin whose host owns every device allocation), or
+ * a process whose device memory is entirely reserved by someone else's pool.
+ *
+ * Same inputs, outputs and results as sparse_attn_select for single-level
+ * selection (two_level must be 0).  The scratch it needs -- error word, per-unit
+ * completion counters and the fp32 score rows -- lives in a fixed array of
+ * SPARSE_ATTN_NOALLOC_SCRATCH_BYTES inside the library, which every device that
+ * loads the library keeps until the process exits.  Nothing is allocated and no
+ * allocating library routine is called.
+ *
+ * - A problem whose scratch (256 B + 3 counter rows + units x candidates x 4 B,
+ *   each part rounded up to 256 B) exceeds the array returns
+ *   SPARSE_ATTN_UNSUPPORTED before any launch; two_level = 1 does too.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ * - Every call shares the one array: the counters are cleared at the start of each
+ *   call (stream-ordered), but calls whose execution overlaps on the GPU -- on
+ *   different streams, or from different host threads -- race on it and must be
+ *   serialised by the caller.
+ * - Device-side error bits of this call stay in the private array (select has no
+ *   data-dependent indexing; only a timed-out copy wait could set one). */
+#define SPARSE_ATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
+int sparse_attn_select_noalloc(const sparse_attn_params* p, const void* q, const void* kmin,
+                               const void* kmax, const float* kmean, int32_t* sel_ids,
+                               int32_t* sel_count, sparse_attn_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -93,6 +93,7 @@ def lib():
             "sparse_attn_diff": ([P, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                   vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_get_device_error": ([vp, sz, vp, u32p], C.c_int),
+            "sparse_attn_select_noalloc": ([P, vp, vp, vp, vp, vp, vp, vp], C.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -106,7 +107,7 @@ def exported_symbols():
     return ["sparse_attn_status_string", "sparse_attn_num_blocks", "sparse_attn_sel_stride",
             "sparse_attn_workspace_size", "sparse_attn_workspace_init", "sparse_attn_build_meta",
             "sparse_attn_select", "sparse_attn_decode", "sparse_attn_diff",
-            "sparse_attn_get_device_error"]
+            "sparse_attn_get_device_error", "sparse_attn_select_noalloc"]
 
 
 def _status_string(status: int) -> str:
@@ -195,6 +196,14 @@ def sparse_attn_diff(p, step, sel_ids, sel_count, prev_ids, prev_count, cache_sl
         int(cache_slots), _ptr(slot_block), _ptr(slot_last_use), _ptr(hit_ids), _ptr(miss_ids),
         _ptr(miss_slot), _ptr(evict_ids), _ptr(evict_slot), _ptr(new_ids), _ptr(dropped_ids),
         _ptr(counts), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_select_noalloc(p, q, kmin, kmax, kmean, sel_ids, sel_count, stream=None) -> None:
+    """sparse_attn_select with the library's fixed scratch instead of a workspace, for
+    callers that cannot allocate device memory (see the C header)."""
+    _check("sparse_attn_select_noalloc", lib().sparse_attn_select_noalloc(
+        C.byref(p), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(kmean), _ptr(sel_ids), _ptr(sel_count),
+        _stream(stream)))
 
 
 def sparse_attn_get_device_error(ws, stream=None) -> int:

@@ -296,4 +296,60 @@ int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream s
     return word ? SPARSE_ATTN_DEVICE_BOUNDS : SPARSE_ATTN_OK;
 }
 
+// ---- selection for callers that cannot allocate device memory ---------------
+// The scratch lives in this file-scope array; host code needs its device address,
+// looked up once per device (cudaGetSymbolAddress) with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPARSE_ATTN_NOALLOC_SCRATCH_BYTES];
+
+static void* noalloc_scratch_address(int* status)
+{
+    static void* cached[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = SPARSE_ATTN_CUDA_ERROR;
+        return nullptr;
+    }
+    if (cached[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            *status = SPARSE_ATTN_CUDA_ERROR;
+            return nullptr;
+        }
+        cached[dev] = ptr;
+    }
+    *status = SPARSE_ATTN_OK;
+    return cached[dev];
+}
+
+int sparse_attn_select_noalloc(const sparse_attn_params* p, const void* q, const void* kmin,
+                               const void* kmax, const float* kmean, int32_t* sel_ids,
+                               int32_t* sel_count, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    if (g.two_level) return SPARSE_ATTN_UNSUPPORTED;
+    const WorkspaceLayout L = workspace_layout(g);
+    // select touches the header, the counter rows and the score rows only
+    const size_t need = L.scores + size_t(g.units()) * L.score_cols * sizeof(float);
+    if (need > SPARSE_ATTN_NOALLOC_SCRATCH_BYTES) return SPARSE_ATTN_UNSUPPORTED;
+    if (g.units() > 0) {
+        if (!q || !sel_ids || !sel_count || !aligned(q, 16) || !aligned(sel_ids, 4) ||
+            !aligned(sel_count, 4))
+            return SPARSE_ATTN_INVALID_ARG;
+        const bool need_mean = g.score_kind == SPARSE_ATTN_SCORE_MEAN;
+        if (g.nb > 0) {
+            if (need_mean && (!kmean || !aligned(kmean, 16))) return SPARSE_ATTN_INVALID_ARG;
+            if (!need_mean && (!kmin || !kmax || !aligned(kmin, 16) || !aligned(kmax, 16)))
+                return SPARSE_ATTN_INVALID_ARG;
+        }
+    }
+    char* ws = static_cast<char*>(noalloc_scratch_address(&st));
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // error word and completion counters must start at zero; scores need no clearing
+    if (cudaMemsetAsync(ws, 0, L.scores, s) != cudaSuccess) return SPARSE_ATTN_CUDA_ERROR;
+    return status_of(launch_select(g, L, ws, q, kmin, kmax, kmean, sel_ids, sel_count, s));
+}
+
 }  // extern "C"
