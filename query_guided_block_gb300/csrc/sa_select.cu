@@ -31,8 +31,8 @@ namespace {
 
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kStages = 4;                // chunks in flight per CTA
-constexpr int kStageBytes = 16 * 1024;    // metadata bytes per chunk
+constexpr int kMaxStages = 3;             // chunks in flight per CTA (2 or 3, set at launch)
+constexpr int kStageBytes = 32 * 1024;    // metadata bytes per chunk
 constexpr int kMaxSelectKeys = 16384;     // candidates per unit held in shared memory
 
 enum { KIND_QUEST = 0, KIND_MEAN = 1 };
@@ -56,6 +56,7 @@ struct SelectArgs {
     int n_cand;              // candidate slots per unit = groups * group_rows
     int groups, group_rows;  // candidate slots come in groups of contiguous rows
     int chunks_per_group, chunks_per_unit, total_chunks;
+    int stages;
     // selection
     int k;
     int win_first, win_count;
@@ -81,10 +82,18 @@ __device__ __forceinline__ int candidate_row(const SelectArgs& a, int u, int c)
 
 // ------------------------------------------------------------- top-k ----
 // Runs in one CTA.  keys[0..n) hold order keys (0 = not a candidate).
+//
+// Radix select with digits taken below the common prefix of the candidates' keys:
+// the keys of one unit share their top bits (same sign, nearby exponents), so the
+// first digit starts where the smallest and largest key differ.  11-bit digits,
+// 2048-bin shared-memory histograms, at most three passes; a pass ends the search
+// as soon as the boundary bin holds exactly the remaining count.
 __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n, int n_valid)
 {
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t s_bin, s_above, s_binc;
+    constexpr int kBins = 2048;
+    constexpr int kBinsPerThread = kBins / kSelThreads;
+    __shared__ uint32_t hist[kBins];
+    __shared__ uint32_t s_bin, s_above, s_binc, s_lo, s_hi;
     __shared__ int s_wtot[kSelWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -93,39 +102,63 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
 
     uint32_t prefix = 0, mask = 0;
     int krem = k_eff;
-    bool all_of_prefix = false;
-    for (int pass = 0; pass < 4 && k_eff > 0; ++pass) {
-        const int shift = 24 - 8 * pass;
-        if (tid < 256) hist[tid] = 0;
+    bool all_of_prefix = true;         // k_eff == n_valid (or 0): every candidate / none
+    if (k_eff > 0 && k_eff < n_valid) {
+        // common prefix of the candidates' keys
+        if (tid == 0) { s_lo = 0xffffffffu; s_hi = 0u; }
         __syncthreads();
-        for (int base = 0; base < n; base += kSelThreads) {
-            const int c = base + tid;
-            const uint32_t key = c < n ? keys[c] : 0u;
-            const bool match = c < n && key != 0u && (key & mask) == prefix;
-            const uint32_t bin = match ? ((key >> shift) & 255u) : 256u;
-            const uint32_t peers = __match_any_sync(kFullMask, bin);
-            if (match && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+        uint32_t lo = 0xffffffffu, hi = 0u;
+        for (int c = tid; c < n; c += kSelThreads) {
+            const uint32_t key = keys[c];
+            if (key) { lo = min(lo, key); hi = max(hi, key); }
         }
-        __syncthreads();
-        if (warp == 0) {
-            uint32_t cnt[8], sum = 0;
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                cnt[r] = hist[255 - 8 * lane - r];
+        for (int off = 16; off >= 1; off >>= 1) {
+            lo = min(lo, __shfl_xor_sync(kFullMask, lo, off));
+            hi = max(hi, __shfl_xor_sync(kFullMask, hi, off));
+        }
+        if (lane == 0) { atomicMin(&s_lo, lo); atomicMax(&s_hi, hi); }
+        __syncthreads();
+        lo = s_lo;
+        hi = s_hi;
+        int low_bits = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
+        mask = low_bits >= 32 ? 0u : ~((1u << low_bits) - 1u);
+        prefix = hi & mask;
+        all_of_prefix = false;
+        while (low_bits > 0) {
+            const int w = min(11, low_bits);
+            const int shift = low_bits - w;
+            const uint32_t dmask = (1u << w) - 1u;
+#pragma unroll
+            for (int i = 0; i < kBinsPerThread; ++i) hist[tid + i * kSelThreads] = 0u;
+            __syncthreads();
+            for (int c = tid; c < n; c += kSelThreads) {
+                const uint32_t key = keys[c];
+                if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+            }
+            __syncthreads();
+            // thread t owns bins 2047-8t .. 2040-8t (descending); scan from the top
+            uint32_t cnt[kBinsPerThread], sum = 0;
+#pragma unroll
+            for (int r = 0; r < kBinsPerThread; ++r) {
+                cnt[r] = hist[kBins - 1 - kBinsPerThread * tid - r];
                 sum += cnt[r];
             }
             uint32_t inc = sum;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                uint32_t t = __shfl_up_sync(kFullMask, inc, off);
+                const uint32_t t = __shfl_up_sync(kFullMask, inc, off);
                 if (lane >= off) inc += t;
             }
-            const uint32_t hit = __ballot_sync(kFullMask, inc >= uint32_t(krem));
-            if (lane == __ffs(hit) - 1) {
-                uint32_t above = inc - sum;
-                for (int r = 0; r < 8; ++r) {
+            if (lane == 31) s_wtot[warp] = int(inc);
+            __syncthreads();
+            for (int wv = 0; wv < warp; ++wv) inc += uint32_t(s_wtot[wv]);
+            const uint32_t before = inc - sum;
+            if (before < uint32_t(krem) && inc >= uint32_t(krem)) {
+                uint32_t above = before;
+                for (int r = 0; r < kBinsPerThread; ++r) {
                     if (above + cnt[r] >= uint32_t(krem)) {
-                        s_bin = 255 - 8 * lane - r;
+                        s_bin = uint32_t(kBins - 1 - kBinsPerThread * tid - r);
                         s_above = above;
                         s_binc = cnt[r];
                         break;
@@ -133,14 +166,16 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
                     above += cnt[r];
                 }
             }
-        }
-        __syncthreads();
-        krem -= int(s_above);
-        prefix |= s_bin << shift;
-        mask |= 255u << shift;
-        if (int(s_binc) == krem) {
-            all_of_prefix = true;   // every key with this prefix is selected
-            break;
+            __syncthreads();
+            krem -= int(s_above);
+            prefix |= s_bin << shift;
+            mask |= dmask << shift;
+            low_bits = shift;
+            if (int(s_binc) == krem) {
+                all_of_prefix = true;   // every key with this prefix is selected
+                break;
+            }
+            __syncthreads();   // s_wtot / s_bin are rewritten by the next pass
         }
     }
     // Threshold rule:  all_of_prefix: (key & mask) >= prefix
@@ -257,8 +292,8 @@ struct SelectShape {
     static constexpr int ROW_BYTES = D * ESZ;
     static constexpr int ARRAYS = KIND == KIND_QUEST ? 2 : 1;
     static constexpr int ROWS = kStageBytes / (ARRAYS * ROW_BYTES);   // rows per chunk
-    static constexpr int ROWS_PER_PASS = kSelWarps * RPW;
-    static_assert(ROWS % ROWS_PER_PASS == 0, "chunk rows must split over the warps");
+    static constexpr int R = ROWS / (kSelWarps * RPW);                 // rows per lane group
+    static_assert(R >= 1 && ROWS % (kSelWarps * RPW) == 0, "chunk rows must split over the warps");
 };
 
 struct ChunkInfo {
@@ -288,19 +323,30 @@ __device__ __forceinline__ ChunkInfo chunk_info(const SelectArgs& a, int cid, in
     return c;
 }
 
+// Device-scope counter add with release (our scores, ordered before it by the CTA
+// barrier) and acquire (the other CTAs' scores, when we complete the count).
+__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 template <int KIND, bool MBF16, int D>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
 {
     using SS = SelectShape<KIND, MBF16, D>;
-    constexpr int EPL = SS::EPL, LPR = SS::LPR, RPW = SS::RPW, ROWS = SS::ROWS;
+    constexpr int EPL = SS::EPL, LPR = SS::LPR, RPW = SS::RPW, ROWS = SS::ROWS, R = SS::R;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);
-    __shared__ __align__(8) uint64_t full[kStages];
+    const int stages = a.stages;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + stages * kStageBytes);
+    __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ int s_topk_unit, s_nvalid;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sub = lane % LPR, rsub = lane / LPR;
     const int d0 = sub * EPL;
+    const int row_group = warp * RPW + rsub;            // rows row_group*R .. +R-1 of a chunk
     const char* hi_src = reinterpret_cast<const char*>(KIND == KIND_QUEST ? a.kmax : (const void*)a.kmean);
     const char* lo_src = reinterpret_cast<const char*>(a.kmin);
     const int c_begin = int((long long)a.total_chunks * blockIdx.x / gridDim.x);
@@ -309,7 +355,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
     // Copies issued by one thread complete one after another, so each stage's copies
     // come from different warps (lane 0): stage s, array a -> warp (2 s + a) mod 8.
     auto issue = [&](int cid, int array) {
-        const int s = (cid - c_begin) % kStages;
+        const int s = (cid - c_begin) % stages;
         const ChunkInfo c = chunk_info(a, cid, ROWS);
         const uint32_t bytes = uint32_t(c.nrows) * SS::ROW_BYTES;
         if (array == 0) mbar_arrive_expect_tx(&full[s], bytes * SS::ARRAYS);
@@ -321,25 +367,26 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
         }
     };
     auto issue_mine = [&](int cid) {   // every warp's lane 0
-        const int s = (cid - c_begin) % kStages;
+        const int s = (cid - c_begin) % stages;
         for (int arr = 0; arr < SS::ARRAYS; ++arr)
             if ((s * SS::ARRAYS + arr) % kSelWarps == warp) issue(cid, arr);
     };
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
     if (lane == 0)
-        for (int cid = c_begin; cid < c_end && cid < c_begin + kStages; ++cid) issue_mine(cid);
+        for (int cid = c_begin; cid < c_end && cid < c_begin + stages; ++cid) issue_mine(cid);
 
     int cur_u = -1;
     uint32_t seg_slots = 0;
     float cp[EPL], cn[EPL];
     for (int cid = c_begin; cid < c_end; ++cid) {
-        const int s = (cid - c_begin) % kStages;
-        const uint32_t parity = uint32_t((cid - c_begin) / kStages) & 1u;
+        const int k = cid - c_begin;
+        const int s = k % stages;
+        const uint32_t parity = uint32_t(k / stages) & 1u;
         const ChunkInfo c = chunk_info(a, cid, ROWS);
         if (c.u != cur_u) {   // query coefficients of this unit (uniform across the CTA)
             cur_u = c.u;
@@ -362,44 +409,55 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
         }
         if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
 
+        // R rows per lane group, partial dots summed over the group's LPR lanes at once
         const unsigned char* hi = smem + s * kStageBytes + d0 * SS::ESZ;
         const unsigned char* lo = hi + ROWS * SS::ROW_BYTES;
-        float* srow = a.scores + size_t(c.u) * a.n_cand + c.cand0;
+        float part[R];
 #pragma unroll
-        for (int pass = 0; pass < ROWS / SS::ROWS_PER_PASS; ++pass) {
-            const int r = pass * SS::ROWS_PER_PASS + warp * RPW + rsub;
-            float fh[EPL], sc = 0.f;
-            unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(hi + r * SS::ROW_BYTES), fh);
+        for (int r = 0; r < R; ++r) {
+            const int row = row_group * R + r;
+            float fh[EPL], acc = 0.f;
+            unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(hi + row * SS::ROW_BYTES), fh);
             if constexpr (KIND == KIND_QUEST) {
                 float fl[EPL];
-                unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(lo + r * SS::ROW_BYTES), fl);
+                unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(lo + row * SS::ROW_BYTES), fl);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) sc = fmaf(cp[e], fh[e], fmaf(cn[e], fl[e], sc));
+                for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], fmaf(cn[e], fl[e], acc));
             } else {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) sc = fmaf(cp[e], fh[e], sc);
+                for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], acc);
             }
+            part[r] = acc;
+        }
+        group_reduce_transposed<R, LPR>(part, lane);
+        {
+            constexpr int OUT = R >= LPR ? R / LPR : 1;
+            constexpr int SPREAD = R >= LPR ? 1 : LPR / R;
+            float* srow = a.scores + size_t(c.u) * a.n_cand + c.cand0;
+            if (sub % SPREAD == 0) {
 #pragma unroll
-            for (int m = LPR / 2; m >= 1; m >>= 1) sc += __shfl_xor_sync(kFullMask, sc, m);
-            if (sub == 0 && r < c.nrows) srow[r] = sc;
+                for (int i = 0; i < OUT; ++i) {
+                    const int r = R >= LPR ? sub * (R / LPR) + i : sub / SPREAD;
+                    const int row = row_group * R + r;
+                    if (row < c.nrows) srow[row] = part[i];
+                }
+            }
         }
         seg_slots += uint32_t(c.nslots);
         __syncthreads();   // stage s fully read; this chunk's scores written
-        if (lane == 0 && cid + kStages < c_end) issue_mine(cid + kStages);
+        if (lane == 0 && cid + stages < c_end) issue_mine(cid + stages);
 
         // end of this CTA's segment of unit c.u: report it; the completing CTA selects
         const bool seg_end = cid + 1 == c_end || (cid + 1) / a.chunks_per_unit != c.u;
         if (seg_end) {
             if (tid == 0) {
-                __threadfence();
-                const uint32_t before = atomicAdd(&a.counters[c.u], seg_slots);
+                const uint32_t before = atomic_add_acq_rel(&a.counters[c.u], seg_slots);
                 s_topk_unit = (before + seg_slots == uint32_t(a.n_cand)) ? c.u : -1;
             }
             seg_slots = 0;
             __syncthreads();
             const int tu = s_topk_unit;
             if (tu >= 0) {
-                __threadfence();
                 if (tid == 0) {
                     a.counters[tu] = 0u;   // every slot of this unit is scored
                     s_nvalid = 0;
@@ -421,16 +479,21 @@ cudaError_t launch_select_t(const SelectArgs& a0, int units, cudaStream_t s)
     a.chunks_per_group = (a.group_rows + SS::ROWS - 1) / SS::ROWS;
     a.chunks_per_unit = a.groups * a.chunks_per_group;
     a.total_chunks = units * a.chunks_per_unit;
-    const size_t smem = size_t(kStages) * kStageBytes + size_t(a.n_cand) * sizeof(uint32_t);
+    const size_t keys_bytes = size_t(a.n_cand) * sizeof(uint32_t);
+    // two CTAs per SM when they fit: dynamic stages + keys, plus static (histogram) and
+    // the per-CTA reservation
+    constexpr size_t kStatic = 10 * 1024;
+    a.stages = (2 * (3 * size_t(kStageBytes) + keys_bytes + kStatic) <= size_t(kSmemPerSm)) ? 3 : 2;
+    const size_t smem = size_t(a.stages) * kStageBytes + keys_bytes;
     static bool configured = false;   // once per instantiation, before any graph capture
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(select_kernel<KIND, MBF16, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(kStages * kStageBytes + kMaxSelectKeys * sizeof(uint32_t)));
+                                             int(2 * kStageBytes + kMaxSelectKeys * sizeof(uint32_t)));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int per_sm = smem + 4096 <= (kSmemPerSm / 2) ? 2 : 1;
+    const int per_sm = (2 * (smem + kStatic) <= size_t(kSmemPerSm)) ? 2 : 1;
     int ctas = num_sms() * per_sm;
     if (ctas > a.total_chunks) ctas = a.total_chunks;
     select_kernel<KIND, MBF16, D><<<dim3(unsigned(ctas)), kSelThreads, smem, s>>>(a);
