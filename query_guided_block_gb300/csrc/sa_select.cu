@@ -81,30 +81,36 @@ __device__ __forceinline__ int candidate_row(const SelectArgs& a, int u, int c)
 }
 
 // ------------------------------------------------------------- top-k ----
-// Runs in one CTA.  keys[0..n) hold order keys (0 = not a candidate).
+// Runs in one CTA.  keys[0..n) hold order keys (0 = not a candidate); candidate order
+// is block-id order.  Finds the k-th candidate (T, cT) in (key desc, index asc) order;
+// the selection is then {c : key > T, or key == T and c <= cT}.
 //
-// Radix select with digits taken below the common prefix of the candidates' keys:
-// the keys of one unit share their top bits (same sign, nearby exponents), so the
-// first digit starts where the smallest and largest key differ.  11-bit digits,
-// 2048-bin shared-memory histograms, at most three passes; a pass ends the search
-// as soon as the boundary bin holds exactly the remaining count.
+// Radix passes take 11-bit digits below the common prefix of the candidates' keys
+// (2048-bin shared-memory histograms).  As soon as the boundary bin holds at most
+// kGather candidates they are gathered and ranked directly; if it holds exactly the
+// remaining count, every key of that bin is in.
 __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n, int n_valid)
 {
     constexpr int kBins = 2048;
     constexpr int kBinsPerThread = kBins / kSelThreads;
+    constexpr int kGather = kSelThreads;
     __shared__ uint32_t hist[kBins];
-    __shared__ uint32_t s_bin, s_above, s_binc, s_lo, s_hi;
+    __shared__ uint32_t s_bin, s_above, s_binc, s_lo, s_hi, s_T;
+    __shared__ int s_cT, s_ng;
+    __shared__ uint32_t g_key[kGather];
+    __shared__ int g_idx[kGather];
     __shared__ int s_wtot[kSelWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k_eff = min(a.k, n_valid);
     int32_t* out = a.out_ids + size_t(u) * a.out_stride;
 
-    uint32_t prefix = 0, mask = 0;
+    // mode 0: none / all candidates; 1: (key & mask) >= prefix; 2: threshold (T, cT)
+    int mode = 0;
+    uint32_t prefix = 0, mask = 0, T = 0;
+    int cT = -1;
     int krem = k_eff;
-    bool all_of_prefix = true;         // k_eff == n_valid (or 0): every candidate / none
     if (k_eff > 0 && k_eff < n_valid) {
-        // common prefix of the candidates' keys
         if (tid == 0) { s_lo = 0xffffffffu; s_hi = 0u; }
         __syncthreads();
         uint32_t lo = 0xffffffffu, hi = 0u;
@@ -124,8 +130,9 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
         int low_bits = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
         mask = low_bits >= 32 ? 0u : ~((1u << low_bits) - 1u);
         prefix = hi & mask;
-        all_of_prefix = false;
-        while (low_bits > 0) {
+        uint32_t binc = uint32_t(n_valid);   // candidates matching the current prefix
+        while (true) {
+            if (binc <= uint32_t(kGather) || low_bits == 0) break;
             const int w = min(11, low_bits);
             const int shift = low_bits - w;
             const uint32_t dmask = (1u << w) - 1u;
@@ -171,72 +178,89 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
             prefix |= s_bin << shift;
             mask |= dmask << shift;
             low_bits = shift;
-            if (int(s_binc) == krem) {
-                all_of_prefix = true;   // every key with this prefix is selected
-                break;
-            }
-            __syncthreads();   // s_wtot / s_bin are rewritten by the next pass
+            binc = s_binc;
+            __syncthreads();   // s_wtot / s_bin are rewritten below
+            if (int(binc) == krem) break;
         }
+        if (int(binc) == krem) {
+            mode = 1;   // the whole boundary bin is in
+        } else if (binc <= uint32_t(kGather)) {
+            // gather the boundary candidates and rank them by (key desc, index asc)
+            if (tid == 0) s_ng = 0;
+            __syncthreads();
+            for (int c = tid; c < n; c += kSelThreads) {
+                const uint32_t key = keys[c];
+                if (key != 0u && (key & mask) == prefix) {
+                    const int slot = atomicAdd(&s_ng, 1);
+                    g_key[slot] = key;
+                    g_idx[slot] = c;
+                }
+            }
+            __syncthreads();
+            const int ng = s_ng;
+            if (tid < ng) {
+                const uint32_t mk = g_key[tid];
+                const int mi = g_idx[tid];
+                int rank = 0;
+                for (int j = 0; j < ng; ++j)
+                    rank += (g_key[j] > mk) || (g_key[j] == mk && g_idx[j] < mi);
+                if (rank == krem - 1) { s_T = mk; s_cT = mi; }
+            }
+            __syncthreads();
+            mode = 2;
+            T = s_T;
+            cT = s_cT;
+        } else {
+            // more than kGather candidates share every key bit: ties on one key value;
+            // the krem lowest indices among them are in (ordered count over indices)
+            const int chunk = ((n + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;
+            const int c0 = warp * chunk, c1 = min(n, c0 + chunk);
+            int eq = 0;
+            for (int c = c0 + lane; c - lane < c1; c += 32) {
+                const bool e = c < c1 && keys[c] == prefix;
+                eq += __popc(__ballot_sync(kFullMask, e));
+            }
+            if (lane == 0) s_wtot[warp] = eq;
+            __syncthreads();
+            int run = 0;
+            for (int wv = 0; wv < warp; ++wv) run += s_wtot[wv];
+            for (int c = c0 + lane; c - lane < c1; c += 32) {
+                const bool e = c < c1 && keys[c] == prefix;
+                const uint32_t eb = __ballot_sync(kFullMask, e);
+                if (e && run + __popc(eb & lanemask_lt()) == krem - 1) s_cT = c;
+                run += __popc(eb);
+            }
+            __syncthreads();
+            mode = 2;
+            T = prefix;
+            cT = s_cT;
+        }
+    } else if (k_eff > 0) {
+        mode = 1;   // every candidate (mask = prefix = 0)
     }
-    // Threshold rule:  all_of_prefix: (key & mask) >= prefix
-    //                  otherwise:      key > T, or key == T among the first krem (by id)
-    const uint32_t T = prefix;
-    const bool need_ties = k_eff > 0 && !all_of_prefix;
 
+    auto selected = [&](int c) -> bool {
+        const uint32_t key = keys[c];
+        if (mode == 0 || key == 0u) return false;
+        if (mode == 1) return (key & mask) >= prefix;
+        return key > T || (key == T && c <= cT);
+    };
     // Each warp owns a contiguous chunk of candidates, read lane-interleaved, so ballot
     // order is candidate order.
     const int chunk = ((n + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;
     const int c0 = warp * chunk, c1 = min(n, c0 + chunk);
-
-    int eq_base = 0;
-    if (need_ties) {
-        int eq = 0;
-        for (int c = c0 + lane; c - lane < c1; c += 32) {
-            const bool e = c < c1 && keys[c] == T;
-            eq += __popc(__ballot_sync(kFullMask, e));
-        }
-        if (lane == 0) s_wtot[warp] = eq;
-        __syncthreads();
-        for (int w = 0; w < warp; ++w) eq_base += s_wtot[w];
-        __syncthreads();
-    }
-    auto selected = [&](int c, int eq_rank) -> bool {
-        const uint32_t key = keys[c];
-        if (k_eff == 0 || key == 0u) return false;
-        if (all_of_prefix) return (key & mask) >= prefix;
-        return key > T || (key == T && eq_rank < krem);
-    };
-    // count per warp
     int cnt = 0;
-    {
-        int eq_run = eq_base;
-        for (int c = c0 + lane; c - lane < c1; c += 32) {
-            const bool in = c < c1;
-            const bool e = in && need_ties && keys[c] == T;
-            const uint32_t eb = __ballot_sync(kFullMask, e);
-            const int rank = eq_run + __popc(eb & lanemask_lt());
-            const bool s = in && selected(c, rank);
-            cnt += __popc(__ballot_sync(kFullMask, s));
-            eq_run += __popc(eb);
-        }
-    }
+    for (int c = c0 + lane; c - lane < c1; c += 32)
+        cnt += __popc(__ballot_sync(kFullMask, c < c1 && selected(c)));
     if (lane == 0) s_wtot[warp] = cnt;
     __syncthreads();
     int pos = 0;
-    for (int w = 0; w < warp; ++w) pos += s_wtot[w];
-    {
-        int eq_run = eq_base;
-        for (int c = c0 + lane; c - lane < c1; c += 32) {
-            const bool in = c < c1;
-            const bool e = in && need_ties && keys[c] == T;
-            const uint32_t eb = __ballot_sync(kFullMask, e);
-            const int rank = eq_run + __popc(eb & lanemask_lt());
-            const bool s = in && selected(c, rank);
-            const uint32_t sb = __ballot_sync(kFullMask, s);
-            if (s) out[pos + __popc(sb & lanemask_lt())] = candidate_row(a, u, c);
-            pos += __popc(sb);
-            eq_run += __popc(eb);
-        }
+    for (int wv = 0; wv < warp; ++wv) pos += s_wtot[wv];
+    for (int c = c0 + lane; c - lane < c1; c += 32) {
+        const bool sl = c < c1 && selected(c);
+        const uint32_t sb = __ballot_sync(kFullMask, sl);
+        if (sl) out[pos + __popc(sb & lanemask_lt())] = candidate_row(a, u, c);
+        pos += __popc(sb);
     }
     for (int i = tid; i < a.win_count; i += kSelThreads) out[k_eff + i] = a.win_first + i;
     if (tid == 0) a.out_count[u] = k_eff + a.win_count;
