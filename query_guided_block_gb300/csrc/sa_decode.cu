@@ -28,6 +28,10 @@
 //     count merges the unit's partials (log-sum-exp) into fp32 outputs.
 // GQA tiles are G x tokens: far too narrow for a tensor-core tile to pay (>= 64 rows),
 // and the kernel is HBM-bound at ~2 FMA per byte, so the contraction stays on FMA units.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
 #include "sa_common.cuh"
 #include "sa_internal.h"
 
@@ -81,6 +85,43 @@ struct DecodeShape {
 size_t decode_fixed_smem(int G, int item_tokens)
 {
     return size_t(2) * G * item_tokens * sizeof(float) + size_t(2) * kMaxRangeBlocks * sizeof(int);
+}
+
+// The CTA that completed unit u merges the unit's partials.  A unit's segments start
+// at its first item and at every CTA range start inside it; each segment wrote one
+// (m, l, o) partial at the slot of its first item.
+__device__ void merge_unit(const DecodeArgs& a, int u, int G, int D)
+{
+    if (threadIdx.x == 0) a.counters[u] = 0u;
+    const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+    const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
+    const int ipu = a.items_per_unit;
+    const int x0 = u * ipu, x1 = x0 + ipu;
+    const long long T = a.total_items, C = gridDim.x;
+    int c0 = int((long long)x0 * C / T);                         // CTA holding item x0
+    while (c0 + 1 < C && (T * (c0 + 1)) / C <= x0) ++c0;
+    while (c0 > 0 && (T * c0) / C > x0) --c0;
+    for (int i = threadIdx.x; i < G * D; i += kDecThreads) {
+        const int g = i / D, d = i - g * D;
+        const size_t h = head0 + g;
+        float mx = -INFINITY;
+        for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
+            const int slot = int(max((T * c) / C, (long long)x0) - x0);
+            mx = fmaxf(mx, __ldcg(a.part_m + h * ipu + slot));
+        }
+        float num = 0.f, den = 0.f;
+        if (mx != -INFINITY) {
+            for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
+                const int slot = int(max((T * c) / C, (long long)x0) - x0);
+                const float ms = __ldcg(a.part_m + h * ipu + slot);
+                if (ms == -INFINITY) continue;
+                const float wgt = fast_exp2(ms - mx);
+                den = fmaf(wgt, __ldcg(a.part_l + h * ipu + slot), den);
+                num = fmaf(wgt, __ldcg(a.part_o + (h * ipu + slot) * D + d), num);
+            }
+        }
+        a.out[h * D + d] = den > 0.f ? num / den : 0.f;
+    }
 }
 
 template <int D, bool BF16, int G>
@@ -341,9 +382,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
             }
             __syncthreads();   // the stage buffer is free again
             if (tid == 0) {
-                __threadfence();
                 const uint32_t n = uint32_t(item - seg_first + 1);
-                const uint32_t before = atomicAdd(&a.counters[u], n);
+                const uint32_t before = atomic_add_acq_rel_u32(&a.counters[u], n);
                 s_merge_unit = before + n == uint32_t(ipu) ? u : -1;
             }
         }
@@ -363,40 +403,339 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
         __syncthreads();
         if (s_merge_unit < 0) continue;
 
-        // ---- this CTA completed unit u: merge its partials ------------------------
-        // A unit's segments start at its first item and at every CTA range start inside
-        // it; each segment wrote one partial at its first item's slot.
-        __threadfence();
-        if (tid == 0) a.counters[u] = 0u;
-        const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
-        const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
-        const int ipu = a.items_per_unit;
-        const int x0 = u * ipu, x1 = x0 + ipu;
-        const long long T = a.total_items, C = gridDim.x;
-        int c0 = int((long long)x0 * C / T);                         // CTA holding item x0
-        while (c0 + 1 < C && (T * (c0 + 1)) / C <= x0) ++c0;
-        while (c0 > 0 && (T * c0) / C > x0) --c0;
-        for (int i = tid; i < G * D; i += kDecThreads) {
-            const int g = i / D, d = i - g * D;
-            const size_t h = head0 + g;
-            float mx = -INFINITY;
-            for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
-                const int slot = int(max((T * c) / C, (long long)x0) - x0);
-                mx = fmaxf(mx, __ldcg(a.part_m + h * ipu + slot));
-            }
-            float num = 0.f, den = 0.f;
-            if (mx != -INFINITY) {
-                for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
-                    const int slot = int(max((T * c) / C, (long long)x0) - x0);
-                    const float ms = __ldcg(a.part_m + h * ipu + slot);
-                    if (ms == -INFINITY) continue;
-                    const float wgt = fast_exp2(ms - mx);
-                    den = fmaf(wgt, __ldcg(a.part_l + h * ipu + slot), den);
-                    num = fmaf(wgt, __ldcg(a.part_o + (h * ipu + slot) * D + d), num);
+        merge_unit(a, u, G, D);
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 K/V: the same persistent item pipeline, with the GQA contractions on tensor
+// cores.  K and V tiles are staged by 2-D TMA tensor copies with 128-byte swizzle
+// (each (page, KV head) tile split into 64-channel halves of 128-byte rows), which
+// makes the 8-row ldmatrix accesses below conflict-free.
+//   S = Q K^T : mma.sync m16n8k16, rows = the G query heads (padded to 16),
+//               columns = 8 tokens per tile, warps split the item's tokens;
+//   O += P V  : rows = heads, columns = 8 channels per tile, k = 16 tokens,
+//               warps split the head dimension, so no cross-warp reduction;
+//               P enters as a bf16 hi + lo pair (two MMAs), so the weights keep
+//               ~16 mantissa bits; accumulation is fp32 throughout.
+// A bf16 query is exact in the MMA; an fp32 query is split into hi + lo too.
+constexpr int kRowBytes = 128;   // one 64-channel half of a token row
+
+__device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk)
+{
+    // 128-byte swizzle: the 16-byte chunk index is XOR-ed with the row index mod 8
+    return half_base + uint32_t(token) * kRowBytes + uint32_t((chunk ^ (token & 7)) << 4);
+}
+
+template <int D, int G, bool QSPLIT>
+__global__ void __launch_bounds__(kDecThreads, 2)
+decode_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v)
+{
+    constexpr int HALVES = D / 64;
+    constexpr int DT = D / 8;                      // 8-channel tiles
+    constexpr int DT_PER_WARP = DT / kDecWarps;    // 2 (D = 128) or 1 (D = 64)
+    static_assert(DT % kDecWarps == 0, "channel tiles must split over the warps");
+    static_assert(G <= 8, "query rows live in the first 8 MMA rows");
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g4 = lane >> 2, t4 = lane & 3;       // MMA fragment coordinates
+    const int bpi = a.blocks_per_item;
+    const int item_tokens = bpi * a.bs;
+    const uint32_t half_bytes = uint32_t(item_tokens) * kRowBytes;
+    const uint32_t stage_bytes = 2u * HALVES * half_bytes;
+    const int p_pitch = item_tokens + 8;           // bf16 elements per P row (bank spread)
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzled tiles need 1024-byte alignment
+    unsigned char* smem = smem_raw + (base - raw);
+    float* s_s = reinterpret_cast<float*>(smem + a.stages * stage_bytes);       // [G][item_tokens]
+    uint16_t* p_s = reinterpret_cast<uint16_t*>(s_s + G * item_tokens);       // [2][G][p_pitch]
+    int* blk_page = reinterpret_cast<int*>(p_s + 2 * G * p_pitch + 8);         // [range blocks]
+    int* blk_valid = blk_page + kMaxRangeBlocks;
+    __shared__ __align__(8) uint64_t full[4], empty[4];
+    __shared__ float s_alpha[8];
+    __shared__ int s_counts[64];
+    __shared__ int s_merge_unit;
+
+    const int i_begin = int((long long)a.total_items * blockIdx.x / gridDim.x);
+    const int i_end = int((long long)a.total_items * (blockIdx.x + 1) / gridDim.x);
+    if (i_begin >= i_end) return;
+    const int u_lo = i_begin / a.items_per_unit;
+    const int u_hi = (i_end - 1) / a.items_per_unit;
+
+    // ---- resolve the range: counts, selected ids -> pages ---------------------
+    for (int u = u_lo + tid; u <= u_hi; u += kDecThreads) {
+        int count = a.sel_count[u];
+        if (count < 0 || count > a.sel_stride) {
+            raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
+            count = count < 0 ? 0 : a.sel_stride;
+        }
+        s_counts[u - u_lo] = count;
+    }
+    __syncthreads();
+    const int n_range_blocks = (i_end - i_begin) * bpi;
+    for (int e = tid; e < n_range_blocks; e += kDecThreads) {
+        const int item = i_begin + e / bpi;
+        const int u = item / a.items_per_unit;
+        const int slot = (item - u * a.items_per_unit) * bpi + e % bpi;
+        int page = -1, valid = 0;
+        if (slot < s_counts[u - u_lo]) {
+            const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
+            if (j < 0 || j >= a.nb) {
+                raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
+            } else {
+                const int p = a.block_table[size_t(u / a.Hkv) * a.nb + j];
+                if (p < 0 || p >= a.num_pages) {
+                    raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
+                } else {
+                    page = p;
+                    valid = min(a.bs, a.N - j * a.bs);
                 }
             }
-            a.out[h * D + d] = den > 0.f ? num / den : 0.f;
         }
+        blk_page[e] = page;
+        blk_valid[e] = valid;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kDecWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // An item's copies: for each block j, K and V, each channel half -> 4 * bpi (D = 128).
+    // Copy i of the item in stage s is issued by warp (s * n + i) mod 8.
+    const int n_copies = 2 * HALVES * bpi;
+    auto issue_mine = [&](int item) {   // every warp's lane 0
+        const int k = item - i_begin;
+        const int s = k % a.stages;
+        const uint32_t kd = base + s * stage_bytes;
+        const uint32_t vd = kd + HALVES * half_bytes;
+        const int kvh = (item / a.items_per_unit) % a.Hkv;
+        for (int i = 0; i < n_copies; ++i) {
+            if ((s * n_copies + i) % kDecWarps != warp) continue;
+            if (i == 0) {
+                uint32_t nbytes = 0;
+                for (int j = 0; j < bpi; ++j)
+                    nbytes += blk_page[k * bpi + j] >= 0 ? uint32_t(a.bs) * kRowBytes : 0u;
+                mbar_arrive_expect_tx(&full[s], 2 * HALVES * nbytes);
+            }
+            const int j = i / (2 * HALVES), rem = i % (2 * HALVES);
+            const int is_v = rem / HALVES, h = rem % HALVES;
+            const int page = blk_page[k * bpi + j];
+            if (page < 0) continue;
+            const int row = (page * a.Hkv + kvh) * a.bs;
+            const uint32_t dst = (is_v ? vd : kd) + h * half_bytes + uint32_t(j * a.bs) * kRowBytes;
+            tma_load_2d(smem_raw + (dst - raw), is_v ? (const void*)&tmap_v : (const void*)&tmap_k,
+                        h * 64, row, &full[s]);
+        }
+    };
+    if (lane == 0)
+        for (int item = i_begin; item < i_end && item < i_begin + a.stages; ++item) issue_mine(item);
+
+    // query A-fragments (rows g4 < G), per 16-channel k-step: a0 = (g4, 2t4..), a2 = (g4, 2t4+8..)
+    uint32_t qa0[D / 16], qa2[D / 16];                       // bf16 (hi) part
+    uint32_t qb0[QSPLIT ? D / 16 : 1], qb2[QSPLIT ? D / 16 : 1];  // lo part (fp32 query)
+    float acc[DT_PER_WARP][4];
+    float m_run = -INFINITY, l_run = 0.f;   // warp g < G keeps head g's statistics
+    int cur_u = -1, seg_first = 0;
+
+    for (int item = i_begin; item < i_end; ++item) {
+        const int k = item - i_begin;
+        const int s = k % a.stages;
+        const uint32_t parity = uint32_t(k / a.stages) & 1u;
+        const int u = item / a.items_per_unit;
+        if (u != cur_u) {
+            cur_u = u;
+            seg_first = item;
+            const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                float f[4] = {0.f, 0.f, 0.f, 0.f};
+                if (g4 < G) {
+                    const size_t qrow = (size_t(b) * a.Hq + size_t(kvh) * G + g4) * D + ks * 16 + 2 * t4;
+                    f[0] = load_q(a.q, qrow, a.q_bf16 != 0);
+                    f[1] = load_q(a.q, qrow + 1, a.q_bf16 != 0);
+                    f[2] = load_q(a.q, qrow + 8, a.q_bf16 != 0);
+                    f[3] = load_q(a.q, qrow + 9, a.q_bf16 != 0);
+                }
+                qa0[ks] = pack_bf16x2(f[0], f[1]);
+                qa2[ks] = pack_bf16x2(f[2], f[3]);
+                if constexpr (QSPLIT) {   // remainder after bf16 rounding
+                    qb0[ks] = pack_bf16x2(f[0] - bf16_lo(qa0[ks]), f[1] - bf16_hi(qa0[ks]));
+                    qb2[ks] = pack_bf16x2(f[2] - bf16_lo(qa2[ks]), f[3] - bf16_hi(qa2[ks]));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < DT_PER_WARP; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+            m_run = -INFINITY;
+            l_run = 0.f;
+        }
+        const uint32_t ks_base = base + s * stage_bytes;
+        const uint32_t vs_base = ks_base + HALVES * half_bytes;
+        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+
+        // tokens that carry no data (empty block slots, tail past the context): zero
+        // their V rows so 0-weight products stay 0 in the MMA
+        bool ragged = false;
+        for (int j = 0; j < bpi; ++j) ragged |= blk_valid[k * bpi + j] < a.bs;
+        if (ragged) {
+            for (int e = tid; e < item_tokens * HALVES * (kRowBytes / 16); e += kDecThreads) {
+                const int t = e / (HALVES * (kRowBytes / 16));
+                const int r = e % (HALVES * (kRowBytes / 16));
+                const int j = t / a.bs;
+                if ((t - j * a.bs) < blk_valid[k * bpi + j]) continue;
+                const int h = r / (kRowBytes / 16), c = r % (kRowBytes / 16);
+                *reinterpret_cast<uint4*>(smem_raw + (vs_base + h * half_bytes + t * kRowBytes + c * 16 - raw)) =
+                    make_uint4(0, 0, 0, 0);
+            }
+            __syncthreads();
+        }
+
+        // ---- S = q K^T: warp w takes token tiles w, w + 8, ... ----------------
+        for (int nt = warp; nt < item_tokens / 8; nt += kDecWarps) {
+            const int n0 = nt * 8;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kp = 0; kp < D / 32; ++kp) {   // two 16-channel k-steps per ldmatrix.x4
+                const int ch = kp * 4 + (lane >> 3);       // 8-channel chunk of this lane's matrix
+                const uint32_t addr = swz(ks_base + (ch >> 3) * half_bytes, n0 + (lane & 7), ch & 7);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(addr, b0, b1, b2, b3);
+                mma_bf16_16816(c, qa0[2 * kp], 0u, qa2[2 * kp], 0u, b0, b1);
+                mma_bf16_16816(c, qa0[2 * kp + 1], 0u, qa2[2 * kp + 1], 0u, b2, b3);
+                if constexpr (QSPLIT) {
+                    mma_bf16_16816(c, qb0[2 * kp], 0u, qb2[2 * kp], 0u, b0, b1);
+                    mma_bf16_16816(c, qb0[2 * kp + 1], 0u, qb2[2 * kp + 1], 0u, b2, b3);
+                }
+            }
+            if (g4 < G) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = n0 + 2 * t4 + e;
+                    const int j = t / a.bs;
+                    const bool ok = (t - j * a.bs) < blk_valid[k * bpi + j];
+                    s_s[g4 * item_tokens + t] = ok ? c[e] * a.scale_log2 : -INFINITY;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- online softmax statistics: warp g owns head g ---------------------
+        if (warp < G) {
+            const int g = warp;
+            float mi = -INFINITY;
+            for (int t = lane; t < item_tokens; t += 32) mi = fmaxf(mi, s_s[g * item_tokens + t]);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) mi = fmaxf(mi, __shfl_xor_sync(kFullMask, mi, off));
+            const float m_new = fmaxf(m_run, mi);
+            const float alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+            float li = 0.f;
+            for (int t = lane; t < item_tokens; t += 32) {
+                const float x = s_s[g * item_tokens + t];
+                const float p = (x == -INFINITY) ? 0.f : fast_exp2(x - m_new);
+                const uint32_t hi = pack_bf16x2(p, 0.f) & 0xffffu;
+                const float rest = p - __uint_as_float(hi << 16);
+                p_s[g * p_pitch + t] = uint16_t(hi);
+                p_s[(G + g) * p_pitch + t] = uint16_t(pack_bf16x2(rest, 0.f) & 0xffffu);
+                li += p;
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) li += __shfl_xor_sync(kFullMask, li, off);
+            l_run = l_run * alpha + li;
+            m_run = m_new;
+            if (lane == 0) s_alpha[g] = alpha;
+        }
+        __syncthreads();
+
+        // ---- O += P V: warp w owns channel tiles w * DT_PER_WARP .. ---------------
+        {
+            const float al = g4 < G ? s_alpha[g4] : 0.f;
+#pragma unroll
+            for (int j = 0; j < DT_PER_WARP; ++j) {
+                acc[j][0] *= al;
+                acc[j][1] *= al;
+            }
+            const uint32_t* p32 = reinterpret_cast<const uint32_t*>(p_s);
+            for (int kk = 0; kk < item_tokens / 16; ++kk) {
+                const int k0 = kk * 16;
+                uint32_t ah0 = 0, ah2 = 0, al0 = 0, al2 = 0;
+                if (g4 < G) {
+                    ah0 = p32[(g4 * p_pitch + k0 + 2 * t4) >> 1];
+                    ah2 = p32[(g4 * p_pitch + k0 + 8 + 2 * t4) >> 1];
+                    al0 = p32[((G + g4) * p_pitch + k0 + 2 * t4) >> 1];
+                    al2 = p32[((G + g4) * p_pitch + k0 + 8 + 2 * t4) >> 1];
+                }
+#pragma unroll
+                for (int jp = 0; jp < DT_PER_WARP; jp += 2) {
+                    // matrices: (tokens k0.., ch c), (tokens k0+8.., ch c), (k0.., c+1), (k0+8.., c+1)
+                    const int mtx = lane >> 3;
+                    const int tok = k0 + (mtx & 1) * 8 + (lane & 7);
+                    const int chunk = (warp * DT_PER_WARP + jp) + (mtx >> 1);
+                    const uint32_t addr = swz(vs_base + (chunk >> 3) * half_bytes, tok, chunk & 7);
+                    uint32_t r0, r1, r2 = 0, r3 = 0;
+                    if constexpr (DT_PER_WARP >= 2) ldsm_x4_trans(addr, r0, r1, r2, r3);
+                    else ldsm_x2_trans(addr, r0, r1);   // lanes 0..15 address the two matrices
+                    mma_bf16_16816(acc[jp], ah0, 0u, ah2, 0u, r0, r1);
+                    mma_bf16_16816(acc[jp], al0, 0u, al2, 0u, r0, r1);
+                    if constexpr (DT_PER_WARP >= 2) {
+                        mma_bf16_16816(acc[jp + 1], ah0, 0u, ah2, 0u, r2, r3);
+                        mma_bf16_16816(acc[jp + 1], al0, 0u, al2, 0u, r2, r3);
+                    }
+                }
+            }
+        }
+
+        const bool seg_end = item + 1 == i_end || (item + 1) / a.items_per_unit != u;
+        if (seg_end) {
+            // ---- end of this CTA's segment of unit u: one partial (no reduction) --
+            const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+            const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
+            const int slot = seg_first - u * a.items_per_unit;
+            const int ipu = a.items_per_unit;
+            if (g4 < G) {
+#pragma unroll
+                for (int j = 0; j < DT_PER_WARP; ++j) {
+                    const int ch = (warp * DT_PER_WARP + j) * 8 + 2 * t4;
+                    float* dst = a.part_o + ((head0 + g4) * ipu + slot) * D + ch;
+                    *reinterpret_cast<float2*>(dst) = make_float2(acc[j][0], acc[j][1]);
+                }
+            }
+            if (warp < G && lane == 0) {
+                a.part_m[(head0 + warp) * ipu + slot] = m_run;
+                a.part_l[(head0 + warp) * ipu + slot] = l_run;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                const uint32_t n = uint32_t(item - seg_first + 1);
+                const uint32_t before = atomic_add_acq_rel_u32(&a.counters[u], n);
+                s_merge_unit = before + n == uint32_t(ipu) ? u : -1;
+            }
+        }
+        // release the stage; its issuing warps refill it with the item kStages ahead
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&empty[s]);
+            const int nxt = item + a.stages;
+            bool mine = false;
+            for (int i = 0; i < n_copies; ++i) mine |= (s * n_copies + i) % kDecWarps == warp;
+            if (nxt < i_end && mine) {
+                if (!mbar_wait_bounded(&empty[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+                issue_mine(nxt);
+            }
+        }
+        if (!seg_end) continue;
+        __syncthreads();
+        if (s_merge_unit < 0) continue;
+        merge_unit(a, u, G, D);
         __syncthreads();
     }
 }
@@ -442,6 +781,89 @@ cudaError_t dispatch_group(const DecodeArgs& a, int G, cudaStream_t s)
     }
 }
 
+
+// ---- tensor-core path (bf16 K/V) ----------------------------------------------
+size_t mma_fixed_smem(int G, int item_tokens)
+{
+    return 1024 /* alignment slack */ + size_t(G) * item_tokens * sizeof(float) +
+           size_t(2) * G * (item_tokens + 8) * sizeof(uint16_t) + 32 + size_t(2) * kMaxRangeBlocks * sizeof(int);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// View a page pool [num_pages, Hkv, bs, D] bf16 as rows of D channels; one TMA box is
+// a 64-channel x block_size-row tile, 128-byte swizzled.
+bool make_page_map(CUtensorMap* m, const void* pages, long long rows, int D, int bs)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+    cuuint32_t box[2] = {64u, cuuint32_t(bs)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pages), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G, bool QSPLIT>
+cudaError_t launch_decode_mma_t(DecodeArgs a, const void* k_pages, const void* v_pages, cudaStream_t s)
+{
+    const int item_tokens = a.blocks_per_item * a.bs;
+    const size_t stage = size_t(2) * item_tokens * D * 2;
+    const size_t fixed = mma_fixed_smem(G, item_tokens);
+    a.stages = (2 * (3 * stage + fixed + 1024) <= size_t(kSmemPerSm)) ? 3 : 2;
+    const size_t smem = a.stages * stage + fixed;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kDecSmemLimit);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const long long rows = (long long)a.num_pages * a.Hkv * a.bs;
+    CUtensorMap tk, tv;
+    memset(&tk, 0, sizeof tk);
+    memset(&tv, 0, sizeof tv);
+    // an empty page pool issues no copy: the maps are never read
+    if (rows > 0 && k_pages && v_pages &&
+        (!make_page_map(&tk, k_pages, rows, D, a.bs) || !make_page_map(&tv, v_pages, rows, D, a.bs)))
+        return cudaErrorInvalidValue;
+    const int per_sm = (2 * (smem + 1024) <= size_t(kSmemPerSm)) ? 2 : 1;
+    long long ctas = (long long)num_sms() * per_sm;
+    const long long min_ctas = ((long long)a.total_items * a.blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
+    if (ctas < min_ctas) ctas = min_ctas;
+    const long long min_ctas_units = (a.units + 61) / 62;
+    if (ctas < min_ctas_units) ctas = min_ctas_units;
+    if (ctas > a.total_items) ctas = a.total_items;
+    decode_mma_kernel<D, G, QSPLIT><<<dim3(unsigned(ctas)), kDecThreads, smem, s>>>(a, tk, tv);
+    return cudaGetLastError();
+}
+
+template <int D, bool QSPLIT>
+cudaError_t dispatch_mma(const DecodeArgs& a, int G, const void* k_pages, const void* v_pages, cudaStream_t s)
+{
+    switch (G) {
+        case 1: return launch_decode_mma_t<D, 1, QSPLIT>(a, k_pages, v_pages, s);
+        case 2: return launch_decode_mma_t<D, 2, QSPLIT>(a, k_pages, v_pages, s);
+        case 4: return launch_decode_mma_t<D, 4, QSPLIT>(a, k_pages, v_pages, s);
+        case 8: return launch_decode_mma_t<D, 8, QSPLIT>(a, k_pages, v_pages, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 int decode_blocks_per_item(int D, bool kv_bf16, int block_size)
@@ -455,7 +877,8 @@ bool decode_supported(int D, bool kv_bf16, int block_size, int G)
     const int bpi = decode_blocks_per_item(D, kv_bf16, block_size);
     const int item_tokens = bpi * block_size;
     const size_t stage = size_t(2) * item_tokens * D * (kv_bf16 ? 2 : 4);
-    return 2 * stage + decode_fixed_smem(G, item_tokens) <= size_t(kDecSmemLimit);
+    const size_t fixed = kv_bf16 ? mma_fixed_smem(G, item_tokens) : decode_fixed_smem(G, item_tokens);
+    return 2 * stage + fixed <= size_t(kDecSmemLimit);
 }
 
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
@@ -491,9 +914,14 @@ cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.part_o = reinterpret_cast<float*>(ws + L.part_o);
     a.counters = reinterpret_cast<uint32_t*>(ws + L.dec_counters);
     a.err = reinterpret_cast<uint32_t*>(ws + L.err);
-    if (g.D == 128)
-        return g.kv_bf16 ? dispatch_group<128, true>(a, g.G, s) : dispatch_group<128, false>(a, g.G, s);
-    return g.kv_bf16 ? dispatch_group<64, true>(a, g.G, s) : dispatch_group<64, false>(a, g.G, s);
+    if (g.kv_bf16) {   // tensor-core path
+        if (g.q_bf16)
+            return g.D == 128 ? dispatch_mma<128, false>(a, g.G, k_pages, v_pages, s)
+                              : dispatch_mma<64, false>(a, g.G, k_pages, v_pages, s);
+        return g.D == 128 ? dispatch_mma<128, true>(a, g.G, k_pages, v_pages, s)
+                          : dispatch_mma<64, true>(a, g.G, k_pages, v_pages, s);
+    }
+    return g.D == 128 ? dispatch_group<128, false>(a, g.G, s) : dispatch_group<64, false>(a, g.G, s);
 }
 
 }  // namespace sa

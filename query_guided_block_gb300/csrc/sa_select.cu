@@ -347,15 +347,6 @@ __device__ __forceinline__ ChunkInfo chunk_info(const SelectArgs& a, int cid, in
     return c;
 }
 
-// Device-scope counter add with release (our scores, ordered before it by the CTA
-// barrier) and acquire (the other CTAs' scores, when we complete the count).
-__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
 template <int KIND, bool MBF16, int D>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
 {
@@ -475,7 +466,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
         const bool seg_end = cid + 1 == c_end || (cid + 1) / a.chunks_per_unit != c.u;
         if (seg_end) {
             if (tid == 0) {
-                const uint32_t before = atomic_add_acq_rel(&a.counters[c.u], seg_slots);
+                const uint32_t before = atomic_add_acq_rel_u32(&a.counters[c.u], seg_slots);
                 s_topk_unit = (before + seg_slots == uint32_t(a.n_cand)) ? c.u : -1;
             }
             seg_slots = 0;

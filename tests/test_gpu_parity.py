@@ -105,6 +105,10 @@ SMALL = [
     dict(head_dim=128, num_q_heads=8, kv_dtype=torch.bfloat16, score="mean", block_size=64),
     dict(head_dim=64, num_q_heads=8, kv_dtype=torch.float32, q_dtype=torch.float32, score="mean",
          block_size=32, n_tokens=4097),
+    dict(head_dim=128, num_q_heads=8, kv_dtype=torch.bfloat16, q_dtype=torch.float32, block_size=64,
+         n_tokens=5001),
+    dict(head_dim=64, num_q_heads=16, kv_dtype=torch.bfloat16, q_dtype=torch.float32, block_size=128,
+         n_tokens=3333, window_tokens=200),
 ]
 
 
