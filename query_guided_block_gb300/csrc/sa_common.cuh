@@ -196,6 +196,22 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only); src_bytes < 16 zero-fills the
+// rest (0: the source is not read at all).
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later async-proxy
 // (bulk copy) writes to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -28,9 +28,6 @@
 //     count merges the unit's partials (log-sum-exp) into fp32 outputs.
 // GQA tiles are G x tokens: far too narrow for a tensor-core tile to pay (>= 64 rows),
 // and the kernel is HBM-bound at ~2 FMA per byte, so the contraction stays on FMA units.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <string.h>
 
 #include "sa_common.cuh"
 #include "sa_internal.h"
@@ -42,7 +39,7 @@ constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kItemKBytes = 16 * 1024;     // K bytes per item (V the same)
 constexpr int kMaxRangeBlocks = 1024;      // page lookups a CTA caches in shared memory
-constexpr int kDecSmemLimit = 200 * 1024;  // dynamic shared memory a decode CTA may use
+constexpr int kDecSmemLimit = 224 * 1024;  // dynamic shared memory a decode CTA may use
 
 struct DecodeArgs {
     const void* q;
@@ -410,9 +407,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
 
 // ---------------------------------------------------------------------------
 // bf16 K/V: the same persistent item pipeline, with the GQA contractions on tensor
-// cores.  K and V tiles are staged by 2-D TMA tensor copies with 128-byte swizzle
-// (each (page, KV head) tile split into 64-channel halves of 128-byte rows), which
-// makes the 8-row ldmatrix accesses below conflict-free.
+// cores.  Staging: every thread issues 16-byte cp.async copies (global -> shared,
+// L2 only) of its share of the item's K and V rows into a 128-byte-swizzled layout --
+// each token row split into 64-channel halves of 128-byte rows, the 16-byte chunk index
+// XOR-ed with the row index mod 8 -- so the 8-row ldmatrix accesses below are
+// conflict-free.  Rows that carry no token (empty block slots, the tail past the
+// context) are zero-filled by the copy itself.  Per-thread copies never stall the
+// issuing warp the way a bulk copy issued per page tile did (measured: ~0.8 us per issue
+// with 4-8 KB page tiles).  kDecStages - 1 items stay in flight.
 //   S = Q K^T : mma.sync m16n8k16, rows = the G query heads (padded to 16),
 //               columns = 8 tokens per tile, warps split the item's tokens;
 //   O += P V  : rows = heads, columns = 8 channels per tile, k = 16 tokens,
@@ -421,6 +423,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
 //               ~16 mantissa bits; accumulation is fp32 throughout.
 // A bf16 query is exact in the MMA; an fp32 query is split into hi + lo too.
 constexpr int kRowBytes = 128;   // one 64-channel half of a token row
+constexpr int kDecStages = 3;
 
 __device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk)
 {
@@ -429,13 +432,12 @@ __device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk
 }
 
 template <int D, int G, bool QSPLIT>
-__global__ void __launch_bounds__(kDecThreads, 2)
-decode_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v)
+__global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a)
 {
     constexpr int HALVES = D / 64;
     constexpr int DT = D / 8;                      // 8-channel tiles
     constexpr int DT_PER_WARP = DT / kDecWarps;    // 2 (D = 128) or 1 (D = 64)
+    constexpr int CPR = D / 8;                     // 16-byte chunks per token row
     static_assert(DT % kDecWarps == 0, "channel tiles must split over the warps");
     static_assert(G <= 8, "query rows live in the first 8 MMA rows");
 
@@ -449,13 +451,12 @@ decode_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzled tiles need 1024-byte alignment
+    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle pattern repeats every 1024 bytes
     unsigned char* smem = smem_raw + (base - raw);
-    float* s_s = reinterpret_cast<float*>(smem + a.stages * stage_bytes);       // [G][item_tokens]
+    float* s_s = reinterpret_cast<float*>(smem + kDecStages * stage_bytes);    // [G][item_tokens]
     uint16_t* p_s = reinterpret_cast<uint16_t*>(s_s + G * item_tokens);       // [2][G][p_pitch]
     int* blk_page = reinterpret_cast<int*>(p_s + 2 * G * p_pitch + 8);         // [range blocks]
     int* blk_valid = blk_page + kMaxRangeBlocks;
-    __shared__ __align__(8) uint64_t full[4], empty[4];
     __shared__ float s_alpha[8];
     __shared__ int s_counts[64];
     __shared__ int s_merge_unit;
@@ -499,44 +500,33 @@ decode_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
         blk_page[e] = page;
         blk_valid[e] = valid;
     }
-    if (tid == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kDecWarps);
-        }
-        fence_mbar_init();
-    }
     __syncthreads();
 
-    // An item's copies: for each block j, K and V, each channel half -> 4 * bpi (D = 128).
-    // Copy i of the item in stage s is issued by warp (s * n + i) mod 8.
-    const int n_copies = 2 * HALVES * bpi;
-    auto issue_mine = [&](int item) {   // every warp's lane 0
+    // Stage an item: K then V, token t of the item, 16-byte chunk c of its row.
+    const char* kbase = reinterpret_cast<const char*>(a.k_pages);
+    const char* vbase = reinterpret_cast<const char*>(a.v_pages);
+    auto issue_item = [&](int item) {   // every thread
         const int k = item - i_begin;
-        const int s = k % a.stages;
-        const uint32_t kd = base + s * stage_bytes;
-        const uint32_t vd = kd + HALVES * half_bytes;
+        const uint32_t kd = base + (k % kDecStages) * stage_bytes;
         const int kvh = (item / a.items_per_unit) % a.Hkv;
-        for (int i = 0; i < n_copies; ++i) {
-            if ((s * n_copies + i) % kDecWarps != warp) continue;
-            if (i == 0) {
-                uint32_t nbytes = 0;
-                for (int j = 0; j < bpi; ++j)
-                    nbytes += blk_page[k * bpi + j] >= 0 ? uint32_t(a.bs) * kRowBytes : 0u;
-                mbar_arrive_expect_tx(&full[s], 2 * HALVES * nbytes);
-            }
-            const int j = i / (2 * HALVES), rem = i % (2 * HALVES);
-            const int is_v = rem / HALVES, h = rem % HALVES;
+        const int per_tensor = item_tokens * CPR;
+        for (int e = tid; e < 2 * per_tensor; e += kDecThreads) {
+            const int is_v = e >= per_tensor;
+            const int rem = e - is_v * per_tensor;
+            const int t = rem / CPR, c = rem - (rem / CPR) * CPR;
+            const int j = t / a.bs, r = t - (t / a.bs) * a.bs;
             const int page = blk_page[k * bpi + j];
-            if (page < 0) continue;
-            const int row = (page * a.Hkv + kvh) * a.bs;
-            const uint32_t dst = (is_v ? vd : kd) + h * half_bytes + uint32_t(j * a.bs) * kRowBytes;
-            tma_load_2d(smem_raw + (dst - raw), is_v ? (const void*)&tmap_v : (const void*)&tmap_k,
-                        h * 64, row, &full[s]);
+            const bool ok = page >= 0 && r < blk_valid[k * bpi + j];
+            const char* src = is_v ? vbase : kbase;
+            if (ok) src += ((size_t(page) * a.Hkv + kvh) * a.bs + r) * (D * 2) + c * 16;
+            const uint32_t dst = swz(kd + is_v * HALVES * half_bytes + (c >> 3) * half_bytes, t, c & 7);
+            cp_async_16_zfill(dst, src, ok ? 16u : 0u);
         }
     };
-    if (lane == 0)
-        for (int item = i_begin; item < i_end && item < i_begin + a.stages; ++item) issue_mine(item);
+    for (int kk = 0; kk < kDecStages - 1; ++kk) {
+        if (i_begin + kk < i_end) issue_item(i_begin + kk);
+        cp_async_commit();
+    }
 
     // query A-fragments (rows g4 < G), per 16-channel k-step: a0 = (g4, 2t4..), a2 = (g4, 2t4+8..)
     uint32_t qa0[D / 16], qa2[D / 16];                       // bf16 (hi) part
@@ -547,8 +537,7 @@ decode_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
 
     for (int item = i_begin; item < i_end; ++item) {
         const int k = item - i_begin;
-        const int s = k % a.stages;
-        const uint32_t parity = uint32_t(k / a.stages) & 1u;
+        const int s = k % kDecStages;
         const int u = item / a.items_per_unit;
         if (u != cur_u) {
             cur_u = u;
@@ -580,24 +569,12 @@ decode_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
         }
         const uint32_t ks_base = base + s * stage_bytes;
         const uint32_t vs_base = ks_base + HALVES * half_bytes;
-        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
-
-        // tokens that carry no data (empty block slots, tail past the context): zero
-        // their V rows so 0-weight products stay 0 in the MMA
-        bool ragged = false;
-        for (int j = 0; j < bpi; ++j) ragged |= blk_valid[k * bpi + j] < a.bs;
-        if (ragged) {
-            for (int e = tid; e < item_tokens * HALVES * (kRowBytes / 16); e += kDecThreads) {
-                const int t = e / (HALVES * (kRowBytes / 16));
-                const int r = e % (HALVES * (kRowBytes / 16));
-                const int j = t / a.bs;
-                if ((t - j * a.bs) < blk_valid[k * bpi + j]) continue;
-                const int h = r / (kRowBytes / 16), c = r % (kRowBytes / 16);
-                *reinterpret_cast<uint4*>(smem_raw + (vs_base + h * half_bytes + t * kRowBytes + c * 16 - raw)) =
-                    make_uint4(0, 0, 0, 0);
-            }
-            __syncthreads();
-        }
+        // this item's copies (this thread's) are done; after the barrier everyone's are,
+        // and every thread has finished the previous item, whose stage is refilled now
+        cp_async_wait_group<kDecStages - 2>();
+        __syncthreads();
+        if (item + kDecStages - 1 < i_end) issue_item(item + kDecStages - 1);
+        cp_async_commit();
 
         // ---- S = q K^T: warp w takes token tiles w, w + 8, ... ----------------
         for (int nt = warp; nt < item_tokens / 8; nt += kDecWarps) {
@@ -719,25 +696,13 @@ decode_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
                 s_merge_unit = before + n == uint32_t(ipu) ? u : -1;
             }
         }
-        // release the stage; its issuing warps refill it with the item kStages ahead
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&empty[s]);
-            const int nxt = item + a.stages;
-            bool mine = false;
-            for (int i = 0; i < n_copies; ++i) mine |= (s * n_copies + i) % kDecWarps == warp;
-            if (nxt < i_end && mine) {
-                if (!mbar_wait_bounded(&empty[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
-                issue_mine(nxt);
-            }
-        }
         if (!seg_end) continue;
         __syncthreads();
         if (s_merge_unit < 0) continue;
         merge_unit(a, u, G, D);
         __syncthreads();
     }
+    cp_async_wait_group<0>();
 }
 
 template <int D, bool BF16, int G>
@@ -789,43 +754,12 @@ size_t mma_fixed_smem(int G, int item_tokens)
            size_t(2) * G * (item_tokens + 8) * sizeof(uint16_t) + 32 + size_t(2) * kMaxRangeBlocks * sizeof(int);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// View a page pool [num_pages, Hkv, bs, D] bf16 as rows of D channels; one TMA box is
-// a 64-channel x block_size-row tile, 128-byte swizzled.
-bool make_page_map(CUtensorMap* m, const void* pages, long long rows, int D, int bs)
-{
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
-    cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-    cuuint32_t box[2] = {64u, cuuint32_t(bs)};
-    cuuint32_t estr[2] = {1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pages), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int G, bool QSPLIT>
-cudaError_t launch_decode_mma_t(DecodeArgs a, const void* k_pages, const void* v_pages, cudaStream_t s)
+cudaError_t launch_decode_mma_t(DecodeArgs a, cudaStream_t s)
 {
     const int item_tokens = a.blocks_per_item * a.bs;
     const size_t stage = size_t(2) * item_tokens * D * 2;
-    const size_t fixed = mma_fixed_smem(G, item_tokens);
-    a.stages = (2 * (3 * stage + fixed + 1024) <= size_t(kSmemPerSm)) ? 3 : 2;
-    const size_t smem = a.stages * stage + fixed;
+    const size_t smem = kDecStages * stage + mma_fixed_smem(G, item_tokens);
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -833,14 +767,6 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, const void* k_pages, const void* v
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const long long rows = (long long)a.num_pages * a.Hkv * a.bs;
-    CUtensorMap tk, tv;
-    memset(&tk, 0, sizeof tk);
-    memset(&tv, 0, sizeof tv);
-    // an empty page pool issues no copy: the maps are never read
-    if (rows > 0 && k_pages && v_pages &&
-        (!make_page_map(&tk, k_pages, rows, D, a.bs) || !make_page_map(&tv, v_pages, rows, D, a.bs)))
-        return cudaErrorInvalidValue;
     const int per_sm = (2 * (smem + 1024) <= size_t(kSmemPerSm)) ? 2 : 1;
     long long ctas = (long long)num_sms() * per_sm;
     const long long min_ctas = ((long long)a.total_items * a.blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
@@ -848,7 +774,7 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, const void* k_pages, const void* v
     const long long min_ctas_units = (a.units + 61) / 62;
     if (ctas < min_ctas_units) ctas = min_ctas_units;
     if (ctas > a.total_items) ctas = a.total_items;
-    decode_mma_kernel<D, G, QSPLIT><<<dim3(unsigned(ctas)), kDecThreads, smem, s>>>(a, tk, tv);
+    decode_mma_kernel<D, G, QSPLIT><<<dim3(unsigned(ctas)), kDecThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -856,10 +782,10 @@ template <int D, bool QSPLIT>
 cudaError_t dispatch_mma(const DecodeArgs& a, int G, const void* k_pages, const void* v_pages, cudaStream_t s)
 {
     switch (G) {
-        case 1: return launch_decode_mma_t<D, 1, QSPLIT>(a, k_pages, v_pages, s);
-        case 2: return launch_decode_mma_t<D, 2, QSPLIT>(a, k_pages, v_pages, s);
-        case 4: return launch_decode_mma_t<D, 4, QSPLIT>(a, k_pages, v_pages, s);
-        case 8: return launch_decode_mma_t<D, 8, QSPLIT>(a, k_pages, v_pages, s);
+        case 1: return launch_decode_mma_t<D, 1, QSPLIT>(a, s);
+        case 2: return launch_decode_mma_t<D, 2, QSPLIT>(a, s);
+        case 4: return launch_decode_mma_t<D, 4, QSPLIT>(a, s);
+        case 8: return launch_decode_mma_t<D, 8, QSPLIT>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -877,8 +803,8 @@ bool decode_supported(int D, bool kv_bf16, int block_size, int G)
     const int bpi = decode_blocks_per_item(D, kv_bf16, block_size);
     const int item_tokens = bpi * block_size;
     const size_t stage = size_t(2) * item_tokens * D * (kv_bf16 ? 2 : 4);
-    const size_t fixed = kv_bf16 ? mma_fixed_smem(G, item_tokens) : decode_fixed_smem(G, item_tokens);
-    return 2 * stage + fixed <= size_t(kDecSmemLimit);
+    if (kv_bf16) return 3 * stage + mma_fixed_smem(G, item_tokens) <= size_t(kDecSmemLimit);
+    return 2 * stage + decode_fixed_smem(G, item_tokens) <= size_t(kDecSmemLimit);
 }
 
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
