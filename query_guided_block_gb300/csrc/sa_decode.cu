@@ -453,11 +453,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle pattern repeats every 1024 bytes
     unsigned char* smem = smem_raw + (base - raw);
-    float* s_s = reinterpret_cast<float*>(smem + kDecStages * stage_bytes);    // [G][item_tokens]
-    uint16_t* p_s = reinterpret_cast<uint16_t*>(s_s + G * item_tokens);       // [2][G][p_pitch]
+    uint16_t* p_s = reinterpret_cast<uint16_t*>(smem + kDecStages * stage_bytes);   // [2][G][p_pitch]
     int* blk_page = reinterpret_cast<int*>(p_s + 2 * G * p_pitch + 8);         // [range blocks]
     int* blk_valid = blk_page + kMaxRangeBlocks;
-    __shared__ float s_alpha[8];
+    __shared__ float red_m[kDecWarps][8], red_l[kDecWarps][8];   // per-warp max / sum per head
     __shared__ int s_counts[64];
     __shared__ int s_merge_unit;
 
@@ -502,25 +501,31 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a
     }
     __syncthreads();
 
-    // Stage an item: K then V, token t of the item, 16-byte chunk c of its row.
+    // Stage an item: K then V rows of its tokens, 16-byte chunks.  Thread tid always
+    // copies chunk c = tid % CPR of tokens tid / CPR + i * (256 / CPR); the swizzle term
+    // (c ^ token) & 7 is therefore constant per thread.
     const char* kbase = reinterpret_cast<const char*>(a.k_pages);
     const char* vbase = reinterpret_cast<const char*>(a.v_pages);
+    constexpr int TSTEP = kDecThreads / CPR;
+    const int cp_c = tid % CPR, cp_t0 = tid / CPR;
+    const int bs_shift = __ffs(a.bs) - 1;
+    const uint32_t cp_dst0 = (cp_c >> 3) * half_bytes + uint32_t(cp_t0) * kRowBytes +
+                             uint32_t(((cp_c & 7) ^ (cp_t0 & 7)) << 4);
+    const int n_per_tensor = item_tokens / TSTEP;
     auto issue_item = [&](int item) {   // every thread
         const int k = item - i_begin;
-        const uint32_t kd = base + (k % kDecStages) * stage_bytes;
-        const int kvh = (item / a.items_per_unit) % a.Hkv;
-        const int per_tensor = item_tokens * CPR;
-        for (int e = tid; e < 2 * per_tensor; e += kDecThreads) {
-            const int is_v = e >= per_tensor;
-            const int rem = e - is_v * per_tensor;
-            const int t = rem / CPR, c = rem - (rem / CPR) * CPR;
-            const int j = t / a.bs, r = t - (t / a.bs) * a.bs;
+        const uint32_t kd = base + (k % kDecStages) * stage_bytes + cp_dst0;
+        const uint32_t vd = kd + HALVES * half_bytes;
+        const size_t head_rows = size_t((item / a.items_per_unit) % a.Hkv) * a.bs;
+        for (int i = 0; i < n_per_tensor; ++i) {
+            const int t = cp_t0 + i * TSTEP;
+            const int j = t >> bs_shift, r = t & (a.bs - 1);
             const int page = blk_page[k * bpi + j];
             const bool ok = page >= 0 && r < blk_valid[k * bpi + j];
-            const char* src = is_v ? vbase : kbase;
-            if (ok) src += ((size_t(page) * a.Hkv + kvh) * a.bs + r) * (D * 2) + c * 16;
-            const uint32_t dst = swz(kd + is_v * HALVES * half_bytes + (c >> 3) * half_bytes, t, c & 7);
-            cp_async_16_zfill(dst, src, ok ? 16u : 0u);
+            const size_t off = ok ? ((size_t(page) * a.Hkv * a.bs + head_rows + r) * (D * 2) + cp_c * 16) : 0;
+            const uint32_t bytes = ok ? 16u : 0u;
+            cp_async_16_zfill(kd + uint32_t(i * TSTEP) * kRowBytes, kbase + off, bytes);
+            cp_async_16_zfill(vd + uint32_t(i * TSTEP) * kRowBytes, vbase + off, bytes);
         }
     };
     for (int kk = 0; kk < kDecStages - 1; ++kk) {
@@ -532,7 +537,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a
     uint32_t qa0[D / 16], qa2[D / 16];                       // bf16 (hi) part
     uint32_t qb0[QSPLIT ? D / 16 : 1], qb2[QSPLIT ? D / 16 : 1];  // lo part (fp32 query)
     float acc[DT_PER_WARP][4];
-    float m_run = -INFINITY, l_run = 0.f;   // warp g < G keeps head g's statistics
+    float m_run = -INFINITY, l_run = 0.f;   // head g4's running statistics (all warps agree)
     int cur_u = -1, seg_first = 0;
 
     for (int item = i_begin; item < i_end; ++item) {
@@ -576,9 +581,16 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a
         if (item + kDecStages - 1 < i_end) issue_item(item + kDecStages - 1);
         cp_async_commit();
 
-        // ---- S = q K^T: warp w takes token tiles w, w + 8, ... ----------------
-        for (int nt = warp; nt < item_tokens / 8; nt += kDecWarps) {
-            const int n0 = nt * 8;
+        // ---- S = q K^T: warp w takes token tiles w, w + 8, ...; softmax on the fragments
+        constexpr int NT_MAX = 4;                  // token tiles per warp (item <= 256 tokens)
+        const int nt_per_warp = item_tokens / (8 * kDecWarps);
+        float sv[NT_MAX][2];
+        float wmax = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < NT_MAX; ++q) {
+            sv[q][0] = sv[q][1] = -INFINITY;
+            if (q >= nt_per_warp) continue;
+            const int n0 = (warp + q * kDecWarps) * 8;
             float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kp = 0; kp < D / 32; ++kp) {   // two 16-channel k-steps per ldmatrix.x4
@@ -593,48 +605,61 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a
                     mma_bf16_16816(c, qb0[2 * kp + 1], 0u, qb2[2 * kp + 1], 0u, b2, b3);
                 }
             }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = n0 + 2 * t4 + e;
+                const int j = t >> bs_shift;
+                const bool ok = (t & (a.bs - 1)) < blk_valid[k * bpi + j];
+                sv[q][e] = ok ? c[e] * a.scale_log2 : -INFINITY;
+                wmax = fmaxf(wmax, sv[q][e]);
+            }
+        }
+        // per-head max over the warp's tokens (the 4 lanes of a fragment row), then the CTA
+        wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, 1));
+        wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, 2));
+        if (t4 == 0) red_m[warp][g4] = wmax;
+        __syncthreads();
+        float alpha = 0.f;
+        {
+            float mi = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) mi = fmaxf(mi, red_m[w][g4]);
+            const float m_new = fmaxf(m_run, mi);
+            alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+            float wsum = 0.f;
             if (g4 < G) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = n0 + 2 * t4 + e;
-                    const int j = t / a.bs;
-                    const bool ok = (t - j * a.bs) < blk_valid[k * bpi + j];
-                    s_s[g4 * item_tokens + t] = ok ? c[e] * a.scale_log2 : -INFINITY;
+                for (int q = 0; q < NT_MAX; ++q) {
+                    if (q >= nt_per_warp) continue;
+                    const int t = (warp + q * kDecWarps) * 8 + 2 * t4;
+                    float p[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        p[e] = (sv[q][e] == -INFINITY) ? 0.f : fast_exp2(sv[q][e] - m_new);
+                        wsum += p[e];
+                    }
+                    const uint32_t hi = pack_bf16x2(p[0], p[1]);
+                    const uint32_t lo = pack_bf16x2(p[0] - bf16_lo(hi), p[1] - bf16_hi(hi));
+                    *reinterpret_cast<uint32_t*>(p_s + g4 * p_pitch + t) = hi;
+                    *reinterpret_cast<uint32_t*>(p_s + (G + g4) * p_pitch + t) = lo;
                 }
             }
-        }
-        __syncthreads();
-
-        // ---- online softmax statistics: warp g owns head g ---------------------
-        if (warp < G) {
-            const int g = warp;
-            float mi = -INFINITY;
-            for (int t = lane; t < item_tokens; t += 32) mi = fmaxf(mi, s_s[g * item_tokens + t]);
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) mi = fmaxf(mi, __shfl_xor_sync(kFullMask, mi, off));
-            const float m_new = fmaxf(m_run, mi);
-            const float alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
-            float li = 0.f;
-            for (int t = lane; t < item_tokens; t += 32) {
-                const float x = s_s[g * item_tokens + t];
-                const float p = (x == -INFINITY) ? 0.f : fast_exp2(x - m_new);
-                const uint32_t hi = pack_bf16x2(p, 0.f) & 0xffffu;
-                const float rest = p - __uint_as_float(hi << 16);
-                p_s[g * p_pitch + t] = uint16_t(hi);
-                p_s[(G + g) * p_pitch + t] = uint16_t(pack_bf16x2(rest, 0.f) & 0xffffu);
-                li += p;
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) li += __shfl_xor_sync(kFullMask, li, off);
-            l_run = l_run * alpha + li;
+            wsum += __shfl_xor_sync(kFullMask, wsum, 1);
+            wsum += __shfl_xor_sync(kFullMask, wsum, 2);
+            if (t4 == 0) red_l[warp][g4] = wsum;
             m_run = m_new;
-            if (lane == 0) s_alpha[g] = alpha;
         }
         __syncthreads();
+        {
+            float li = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) li += red_l[w][g4];
+            l_run = l_run * alpha + li;
+        }
 
         // ---- O += P V: warp w owns channel tiles w * DT_PER_WARP .. ---------------
         {
-            const float al = g4 < G ? s_alpha[g4] : 0.f;
+            const float al = g4 < G ? alpha : 0.f;
 #pragma unroll
             for (int j = 0; j < DT_PER_WARP; ++j) {
                 acc[j][0] *= al;
@@ -685,9 +710,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a
                     *reinterpret_cast<float2*>(dst) = make_float2(acc[j][0], acc[j][1]);
                 }
             }
-            if (warp < G && lane == 0) {
-                a.part_m[(head0 + warp) * ipu + slot] = m_run;
-                a.part_l[(head0 + warp) * ipu + slot] = l_run;
+            if (warp == 0 && t4 == 0 && g4 < G) {
+                a.part_m[(head0 + g4) * ipu + slot] = m_run;
+                a.part_l[(head0 + g4) * ipu + slot] = l_run;
             }
             __syncthreads();
             if (tid == 0) {
@@ -750,8 +775,8 @@ cudaError_t dispatch_group(const DecodeArgs& a, int G, cudaStream_t s)
 // ---- tensor-core path (bf16 K/V) ----------------------------------------------
 size_t mma_fixed_smem(int G, int item_tokens)
 {
-    return 1024 /* alignment slack */ + size_t(G) * item_tokens * sizeof(float) +
-           size_t(2) * G * (item_tokens + 8) * sizeof(uint16_t) + 32 + size_t(2) * kMaxRangeBlocks * sizeof(int);
+    return 1024 /* alignment slack */ + size_t(2) * G * (item_tokens + 8) * sizeof(uint16_t) + 32 +
+           size_t(2) * kMaxRangeBlocks * sizeof(int);
 }
 
 template <int D, int G, bool QSPLIT>
