@@ -6,28 +6,18 @@
 // gathering them into a temporary buffer first.  The softmax is exact over the union of
 // the selected tokens (SGLang page §1.2 "select-then-compute").
 //
-// Design: a persistent grid streams "items" (a few selected blocks, ~64 tokens, of one
-// (sequence, KV head) unit) through a kStages-deep shared-memory pipeline.
-//   * Items are numbered unit-major; CTA i owns an equal contiguous range, so it sees
-//     one or two unit boundaries and no CTA ever waits on another.
-//   * At start the CTA resolves, for its whole range, selected id -> page through the
-//     page table into shared memory (bounds-checked), so the producer thread issues
-//     copies without touching global memory.
-//   * kStages items stay in flight: per item, 1-D bulk async copies (cp.async.bulk) of
-//     each (page, KV head) K tile and V tile -- block_size x D contiguous -- complete
-//     on the stage's `full` mbarrier; warps release the stage on its `empty` mbarrier.
-//     Copies from one issuing thread complete one after another, so each item's copies
-//     are issued by different warps.
-//   * QK^T in fp32: a key row is covered by LPR lanes with one 16-byte shared load
-//     each; the G heads' partial dots are summed across the row's lanes with the
-//     transposed halving reduction.  Per head, warps keep the running max / sum of an
-//     online softmax (exp2, scores pre-scaled by scale * log2 e); PV accumulates in
-//     registers, rescaled when the max moves.
-//   * At the end of its segment of a unit, the CTA reduces its accumulators across
-//     warps and writes one (m, l, o) partial; the CTA that completes a unit's item
-//     count merges the unit's partials (log-sum-exp) into fp32 outputs.
-// GQA tiles are G x tokens: far too narrow for a tensor-core tile to pay (>= 64 rows),
-// and the kernel is HBM-bound at ~2 FMA per byte, so the contraction stays on FMA units.
+// Design: a persistent grid over "items" (a few selected blocks, 64-128 tokens, of one
+// (sequence, KV head) unit), numbered unit-major; CTA i owns an equal contiguous range,
+// so it sees one or two unit boundaries and no CTA ever waits on another.  At start the
+// CTA resolves, for its whole range, selected id -> page through the page table into
+// shared memory (bounds-checked).  At the end of its segment of a unit the CTA writes
+// one (m, l, o) partial; the CTA that completes a unit's item count merges the unit's
+// partials (log-sum-exp) into fp32 outputs.
+//   * bf16 K/V (the fast path, decode_mma_kernel below): warps stream 16-token slabs
+//     independently through per-warp cp.async rings and do QK^T and PV on tensor cores
+//     (mma.sync m16n8k16, fp32 accumulate) with the softmax on the fragments.
+//   * fp32 K/V (decode_kernel): items through a CTA-wide bulk-copy pipeline, dots on
+//     FMA units with the G heads' partial sums reduced across a key row's lanes.
 
 #include "sa_common.cuh"
 #include "sa_internal.h"
@@ -86,38 +76,89 @@ size_t decode_fixed_smem(int G, int item_tokens)
 
 // The CTA that completed unit u merges the unit's partials.  A unit's segments start
 // at its first item and at every CTA range start inside it; each segment wrote one
-// (m, l, o) partial at the slot of its first item.
+// (m, l, o) partial at the slot of its first item, so segment i of a unit whose first
+// item lies in CTA c0 sits at slot max(start(c0 + i), x0) - x0.  Segments are taken
+// kMergeChunk at a time, and within a chunk every load is issued before any is used:
+// each thread loads the o values of its outputs and a share of the (m, l) pairs, the
+// pairs go through shared memory, and the outputs are combined against the running
+// maximum (rescaled when a later chunk raises it).
+constexpr int kMergeChunk = 8;
+constexpr int kMergeOut = 4;                   // outputs per thread: G * D <= 4 * kDecThreads
+
 __device__ void merge_unit(const DecodeArgs& a, int u, int G, int D)
 {
-    if (threadIdx.x == 0) a.counters[u] = 0u;
+    __shared__ float s_pm[8][kMergeChunk], s_pl[8][kMergeChunk];
+    const int tid = threadIdx.x;
     const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
     const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
     const int ipu = a.items_per_unit;
-    const int x0 = u * ipu, x1 = x0 + ipu;
+    const long long x0 = (long long)u * ipu, x1 = x0 + ipu;
     const long long T = a.total_items, C = gridDim.x;
-    int c0 = int((long long)x0 * C / T);                         // CTA holding item x0
+    if (tid == 0) a.counters[u] = 0u;
+    long long c0 = x0 * C / T;                                   // CTA holding item x0
     while (c0 + 1 < C && (T * (c0 + 1)) / C <= x0) ++c0;
     while (c0 > 0 && (T * c0) / C > x0) --c0;
-    for (int i = threadIdx.x; i < G * D; i += kDecThreads) {
-        const int g = i / D, d = i - g * D;
-        const size_t h = head0 + g;
-        float mx = -INFINITY;
-        for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
-            const int slot = int(max((T * c) / C, (long long)x0) - x0);
-            mx = fmaxf(mx, __ldcg(a.part_m + h * ipu + slot));
+    long long c1 = (x1 * C + T - 1) / T;                         // first CTA starting at or after x1
+    while (c1 > c0 + 1 && (T * (c1 - 1)) / C >= x1) --c1;
+    while (c1 < C && (T * c1) / C < x1) ++c1;
+    const int nseg = int(c1 - c0);
+    auto slot = [&](int i) -> int { return int(max((T * (c0 + i)) / C, x0) - x0); };
+
+    float num[kMergeOut], den[kMergeOut], mrun[kMergeOut];
+#pragma unroll
+    for (int r = 0; r < kMergeOut; ++r) num[r] = den[r] = 0.f, mrun[r] = -INFINITY;
+    for (int base = 0; base < nseg; base += kMergeChunk) {
+        const int n = min(kMergeChunk, nseg - base);
+        float ov[kMergeOut][kMergeChunk];
+#pragma unroll
+        for (int r = 0; r < kMergeOut; ++r) {
+            const int i = tid + r * kDecThreads;
+            const int g = i / D, d = i - (i / D) * D;
+#pragma unroll
+            for (int e = 0; e < kMergeChunk; ++e)
+                ov[r][e] = (i < G * D && e < n) ? __ldcg(a.part_o + ((head0 + g) * ipu + slot(base + e)) * D + d) : 0.f;
         }
-        float num = 0.f, den = 0.f;
-        if (mx != -INFINITY) {
-            for (long long c = c0; c < C && (T * c) / C < x1; ++c) {
-                const int slot = int(max((T * c) / C, (long long)x0) - x0);
-                const float ms = __ldcg(a.part_m + h * ipu + slot);
-                if (ms == -INFINITY) continue;
-                const float wgt = fast_exp2(ms - mx);
-                den = fmaf(wgt, __ldcg(a.part_l + h * ipu + slot), den);
-                num = fmaf(wgt, __ldcg(a.part_o + (h * ipu + slot) * D + d), num);
+        if (tid < G * kMergeChunk) {
+            const int g = tid / kMergeChunk, e = tid - g * kMergeChunk;
+            float pm = -INFINITY, pl = 0.f;
+            if (e < n) {
+                pm = __ldcg(a.part_m + (head0 + g) * ipu + slot(base + e));
+                pl = __ldcg(a.part_l + (head0 + g) * ipu + slot(base + e));
             }
+            s_pm[g][e] = pm;
+            s_pl[g][e] = pl;
         }
-        a.out[h * D + d] = den > 0.f ? num / den : 0.f;
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kMergeOut; ++r) {
+            const int i = tid + r * kDecThreads;
+            if (i >= G * D) break;
+            const int g = i / D;
+            float mx = mrun[r];
+#pragma unroll
+            for (int e = 0; e < kMergeChunk; ++e) mx = fmaxf(mx, s_pm[g][e]);
+            if (mx == -INFINITY) continue;                       // nothing valid yet
+            const float resc = mrun[r] == -INFINITY ? 0.f : fast_exp2(mrun[r] - mx);
+            float nu = num[r] * resc, de = den[r] * resc;
+#pragma unroll
+            for (int e = 0; e < kMergeChunk; ++e) {
+                const float pm = s_pm[g][e];
+                if (pm == -INFINITY) continue;                   // empty segment (or past n)
+                const float w = fast_exp2(pm - mx);
+                nu = fmaf(w, ov[r][e], nu);
+                de = fmaf(w, s_pl[g][e], de);
+            }
+            num[r] = nu;
+            den[r] = de;
+            mrun[r] = mx;
+        }
+        __syncthreads();                                         // s_pm / s_pl reused
+    }
+#pragma unroll
+    for (int r = 0; r < kMergeOut; ++r) {
+        const int i = tid + r * kDecThreads;
+        if (i >= G * D) break;
+        a.out[head0 * D + i] = den[r] > 0.f ? num[r] / den[r] : 0.f;
     }
 }
 
@@ -405,331 +446,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
     }
 }
 
-// ---------------------------------------------------------------------------
-// bf16 K/V: the same persistent item pipeline, with the GQA contractions on tensor
-// cores.  Staging: every thread issues 16-byte cp.async copies (global -> shared,
-// L2 only) of its share of the item's K and V rows into a 128-byte-swizzled layout --
-// each token row split into 64-channel halves of 128-byte rows, the 16-byte chunk index
-// XOR-ed with the row index mod 8 -- so the 8-row ldmatrix accesses below are
-// conflict-free.  Rows that carry no token (empty block slots, the tail past the
-// context) are zero-filled by the copy itself.  Per-thread copies never stall the
-// issuing warp the way a bulk copy issued per page tile did (measured: ~0.8 us per issue
-// with 4-8 KB page tiles).  kDecStages - 1 items stay in flight.
-//   S = Q K^T : mma.sync m16n8k16, rows = the G query heads (padded to 16),
-//               columns = 8 tokens per tile, warps split the item's tokens;
-//   O += P V  : rows = heads, columns = 8 channels per tile, k = 16 tokens,
-//               warps split the head dimension, so no cross-warp reduction;
-//               P enters as a bf16 hi + lo pair (two MMAs), so the weights keep
-//               ~16 mantissa bits; accumulation is fp32 throughout.
-// A bf16 query is exact in the MMA; an fp32 query is split into hi + lo too.
-constexpr int kRowBytes = 128;   // one 64-channel half of a token row
-constexpr int kDecStages = 3;
-
-__device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk)
-{
-    // 128-byte swizzle: the 16-byte chunk index is XOR-ed with the row index mod 8
-    return half_base + uint32_t(token) * kRowBytes + uint32_t((chunk ^ (token & 7)) << 4);
-}
-
-template <int D, int G, bool QSPLIT>
-__global__ void __launch_bounds__(kDecThreads, 2) decode_mma_kernel(DecodeArgs a)
-{
-    constexpr int HALVES = D / 64;
-    constexpr int DT = D / 8;                      // 8-channel tiles
-    constexpr int DT_PER_WARP = DT / kDecWarps;    // 2 (D = 128) or 1 (D = 64)
-    constexpr int CPR = D / 8;                     // 16-byte chunks per token row
-    static_assert(DT % kDecWarps == 0, "channel tiles must split over the warps");
-    static_assert(G <= 8, "query rows live in the first 8 MMA rows");
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g4 = lane >> 2, t4 = lane & 3;       // MMA fragment coordinates
-    const int bpi = a.blocks_per_item;
-    const int item_tokens = bpi * a.bs;
-    const uint32_t half_bytes = uint32_t(item_tokens) * kRowBytes;
-    const uint32_t stage_bytes = 2u * HALVES * half_bytes;
-    const int p_pitch = item_tokens + 8;           // bf16 elements per P row (bank spread)
-
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle pattern repeats every 1024 bytes
-    unsigned char* smem = smem_raw + (base - raw);
-    uint16_t* p_s = reinterpret_cast<uint16_t*>(smem + kDecStages * stage_bytes);   // [2][G][p_pitch]
-    int* blk_page = reinterpret_cast<int*>(p_s + 2 * G * p_pitch + 8);         // [range blocks]
-    int* blk_valid = blk_page + kMaxRangeBlocks;
-    __shared__ float red_m[kDecWarps][8], red_l[kDecWarps][8];   // per-warp max / sum per head
-    __shared__ int s_counts[64];
-    __shared__ int s_merge_unit;
-
-    const int i_begin = int((long long)a.total_items * blockIdx.x / gridDim.x);
-    const int i_end = int((long long)a.total_items * (blockIdx.x + 1) / gridDim.x);
-    if (i_begin >= i_end) return;
-    const int u_lo = i_begin / a.items_per_unit;
-    const int u_hi = (i_end - 1) / a.items_per_unit;
-
-    // ---- resolve the range: counts, selected ids -> pages ---------------------
-    for (int u = u_lo + tid; u <= u_hi; u += kDecThreads) {
-        int count = a.sel_count[u];
-        if (count < 0 || count > a.sel_stride) {
-            raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
-            count = count < 0 ? 0 : a.sel_stride;
-        }
-        s_counts[u - u_lo] = count;
-    }
-    __syncthreads();
-    const int n_range_blocks = (i_end - i_begin) * bpi;
-    for (int e = tid; e < n_range_blocks; e += kDecThreads) {
-        const int item = i_begin + e / bpi;
-        const int u = item / a.items_per_unit;
-        const int slot = (item - u * a.items_per_unit) * bpi + e % bpi;
-        int page = -1, valid = 0;
-        if (slot < s_counts[u - u_lo]) {
-            const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
-            if (j < 0 || j >= a.nb) {
-                raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
-            } else {
-                const int p = a.block_table[size_t(u / a.Hkv) * a.nb + j];
-                if (p < 0 || p >= a.num_pages) {
-                    raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
-                } else {
-                    page = p;
-                    valid = min(a.bs, a.N - j * a.bs);
-                }
-            }
-        }
-        blk_page[e] = page;
-        blk_valid[e] = valid;
-    }
-    __syncthreads();
-
-    // Stage an item: K then V rows of its tokens, 16-byte chunks.  Thread tid always
-    // copies chunk c = tid % CPR of tokens tid / CPR + i * (256 / CPR); the swizzle term
-    // (c ^ token) & 7 is therefore constant per thread.
-    const char* kbase = reinterpret_cast<const char*>(a.k_pages);
-    const char* vbase = reinterpret_cast<const char*>(a.v_pages);
-    constexpr int TSTEP = kDecThreads / CPR;
-    const int cp_c = tid % CPR, cp_t0 = tid / CPR;
-    const int bs_shift = __ffs(a.bs) - 1;
-    const uint32_t cp_dst0 = (cp_c >> 3) * half_bytes + uint32_t(cp_t0) * kRowBytes +
-                             uint32_t(((cp_c & 7) ^ (cp_t0 & 7)) << 4);
-    const int n_per_tensor = item_tokens / TSTEP;
-    auto issue_item = [&](int item) {   // every thread
-        const int k = item - i_begin;
-        const uint32_t kd = base + (k % kDecStages) * stage_bytes + cp_dst0;
-        const uint32_t vd = kd + HALVES * half_bytes;
-        const size_t head_rows = size_t((item / a.items_per_unit) % a.Hkv) * a.bs;
-        for (int i = 0; i < n_per_tensor; ++i) {
-            const int t = cp_t0 + i * TSTEP;
-            const int j = t >> bs_shift, r = t & (a.bs - 1);
-            const int page = blk_page[k * bpi + j];
-            const bool ok = page >= 0 && r < blk_valid[k * bpi + j];
-            const size_t off = ok ? ((size_t(page) * a.Hkv * a.bs + head_rows + r) * (D * 2) + cp_c * 16) : 0;
-            const uint32_t bytes = ok ? 16u : 0u;
-            cp_async_16_zfill(kd + uint32_t(i * TSTEP) * kRowBytes, kbase + off, bytes);
-            cp_async_16_zfill(vd + uint32_t(i * TSTEP) * kRowBytes, vbase + off, bytes);
-        }
-    };
-    for (int kk = 0; kk < kDecStages - 1; ++kk) {
-        if (i_begin + kk < i_end) issue_item(i_begin + kk);
-        cp_async_commit();
-    }
-
-    // query A-fragments (rows g4 < G), per 16-channel k-step: a0 = (g4, 2t4..), a2 = (g4, 2t4+8..)
-    uint32_t qa0[D / 16], qa2[D / 16];                       // bf16 (hi) part
-    uint32_t qb0[QSPLIT ? D / 16 : 1], qb2[QSPLIT ? D / 16 : 1];  // lo part (fp32 query)
-    float acc[DT_PER_WARP][4];
-    float m_run = -INFINITY, l_run = 0.f;   // head g4's running statistics (all warps agree)
-    int cur_u = -1, seg_first = 0;
-
-    for (int item = i_begin; item < i_end; ++item) {
-        const int k = item - i_begin;
-        const int s = k % kDecStages;
-        const int u = item / a.items_per_unit;
-        if (u != cur_u) {
-            cur_u = u;
-            seg_first = item;
-            const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                float f[4] = {0.f, 0.f, 0.f, 0.f};
-                if (g4 < G) {
-                    const size_t qrow = (size_t(b) * a.Hq + size_t(kvh) * G + g4) * D + ks * 16 + 2 * t4;
-                    f[0] = load_q(a.q, qrow, a.q_bf16 != 0);
-                    f[1] = load_q(a.q, qrow + 1, a.q_bf16 != 0);
-                    f[2] = load_q(a.q, qrow + 8, a.q_bf16 != 0);
-                    f[3] = load_q(a.q, qrow + 9, a.q_bf16 != 0);
-                }
-                qa0[ks] = pack_bf16x2(f[0], f[1]);
-                qa2[ks] = pack_bf16x2(f[2], f[3]);
-                if constexpr (QSPLIT) {   // remainder after bf16 rounding
-                    qb0[ks] = pack_bf16x2(f[0] - bf16_lo(qa0[ks]), f[1] - bf16_hi(qa0[ks]));
-                    qb2[ks] = pack_bf16x2(f[2] - bf16_lo(qa2[ks]), f[3] - bf16_hi(qa2[ks]));
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < DT_PER_WARP; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-            m_run = -INFINITY;
-            l_run = 0.f;
-        }
-        const uint32_t ks_base = base + s * stage_bytes;
-        const uint32_t vs_base = ks_base + HALVES * half_bytes;
-        // this item's copies (this thread's) are done; after the barrier everyone's are,
-        // and every thread has finished the previous item, whose stage is refilled now
-        cp_async_wait_group<kDecStages - 2>();
-        __syncthreads();
-        if (item + kDecStages - 1 < i_end) issue_item(item + kDecStages - 1);
-        cp_async_commit();
-
-        // ---- S = q K^T: warp w takes token tiles w, w + 8, ...; softmax on the fragments
-        constexpr int NT_MAX = 4;                  // token tiles per warp (item <= 256 tokens)
-        const int nt_per_warp = item_tokens / (8 * kDecWarps);
-        float sv[NT_MAX][2];
-        float wmax = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < NT_MAX; ++q) {
-            sv[q][0] = sv[q][1] = -INFINITY;
-            if (q >= nt_per_warp) continue;
-            const int n0 = (warp + q * kDecWarps) * 8;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kp = 0; kp < D / 32; ++kp) {   // two 16-channel k-steps per ldmatrix.x4
-                const int ch = kp * 4 + (lane >> 3);       // 8-channel chunk of this lane's matrix
-                const uint32_t addr = swz(ks_base + (ch >> 3) * half_bytes, n0 + (lane & 7), ch & 7);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(addr, b0, b1, b2, b3);
-                mma_bf16_16816(c, qa0[2 * kp], 0u, qa2[2 * kp], 0u, b0, b1);
-                mma_bf16_16816(c, qa0[2 * kp + 1], 0u, qa2[2 * kp + 1], 0u, b2, b3);
-                if constexpr (QSPLIT) {
-                    mma_bf16_16816(c, qb0[2 * kp], 0u, qb2[2 * kp], 0u, b0, b1);
-                    mma_bf16_16816(c, qb0[2 * kp + 1], 0u, qb2[2 * kp + 1], 0u, b2, b3);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t = n0 + 2 * t4 + e;
-                const int j = t >> bs_shift;
-                const bool ok = (t & (a.bs - 1)) < blk_valid[k * bpi + j];
-                sv[q][e] = ok ? c[e] * a.scale_log2 : -INFINITY;
-                wmax = fmaxf(wmax, sv[q][e]);
-            }
-        }
-        // per-head max over the warp's tokens (the 4 lanes of a fragment row), then the CTA
-        wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, 1));
-        wmax = fmaxf(wmax, __shfl_xor_sync(kFullMask, wmax, 2));
-        if (t4 == 0) red_m[warp][g4] = wmax;
-        __syncthreads();
-        float alpha = 0.f;
-        {
-            float mi = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) mi = fmaxf(mi, red_m[w][g4]);
-            const float m_new = fmaxf(m_run, mi);
-            alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
-            float wsum = 0.f;
-            if (g4 < G) {
-#pragma unroll
-                for (int q = 0; q < NT_MAX; ++q) {
-                    if (q >= nt_per_warp) continue;
-                    const int t = (warp + q * kDecWarps) * 8 + 2 * t4;
-                    float p[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        p[e] = (sv[q][e] == -INFINITY) ? 0.f : fast_exp2(sv[q][e] - m_new);
-                        wsum += p[e];
-                    }
-                    const uint32_t hi = pack_bf16x2(p[0], p[1]);
-                    const uint32_t lo = pack_bf16x2(p[0] - bf16_lo(hi), p[1] - bf16_hi(hi));
-                    *reinterpret_cast<uint32_t*>(p_s + g4 * p_pitch + t) = hi;
-                    *reinterpret_cast<uint32_t*>(p_s + (G + g4) * p_pitch + t) = lo;
-                }
-            }
-            wsum += __shfl_xor_sync(kFullMask, wsum, 1);
-            wsum += __shfl_xor_sync(kFullMask, wsum, 2);
-            if (t4 == 0) red_l[warp][g4] = wsum;
-            m_run = m_new;
-        }
-        __syncthreads();
-        {
-            float li = 0.f;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) li += red_l[w][g4];
-            l_run = l_run * alpha + li;
-        }
-
-        // ---- O += P V: warp w owns channel tiles w * DT_PER_WARP .. ---------------
-        {
-            const float al = g4 < G ? alpha : 0.f;
-#pragma unroll
-            for (int j = 0; j < DT_PER_WARP; ++j) {
-                acc[j][0] *= al;
-                acc[j][1] *= al;
-            }
-            const uint32_t* p32 = reinterpret_cast<const uint32_t*>(p_s);
-            for (int kk = 0; kk < item_tokens / 16; ++kk) {
-                const int k0 = kk * 16;
-                uint32_t ah0 = 0, ah2 = 0, al0 = 0, al2 = 0;
-                if (g4 < G) {
-                    ah0 = p32[(g4 * p_pitch + k0 + 2 * t4) >> 1];
-                    ah2 = p32[(g4 * p_pitch + k0 + 8 + 2 * t4) >> 1];
-                    al0 = p32[((G + g4) * p_pitch + k0 + 2 * t4) >> 1];
-                    al2 = p32[((G + g4) * p_pitch + k0 + 8 + 2 * t4) >> 1];
-                }
-#pragma unroll
-                for (int jp = 0; jp < DT_PER_WARP; jp += 2) {
-                    // matrices: (tokens k0.., ch c), (tokens k0+8.., ch c), (k0.., c+1), (k0+8.., c+1)
-                    const int mtx = lane >> 3;
-                    const int tok = k0 + (mtx & 1) * 8 + (lane & 7);
-                    const int chunk = (warp * DT_PER_WARP + jp) + (mtx >> 1);
-                    const uint32_t addr = swz(vs_base + (chunk >> 3) * half_bytes, tok, chunk & 7);
-                    uint32_t r0, r1, r2 = 0, r3 = 0;
-                    if constexpr (DT_PER_WARP >= 2) ldsm_x4_trans(addr, r0, r1, r2, r3);
-                    else ldsm_x2_trans(addr, r0, r1);   // lanes 0..15 address the two matrices
-                    mma_bf16_16816(acc[jp], ah0, 0u, ah2, 0u, r0, r1);
-                    mma_bf16_16816(acc[jp], al0, 0u, al2, 0u, r0, r1);
-                    if constexpr (DT_PER_WARP >= 2) {
-                        mma_bf16_16816(acc[jp + 1], ah0, 0u, ah2, 0u, r2, r3);
-                        mma_bf16_16816(acc[jp + 1], al0, 0u, al2, 0u, r2, r3);
-                    }
-                }
-            }
-        }
-
-        const bool seg_end = item + 1 == i_end || (item + 1) / a.items_per_unit != u;
-        if (seg_end) {
-            // ---- end of this CTA's segment of unit u: one partial (no reduction) --
-            const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
-            const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
-            const int slot = seg_first - u * a.items_per_unit;
-            const int ipu = a.items_per_unit;
-            if (g4 < G) {
-#pragma unroll
-                for (int j = 0; j < DT_PER_WARP; ++j) {
-                    const int ch = (warp * DT_PER_WARP + j) * 8 + 2 * t4;
-                    float* dst = a.part_o + ((head0 + g4) * ipu + slot) * D + ch;
-                    *reinterpret_cast<float2*>(dst) = make_float2(acc[j][0], acc[j][1]);
-                }
-            }
-            if (warp == 0 && t4 == 0 && g4 < G) {
-                a.part_m[(head0 + g4) * ipu + slot] = m_run;
-                a.part_l[(head0 + g4) * ipu + slot] = l_run;
-            }
-            __syncthreads();
-            if (tid == 0) {
-                const uint32_t n = uint32_t(item - seg_first + 1);
-                const uint32_t before = atomic_add_acq_rel_u32(&a.counters[u], n);
-                s_merge_unit = before + n == uint32_t(ipu) ? u : -1;
-            }
-        }
-        if (!seg_end) continue;
-        __syncthreads();
-        if (s_merge_unit < 0) continue;
-        merge_unit(a, u, G, D);
-        __syncthreads();
-    }
-    cp_async_wait_group<0>();
-}
-
 template <int D, bool BF16, int G>
 cudaError_t launch_decode_t(DecodeArgs a, cudaStream_t s)
 {
@@ -771,20 +487,339 @@ cudaError_t dispatch_group(const DecodeArgs& a, int G, cudaStream_t s)
     }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 K/V: warps stream 16-token slabs independently, contractions on tensor cores.
+//   * The CTA owns the same contiguous item range as above; its items are cut into
+//     16-token slabs and warp w takes slabs w, w + 8, ... of the range.  Each warp runs
+//     its own kSlabStages-deep ring of slabs in shared memory, filled with 16-byte
+//     cp.async copies (global -> shared, L2 only) issued by its own lanes, so a warp
+//     waits only on its own copies (cp.async.wait_group + __syncwarp) and the CTA never
+//     synchronises inside a unit.  Rows without a token (empty block slots, the tail
+//     past the context) are zero-filled by the copy.
+//   * Layout per slab: K then V, each token row split into 64-channel halves of
+//     128-byte rows with the 16-byte chunk index XOR-ed with the row index mod 8, so
+//     the 8-row ldmatrix reads are conflict-free.
+//   * S = q K^T with mma.sync m16n8k16 (bf16 in, fp32 accumulate): A rows 0..7 are the
+//     G query heads, columns the 8 tokens of a tile.  An fp32 query is split into
+//     bf16 hi + lo; the lo part rides in A rows 8..15, so one MMA yields both halves
+//     of the dot and the score is c0 + c2.
+//   * Online softmax on the accumulator fragments: a head's row lives in the 4 lanes
+//     of a quad, so the slab maximum takes two shuffles; the running sum stays per
+//     lane until the segment ends.
+//   * O += P V with the score fragments reused as the A operand (the C layout of two
+//     8-token tiles is the A layout of one 16-token k-step).  P is carried as bf16
+//     hi (rows 0..7) + lo (rows 8..15): the weights keep ~16 mantissa bits at the cost
+//     of no extra MMA, and each output is c0 + c2 of its accumulator.
+//   * At the end of the CTA's segment of a unit every warp writes its (m, l, o) to the
+//     ring stage it has just freed; the CTA combines the 8 into one partial and the
+//     completing CTA merges the unit, as on the fp32 path.
+constexpr int kSlabTokens = 16;
+constexpr int kRowBytes = 128;   // one 64-channel half of a token row
 
-// ---- tensor-core path (bf16 K/V) ----------------------------------------------
-size_t mma_fixed_smem(int G, int item_tokens)
+template <int D>
+struct SlabShape {
+    static constexpr int HALVES = D / 64;
+    static constexpr int HALF_BYTES = kSlabTokens * kRowBytes;       // 2 KB
+    static constexpr int TENSOR_BYTES = HALVES * HALF_BYTES;        // K (or V) of a slab
+    static constexpr int SLAB_BYTES = 2 * TENSOR_BYTES;             // 8 KB (D 128) / 4 KB (D 64)
+    static constexpr int STAGES = D == 128 ? 3 : 6;                 // 192 KB of rings per CTA
+    static constexpr int CPR = D / 8;                               // 16-byte chunks per token row
+    static constexpr int RPI = 32 / CPR;                            // rows one warp copy covers
+    static constexpr int CP_ITERS = kSlabTokens / RPI;
+    static constexpr int DT = D / 8;                                // 8-channel tiles
+    static constexpr size_t RING_BYTES = size_t(kDecWarps) * STAGES * SLAB_BYTES;
+    static_assert(8 * D * 4 <= SLAB_BYTES, "a warp's flushed G x D outputs must fit one stage");
+};
+
+__device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk)
 {
-    return 1024 /* alignment slack */ + size_t(2) * G * (item_tokens + 8) * sizeof(uint16_t) + 32 +
-           size_t(2) * kMaxRangeBlocks * sizeof(int);
+    return half_base + uint32_t(token) * kRowBytes + uint32_t((chunk ^ (token & 7)) << 4);
+}
+
+template <int D>
+constexpr size_t slab_smem_bytes()
+{
+    return 1024 /* alignment slack */ + SlabShape<D>::RING_BYTES + size_t(2) * kMaxRangeBlocks * sizeof(int);
+}
+
+template <int D, int G, bool QSPLIT>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a)
+{
+    using SS = SlabShape<D>;
+    constexpr int S = SS::STAGES;
+    constexpr int DT = SS::DT;
+    static_assert(G <= 8, "query rows live in the first 8 MMA rows");
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g4 = lane >> 2, t4 = lane & 3;       // MMA fragment coordinates
+    const int bpi = a.blocks_per_item;
+    const int ipu = a.items_per_unit;
+    const int item_tokens = bpi * a.bs;            // a power of two >= 64
+    const int spi_shift = __ffs(item_tokens / kSlabTokens) - 1;
+    const int spi_mask = (1 << spi_shift) - 1;
+    const int bs_shift = __ffs(a.bs) - 1;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle pattern repeats every 1024 bytes
+    unsigned char* smem = smem_raw + (base - raw);
+    const uint32_t ring = base + uint32_t(warp) * (S * SS::SLAB_BYTES);
+    int* blk_page = reinterpret_cast<int*>(smem + SS::RING_BYTES);
+    int* blk_valid = blk_page + kMaxRangeBlocks;
+    __shared__ float s_m[kDecWarps][8], s_l[kDecWarps][8];
+    __shared__ int s_flush[kDecWarps];             // byte offset of each warp's flushed (o)
+    __shared__ int s_merge_unit;
+
+    const int i_begin = int((long long)a.total_items * blockIdx.x / gridDim.x);
+    const int i_end = int((long long)a.total_items * (blockIdx.x + 1) / gridDim.x);
+    if (i_begin >= i_end) return;
+    const int u_lo = i_begin / ipu;
+    const int u_hi = (i_end - 1) / ipu;
+
+    // query A fragments: rows g4 < G; the lo part of an fp32 query in rows 8..15.  A bf16
+    // query's pair (2 t4, 2 t4 + 1) is one aligned 32-bit word, loaded straight into the
+    // fragment, so the load latency is paid at the first MMA rather than here.
+    uint32_t qa[D / 16][4];
+    auto load_qfrag = [&](int u) {
+        const size_t head0 = size_t(u / a.Hkv) * a.Hq + size_t(u % a.Hkv) * G;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const size_t qrow = (head0 + g4) * D + ks * 16 + 2 * t4;
+            if constexpr (!QSPLIT) {
+                const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q);
+                qa[ks][0] = g4 < G ? __ldg(q32 + qrow / 2) : 0u;
+                qa[ks][2] = g4 < G ? __ldg(q32 + qrow / 2 + 4) : 0u;
+                qa[ks][1] = qa[ks][3] = 0u;
+            } else {
+                const float2* q64 = reinterpret_cast<const float2*>(a.q);
+                const float2 f0 = g4 < G ? __ldg(q64 + qrow / 2) : make_float2(0.f, 0.f);
+                const float2 f2 = g4 < G ? __ldg(q64 + qrow / 2 + 4) : make_float2(0.f, 0.f);
+                qa[ks][0] = pack_bf16x2(f0.x, f0.y);
+                qa[ks][2] = pack_bf16x2(f2.x, f2.y);
+                qa[ks][1] = pack_bf16x2(f0.x - bf16_lo(qa[ks][0]), f0.y - bf16_hi(qa[ks][0]));
+                qa[ks][3] = pack_bf16x2(f2.x - bf16_lo(qa[ks][2]), f2.y - bf16_hi(qa[ks][2]));
+            }
+        }
+    };
+    load_qfrag(u_lo);
+
+    // ---- resolve the range: selected ids -> pages (two dependent loads) --------
+    const int n_range_blocks = (i_end - i_begin) * bpi;
+    for (int e = tid; e < n_range_blocks; e += kDecThreads) {
+        const int item = i_begin + e / bpi;
+        const int u = item / ipu;
+        const int slot = (item - u * ipu) * bpi + e % bpi;
+        int count = a.sel_count[u];
+        const int j = slot < a.sel_stride ? a.sel_ids[size_t(u) * a.sel_stride + slot] : -1;
+        if (count < 0 || count > a.sel_stride) {
+            raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
+            count = count < 0 ? 0 : a.sel_stride;
+        }
+        int page = -1, valid = 0;
+        if (slot < count) {
+            if (j < 0 || j >= a.nb) {
+                raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
+            } else {
+                const int p = a.block_table[size_t(u / a.Hkv) * a.nb + j];
+                if (p < 0 || p >= a.num_pages) {
+                    raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
+                } else {
+                    page = p;
+                    valid = min(a.bs, a.N - j * a.bs);
+                }
+            }
+        }
+        blk_page[e] = page;
+        blk_valid[e] = valid;
+    }
+    __syncthreads();
+
+    // Stage slab s of the range into this warp's stage st: lane copies chunk cp_c of
+    // slab rows cp_r, cp_r + RPI, ...; a warp instruction covers RPI whole token rows.
+    const char* kbase = reinterpret_cast<const char*>(a.k_pages);
+    const char* vbase = reinterpret_cast<const char*>(a.v_pages);
+    const int cp_c = lane % SS::CPR, cp_r = lane / SS::CPR;
+    const int n_slabs = (i_end - i_begin) << spi_shift;
+    auto issue_slab = [&](int s, int st) {
+        const int k = s >> spi_shift;                                  // item within the range
+        const int t0 = (s & spi_mask) * kSlabTokens;                  // first token in the item
+        const size_t head_rows = size_t(((i_begin + k) / ipu) % a.Hkv) * a.bs;
+        const uint32_t kd = ring + uint32_t(st) * SS::SLAB_BYTES + uint32_t(cp_c >> 3) * SS::HALF_BYTES;
+        const uint32_t vd = kd + SS::TENSOR_BYTES;
+#pragma unroll
+        for (int i = 0; i < SS::CP_ITERS; ++i) {
+            const int tr = cp_r + i * SS::RPI;                         // row within the slab
+            const int t = t0 + tr;
+            const int e = k * bpi + (t >> bs_shift), r = t & (a.bs - 1);
+            const bool ok = r < blk_valid[e];                          // 0 for an empty slot
+            const size_t off = ok ? ((size_t(blk_page[e]) * a.Hkv * a.bs + head_rows + r) * (D * 2) + cp_c * 16) : 0;
+            const uint32_t so = uint32_t(tr) * kRowBytes + uint32_t(((cp_c & 7) ^ (tr & 7)) << 4);
+            cp_async_16_zfill(kd + so, kbase + off, ok ? 16u : 0u);
+            cp_async_16_zfill(vd + so, vbase + off, ok ? 16u : 0u);
+        }
+    };
+#pragma unroll
+    for (int kk = 0; kk < S - 1; ++kk) {
+        const int s = warp + kk * kDecWarps;
+        if (s < n_slabs) issue_slab(s, kk);
+        cp_async_commit();
+    }
+
+    int my = 0;                                    // slabs this warp has consumed
+    for (int u = u_lo; u <= u_hi; ++u) {
+        const int seg_i0 = max(i_begin, u * ipu), seg_i1 = min(i_end, (u + 1) * ipu);
+        const int se = (seg_i1 - i_begin) << spi_shift;
+        const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+        const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
+
+        float acc[DT][4];
+#pragma unroll
+        for (int j = 0; j < DT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;      // head g4: running max (quad-uniform), lane sum
+
+        for (int s = warp + my * kDecWarps; s < se; s += kDecWarps, ++my) {
+            cp_async_wait_group<S - 2>();          // this lane's copies of slab s are done
+            __syncwarp();                          // ... and every lane's; stage my - 1 is free
+            {
+                const int nx = s + (S - 1) * kDecWarps;
+                if (nx < n_slabs) issue_slab(nx, (my + S - 1) % S);
+                cp_async_commit();
+            }
+            const uint32_t kst = ring + uint32_t(my % S) * SS::SLAB_BYTES;
+            const uint32_t vst = kst + SS::TENSOR_BYTES;
+
+            // ---- S = q K^T over the slab's two 8-token tiles ----------------------
+            float c[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+#pragma unroll
+                for (int kp = 0; kp < D / 32; ++kp) {   // two 16-channel k-steps per ldmatrix.x4
+                    const int ch = kp * 4 + (lane >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(swz(kst + uint32_t(ch >> 3) * SS::HALF_BYTES, nt * 8 + (lane & 7), ch & 7), b0, b1, b2, b3);
+                    mma_bf16_16816(c[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+                    mma_bf16_16816(c[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+                }
+            }
+            // ---- online softmax on the fragments ----------------------------------
+            const int k = s >> spi_shift;
+            const int tb = (s & spi_mask) * kSlabTokens + 2 * t4;
+            float sc[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = tb + nt * 8 + e;
+                    const bool ok = (t & (a.bs - 1)) < blk_valid[k * bpi + (t >> bs_shift)];
+                    sc[nt][e] = ok ? (c[nt][e] + c[nt][e + 2]) * a.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sc[nt][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+            m_run = m_new;
+            float p[2][2];
+            float psum = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    p[nt][e] = (sc[nt][e] == -INFINITY) ? 0.f : fast_exp2(sc[nt][e] - m_new);
+                    psum += p[nt][e];
+                }
+            l_run = fmaf(l_run, alpha, psum);
+            const uint32_t ph0 = pack_bf16x2(p[0][0], p[0][1]);
+            const uint32_t ph2 = pack_bf16x2(p[1][0], p[1][1]);
+            const uint32_t pl0 = pack_bf16x2(p[0][0] - bf16_lo(ph0), p[0][1] - bf16_hi(ph0));
+            const uint32_t pl2 = pack_bf16x2(p[1][0] - bf16_lo(ph2), p[1][1] - bf16_hi(ph2));
+
+            // ---- O += P V: all D channels, k = the slab's 16 tokens ---------------
+#pragma unroll
+            for (int j = 0; j < DT; ++j) {
+                acc[j][0] *= alpha;
+                acc[j][1] *= alpha;
+                acc[j][2] *= alpha;
+                acc[j][3] *= alpha;
+            }
+#pragma unroll
+            for (int jp = 0; jp < DT; jp += 2) {
+                // matrices: (tokens 0..7, chunk jp), (8..15, jp), (0..7, jp + 1), (8..15, jp + 1)
+                const int mtx = lane >> 3;
+                const int chunk = jp + (mtx >> 1);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_trans(swz(vst + uint32_t(chunk >> 3) * SS::HALF_BYTES, (mtx & 1) * 8 + (lane & 7), chunk & 7),
+                              r0, r1, r2, r3);
+                mma_bf16_16816(acc[jp], ph0, pl0, ph2, pl2, r0, r1);
+                mma_bf16_16816(acc[jp + 1], ph0, pl0, ph2, pl2, r2, r3);
+            }
+        }
+
+        if (u < u_hi) load_qfrag(u + 1);           // in flight across the combine below
+
+        // ---- end of the CTA's segment of unit u: combine the warps ---------------
+        l_run += __shfl_xor_sync(kFullMask, l_run, 1);
+        l_run += __shfl_xor_sync(kFullMask, l_run, 2);
+        {
+            const int free_off = int((warp * S + (my + S - 1) % S) * SS::SLAB_BYTES);
+            float* ob = reinterpret_cast<float*>(smem + free_off);
+            if (g4 < G) {
+#pragma unroll
+                for (int j = 0; j < DT; ++j)
+                    *reinterpret_cast<float2*>(ob + g4 * D + j * 8 + 2 * t4) =
+                        make_float2(acc[j][0] + acc[j][2], acc[j][1] + acc[j][3]);
+                if (t4 == 0) {
+                    s_m[warp][g4] = m_run;
+                    s_l[warp][g4] = l_run;
+                }
+            }
+            if (lane == 0) s_flush[warp] = free_off;
+        }
+        __syncthreads();
+        const int slot = seg_i0 - u * ipu;
+        for (int i = tid; i < G * D; i += kDecThreads) {
+            const int g = i / D, d = i - g * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, s_m[w][g]);
+            float o = 0.f, l = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) {
+                const float mw = s_m[w][g];
+                if (mw == -INFINITY) continue;     // a warp without a token here wrote nothing useful
+                const float wt = fast_exp2(mw - M);
+                o = fmaf(wt, reinterpret_cast<const float*>(smem + s_flush[w])[g * D + d], o);
+                l = fmaf(wt, s_l[w][g], l);
+            }
+            const size_t ps = (head0 + g) * ipu + slot;
+            a.part_o[ps * D + d] = o;
+            if (d == 0) {
+                a.part_m[ps] = M;
+                a.part_l[ps] = l;
+            }
+        }
+        __syncthreads();                           // partials written; flush stages free again
+        if (tid == 0) {
+            const uint32_t n = uint32_t(seg_i1 - seg_i0);
+            const uint32_t before = atomic_add_acq_rel_u32(&a.counters[u], n);
+            s_merge_unit = before + n == uint32_t(ipu) ? u : -1;
+        }
+        __syncthreads();
+        if (s_merge_unit >= 0) {
+            merge_unit(a, u, G, D);
+            __syncthreads();
+        }
+    }
+    cp_async_wait_group<0>();
 }
 
 template <int D, int G, bool QSPLIT>
 cudaError_t launch_decode_mma_t(DecodeArgs a, cudaStream_t s)
 {
-    const int item_tokens = a.blocks_per_item * a.bs;
-    const size_t stage = size_t(2) * item_tokens * D * 2;
-    const size_t smem = kDecStages * stage + mma_fixed_smem(G, item_tokens);
+    constexpr size_t smem = slab_smem_bytes<D>();
+    static_assert(smem <= size_t(kDecSmemLimit), "slab rings must fit a CTA");
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -792,8 +827,7 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, cudaStream_t s)
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int per_sm = (2 * (smem + 1024) <= size_t(kSmemPerSm)) ? 2 : 1;
-    long long ctas = (long long)num_sms() * per_sm;
+    long long ctas = num_sms();                    // one CTA (8 independent warps) per SM
     const long long min_ctas = ((long long)a.total_items * a.blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
     if (ctas < min_ctas) ctas = min_ctas;
     const long long min_ctas_units = (a.units + 61) / 62;
@@ -804,7 +838,7 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, cudaStream_t s)
 }
 
 template <int D, bool QSPLIT>
-cudaError_t dispatch_mma(const DecodeArgs& a, int G, const void* k_pages, const void* v_pages, cudaStream_t s)
+cudaError_t dispatch_mma(const DecodeArgs& a, int G, cudaStream_t s)
 {
     switch (G) {
         case 1: return launch_decode_mma_t<D, 1, QSPLIT>(a, s);
@@ -828,7 +862,7 @@ bool decode_supported(int D, bool kv_bf16, int block_size, int G)
     const int bpi = decode_blocks_per_item(D, kv_bf16, block_size);
     const int item_tokens = bpi * block_size;
     const size_t stage = size_t(2) * item_tokens * D * (kv_bf16 ? 2 : 4);
-    if (kv_bf16) return 3 * stage + mma_fixed_smem(G, item_tokens) <= size_t(kDecSmemLimit);
+    if (kv_bf16) return item_tokens % kSlabTokens == 0;   // slab rings have a fixed size
     return 2 * stage + decode_fixed_smem(G, item_tokens) <= size_t(kDecSmemLimit);
 }
 
@@ -867,10 +901,8 @@ cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.err = reinterpret_cast<uint32_t*>(ws + L.err);
     if (g.kv_bf16) {   // tensor-core path
         if (g.q_bf16)
-            return g.D == 128 ? dispatch_mma<128, false>(a, g.G, k_pages, v_pages, s)
-                              : dispatch_mma<64, false>(a, g.G, k_pages, v_pages, s);
-        return g.D == 128 ? dispatch_mma<128, true>(a, g.G, k_pages, v_pages, s)
-                          : dispatch_mma<64, true>(a, g.G, k_pages, v_pages, s);
+            return g.D == 128 ? dispatch_mma<128, false>(a, g.G, s) : dispatch_mma<64, false>(a, g.G, s);
+        return g.D == 128 ? dispatch_mma<128, true>(a, g.G, s) : dispatch_mma<64, true>(a, g.G, s);
     }
     return g.D == 128 ? dispatch_group<128, false>(a, g.G, s) : dispatch_group<64, false>(a, g.G, s);
 }
