@@ -271,7 +271,7 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
 // independent requests so the L2 latency is paid once per batch, not per element.
 __device__ int load_keys(const SelectArgs& a, int u, uint32_t* keys, int* s_count)
 {
-    constexpr int kBatch = 8;
+    constexpr int kBatch = 16;   // 4096 candidates: one round trip
     const float* row = a.scores + size_t(u) * a.n_cand;
     int mine = 0;
     for (int base = threadIdx.x; base < a.n_cand; base += kSelThreads * kBatch) {
