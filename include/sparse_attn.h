@@ -19,7 +19,10 @@
  *  * All tensor pointers are DEVICE pointers into memory the caller owns.  The library
  *    never allocates or frees device memory and keeps no pointer after a call returns.
  *  * Calls are asynchronous on the given stream (a cudaStream_t; NULL = legacy default
- *    stream).  Only sparse_attn_get_device_error synchronises.
+ *    stream).  Only sparse_attn_get_device_error synchronises.  select, decode and diff
+ *    are launched as programmatic dependents of the stream's previous kernel: they may
+ *    be scheduled while it finishes, but read no memory before it has completed, so
+ *    stream order is kept exactly.
  *  * "unit" = one (sequence b, KV head kvh) pair, index u = b * Hkv + kvh.
  *  * Query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
  *  * Layouts (row-major, contiguous):

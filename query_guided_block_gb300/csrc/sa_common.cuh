@@ -264,6 +264,38 @@ __device__ __forceinline__ uint32_t atomic_add_acq_rel_u32(uint32_t* p, uint32_t
     return old;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_after_previous() may
+// start while the previous kernel on the stream is still running; it must call
+// grid_dependency_wait() before its first global-memory access, which returns once the
+// previous kernel has completed and its writes are visible.  Kernels that call
+// allow_dependents_early() let the next such kernel be scheduled before they finish.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents_early()
+{
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                        cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Two floats -> bf16x2 (round to nearest even); `lo` lands in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {

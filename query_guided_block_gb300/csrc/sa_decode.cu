@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
     if (i_begin >= i_end) return;
     const int u_lo = i_begin / a.items_per_unit;
     const int u_hi = (i_end - 1) / a.items_per_unit;
+    allow_dependents_early();
+    grid_dependency_wait();   // inputs and workspace may come from the previous kernel
 
     // ---- resolve the range: counts, selected ids -> pages ---------------------
     for (int u = u_lo + tid; u <= u_hi; u += kDecThreads) {
@@ -471,8 +473,7 @@ cudaError_t launch_decode_t(DecodeArgs a, cudaStream_t s)
     const long long min_ctas_units = (a.units + 61) / 62;
     if (ctas < min_ctas_units) ctas = min_ctas_units;
     if (ctas > a.total_items) ctas = a.total_items;
-    decode_kernel<D, BF16, G><<<dim3(unsigned(ctas)), kDecThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_after_previous(decode_kernel<D, BF16, G>, dim3(unsigned(ctas)), dim3(kDecThreads), smem, s, a);
 }
 
 template <int D, bool BF16>
@@ -575,6 +576,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a
     if (i_begin >= i_end) return;
     const int u_lo = i_begin / ipu;
     const int u_hi = (i_end - 1) / ipu;
+    allow_dependents_early();
+    grid_dependency_wait();   // inputs and workspace may come from the previous kernel
 
     // query A fragments: rows g4 < G; the lo part of an fp32 query in rows 8..15.  A bf16
     // query's pair (2 t4, 2 t4 + 1) is one aligned 32-bit word, loaded straight into the
@@ -833,8 +836,7 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, cudaStream_t s)
     const long long min_ctas_units = (a.units + 61) / 62;
     if (ctas < min_ctas_units) ctas = min_ctas_units;
     if (ctas > a.total_items) ctas = a.total_items;
-    decode_mma_kernel<D, G, QSPLIT><<<dim3(unsigned(ctas)), kDecThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_after_previous(decode_mma_kernel<D, G, QSPLIT>, dim3(unsigned(ctas)), dim3(kDecThreads), smem, s, a);
 }
 
 template <int D, bool QSPLIT>

@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kDiffWarps * 32) diff_kernel(DiffArgs a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int u = blockIdx.x * kDiffWarps + warp;
     if (u >= a.units) return;
+    allow_dependents_early();
+    grid_dependency_wait();   // inputs and slot state may come from the previous kernel
     const int W = a.stride, C = a.C;
     int* S = dsm + warp * (3 * W + 5 * C);
     int* P = S + W;
@@ -205,8 +207,8 @@ cudaError_t launch_diff(const Geometry& g, int step, const int32_t* sel_ids,
                                              int(smem));
         if (e != cudaSuccess) return e;
     }
-    diff_kernel<<<dim3(unsigned((units + kDiffWarps - 1) / kDiffWarps)), kDiffWarps * 32, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_after_previous(diff_kernel, dim3(unsigned((units + kDiffWarps - 1) / kDiffWarps)),
+                                 dim3(kDiffWarps * 32), smem, s, a);
 }
 
 }  // namespace sa

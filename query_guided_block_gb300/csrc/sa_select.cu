@@ -391,6 +391,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
         for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
+    allow_dependents_early();
+    grid_dependency_wait();   // inputs and workspace may come from the previous kernel
     __syncthreads();
     if (lane == 0)
         for (int cid = c_begin; cid < c_end && cid < c_begin + stages; ++cid) issue_mine(cid);
@@ -511,8 +513,7 @@ cudaError_t launch_select_t(const SelectArgs& a0, int units, cudaStream_t s)
     const int per_sm = (2 * (smem + kStatic) <= size_t(kSmemPerSm)) ? 2 : 1;
     int ctas = num_sms() * per_sm;
     if (ctas > a.total_chunks) ctas = a.total_chunks;
-    select_kernel<KIND, MBF16, D><<<dim3(unsigned(ctas)), kSelThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_after_previous(select_kernel<KIND, MBF16, D>, dim3(unsigned(ctas)), dim3(kSelThreads), smem, s, a);
 }
 
 cudaError_t dispatch_select(const SelectArgs& a, int kind, bool mbf16, int D, int units,
