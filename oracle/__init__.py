@@ -96,6 +96,8 @@ def lib():
             "oracle_decode": [P, i, i, vp, vp, vp, ip, ip, ip, i, dp],
             "oracle_lru_step": [i, i, i, ip, ip, i, ip, ip, i, ip, ip, ip, ip, ip, ip, ip, ip,
                                 ip, i, ip],
+            "oracle_union_reserve": [P, i, i, ip, ip, i, ip, i, ip, ip, i],
+            "oracle_topk_for_length": [i, i],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -243,6 +245,31 @@ def decode(p: Problem, q, k_pages, v_pages, block_table, sel_ids, sel_count, uni
     _check(lib().oracle_decode(C.byref(p), u0, u1, _ptr(qa), _ptr(k), _ptr(v), _ptr(bt),
                                _ptr(ids), _ptr(cnt), ids.shape[-1], _ptr(out)), "decode")
     return out
+
+
+def union_reserve(p: Problem, sel_ids, sel_count, reserve, units=None):
+    """Each unit's selection united with its reserve block ids [units, n_reserve]
+    (SparDA page §3.4), ascending without repeats.  Returns (ids, count) with room for
+    sel_stride + n_reserve ids per unit."""
+    u0, u1 = _units(p, units)
+    sel = np.ascontiguousarray(sel_ids, np.int32)
+    res = np.ascontiguousarray(reserve, np.int32).reshape(p.units, -1)
+    stride = sel.shape[1] + res.shape[1]
+    ids = np.full((p.units, max(1, stride)), -1, np.int32)
+    cnt = np.zeros(p.units, np.int32)
+    _check(lib().oracle_union_reserve(C.byref(p), u0, u1, _ptr(sel),
+                                      _ptr(np.ascontiguousarray(sel_count, np.int32)), sel.shape[1],
+                                      _ptr(res), res.shape[1], _ptr(ids), _ptr(cnt), ids.shape[1]),
+           "union_reserve")
+    return ids, cnt
+
+
+def topk_for_length(n_tokens: int, block_size: int) -> int:
+    """k from the context length (SparDA page §3.2)."""
+    k = lib().oracle_topk_for_length(int(n_tokens), int(block_size))
+    if k < 0:
+        raise ValueError("oracle_topk_for_length: bad argument")
+    return k
 
 
 def lru_step(step: int, cache_slots: int, cur_ids, cur_count, prev_ids, prev_count,

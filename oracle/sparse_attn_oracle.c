@@ -237,6 +237,57 @@ int oracle_select(const oracle_problem* p, int unit_begin, int unit_end, const d
     return 0;
 }
 
+/* SparDA page §3.4: the selection result is extended by a reserve set of blocks kept
+ * at random; the union is taken as sets and emitted in ascending id order. */
+int oracle_union_reserve(const oracle_problem* p, int unit_begin, int unit_end,
+                         const int32_t* sel_ids, const int32_t* sel_count, int sel_stride,
+                         const int32_t* reserve, int n_reserve,
+                         int32_t* out_ids, int32_t* out_count, int out_stride)
+{
+    if (check_problem(p) || n_reserve < 0) return -1;
+    const int nb = oracle_num_blocks(p);
+    int32_t* all = (int32_t*)malloc(sizeof(int32_t) * (size_t)(sel_stride + n_reserve + 1));
+    if (!all) return -4;
+    for (int u = unit_begin; u < unit_end; ++u) {
+        int n = 0;
+        for (int i = 0; i < sel_count[u]; ++i) all[n++] = sel_ids[(size_t)u * sel_stride + i];
+        for (int i = 0; i < n_reserve; ++i) {
+            const int32_t j = reserve[(size_t)u * n_reserve + i];
+            if (j < 0 || j >= nb) {
+                free(all);
+                return -5;
+            }
+            all[n++] = j;
+        }
+        qsort(all, (size_t)n, sizeof *all, by_int_asc);
+        int m = 0;   /* drop repeats of the sorted list */
+        for (int i = 0; i < n; ++i)
+            if (m == 0 || all[i] != all[m - 1]) all[m++] = all[i];
+        if (m > out_stride) {
+            free(all);
+            return -3;
+        }
+        for (int i = 0; i < m; ++i) out_ids[(size_t)u * out_stride + i] = all[i];
+        out_count[u] = m;
+    }
+    free(all);
+    return 0;
+}
+
+/* SparDA page §3.2: the kept fraction falls with the sequence length -- none dropped
+ * up to 8K tokens, 15% at 16K, 10% at 32K, 5% at 128K; lengths between two listed
+ * points take the next listed point's ratio, and k = max(1, floor(nb * ratio)) as in
+ * the page's decode sketch (§3.4), in integer arithmetic. */
+int oracle_topk_for_length(int n_tokens, int block_size)
+{
+    if (n_tokens < 0 || block_size < 1) return -1;
+    const long long nb = ((long long)n_tokens + block_size - 1) / block_size;
+    if (n_tokens <= 8192) return (int)nb;
+    const long long percent = n_tokens <= 16384 ? 15 : (n_tokens <= 32768 ? 10 : 5);
+    const long long k = nb * percent / 100;
+    return (int)(k > 1 ? k : 1);
+}
+
 int oracle_select_level2(const oracle_problem* p, int unit_begin, int unit_end, const void* q,
                          const double* kmin, const double* kmax,
                          const int32_t* survivors, const int32_t* n_survivors, int surv_stride,

@@ -27,6 +27,12 @@
  *   decode          exact softmax attention over the union of the selected tokens
  *                   only (HiSparse->QSA page §3.3; SGLang page §1.2 select-then-compute).
  *   lru_step        step-to-step diff and LRU slot cache (SGLang page §3.2, steps a-d).
+ *   union_reserve   a selection united with a reserve set of extra blocks drawn at
+ *                   random by the caller (SparDA page §3.4: a small randomly kept
+ *                   "reserve set" added to the selection result).
+ *   topk_for_length k from the context length: no compression up to 8K tokens, then
+ *                   15% / 10% / 5% of the blocks up to 16K / 32K / beyond (SparDA page
+ *                   §3.2, sparsity ratio by sequence length; k = max(1, floor(nb * r))).
  *
  * Readings where the pages are silent are listed in the repository's design notes
  * and restated at each routine.  All arithmetic is double precision; stored bf16 /
@@ -97,6 +103,20 @@ int oracle_select_level2(const oracle_problem* p, int unit_begin, int unit_end, 
                          const int32_t* survivors, const int32_t* n_survivors, int surv_stride,
                          double* slice_scores, int32_t* sel_ids, int32_t* sel_count,
                          int sel_stride);
+
+/* Union of each unit's selection (ascending ids, sel_count[u] of them) with its
+ * n_reserve reserve block ids (any order; duplicates and window ids allowed), written
+ * ascending without duplicates to out_ids [units, out_stride] / out_count.  A reserve
+ * id outside [0, nb) is an error (-5). */
+int oracle_union_reserve(const oracle_problem* p, int unit_begin, int unit_end,
+                         const int32_t* sel_ids, const int32_t* sel_count, int sel_stride,
+                         const int32_t* reserve, int n_reserve,
+                         int32_t* out_ids, int32_t* out_count, int out_stride);
+
+/* k for a context of n_tokens in blocks of block_size tokens: every block when
+ * n_tokens <= 8192, else max(1, floor(nb * r)) with r = 15% (n_tokens <= 16384),
+ * 10% (<= 32768), 5% (beyond).  Negative on a bad argument. */
+int oracle_topk_for_length(int n_tokens, int block_size);
 
 /* out: [B, Hq, D]; only the heads of units [unit_begin, unit_end) are written. */
 int oracle_decode(const oracle_problem* p, int unit_begin, int unit_end, const void* q,
