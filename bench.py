@@ -255,8 +255,10 @@ def run_gpu_arm(args):
     launches_per_step = (3 if w.two_level else 2) + (1 if cache else 0)
     step_counter = [0]
 
+    reserve = inp.get("reserve_ids")   # random reserve set, drawn with the inputs
+
     def one_step(q):
-        dec.select(q)
+        dec.select(q, reserve)
         dec.decode(q, kp, vp, bt)
         if cache:
             cache.diff(step_counter[0])
@@ -282,7 +284,7 @@ def run_gpu_arm(args):
         q = q_all[(args.warmup + i) % q_all.shape[0]] if cache else q_static
         a, b, c, d = ev[i]
         a.record(stream)
-        dec.select(q)
+        dec.select(q, reserve)
         b.record(stream)
         dec.decode(q, kp, vp, bt)
         c.record(stream)
@@ -336,6 +338,8 @@ def run_gpu_arm(args):
     q_host = q_static.cpu().pin_memory()
     out_host = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
     q_dev = torch.empty_like(q_static)
+    res_host = reserve.cpu().pin_memory() if reserve is not None else None
+    res_dev = torch.empty_like(reserve) if reserve is not None else None
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     torch.cuda.synchronize()
     for i in range(K):
@@ -343,14 +347,17 @@ def run_gpu_arm(args):
         a, b = e2e_ev[i]
         a.record(stream)
         q_dev.copy_(q_host, non_blocking=True)
-        dec.select(q_dev)
+        if reserve is not None:
+            res_dev.copy_(res_host, non_blocking=True)
+        dec.select(q_dev, res_dev if reserve is not None else None)
         dec.decode(q_dev, kp, vp, bt)
         out_host.copy_(dec.out, non_blocking=True)
         b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = aggregate_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
     e2e = {"value": world * queries * K / (e2e_ms / 1e3), "unit": "queries/s",
-           "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+           "h2d_bytes_per_step": q_host.numel() * q_host.element_size() +
+                                 (res_host.numel() * 4 if res_host is not None else 0),
            "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
            "ms_per_step": e2e_ms / K}
 
@@ -433,6 +440,8 @@ def oracle_unit_step(p, a, kmin, kmax, kmean, u):
         else:
             sc = oracle.quest_scores(p, a["q"], kmin, kmax, units=rng)
         ids, cnt = oracle.select(p, sc, units=rng)
+    if "reserve_ids" in a:   # the reserve set joins the selection
+        ids, cnt = oracle.union_reserve(p, ids, cnt, a["reserve_ids"].reshape(p.units, -1), units=rng)
     oracle.decode(p, a["q"], a["k_pages"], a["v_pages"], a["block_table"], ids, cnt, units=rng)
 
 

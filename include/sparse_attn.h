@@ -102,6 +102,8 @@ typedef struct sparse_attn_params {
     int32_t kv_dtype;       /* SPARSE_ATTN_F32 or SPARSE_ATTN_BF16 for K/V pages and kmin/kmax */
     int32_t q_dtype;        /* SPARSE_ATTN_F32 or SPARSE_ATTN_BF16 */
     float softmax_scale;    /* <= 0: 1/sqrt(D) */
+    int32_t num_reserve;    /* >= 0 reserve block ids per unit (sparse_attn_select_reserved);
+                               0 for sparse_attn_select */
 } sparse_attn_params;
 
 /* Human-readable name of a status code (static storage). */
@@ -111,8 +113,16 @@ const char* sparse_attn_status_string(int status);
 int32_t sparse_attn_num_blocks(const sparse_attn_params* p);
 
 /* int32 entries per unit row of sel_ids (and of every diff list): the largest
- * selection possible, min(topk, candidates) + window blocks; -1 on bad params. */
+ * selection possible, min(topk, candidates) + min(num_reserve, candidates) + window
+ * blocks; -1 on bad params. */
 int32_t sparse_attn_sel_stride(const sparse_attn_params* p);
+
+/* k for a context of n_tokens in pages of block_size tokens, by the SparDA page's §3.2
+ * rule of a kept fraction falling with the sequence length: every block when
+ * n_tokens <= 8192, else max(1, floor(nb * r)) with r = 15% (n_tokens <= 16384),
+ * 10% (<= 32768) and 5% beyond (the page lists 16K, 32K, 128K; a length between two
+ * listed points takes the next point's ratio).  Host-only; -1 on a bad argument. */
+int32_t sparse_attn_topk_for_length(int32_t n_tokens, int32_t block_size);
 
 /* Bytes of workspace the calls below need for this problem. */
 int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes);
@@ -151,6 +161,18 @@ int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
 int sparse_attn_select(const sparse_attn_params* p, const void* q, const void* kmin,
                        const void* kmax, const float* kmean, int32_t* sel_ids,
                        int32_t* sel_count, void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
+/* sparse_attn_select plus a reserve set (SparDA page §3.4: a small set of extra blocks
+ * kept at random is added to every selection result).  reserve_ids: device int32
+ * [units, p->num_reserve], drawn by the caller (this library draws no random numbers);
+ * any order, repeats and window or top-k blocks allowed.  The output row is the union
+ * of the top-k, the reserve blocks and the window, ascending without repeats, so
+ * sel_count[u] varies with the overlap.  An id outside [0, nb) sets
+ * SPARSE_ATTN_ERR_SEL_ID and is skipped.  num_reserve = 0 is sparse_attn_select. */
+int sparse_attn_select_reserved(const sparse_attn_params* p, const void* q, const void* kmin,
+                                const void* kmax, const float* kmean, const int32_t* reserve_ids,
+                                int32_t* sel_ids, int32_t* sel_count, void* ws, size_t ws_bytes,
+                                sparse_attn_stream stream);
 
 /* Sparse decode attention (从HiSparse到QSA的移植实战 §3.3: iterate only the selected
  * blocks given as a compact index array; SGLang page §2.2, "finally the sparse attention").

@@ -36,13 +36,13 @@ class sparse_attn_params(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "n_tokens", "block_size",
         "num_pages", "window_tokens", "topk", "two_level", "coarse_block", "topk_coarse",
-        "score_kind", "kv_dtype", "q_dtype")] + [("softmax_scale", C.c_float)]
+        "score_kind", "kv_dtype", "q_dtype")] + [("softmax_scale", C.c_float), ("num_reserve", C.c_int32)]
 
 
 def make_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size, num_pages,
                 window_tokens, topk, two_level=False, coarse_block=1024, topk_coarse=48,
                 score_kind=SCORE_QUEST, kv_dtype=torch.bfloat16, q_dtype=torch.bfloat16,
-                softmax_scale=0.0) -> sparse_attn_params:
+                softmax_scale=0.0, num_reserve=0) -> sparse_attn_params:
     def code(dt):
         if dt in (torch.bfloat16, BF16):
             return BF16
@@ -54,7 +54,7 @@ def make_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size
     return sparse_attn_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size,
                               num_pages, window_tokens, topk, int(bool(two_level)), coarse_block,
                               topk_coarse, int(score_kind), code(kv_dtype), code(q_dtype),
-                              float(softmax_scale))
+                              float(softmax_scale), int(num_reserve))
 
 
 def params_for(w, **over) -> sparse_attn_params:
@@ -63,7 +63,8 @@ def params_for(w, **over) -> sparse_attn_params:
               head_dim=w.head_dim, n_tokens=w.n_tokens, block_size=w.block_size,
               num_pages=w.num_pages, window_tokens=w.window_tokens, topk=w.topk,
               two_level=w.two_level, coarse_block=w.coarse_block, topk_coarse=w.topk_coarse,
-              score_kind=w.score, kv_dtype=w.kv_dtype, q_dtype=w.q_dtype)
+              score_kind=w.score, kv_dtype=w.kv_dtype, q_dtype=w.q_dtype,
+              num_reserve=w.num_reserve)
     kw.update(over)
     return make_params(**kw)
 
@@ -94,6 +95,8 @@ def lib():
                                   vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_get_device_error": ([vp, sz, vp, u32p], C.c_int),
             "sparse_attn_select_noalloc": ([P, vp, vp, vp, vp, vp, vp, vp], C.c_int),
+            "sparse_attn_select_reserved": ([P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
+            "sparse_attn_topk_for_length": ([i32, i32], C.c_int32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -107,7 +110,8 @@ def exported_symbols():
     return ["sparse_attn_status_string", "sparse_attn_num_blocks", "sparse_attn_sel_stride",
             "sparse_attn_workspace_size", "sparse_attn_workspace_init", "sparse_attn_build_meta",
             "sparse_attn_select", "sparse_attn_decode", "sparse_attn_diff",
-            "sparse_attn_get_device_error", "sparse_attn_select_noalloc"]
+            "sparse_attn_get_device_error", "sparse_attn_select_noalloc",
+            "sparse_attn_select_reserved", "sparse_attn_topk_for_length"]
 
 
 def _status_string(status: int) -> str:
@@ -179,6 +183,20 @@ def sparse_attn_select(p, q, kmin, kmax, kmean, sel_ids, sel_count, ws, stream=N
     _check("sparse_attn_select", lib().sparse_attn_select(
         C.byref(p), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(kmean), _ptr(sel_ids), _ptr(sel_count),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_select_reserved(p, q, kmin, kmax, kmean, reserve_ids, sel_ids, sel_count, ws,
+                                stream=None) -> None:
+    _check("sparse_attn_select_reserved", lib().sparse_attn_select_reserved(
+        C.byref(p), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(kmean), _ptr(reserve_ids), _ptr(sel_ids),
+        _ptr(sel_count), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_topk_for_length(n_tokens: int, block_size: int) -> int:
+    k = lib().sparse_attn_topk_for_length(int(n_tokens), int(block_size))
+    if k < 0:
+        raise SparseAttnError("sparse_attn_topk_for_length", INVALID_ARG)
+    return int(k)
 
 
 def sparse_attn_decode(p, q, k_pages, v_pages, block_table, sel_ids, sel_count, out, ws,

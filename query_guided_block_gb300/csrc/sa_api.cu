@@ -21,7 +21,7 @@ int make_geometry(const sparse_attn_params* p, Geometry* g)
     memset(g, 0, sizeof *g);
     if (p->batch < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->head_dim < 1 ||
         p->n_tokens < 0 || p->block_size < 1 || p->num_pages < 0 || p->window_tokens < 0 ||
-        p->topk < 0 || p->topk_coarse < 0)
+        p->topk < 0 || p->topk_coarse < 0 || p->num_reserve < 0)
         return SPARSE_ATTN_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return SPARSE_ATTN_INVALID_ARG;
     if (p->two_level != 0 && p->two_level != 1) return SPARSE_ATTN_INVALID_ARG;
@@ -61,8 +61,11 @@ int make_geometry(const sparse_attn_params* p, Geometry* g)
     g->win_count = g->nb - g->win_first;
     g->n_cand = g->win_first;
     g->topk = p->topk;
+    g->n_reserve = p->num_reserve;
     const int k_max = p->topk < g->n_cand ? p->topk : g->n_cand;
-    g->sel_stride = k_max + g->win_count > 0 ? k_max + g->win_count : 1;
+    const int r_max = p->num_reserve < g->n_cand ? p->num_reserve : g->n_cand;
+    const int stride = k_max + r_max + g->win_count;
+    g->sel_stride = stride > 0 ? stride : 1;
     g->kv_bf16 = kv_bf16;
     g->q_bf16 = p->q_dtype == SPARSE_ATTN_BF16;
     g->two_level = p->two_level != 0;
@@ -207,13 +210,16 @@ int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int sparse_attn_select(const sparse_attn_params* p, const void* q, const void* kmin,
-                       const void* kmax, const float* kmean, int32_t* sel_ids,
-                       int32_t* sel_count, void* ws, size_t ws_bytes, sparse_attn_stream stream)
+static int select_common(const sparse_attn_params* p, const void* q, const void* kmin,
+                         const void* kmax, const float* kmean, const int32_t* reserve_ids,
+                         int32_t* sel_ids, int32_t* sel_count, void* ws, size_t ws_bytes,
+                         sparse_attn_stream stream)
 {
     Geometry g;
     int st = make_geometry(p, &g);
     if (st) return st;
+    if (g.n_reserve > 0 && g.units() > 0 && (!reserve_ids || !aligned(reserve_ids, 4)))
+        return SPARSE_ATTN_INVALID_ARG;
     const WorkspaceLayout L = workspace_layout(g);
     if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
     if (g.units() > 0) {
@@ -228,8 +234,34 @@ int sparse_attn_select(const sparse_attn_params* p, const void* q, const void* k
                 return SPARSE_ATTN_INVALID_ARG;
         }
     }
-    return status_of(launch_select(g, L, static_cast<char*>(ws), q, kmin, kmax, kmean, sel_ids,
+    return status_of(launch_select(g, L, static_cast<char*>(ws), q, kmin, kmax, kmean, reserve_ids, sel_ids,
                                    sel_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_select(const sparse_attn_params* p, const void* q, const void* kmin,
+                       const void* kmax, const float* kmean, int32_t* sel_ids,
+                       int32_t* sel_count, void* ws, size_t ws_bytes, sparse_attn_stream stream)
+{
+    if (p && p->num_reserve != 0) return SPARSE_ATTN_INVALID_ARG;   // use sparse_attn_select_reserved
+    return select_common(p, q, kmin, kmax, kmean, nullptr, sel_ids, sel_count, ws, ws_bytes, stream);
+}
+
+int sparse_attn_select_reserved(const sparse_attn_params* p, const void* q, const void* kmin,
+                                const void* kmax, const float* kmean, const int32_t* reserve_ids,
+                                int32_t* sel_ids, int32_t* sel_count, void* ws, size_t ws_bytes,
+                                sparse_attn_stream stream)
+{
+    return select_common(p, q, kmin, kmax, kmean, reserve_ids, sel_ids, sel_count, ws, ws_bytes, stream);
+}
+
+int32_t sparse_attn_topk_for_length(int32_t n_tokens, int32_t block_size)
+{
+    if (n_tokens < 0 || block_size < 1) return -1;
+    const long long nb = ((long long)n_tokens + block_size - 1) / block_size;
+    if (n_tokens <= 8192) return int32_t(nb);                 // short contexts keep every block
+    const long long percent = n_tokens <= 16384 ? 15 : (n_tokens <= 32768 ? 10 : 5);
+    const long long k = nb * percent / 100;
+    return int32_t(k > 1 ? k : 1);
 }
 
 int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k_pages,
@@ -328,7 +360,7 @@ int sparse_attn_select_noalloc(const sparse_attn_params* p, const void* q, const
     Geometry g;
     int st = make_geometry(p, &g);
     if (st) return st;
-    if (g.two_level) return SPARSE_ATTN_UNSUPPORTED;
+    if (g.two_level || g.n_reserve != 0) return SPARSE_ATTN_UNSUPPORTED;
     const WorkspaceLayout L = workspace_layout(g);
     // select touches the header, the counter rows and the score rows only
     const size_t need = L.scores + size_t(g.units()) * L.score_cols * sizeof(float);
@@ -349,7 +381,7 @@ int sparse_attn_select_noalloc(const sparse_attn_params* p, const void* q, const
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // error word and completion counters must start at zero; scores need no clearing
     if (cudaMemsetAsync(ws, 0, L.scores, s) != cudaSuccess) return SPARSE_ATTN_CUDA_ERROR;
-    return status_of(launch_select(g, L, ws, q, kmin, kmax, kmean, sel_ids, sel_count, s));
+    return status_of(launch_select(g, L, ws, q, kmin, kmax, kmean, nullptr, sel_ids, sel_count, s));
 }
 
 }  // extern "C"

@@ -22,6 +22,7 @@ struct Geometry {
     int coarse_block, per_coarse, n_coarse, topk_coarse;
     int mean_block, n_mean;        // kmean rows per unit
     int topk;
+    int n_reserve;                 // reserve block ids per unit (0: none)
     int score_kind;
     float scale_log2;              // softmax_scale * log2(e)
     int units() const { return B * Hkv; }
@@ -66,7 +67,8 @@ cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int3
 
 cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* kmin, const void* kmax, const float* kmean,
-                          int32_t* sel_ids, int32_t* sel_count, cudaStream_t s);
+                          const int32_t* reserve_ids, int32_t* sel_ids, int32_t* sel_count,
+                          cudaStream_t s);
 
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* k_pages, const void* v_pages, const int32_t* block_table,

@@ -60,6 +60,8 @@ struct SelectArgs {
     // selection
     int k;
     int win_first, win_count;
+    const int32_t* reserve;  // [units, n_reserve] extra block ids united with the top-k (or null)
+    int n_reserve;
     int32_t* out_ids;
     int out_stride;
     int32_t* out_count;
@@ -245,6 +247,48 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
         if (mode == 1) return (key & mask) >= prefix;
         return key > T || (key == T && c <= cT);
     };
+    if (a.n_reserve > 0) {
+        // Reserve set (SparDA page §3.4): the top-k rows and the unit's reserve blocks
+        // outside the window are marked in a bitmap over block ids (the histogram's
+        // storage, free now), then emitted in ascending order, then the window.
+        uint32_t* bits = hist;
+        const int nw = (a.rows + 31) >> 5;   // <= kBins words: rows <= 16384
+        for (int i = tid; i < nw; i += kSelThreads) bits[i] = 0u;
+        __syncthreads();
+        for (int c = tid; c < n; c += kSelThreads)
+            if (selected(c)) {
+                const int r = candidate_row(a, u, c);
+                atomicOr(&bits[r >> 5], 1u << (r & 31));
+            }
+        for (int i = tid; i < a.n_reserve; i += kSelThreads) {
+            const int j = a.reserve[size_t(u) * a.n_reserve + i];
+            if (j < 0 || j >= a.rows) raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
+            else if (j < a.win_first) atomicOr(&bits[j >> 5], 1u << (j & 31));
+        }
+        __syncthreads();
+        const int per = (nw + kSelThreads - 1) / kSelThreads;   // words per thread, in order
+        const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
+        int cnt = 0;
+        for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+        int inc = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(kFullMask, inc, off);
+            if (lane >= off) inc += t;
+        }
+        if (lane == 31) s_wtot[warp] = inc;
+        __syncthreads();
+        int pos = inc - cnt, total = 0;
+        for (int wv = 0; wv < kSelWarps; ++wv) {
+            pos += wv < warp ? s_wtot[wv] : 0;
+            total += s_wtot[wv];
+        }
+        for (int w = w0; w < w1; ++w)
+            for (uint32_t m = bits[w]; m; m &= m - 1) out[pos++] = w * 32 + (__ffs(m) - 1);
+        for (int i = tid; i < a.win_count; i += kSelThreads) out[total + i] = a.win_first + i;
+        if (tid == 0) a.out_count[u] = total + a.win_count;
+        return;
+    }
     // Each warp owns a contiguous chunk of candidates, read lane-interleaved, so ballot
     // order is candidate order.
     const int chunk = ((n + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;
@@ -535,7 +579,8 @@ cudaError_t dispatch_select(const SelectArgs& a, int kind, bool mbf16, int D, in
 
 cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* kmin, const void* kmax, const float* kmean,
-                          int32_t* sel_ids, int32_t* sel_count, cudaStream_t s)
+                          const int32_t* reserve_ids, int32_t* sel_ids, int32_t* sel_count,
+                          cudaStream_t s)
 {
     const int units = g.units();
     if (units == 0) return cudaSuccess;
@@ -562,6 +607,8 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
         a.k = g.topk;
         a.win_first = g.win_first;
         a.win_count = g.win_count;
+        a.reserve = reserve_ids;
+        a.n_reserve = g.n_reserve;
         a.out_ids = sel_ids;
         a.out_stride = g.sel_stride;
         a.out_count = sel_count;
@@ -588,6 +635,8 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     l1.k = g.topk_coarse;
     l1.win_first = 0;
     l1.win_count = 0;
+    l1.reserve = nullptr;
+    l1.n_reserve = 0;
     l1.out_ids = surv;
     l1.out_stride = g.topk_coarse > 0 ? g.topk_coarse : 1;
     l1.out_count = n_surv;
@@ -611,6 +660,8 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     l2.k = g.topk;
     l2.win_first = g.win_first;
     l2.win_count = g.win_count;
+    l2.reserve = reserve_ids;
+    l2.n_reserve = g.n_reserve;
     l2.out_ids = sel_ids;
     l2.out_stride = g.sel_stride;
     l2.out_count = sel_count;

@@ -53,7 +53,15 @@ class SparseDecoder:
         B.sparse_attn_build_meta(self.p, k_pages, block_table, self.kmin, self.kmax, self.kmean,
                                  self.ws, stream)
 
-    def select(self, q, stream=None):
+    def select(self, q, reserve_ids=None, stream=None):
+        """Selection; with ``reserve_ids`` [B, Hkv, num_reserve] int32 (drawn by the caller)
+        the reserve set is united with every unit's top-k."""
+        if self.p.num_reserve > 0:
+            if reserve_ids is None:
+                raise ValueError("this problem has num_reserve > 0: pass reserve_ids")
+            B.sparse_attn_select_reserved(self.p, q, self.kmin, self.kmax, self.kmean, reserve_ids,
+                                          self.sel_ids, self.sel_count, self.ws, stream)
+            return
         B.sparse_attn_select(self.p, q, self.kmin, self.kmax, self.kmean, self.sel_ids,
                              self.sel_count, self.ws, stream)
 
@@ -64,9 +72,9 @@ class SparseDecoder:
                              self.sel_count if sel_count is None else sel_count,
                              self.out if out is None else out, self.ws, stream)
 
-    def step(self, q, k_pages, v_pages, block_table, stream=None):
+    def step(self, q, k_pages, v_pages, block_table, reserve_ids=None, stream=None):
         """select + decode for one query batch; returns the output tensor."""
-        self.select(q, stream)
+        self.select(q, reserve_ids, stream)
         self.decode(q, k_pages, v_pages, block_table, stream=stream)
         return self.out
 

@@ -60,6 +60,7 @@ class Workload:
     steps: int = 1                   # consecutive decode steps (query drift)
     q_drift: float = 0.15            # q_t = normalise(q_{t-1} + drift*N(0,I)) * |q_0|
     cache_slots: int = 0             # LRU slots per (sequence, KV head); 0 = no diff
+    num_reserve: int = 0             # random reserve blocks per (sequence, KV head)
     seed: int = 0
     description: str = ""
 
@@ -106,6 +107,10 @@ WORKLOADS: Dict[str, Workload] = {
            two_level=True, coarse_block=1024, topk_coarse=48, planted_per_unit=82,
            description="B8 H32/8 D128 N262144 bs64 bf16, L1 mean top-48 of 256x1024, "
                        "L2 Quest top-48 slices + 512 window, 2% planted"),
+        _w(name="reserve_128k", batch=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+           n_tokens=131072, block_size=32, window_tokens=512, topk=64,
+           planted_per_unit=41, num_reserve=41,
+           description="gqa_128k plus a 1% random reserve set (41 blocks) per KV head"),
         _w(name="lru_64k", batch=32, num_q_heads=32, num_kv_heads=8, head_dim=128,
            n_tokens=65536, block_size=64, window_tokens=512, topk=32,
            steps=64, q_drift=0.15, cache_slots=128,
@@ -150,6 +155,8 @@ def make_inputs(w: Workload, device="cpu", planted_blocks: Optional[torch.Tensor
     * ``k_pages``, ``v_pages``  [num_pages, Hkv, block_size, D]; dtype ``kv_dtype``
     * ``block_table``  [B, num_blocks] int32, a seeded permutation of the page pool
     * ``planted``      [B, Hkv, P] int64 logical block ids of planted blocks (P may be 0)
+    * ``reserve_ids``  [B, Hkv, num_reserve] int32 random blocks (only when num_reserve > 0):
+                       the first num_reserve of a seeded permutation of all nb blocks
     """
     device = torch.device(device)
     B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -213,8 +220,13 @@ def make_inputs(w: Workload, device="cpu", planted_blocks: Optional[torch.Tensor
         vals = noise + shift.view(B, Hkv, 1, 1, D)
         k_pages[pages.reshape(-1), h_idx.reshape(-1)] = vals.reshape(-1, bs, D).to(w.kv_dtype)
 
-    return {"q": q, "k_pages": k_pages, "v_pages": v_pages,
-            "block_table": block_table, "planted": planted}
+    out = {"q": q, "k_pages": k_pages, "v_pages": v_pages,
+           "block_table": block_table, "planted": planted}
+    if w.num_reserve > 0:
+        gr = _gen(w, "reserve", device)
+        keys = torch.rand(B * Hkv, nb, generator=gr, device=device)
+        out["reserve_ids"] = keys.argsort(dim=1)[:, :w.num_reserve].to(torch.int32).view(B, Hkv, -1)
+    return out
 
 
 def gather_sequences(inp: dict, seqs, device="cpu") -> dict:
@@ -226,7 +238,10 @@ def gather_sequences(inp: dict, seqs, device="cpu") -> dict:
     pages = bt.reshape(-1)
     q = inp["q"]
     q = q[:, seqs] if q.dim() == 4 else q[seqs]
-    return {"k_pages": inp["k_pages"][pages].to(device),
+    extra = {}
+    if "reserve_ids" in inp:
+        extra["reserve_ids"] = inp["reserve_ids"][seqs].to(device)
+    return {**extra, "k_pages": inp["k_pages"][pages].to(device),
             "v_pages": inp["v_pages"][pages].to(device),
             "block_table": torch.arange(pages.numel(), dtype=torch.int32,
                                         device=device).view(len(seqs), -1),

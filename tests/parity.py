@@ -55,7 +55,8 @@ def check_selection(gpu_ids, gpu_cnt, ora_ids, ora_cnt, scores, k, win_first, un
     return waived
 
 
-def check_two_level(w, p, host_q, kmin, kmax, kmean, gpu_ids, gpu_cnt, units, rel=NEAR_TIE_REL):
+def check_two_level(w, p, host_q, kmin, kmax, kmean, gpu_ids, gpu_cnt, units, rel=NEAR_TIE_REL,
+                    reserve=None):
     """Two-level selection: level-1 survivors are unique unless coarse scores tie within
     `rel` of the K1-th; every admissible survivor set is tried, and level 2 is compared
     with the near-tie waiver."""
@@ -81,6 +82,9 @@ def check_two_level(w, p, host_q, kmin, kmax, kmean, gpu_ids, gpu_cnt, units, re
             sv[u, : len(surv)] = surv
             ns[u] = len(surv)
             r2 = oracle.select_level2(p, host_q, kmin, kmax, sv, ns, units=(u, u + 1))
+            if reserve is not None:   # the reserve set joins the level-2 result
+                r2["sel_ids"], r2["sel_count"] = oracle.union_reserve(
+                    p, r2["sel_ids"], r2["sel_count"], reserve, units=(u, u + 1))
             try:
                 check_selection(gpu_ids, gpu_cnt, r2["sel_ids"], r2["sel_count"],
                                 np.nan_to_num(r2["slice_scores"], nan=-np.inf), p.topk,

@@ -35,7 +35,7 @@ def test_header_and_binding_agree(L):
 
 def test_sizes_for_the_five_workloads(L):
     expect_stride = {"tiny_fp32_4k": 8 + 2, "mha_32k": 32 + 8, "gqa_128k": 64 + 16,
-                     "two_level_256k": 48 + 8, "lru_64k": 32 + 8}
+                     "two_level_256k": 48 + 8, "lru_64k": 32 + 8, "reserve_128k": 64 + 41 + 16}
     for name, w in WORKLOADS.items():
         p = B.params_for(w)
         assert B.sparse_attn_num_blocks(p) == w.num_blocks
@@ -55,7 +55,8 @@ def test_bad_parameters_are_rejected(L):
                          (dict(n_tokens=16384 * 32 + 1), B.UNSUPPORTED),   # > 16384 blocks
                          (dict(two_level=True, coarse_block=1000), B.INVALID_ARG),
                          (dict(softmax_scale=float("nan")), B.INVALID_ARG),
-                         (dict(num_pages=0), B.INVALID_ARG)]:
+                         (dict(num_pages=0), B.INVALID_ARG),
+                         (dict(num_reserve=-1), B.INVALID_ARG)]:
         p = B.params_for(w, **change)
         assert L.sparse_attn_workspace_size(C.byref(p), C.byref(n)) == want, change
     assert L.sparse_attn_workspace_size(None, C.byref(n)) == B.INVALID_ARG
@@ -90,3 +91,21 @@ def test_null_and_misaligned_pointers_are_rejected_before_launch(L):
 def test_status_strings(L):
     for s in range(5):
         assert L.sparse_attn_status_string(s)
+
+
+def test_topk_for_length_matches_the_oracle(L):
+    """The host-side k rule (SparDA page §3.2) agrees with the oracle's statement of it."""
+    import oracle
+    for bs in (8, 32, 64, 128):
+        for n in list(range(0, 70000, 777)) + [8192, 8193, 16384, 16385, 32768, 32769, 131072, 262144]:
+            assert B.sparse_attn_topk_for_length(n, bs) == oracle.topk_for_length(n, bs), (n, bs)
+    assert L.sparse_attn_topk_for_length(-1, 64) == -1
+    assert L.sparse_attn_topk_for_length(100, 0) == -1
+
+
+def test_plain_select_refuses_a_reserve_count(L):
+    """A problem with num_reserve > 0 must go through sparse_attn_select_reserved; the
+    check is on the host, before any device pointer is touched."""
+    p = B.params_for(WORKLOADS["reserve_128k"])
+    rc = L.sparse_attn_select(C.byref(p), None, None, None, None, None, None, None, 0, None)
+    assert rc == B.INVALID_ARG

@@ -36,7 +36,7 @@ def run_gpu(w, inp, params=None):
     dec = SparseDecoder(p)
     dec.build_meta(inp["k_pages"], inp["block_table"])
     q = inp["q"] if inp["q"].dim() == 3 else inp["q"][0]
-    dec.select(q)
+    dec.select(q, inp.get("reserve_ids"))
     dec.decode(q, inp["k_pages"], inp["v_pages"], inp["block_table"])
     flags = dec.device_error()
     assert flags == 0, f"device error flags 0x{flags:x}"
@@ -60,14 +60,18 @@ def compare_all(w, inp, dec, seqs=None):
     gids = as_np(dec.sel_ids).reshape(w.units, -1)[rows]
     gcnt = as_np(dec.sel_count).reshape(-1)[rows]
     hq = host["q"] if host["q"].dim() == 3 else host["q"][0]
+    reserve = as_np(host["reserve_ids"]).reshape(ws.units, -1) if w.num_reserve else None
     if w.two_level:
-        check_two_level(ws, p, hq, kmin, kmax, kmean, gids, gcnt, units=range(ws.units))
+        check_two_level(ws, p, hq, kmin, kmax, kmean, gids, gcnt, units=range(ws.units),
+                        reserve=reserve)
     else:
         if w.score == "mean":
             scores = oracle.mean_scores(p, hq, kmean)
         else:
             scores = oracle.quest_scores(p, hq, kmin, kmax)
         oid, ocnt = oracle.select(p, scores)
+        if reserve is not None:   # SparDA page §3.4: the reserve set joins the selection
+            oid, ocnt = oracle.union_reserve(p, oid, ocnt, reserve)
         check_selection(gids, gcnt, oid, ocnt, scores, w.topk, p.first_window_block())
     # attention on the GPU's own selection
     out = oracle.decode(p, hq, host["k_pages"], host["v_pages"], host["block_table"], gids, gcnt)
@@ -127,6 +131,43 @@ def test_two_level_small(n_tokens, topk, window):
     inp = make_inputs(w, "cuda")
     dec = run_gpu(w, inp)
     compare_all(w, inp, dec)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(n_tokens=20000, block_size=32, topk=10, num_reserve=7, planted_per_unit=4),
+    dict(n_tokens=9001, block_size=64, topk=3, num_reserve=40, window_tokens=700),
+    dict(n_tokens=7000, block_size=16, topk=0, num_reserve=5, head_dim=64, num_q_heads=16),
+    dict(n_tokens=60000, block_size=64, topk=9, num_reserve=6, two_level=True, coarse_block=1024,
+         topk_coarse=5, planted_per_unit=8),
+], ids=["single", "many", "k0", "two_level"])
+def test_reserve_set(cfg):
+    """Selection united with a caller-drawn reserve set (SparDA page §3.4); the drawn
+    ids are overwritten so that repeats, window blocks and top-k blocks all occur."""
+    w = _w(**cfg)
+    inp = make_inputs(w, "cuda")
+    r = inp["reserve_ids"]
+    nb, wf = w.num_blocks, (max(0, w.n_tokens - w.window_tokens) // w.block_size
+                            if w.window_tokens else w.num_blocks)
+    r[..., 0] = r[..., 1]                        # a repeat
+    r[..., 2] = nb - 1                           # a window block (or the last block)
+    if w.planted_per_unit:
+        r[..., 3] = inp["planted"][..., 0].to(torch.int32)   # very likely a top-k block
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+    cnt = as_np(dec.sel_count).reshape(-1)
+    assert cnt.max() <= dec.sel_stride
+
+
+def test_reserve_id_out_of_range_sets_the_error_bit():
+    w = _w(n_tokens=8192, block_size=64, topk=4, num_reserve=3)
+    inp = make_inputs(w, "cuda")
+    inp["reserve_ids"][0, 0, 1] = w.num_blocks      # outside [0, nb): reported and skipped
+    dec = SparseDecoder(B.params_for(w))
+    dec.build_meta(inp["k_pages"], inp["block_table"])
+    dec.select(inp["q"], inp["reserve_ids"])
+    assert dec.device_error() & B.ERR_SEL_ID
+    ids = as_np(dec.sel_ids)[0, 0, : as_np(dec.sel_count)[0, 0]]
+    assert w.num_blocks not in ids.tolist() and (np.diff(ids) > 0).all()
 
 
 def test_ties_go_to_the_lower_block_id():
@@ -203,7 +244,7 @@ def test_largest_block_count():
 
 # ----------------------------------------------------------- full sizes ----
 
-@pytest.mark.parametrize("name", ["mha_32k", "gqa_128k", "two_level_256k"])
+@pytest.mark.parametrize("name", ["mha_32k", "gqa_128k", "two_level_256k", "reserve_128k"])
 def test_full_size_sampled(name):
     """The full configuration in the launch configuration the benchmark times; the
     first and last sequences are checked against the oracle in full."""
