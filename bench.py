@@ -217,7 +217,7 @@ def run_gpu_arm(args):
 
     from query_guided_block_gb300 import binding as Bn
     from query_guided_block_gb300.build import build
-    from query_guided_block_gb300.decoder import SlotCache, SparseDecoder
+    from query_guided_block_gb300.decoder import SlotCache, SlotPool, SparseDecoder
     from query_guided_block_gb300.workloads import WORKLOADS, make_inputs
 
     if rank == 0 or world == 1:
@@ -237,6 +237,14 @@ def run_gpu_arm(args):
     kp, vp, bt = inp["k_pages"], inp["v_pages"], inp["block_table"]
     cache = SlotCache(dec, w.cache_slots) if w.cache_slots else None
     stream = torch.cuda.current_stream()
+    # --io: K/V come from a pinned host store through the slot pool (misses loaded each step)
+    io = bool(args.io and cache)
+    if args.io and not cache:
+        raise SystemExit("--io needs a workload with an LRU slot cache (lru_64k)")
+    pool = SlotPool(cache) if io else None
+    host_k = kp.cpu().pin_memory() if io else None
+    host_v = vp.cpu().pin_memory() if io else None
+    miss_total = torch.zeros((), dtype=torch.int64, device=dev) if io else None
 
     # metadata (prefill-time), timed on its own
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -252,16 +260,26 @@ def run_gpu_arm(args):
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    launches_per_step = (3 if w.two_level else 2) + (1 if cache else 0)
+    launches_per_step = (3 if w.two_level else 2) + (1 if cache else 0) + (2 if io else 0)
     step_counter = [0]
 
     reserve = inp.get("reserve_ids")   # random reserve set, drawn with the inputs
 
+    def io_phase():   # diff, misses in from the host store, slot map
+        cache.diff(step_counter[0])
+        pool.load_misses(host_k, host_v, bt)
+        pool.slot_map()
+
     def one_step(q):
         dec.select(q, reserve)
-        dec.decode(q, kp, vp, bt)
+        if io:
+            io_phase()
+            pool.decode(q)
+        else:
+            dec.decode(q, kp, vp, bt)
+            if cache:
+                cache.diff(step_counter[0])
         if cache:
-            cache.diff(step_counter[0])
             cache.advance()
             step_counter[0] += 1
 
@@ -286,13 +304,21 @@ def run_gpu_arm(args):
         a.record(stream)
         dec.select(q, reserve)
         b.record(stream)
-        dec.decode(q, kp, vp, bt)
-        c.record(stream)
+        if io:                       # a select b diff + misses + map c decode d
+            io_phase()
+            c.record(stream)
+            pool.decode(q)
+            d.record(stream)
+            miss_total.add_(cache.counts[:, 1].sum())
+        else:                        # a select b decode c diff d
+            dec.decode(q, kp, vp, bt)
+            c.record(stream)
+            if cache:
+                cache.diff(step_counter[0])
+            d.record(stream)
         if cache:
-            cache.diff(step_counter[0])
             cache.advance()
             step_counter[0] += 1
-        d.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t_end = time.time()
@@ -304,7 +330,7 @@ def run_gpu_arm(args):
         raise RuntimeError(f"device error flags 0x{flags:x}")
 
     sel_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    dec_ms = [e[2].elapsed_time(e[3]) if io else e[1].elapsed_time(e[2]) for e in ev]
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     total_ms_local = sum(step_ms)
     total_ms = aggregate_max(total_ms_local, world, dev)
@@ -321,7 +347,13 @@ def run_gpu_arm(args):
         "decode": {"ms": dec_avg, "bytes": nbytes["decode"], "gbs": nbytes["decode"] / dec_avg / 1e6,
                    "launches_per_step": 1},
     }
-    if cache:
+    if io:
+        io_ms = statistics.mean([e[1].elapsed_time(e[2]) for e in ev])
+        io_bytes = float(miss_total.item()) * 2 * pool.tile_bytes() / K
+        kern["diff_io"] = {"ms": io_ms, "misses_bytes": io_bytes, "host_read_gbs": io_bytes / io_ms / 1e6,
+                           "launches_per_step": 3,
+                           "note": "diff + miss tiles read from pinned host memory + slot map"}
+    elif cache:
         kern["diff"] = {"ms": statistics.mean([e[2].elapsed_time(e[3]) for e in ev]),
                         "launches_per_step": 1}
     dominant = "select" if sel_avg >= dec_avg else "decode"
@@ -350,7 +382,13 @@ def run_gpu_arm(args):
         if reserve is not None:
             res_dev.copy_(res_host, non_blocking=True)
         dec.select(q_dev, res_dev if reserve is not None else None)
-        dec.decode(q_dev, kp, vp, bt)
+        if io:
+            io_phase()
+            pool.decode(q_dev)
+            cache.advance()
+            step_counter[0] += 1
+        else:
+            dec.decode(q_dev, kp, vp, bt)
         out_host.copy_(dec.out, non_blocking=True)
         b.record(stream)
     torch.cuda.synchronize()
@@ -378,7 +416,7 @@ def run_gpu_arm(args):
         "vs_baseline": None,
         "dtype": "bf16" if w.kv_dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded; planted relevant blocks)",
-        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
+        "config": {"workload": w.name + ("+io" if io else ""), "batch": w.batch, "q_heads": w.num_q_heads,
                    "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "context": w.n_tokens,
                    "block_size": w.block_size, "topk_blocks": w.topk,
                    "window_tokens": w.window_tokens, "two_level": w.two_level,
@@ -521,6 +559,9 @@ def main():
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--io", action="store_true",
+                    help="LRU workloads: K/V read through the slot pool, misses loaded each step "
+                         "from a pinned host store")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -206,6 +206,42 @@ int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* s
                      int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, void* ws,
                      size_t ws_bytes, sparse_attn_stream stream);
 
+/* ---- Slot pool: misses loaded from a host-resident store ("SGLang分层稀疏注意力技术解析与
+ * 优化实践" §3.3 IO transfer: full KV cache page-first in pinned / host-registered
+ * memory, zero-copy transfer of a step's misses batched over requests; §3.2 steps c-d:
+ * load the misses into the claimed slots, then update the index).
+ * The pool holds, per unit, cache_slots page tiles: pool_k / pool_v [B*Hkv, cache_slots,
+ * block_size, D] in the KV dtype, owned by the caller; slot s of unit u holds the block
+ * the diff's slot_block[u][s] names. */
+
+/* sel_slot[u][i] = the slot of unit u holding sel_ids[u][i] (i < sel_count[u]), from
+ * the slot_block state after sparse_attn_diff of this step; a selected block that is not
+ * resident gets -1 and sets SPARSE_ATTN_ERR_SLOT.  sel_slot: [B*Hkv, sel_stride] int32. */
+int sparse_attn_slot_map(const sparse_attn_params* p, const int32_t* sel_ids,
+                         const int32_t* sel_count, const int32_t* slot_block, int32_t cache_slots,
+                         int32_t* sel_slot, void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
+/* IO kernel: for every unit u and miss i < counts[u][1], copy the K and V tiles of
+ * block miss_ids[u][i] (page block_table[b][miss_ids], KV head u % Hkv) from the host
+ * store into slot miss_slot[u][i] of pool_k / pool_v, in one launch.  host_k_pages /
+ * host_v_pages: [num_pages, Hkv, block_size, D] page-first, in pinned or
+ * cudaHostRegister'ed host memory (read by the GPU in place) or in device memory;
+ * unregistered host memory is INVALID_ARG.  miss_ids / miss_slot / counts as written by
+ * sparse_attn_diff.  Out-of-range ids, slots or pages set an error bit and are skipped. */
+int sparse_attn_load_misses(const sparse_attn_params* p, const void* host_k_pages,
+                            const void* host_v_pages, const int32_t* block_table,
+                            const int32_t* miss_ids, const int32_t* miss_slot, const int32_t* counts,
+                            int32_t cache_slots, void* pool_k, void* pool_v, void* ws,
+                            size_t ws_bytes, sparse_attn_stream stream);
+
+/* sparse_attn_decode reading K/V through the slot pool: the tokens of selected block
+ * sel_ids[u][i] come from slot sel_slot[u][i] of unit u's pool (the page table and the
+ * page pools are not read).  Same output and error rules as sparse_attn_decode. */
+int sparse_attn_decode_slots(const sparse_attn_params* p, const void* q, const void* pool_k,
+                             const void* pool_v, int32_t cache_slots, const int32_t* sel_ids,
+                             const int32_t* sel_slot, const int32_t* sel_count, float* out,
+                             void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
 /* Synchronise `stream`, copy the device error word to *flags (SPARSE_ATTN_ERR_* bits)
  * and clear it.  Returns SPARSE_ATTN_DEVICE_BOUNDS when any bit was set. */
 int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream stream,

@@ -97,6 +97,9 @@ def lib():
             "sparse_attn_select_noalloc": ([P, vp, vp, vp, vp, vp, vp, vp], C.c_int),
             "sparse_attn_select_reserved": ([P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_topk_for_length": ([i32, i32], C.c_int32),
+            "sparse_attn_slot_map": ([P, vp, vp, vp, i32, vp, vp, sz, vp], C.c_int),
+            "sparse_attn_load_misses": ([P, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp], C.c_int),
+            "sparse_attn_decode_slots": ([P, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp], C.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -111,7 +114,8 @@ def exported_symbols():
             "sparse_attn_workspace_size", "sparse_attn_workspace_init", "sparse_attn_build_meta",
             "sparse_attn_select", "sparse_attn_decode", "sparse_attn_diff",
             "sparse_attn_get_device_error", "sparse_attn_select_noalloc",
-            "sparse_attn_select_reserved", "sparse_attn_topk_for_length"]
+            "sparse_attn_select_reserved", "sparse_attn_topk_for_length",
+            "sparse_attn_slot_map", "sparse_attn_load_misses", "sparse_attn_decode_slots"]
 
 
 def _status_string(status: int) -> str:
@@ -221,6 +225,39 @@ def sparse_attn_select_noalloc(p, q, kmin, kmax, kmean, sel_ids, sel_count, stre
     callers that cannot allocate device memory (see the C header)."""
     _check("sparse_attn_select_noalloc", lib().sparse_attn_select_noalloc(
         C.byref(p), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(kmean), _ptr(sel_ids), _ptr(sel_count),
+        _stream(stream)))
+
+
+def _host_or_cuda_ptr(t: torch.Tensor):
+    """Pointer of a contiguous tensor that may live in pinned host memory (the library
+    reads pinned / registered host memory in place) or on the device."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("host K/V store must be in pinned memory")
+    return C.c_void_p(t.data_ptr())
+
+
+def sparse_attn_slot_map(p, sel_ids, sel_count, slot_block, cache_slots, sel_slot, ws,
+                         stream=None) -> None:
+    _check("sparse_attn_slot_map", lib().sparse_attn_slot_map(
+        C.byref(p), _ptr(sel_ids), _ptr(sel_count), _ptr(slot_block), int(cache_slots),
+        _ptr(sel_slot), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_load_misses(p, host_k_pages, host_v_pages, block_table, miss_ids, miss_slot,
+                            counts, cache_slots, pool_k, pool_v, ws, stream=None) -> None:
+    _check("sparse_attn_load_misses", lib().sparse_attn_load_misses(
+        C.byref(p), _host_or_cuda_ptr(host_k_pages), _host_or_cuda_ptr(host_v_pages),
+        _ptr(block_table), _ptr(miss_ids), _ptr(miss_slot), _ptr(counts), int(cache_slots),
+        _ptr(pool_k), _ptr(pool_v), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_decode_slots(p, q, pool_k, pool_v, cache_slots, sel_ids, sel_slot, sel_count,
+                             out, ws, stream=None) -> None:
+    _check("sparse_attn_decode_slots", lib().sparse_attn_decode_slots(
+        C.byref(p), _ptr(q), _ptr(pool_k), _ptr(pool_v), int(cache_slots), _ptr(sel_ids),
+        _ptr(sel_slot), _ptr(sel_count), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
 
 

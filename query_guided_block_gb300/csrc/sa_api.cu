@@ -283,7 +283,7 @@ int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k
             return SPARSE_ATTN_INVALID_ARG;
     }
     return status_of(launch_decode(g, L, static_cast<char*>(ws), q, k_pages, v_pages, block_table,
-                                   sel_ids, sel_count, out, reinterpret_cast<cudaStream_t>(stream)));
+                                   sel_ids, sel_count, out, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
@@ -327,6 +327,87 @@ int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream s
     *flags = word;
     return word ? SPARSE_ATTN_DEVICE_BOUNDS : SPARSE_ATTN_OK;
 }
+
+// ---- slot pool: misses from a host-resident store, decode through the slots ----
+// A device-accessible address for a caller buffer that may be pinned / registered host
+// memory (page-first K/V store) or device memory; null for unregistered host memory.
+static const void* device_view(const void* ptr)
+{
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return ptr;
+    if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+    return nullptr;
+}
+
+int sparse_attn_slot_map(const sparse_attn_params* p, const int32_t* sel_ids, const int32_t* sel_count,
+                         const int32_t* slot_block, int32_t cache_slots, int32_t* sel_slot, void* ws,
+                         size_t ws_bytes, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (cache_slots < 1 || cache_slots > 1024 || g.sel_stride > cache_slots) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() > 0 && (!sel_ids || !sel_count || !slot_block || !sel_slot || !aligned(sel_ids, 4) ||
+                          !aligned(sel_count, 4) || !aligned(slot_block, 4) || !aligned(sel_slot, 4)))
+        return SPARSE_ATTN_INVALID_ARG;
+    return status_of(launch_slot_map(g, sel_ids, sel_count, slot_block, cache_slots, sel_slot,
+                                     reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.err),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_load_misses(const sparse_attn_params* p, const void* host_k_pages, const void* host_v_pages,
+                            const int32_t* block_table, const int32_t* miss_ids, const int32_t* miss_slot,
+                            const int32_t* counts, int32_t cache_slots, void* pool_k, void* pool_v, void* ws,
+                            size_t ws_bytes, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (cache_slots < 1 || cache_slots > 1024 || g.sel_stride > cache_slots) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() == 0 || g.nb == 0) return SPARSE_ATTN_OK;
+    const void* hk = host_k_pages ? device_view(host_k_pages) : nullptr;
+    const void* hv = host_v_pages ? device_view(host_v_pages) : nullptr;
+    if (!hk || !hv || !aligned(hk, 16) || !aligned(hv, 16) || !block_table || !miss_ids || !miss_slot ||
+        !counts || !pool_k || !pool_v || !aligned(pool_k, 16) || !aligned(pool_v, 16) ||
+        !aligned(block_table, 4) || !aligned(miss_ids, 4) || !aligned(miss_slot, 4) || !aligned(counts, 4))
+        return SPARSE_ATTN_INVALID_ARG;
+    return status_of(launch_load_misses(g, hk, hv, block_table, miss_ids, miss_slot, counts, cache_slots,
+                                        pool_k, pool_v,
+                                        reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.err),
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_decode_slots(const sparse_attn_params* p, const void* q, const void* pool_k,
+                             const void* pool_v, int32_t cache_slots, const int32_t* sel_ids,
+                             const int32_t* sel_slot, const int32_t* sel_count, float* out, void* ws,
+                             size_t ws_bytes, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (cache_slots < 1 || cache_slots > 1024 || g.sel_stride > cache_slots) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() > 0) {
+        if (!q || !out || !sel_ids || !sel_slot || !sel_count || !aligned(q, 16) || !aligned(out, 16) ||
+            !aligned(sel_ids, 4) || !aligned(sel_slot, 4) || !aligned(sel_count, 4))
+            return SPARSE_ATTN_INVALID_ARG;
+        if (g.nb > 0 && (!pool_k || !pool_v || !aligned(pool_k, 16) || !aligned(pool_v, 16)))
+            return SPARSE_ATTN_INVALID_ARG;
+    }
+    return status_of(launch_decode(g, L, static_cast<char*>(ws), q, pool_k, pool_v, nullptr, sel_ids,
+                                   sel_count, out, sel_slot, cache_slots,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 
 // ---- selection for callers that cannot allocate device memory ---------------
 // The scratch lives in this file-scope array; host code needs its device address,

@@ -41,6 +41,11 @@ struct DecodeArgs {
     const int32_t* sel_count;
     float* out;
     int Hq, Hkv, nb, bs, N, num_pages, sel_stride;
+    // slot mode (slot_C > 0): K/V come from a per-unit slot pool [units * slot_C, bs, D]
+    // through sel_slot [units, sel_stride] instead of block_table and the page pools
+    const int32_t* sel_slot;
+    int slot_C;
+    int page_heads;          // KV heads per page: Hkv, or 1 in slot mode
     int blocks_per_item, items_per_unit, total_items, units;
     int stages;
     float scale_log2;
@@ -213,6 +218,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
             const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
             if (j < 0 || j >= a.nb) {
                 raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
+            } else if (a.slot_C > 0) {
+                const int sl = a.sel_slot[size_t(u) * a.sel_stride + slot];
+                if (sl < 0 || sl >= a.slot_C) {
+                    raise_error(a.err, SPARSE_ATTN_ERR_SLOT);
+                } else {
+                    page = u * a.slot_C + sl;
+                    valid = min(a.bs, a.N - j * a.bs);
+                }
             } else {
                 const int b = u / a.Hkv;
                 const int p = a.block_table[size_t(b) * a.nb + j];
@@ -248,8 +261,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
         unsigned char* kd = smem + s * stage_bytes;
         unsigned char* vd = kd + size_t(item_tokens) * S::ROW_BYTES;
         const int u = item / a.items_per_unit;
-        const size_t head_off = size_t(u % a.Hkv) * tile_bytes;
-        const size_t page_stride = size_t(a.Hkv) * tile_bytes;
+        const size_t head_off = a.slot_C > 0 ? 0 : size_t(u % a.Hkv) * tile_bytes;
+        const size_t page_stride = size_t(a.page_heads) * tile_bytes;
         for (int i = 0; i < 2 * bpi; ++i) {
             if ((s * 2 * bpi + i) % kDecWarps != warp) continue;
             if (i == 0) {
@@ -622,6 +635,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a
         if (slot < count) {
             if (j < 0 || j >= a.nb) {
                 raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
+            } else if (a.slot_C > 0) {
+                const int sl = a.sel_slot[size_t(u) * a.sel_stride + slot];
+                if (sl < 0 || sl >= a.slot_C) {
+                    raise_error(a.err, SPARSE_ATTN_ERR_SLOT);
+                } else {
+                    page = u * a.slot_C + sl;
+                    valid = min(a.bs, a.N - j * a.bs);
+                }
             } else {
                 const int p = a.block_table[size_t(u / a.Hkv) * a.nb + j];
                 if (p < 0 || p >= a.num_pages) {
@@ -646,7 +667,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a
     auto issue_slab = [&](int s, int st) {
         const int k = s >> spi_shift;                                  // item within the range
         const int t0 = (s & spi_mask) * kSlabTokens;                  // first token in the item
-        const size_t head_rows = size_t(((i_begin + k) / ipu) % a.Hkv) * a.bs;
+        const size_t head_rows = a.slot_C > 0 ? 0 : size_t(((i_begin + k) / ipu) % a.Hkv) * a.bs;
         const uint32_t kd = ring + uint32_t(st) * SS::SLAB_BYTES + uint32_t(cp_c >> 3) * SS::HALF_BYTES;
         const uint32_t vd = kd + SS::TENSOR_BYTES;
 #pragma unroll
@@ -655,7 +676,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a
             const int t = t0 + tr;
             const int e = k * bpi + (t >> bs_shift), r = t & (a.bs - 1);
             const bool ok = r < blk_valid[e];                          // 0 for an empty slot
-            const size_t off = ok ? ((size_t(blk_page[e]) * a.Hkv * a.bs + head_rows + r) * (D * 2) + cp_c * 16) : 0;
+            const size_t off = ok ? ((size_t(blk_page[e]) * a.page_heads * a.bs + head_rows + r) * (D * 2) + cp_c * 16) : 0;
             const uint32_t so = uint32_t(tr) * kRowBytes + uint32_t(((cp_c & 7) ^ (tr & 7)) << 4);
             cp_async_16_zfill(kd + so, kbase + off, ok ? 16u : 0u);
             cp_async_16_zfill(vd + so, vbase + off, ok ? 16u : 0u);
@@ -871,11 +892,14 @@ bool decode_supported(int D, bool kv_bf16, int block_size, int G)
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* k_pages, const void* v_pages, const int32_t* block_table,
                           const int32_t* sel_ids, const int32_t* sel_count, float* out,
-                          cudaStream_t s)
+                          const int32_t* sel_slot, int slot_C, cudaStream_t s)
 {
     const int units = g.units();
     if (units == 0) return cudaSuccess;
     DecodeArgs a{};
+    a.sel_slot = sel_slot;
+    a.slot_C = slot_C;
+    a.page_heads = slot_C > 0 ? 1 : g.Hkv;
     a.q = q;
     a.q_bf16 = g.q_bf16;
     a.k_pages = k_pages;

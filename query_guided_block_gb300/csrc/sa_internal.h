@@ -73,7 +73,16 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* k_pages, const void* v_pages, const int32_t* block_table,
                           const int32_t* sel_ids, const int32_t* sel_count, float* out,
-                          cudaStream_t s);
+                          const int32_t* sel_slot, int slot_C, cudaStream_t s);
+// Slot pool (sa_io.cu): the misses' K/V tiles from a host-resident page-first store
+// into their slots, and each selected block's slot.
+cudaError_t launch_load_misses(const Geometry& g, const void* host_k, const void* host_v,
+                               const int32_t* block_table, const int32_t* miss_ids,
+                               const int32_t* miss_slot, const int32_t* counts, int cache_slots,
+                               void* pool_k, void* pool_v, uint32_t* err, cudaStream_t s);
+cudaError_t launch_slot_map(const Geometry& g, const int32_t* sel_ids, const int32_t* sel_count,
+                            const int32_t* slot_block, int cache_slots, int32_t* sel_slot,
+                            uint32_t* err, cudaStream_t s);
 
 cudaError_t launch_diff(const Geometry& g, int step, const int32_t* sel_ids,
                         const int32_t* sel_count, const int32_t* prev_ids,

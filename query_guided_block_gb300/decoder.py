@@ -117,3 +117,39 @@ class SlotCache:
         d = self.decoder
         self.prev_ids.copy_((d.sel_ids if sel_ids is None else sel_ids).view(self.prev_ids.shape))
         self.prev_count.copy_((d.sel_count if sel_count is None else sel_count).view(-1))
+
+
+class SlotPool:
+    """Per-unit slot pool of K/V page tiles fed from a host-resident page-first store:
+    after the diff of a step, ``load_misses`` brings the misses in (one launch),
+    ``slot_map`` finds each selected block's slot and ``decode`` attends through it."""
+
+    def __init__(self, cache: SlotCache):
+        d = cache.decoder
+        p = d.p
+        self.cache = cache
+        shape = (d.units, cache.cache_slots, p.block_size, p.head_dim)
+        self.pool_k = torch.zeros(shape, dtype=d.kv_dtype, device=d.device)
+        self.pool_v = torch.zeros_like(self.pool_k)
+        self.sel_slot = torch.full((d.units, d.sel_stride), -1, dtype=torch.int32, device=d.device)
+
+    def tile_bytes(self) -> int:
+        p = self.cache.decoder.p
+        return p.block_size * p.head_dim * self.pool_k.element_size()
+
+    def load_misses(self, host_k_pages, host_v_pages, block_table, stream=None):
+        c, d = self.cache, self.cache.decoder
+        B.sparse_attn_load_misses(d.p, host_k_pages, host_v_pages, block_table, c.lists["miss_ids"],
+                                  c.lists["miss_slot"], c.counts, c.cache_slots, self.pool_k,
+                                  self.pool_v, d.ws, stream)
+
+    def slot_map(self, stream=None):
+        c, d = self.cache, self.cache.decoder
+        B.sparse_attn_slot_map(d.p, d.sel_ids, d.sel_count, c.slot_block, c.cache_slots,
+                               self.sel_slot, d.ws, stream)
+
+    def decode(self, q, out=None, stream=None):
+        c, d = self.cache, self.cache.decoder
+        B.sparse_attn_decode_slots(d.p, q, self.pool_k, self.pool_v, c.cache_slots, d.sel_ids,
+                                   self.sel_slot, d.sel_count, d.out if out is None else out, d.ws,
+                                   stream)
