@@ -181,7 +181,8 @@ def algorithmic_bytes(w, sel_count: torch.Tensor, sel_ids: torch.Tensor):
     B, Hq, Hkv, D, bs, N = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.n_tokens
     nb = w.num_blocks
     units = B * Hkv
-    q_bytes = B * Hq * D * qsz
+    Qn = max(1, w.num_queries)
+    q_bytes = B * Qn * Hq * D * qsz
     win_first = (max(0, N - w.window_tokens) // bs) if w.window_tokens > 0 else nb
     cnt = sel_count.detach().cpu().numpy().reshape(-1).astype(np.int64)
     ids_bytes = int(cnt.sum()) * 4 + units * 4
@@ -201,8 +202,10 @@ def algorithmic_bytes(w, sel_count: torch.Tensor, sel_ids: torch.Tensor):
         ids = sel_ids.detach().cpu().numpy().reshape(units, -1)
         holds_last = sum(int((ids[u, : cnt[u]] == nb - 1).any()) for u in range(units))
         tokens -= holds_last * (bs - tail)
-    decode_bytes = q_bytes + tokens * 2 * D * esz + int(cnt.sum()) * 4 * 2 + units * 4 + B * Hq * D * 4
-    return {"select": select_bytes, "decode": decode_bytes}
+    decode_bytes = q_bytes + tokens * 2 * D * esz + int(cnt.sum()) * 4 * 2 + units * 4 + B * Qn * Hq * D * 4
+    # tensor work of the decode: S = q K^T and O = P V over the selected tokens
+    decode_flops = 4.0 * tokens * Qn * (Hq // Hkv) * D   # each unit's tokens meet Q x G query rows
+    return {"select": select_bytes, "decode": decode_bytes, "decode_flops": decode_flops}
 
 
 # ------------------------------------------------------------- GPU arm --
@@ -232,7 +235,8 @@ def run_gpu_arm(args):
     inp = make_inputs(w, dev)
     p = Bn.params_for(w)
     dec = SparseDecoder(p, dev)
-    q_all = inp["q"] if inp["q"].dim() == 4 else inp["q"].unsqueeze(0)
+    multi_q = inp.get("queries_per_seq", 1) > 1    # q is [B, Q, Hq, D]: one step's queries
+    q_all = inp["q"] if (inp["q"].dim() == 4 and not multi_q) else inp["q"].unsqueeze(0)
     q_static = q_all[0].clone()
     kp, vp, bt = inp["k_pages"], inp["v_pages"], inp["block_table"]
     cache = SlotCache(dec, w.cache_slots) if w.cache_slots else None
@@ -334,7 +338,7 @@ def run_gpu_arm(args):
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     total_ms_local = sum(step_ms)
     total_ms = aggregate_max(total_ms_local, world, dev)
-    queries = w.batch * w.num_q_heads
+    queries = w.batch * w.num_q_heads * max(1, w.num_queries)
     value = world * queries * K / (total_ms / 1e3)
     ms_per_step = total_ms / K
 
@@ -345,7 +349,7 @@ def run_gpu_arm(args):
         "select": {"ms": sel_avg, "bytes": nbytes["select"], "gbs": nbytes["select"] / sel_avg / 1e6,
                    "launches_per_step": 2 if w.two_level else 1},
         "decode": {"ms": dec_avg, "bytes": nbytes["decode"], "gbs": nbytes["decode"] / dec_avg / 1e6,
-                   "launches_per_step": 1},
+                   "tflops": nbytes["decode_flops"] / dec_avg / 1e9, "launches_per_step": 1},
     }
     if io:
         io_ms = statistics.mean([e[1].elapsed_time(e[2]) for e in ev])

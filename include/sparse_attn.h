@@ -104,6 +104,11 @@ typedef struct sparse_attn_params {
     float softmax_scale;    /* <= 0: 1/sqrt(D) */
     int32_t num_reserve;    /* >= 0 reserve block ids per unit (sparse_attn_select_reserved);
                                0 for sparse_attn_select */
+    int32_t num_queries;    /* Q: query vectors per sequence sharing one selection per KV
+                               head (0 or 1: one decode query).  With Q > 1, q and out are
+                               [B, Q, Hq, D] (query t of sequence b at row b * Q + t), the
+                               selection scores are summed over the Q queries, and the KV
+                               dtype must be bf16, single level */
 } sparse_attn_params;
 
 /* Human-readable name of a status code (static storage). */

@@ -36,13 +36,14 @@ class sparse_attn_params(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "n_tokens", "block_size",
         "num_pages", "window_tokens", "topk", "two_level", "coarse_block", "topk_coarse",
-        "score_kind", "kv_dtype", "q_dtype")] + [("softmax_scale", C.c_float), ("num_reserve", C.c_int32)]
+        "score_kind", "kv_dtype", "q_dtype")] + [("softmax_scale", C.c_float), ("num_reserve", C.c_int32),
+                                                 ("num_queries", C.c_int32)]
 
 
 def make_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size, num_pages,
                 window_tokens, topk, two_level=False, coarse_block=1024, topk_coarse=48,
                 score_kind=SCORE_QUEST, kv_dtype=torch.bfloat16, q_dtype=torch.bfloat16,
-                softmax_scale=0.0, num_reserve=0) -> sparse_attn_params:
+                softmax_scale=0.0, num_reserve=0, num_queries=1) -> sparse_attn_params:
     def code(dt):
         if dt in (torch.bfloat16, BF16):
             return BF16
@@ -54,7 +55,7 @@ def make_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size
     return sparse_attn_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size,
                               num_pages, window_tokens, topk, int(bool(two_level)), coarse_block,
                               topk_coarse, int(score_kind), code(kv_dtype), code(q_dtype),
-                              float(softmax_scale), int(num_reserve))
+                              float(softmax_scale), int(num_reserve), int(num_queries))
 
 
 def params_for(w, **over) -> sparse_attn_params:
@@ -64,7 +65,7 @@ def params_for(w, **over) -> sparse_attn_params:
               num_pages=w.num_pages, window_tokens=w.window_tokens, topk=w.topk,
               two_level=w.two_level, coarse_block=w.coarse_block, topk_coarse=w.topk_coarse,
               score_kind=w.score, kv_dtype=w.kv_dtype, q_dtype=w.q_dtype,
-              num_reserve=w.num_reserve)
+              num_reserve=w.num_reserve, num_queries=w.num_queries)
     kw.update(over)
     return make_params(**kw)
 

@@ -21,7 +21,7 @@ int make_geometry(const sparse_attn_params* p, Geometry* g)
     memset(g, 0, sizeof *g);
     if (p->batch < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->head_dim < 1 ||
         p->n_tokens < 0 || p->block_size < 1 || p->num_pages < 0 || p->window_tokens < 0 ||
-        p->topk < 0 || p->topk_coarse < 0 || p->num_reserve < 0)
+        p->topk < 0 || p->topk_coarse < 0 || p->num_reserve < 0 || p->num_queries < 0)
         return SPARSE_ATTN_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return SPARSE_ATTN_INVALID_ARG;
     if (p->two_level != 0 && p->two_level != 1) return SPARSE_ATTN_INVALID_ARG;
@@ -62,6 +62,9 @@ int make_geometry(const sparse_attn_params* p, Geometry* g)
     g->n_cand = g->win_first;
     g->topk = p->topk;
     g->n_reserve = p->num_reserve;
+    g->Q = p->num_queries > 1 ? p->num_queries : 1;
+    if (g->Q > 1 && (p->two_level != 0 || !kv_bf16)) return SPARSE_ATTN_UNSUPPORTED;
+    if ((long long)g->Q * G > (1 << 20)) return SPARSE_ATTN_UNSUPPORTED;
     const int k_max = p->topk < g->n_cand ? p->topk : g->n_cand;
     const int r_max = p->num_reserve < g->n_cand ? p->num_reserve : g->n_cand;
     const int stride = k_max + r_max + g->win_count;
@@ -118,7 +121,8 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     L.blocks_per_split = decode_blocks_per_item(g.D, g.kv_bf16, g.bs);
     L.max_splits = (g.sel_stride + L.blocks_per_split - 1) / L.blocks_per_split;
     if (L.max_splits < 1) L.max_splits = 1;
-    const size_t heads = size_t(g.B) * g.Hq;
+    const size_t heads = size_t(g.B) * g.Hq * g.Q;   // query rows (Q queries per sequence)
+    const size_t dec_cells = units * size_t(g.Q > 1 ? mq_row_tiles(g.Q, g.G) : 1);
 
     size_t off = 0;
     // one 256-byte header: error word and the persistent kernels' work counters
@@ -129,7 +133,7 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     L.dec_done = 16;
     off = 256;
     L.sel_counters = off;     off = align256(off + units * sizeof(uint32_t));
-    L.dec_counters = off;     off = align256(off + units * sizeof(uint32_t));
+    L.dec_counters = off;     off = align256(off + dec_cells * sizeof(uint32_t));
     L.l1_counters = off;      off = align256(off + units * sizeof(uint32_t));
     L.scores = off;           off = align256(off + units * L.score_cols * sizeof(float));
     L.survivors = off;        off = align256(off + units * size_t(g.topk_coarse > 0 ? g.topk_coarse : 1) * sizeof(int32_t));
@@ -282,6 +286,9 @@ int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k
                          !aligned(v_pages, 16) || !aligned(block_table, 4)))
             return SPARSE_ATTN_INVALID_ARG;
     }
+    if (g.Q > 1)
+        return status_of(launch_decode_mq(g, L, static_cast<char*>(ws), q, k_pages, v_pages, block_table,
+                                          sel_ids, sel_count, out, reinterpret_cast<cudaStream_t>(stream)));
     return status_of(launch_decode(g, L, static_cast<char*>(ws), q, k_pages, v_pages, block_table,
                                    sel_ids, sel_count, out, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -396,6 +403,7 @@ int sparse_attn_decode_slots(const sparse_attn_params* p, const void* q, const v
     const WorkspaceLayout L = workspace_layout(g);
     if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
     if (cache_slots < 1 || cache_slots > 1024 || g.sel_stride > cache_slots) return SPARSE_ATTN_INVALID_ARG;
+    if (g.Q > 1) return SPARSE_ATTN_UNSUPPORTED;
     if (g.units() > 0) {
         if (!q || !out || !sel_ids || !sel_slot || !sel_count || !aligned(q, 16) || !aligned(out, 16) ||
             !aligned(sel_ids, 4) || !aligned(sel_slot, 4) || !aligned(sel_count, 4))

@@ -1,0 +1,442 @@
+// Multi-query sparse attention: Q query vectors per sequence share one selection per
+// KV head ("从HiSparse到QSA的移植实战" §1.1, §4.3: the long-context prefill setting, where
+// many queries read the same selected blocks), so Q K^T over a unit's Q x G query rows is
+// a dense contraction.  Same exact softmax over the selected tokens as the one-query
+// decode; the output is [B, Q, Hq, D] fp32.
+//
+// Design (FlashAttention-2 style, tensor cores via mma.sync m16n8k16, bf16 in / fp32
+// accumulate):
+//   * CTA = (unit, tile of 64 query rows, split of the unit's selected tokens); 4 warps
+//     own 16 rows each.  Row r of a unit is (query t = r / G, head g = r % G).
+//   * The split's selected tokens are streamed in 64-token K/V tiles through a 3-stage
+//     cp.async ring (128-byte XOR swizzle, rows without a token zero-filled); one CTA
+//     barrier per tile, amortised over 16 x 64 x D of work per warp.
+//   * Per tile and warp: S = Q K^T (8 token groups x D/16 k-steps), the online softmax
+//     on the accumulator fragments (row max across the quad), then O += P V with the
+//     score fragments reused as the A operand; P is carried as bf16 hi + lo (two MMAs),
+//     an fp32 query as bf16 hi + lo too.
+//   * Each split writes (m, l, o) per row; the CTA completing a (unit, row tile) merges
+//     the splits (log-sum-exp).  One split writes the output directly.
+#include "sa_common.cuh"
+#include "sa_internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int kMqThreads = 128;
+constexpr int kMqWarps = 4;
+constexpr int kMqRows = 64;          // query rows per CTA
+constexpr int kMqTile = 64;          // tokens per K/V tile
+constexpr int kMqStages = 3;
+constexpr int kMqMaxBlocks = 1024;   // page lookups per split held in shared memory
+constexpr int kMqMaxSplits = 16;     // token splits of one (unit, row tile)
+constexpr int kRowB = 128;           // bytes of one 64-channel half of a token row
+
+struct MqArgs {
+    const void* q;
+    int q_bf16;
+    const void* k_pages;
+    const void* v_pages;
+    const int32_t* block_table;
+    const int32_t* sel_ids;
+    const int32_t* sel_count;
+    float* out;
+    int Hq, Hkv, G, Q, R, nb, bs, N, num_pages, sel_stride;
+    int row_tiles, nsplit, max_splits;
+    float scale_log2;
+    float* part_m;    // [units * R, max_splits]
+    float* part_l;
+    float* part_o;    // [units * R, max_splits, D]
+    uint32_t* counters;   // [units * row_tiles]
+    uint32_t* err;
+};
+
+__device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk)
+{
+    return half_base + uint32_t(token) * kRowB + uint32_t((chunk ^ (token & 7)) << 4);
+}
+
+template <int D, bool QSPLIT>
+__global__ void __launch_bounds__(kMqThreads, 2) decode_mq_kernel(MqArgs a)
+{
+    constexpr int HALVES = D / 64;
+    constexpr int HALF_BYTES = kMqTile * kRowB;               // 8 KB
+    constexpr int TENSOR_BYTES = HALVES * HALF_BYTES;
+    constexpr int STAGE_BYTES = 2 * TENSOR_BYTES;
+    constexpr int DT = D / 8;
+    constexpr int CPR = D / 8;                                // 16-byte chunks per token row
+    constexpr int CP_PER_THREAD = kMqTile * CPR / kMqThreads;
+    static_assert(kMqTile * CPR % kMqThreads == 0, "tile copy must split over the threads");
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int sp = blockIdx.x % a.nsplit;
+    const int rt = (blockIdx.x / a.nsplit) % a.row_tiles;
+    const int u = blockIdx.x / (a.nsplit * a.row_tiles);
+    const int b = u / a.Hkv, kvh = u - b * a.Hkv;
+    const int bs_shift = __ffs(a.bs) - 1;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* smem = smem_raw + (base - raw);
+    int* blk_page = reinterpret_cast<int*>(smem + kMqStages * STAGE_BYTES);
+    int* blk_valid = blk_page + kMqMaxBlocks;
+    __shared__ int s_merge;
+
+    allow_dependents_early();
+    grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+
+    // ---- the split's tiles and the blocks they touch --------------------------
+    int count = a.sel_count[u];
+    if (count < 0 || count > a.sel_stride) {
+        if (tid == 0) raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
+        count = count < 0 ? 0 : a.sel_stride;
+    }
+    const int ntok = count * a.bs;
+    const int tiles = (ntok + kMqTile - 1) / kMqTile;
+    const int t0 = int((long long)tiles * sp / a.nsplit), t1 = int((long long)tiles * (sp + 1) / a.nsplit);
+    const int blk0 = (t0 * kMqTile) >> bs_shift;
+    const int blk1 = min(count, ((t1 * kMqTile - 1) >> bs_shift) + 1);
+    const int nblk = t1 > t0 ? blk1 - blk0 : 0;
+    for (int e = tid; e < nblk; e += kMqThreads) {
+        const int slot = blk0 + e;
+        int page = -1, valid = 0;
+        const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
+        if (j < 0 || j >= a.nb) {
+            raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
+        } else {
+            const int p = a.block_table[size_t(b) * a.nb + j];
+            if (p < 0 || p >= a.num_pages) {
+                raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
+            } else {
+                page = p;
+                valid = min(a.bs, a.N - j * a.bs);
+            }
+        }
+        if (e < kMqMaxBlocks) {
+            blk_page[e] = page;
+            blk_valid[e] = valid;
+        }
+    }
+    __syncthreads();
+
+    // ---- staging: thread copies chunk cp_c of tile rows cp_r + i * (128 / CPR) -------
+    const char* kbase = reinterpret_cast<const char*>(a.k_pages);
+    const char* vbase = reinterpret_cast<const char*>(a.v_pages);
+    const int cp_c = tid % CPR, cp_r = tid / CPR;
+    constexpr int ROWS_PER_PASS = kMqThreads / CPR;
+    auto issue_tile = [&](int tile, int st) {
+        const uint32_t kd = base + uint32_t(st) * STAGE_BYTES + uint32_t(cp_c >> 3) * HALF_BYTES;
+        const uint32_t vd = kd + TENSOR_BYTES;
+#pragma unroll
+        for (int i = 0; i < CP_PER_THREAD; ++i) {
+            const int tr = cp_r + i * ROWS_PER_PASS;                // row in the tile
+            const int gi = tile * kMqTile + tr;                     // selected-token index
+            const int e = (gi >> bs_shift) - blk0, r = gi & (a.bs - 1);
+            const bool ok = gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && r < blk_valid[max(0, min(e, kMqMaxBlocks - 1))];
+            const size_t off = ok ? ((size_t(blk_page[e]) * a.Hkv * a.bs + size_t(kvh) * a.bs + r) * (D * 2) + cp_c * 16) : 0;
+            const uint32_t so = uint32_t(tr) * kRowB + uint32_t(((cp_c & 7) ^ (tr & 7)) << 4);
+            cp_async_16_zfill(kd + so, kbase + off, ok ? 16u : 0u);
+            cp_async_16_zfill(vd + so, vbase + off, ok ? 16u : 0u);
+        }
+    };
+#pragma unroll
+    for (int kk = 0; kk < kMqStages - 1; ++kk) {
+        if (t0 + kk < t1) issue_tile(t0 + kk, kk);
+        cp_async_commit();
+    }
+
+    // ---- query A fragments: rows r_lo = row g4, r_hi = row g4 + 8 of the warp ----------
+    const int r_lo = rt * kMqRows + warp * 16 + g4, r_hi = r_lo + 8;
+    auto head_of = [&](int r) -> size_t {   // q / out row of unit row r
+        const int t = r / a.G, g = r - (r / a.G) * a.G;
+        return (size_t(b) * a.Q + t) * a.Hq + size_t(kvh) * a.G + g;
+    };
+    uint32_t qa[D / 16][4], qb[QSPLIT ? D / 16 : 1][4];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        float f[2][4];
+#pragma unroll
+        for (int hrow = 0; hrow < 2; ++hrow) {
+            const int r = hrow ? r_hi : r_lo;
+            const size_t qrow = r < a.R ? head_of(r) * D + ks * 16 + 2 * t4 : 0;
+            f[hrow][0] = r < a.R ? load_q(a.q, qrow, a.q_bf16 != 0) : 0.f;
+            f[hrow][1] = r < a.R ? load_q(a.q, qrow + 1, a.q_bf16 != 0) : 0.f;
+            f[hrow][2] = r < a.R ? load_q(a.q, qrow + 8, a.q_bf16 != 0) : 0.f;
+            f[hrow][3] = r < a.R ? load_q(a.q, qrow + 9, a.q_bf16 != 0) : 0.f;
+        }
+        qa[ks][0] = pack_bf16x2(f[0][0], f[0][1]);
+        qa[ks][1] = pack_bf16x2(f[1][0], f[1][1]);
+        qa[ks][2] = pack_bf16x2(f[0][2], f[0][3]);
+        qa[ks][3] = pack_bf16x2(f[1][2], f[1][3]);
+        if constexpr (QSPLIT) {
+            qb[ks][0] = pack_bf16x2(f[0][0] - bf16_lo(qa[ks][0]), f[0][1] - bf16_hi(qa[ks][0]));
+            qb[ks][1] = pack_bf16x2(f[1][0] - bf16_lo(qa[ks][1]), f[1][1] - bf16_hi(qa[ks][1]));
+            qb[ks][2] = pack_bf16x2(f[0][2] - bf16_lo(qa[ks][2]), f[0][3] - bf16_hi(qa[ks][2]));
+            qb[ks][3] = pack_bf16x2(f[1][2] - bf16_lo(qa[ks][3]), f[1][3] - bf16_hi(qa[ks][3]));
+        }
+    }
+
+    float acc[DT][4];
+#pragma unroll
+    for (int j = 0; j < DT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};   // rows g4, g4 + 8
+
+    for (int tile = t0; tile < t1; ++tile) {
+        const int k = tile - t0;
+        cp_async_wait_group<kMqStages - 2>();
+        __syncthreads();                     // tile k staged by everyone; stage k - 1 is free
+        if (tile + kMqStages - 1 < t1) issue_tile(tile + kMqStages - 1, (k + kMqStages - 1) % kMqStages);
+        cp_async_commit();
+        const uint32_t kst = base + uint32_t(k % kMqStages) * STAGE_BYTES;
+        const uint32_t vst = kst + TENSOR_BYTES;
+
+        // S = Q K^T: 8 groups of 8 tokens
+        float c[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+#pragma unroll
+            for (int kp = 0; kp < D / 32; ++kp) {
+                const int ch = kp * 4 + (lane >> 3);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(swz(kst + uint32_t(ch >> 3) * HALF_BYTES, nt * 8 + (lane & 7), ch & 7), b0, b1, b2, b3);
+                mma_bf16_16816(c[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+                mma_bf16_16816(c[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+                if constexpr (QSPLIT) {
+                    mma_bf16_16816(c[nt], qb[2 * kp][0], qb[2 * kp][1], qb[2 * kp][2], qb[2 * kp][3], b0, b1);
+                    mma_bf16_16816(c[nt], qb[2 * kp + 1][0], qb[2 * kp + 1][1], qb[2 * kp + 1][2], qb[2 * kp + 1][3], b2, b3);
+                }
+            }
+        }
+        // online softmax: scale, mask tokens that do not exist, row max over the quad
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int gi = tile * kMqTile + nt * 8 + 2 * t4 + e;
+                const int eb = (gi >> bs_shift) - blk0, r = gi & (a.bs - 1);
+                const bool ok = gi < ntok && eb >= 0 && eb < min(nblk, kMqMaxBlocks) &&
+                                r < blk_valid[max(0, min(eb, kMqMaxBlocks - 1))];
+                c[nt][e] = ok ? c[nt][e] * a.scale_log2 : -INFINITY;
+                c[nt][e + 2] = ok ? c[nt][e + 2] * a.scale_log2 : -INFINITY;
+                mx[0] = fmaxf(mx[0], c[nt][e]);
+                mx[1] = fmaxf(mx[1], c[nt][e + 2]);
+            }
+        float alpha[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFullMask, mx[h], 1));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFullMask, mx[h], 2));
+            const float m_new = fmaxf(m_run[h], mx[h]);
+            alpha[h] = (m_run[h] == -INFINITY) ? 0.f : fast_exp2(m_run[h] - m_new);
+            m_run[h] = m_new;
+        }
+        float psum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int h = e >> 1;
+                c[nt][e] = (c[nt][e] == -INFINITY) ? 0.f : fast_exp2(c[nt][e] - m_run[h]);
+                psum[h] += c[nt][e];
+            }
+        l_run[0] = fmaf(l_run[0], alpha[0], psum[0]);
+        l_run[1] = fmaf(l_run[1], alpha[1], psum[1]);
+#pragma unroll
+        for (int j = 0; j < DT; ++j) {
+            acc[j][0] *= alpha[0];
+            acc[j][1] *= alpha[0];
+            acc[j][2] *= alpha[1];
+            acc[j][3] *= alpha[1];
+        }
+        // O += P V, k = 16 tokens per step; P from the score fragments, bf16 hi + lo
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float* p0 = c[2 * kk];
+            const float* p1 = c[2 * kk + 1];
+            const uint32_t h0 = pack_bf16x2(p0[0], p0[1]), h1 = pack_bf16x2(p0[2], p0[3]);
+            const uint32_t h2 = pack_bf16x2(p1[0], p1[1]), h3 = pack_bf16x2(p1[2], p1[3]);
+            const uint32_t l0 = pack_bf16x2(p0[0] - bf16_lo(h0), p0[1] - bf16_hi(h0));
+            const uint32_t l1 = pack_bf16x2(p0[2] - bf16_lo(h1), p0[3] - bf16_hi(h1));
+            const uint32_t l2 = pack_bf16x2(p1[0] - bf16_lo(h2), p1[1] - bf16_hi(h2));
+            const uint32_t l3 = pack_bf16x2(p1[2] - bf16_lo(h3), p1[3] - bf16_hi(h3));
+#pragma unroll
+            for (int jp = 0; jp < DT; jp += 2) {
+                const int mtx = lane >> 3;
+                const int chunk = jp + (mtx >> 1);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_trans(swz(vst + uint32_t(chunk >> 3) * HALF_BYTES, kk * 16 + (mtx & 1) * 8 + (lane & 7), chunk & 7),
+                              r0, r1, r2, r3);
+                mma_bf16_16816(acc[jp], h0, h1, h2, h3, r0, r1);
+                mma_bf16_16816(acc[jp], l0, l1, l2, l3, r0, r1);
+                mma_bf16_16816(acc[jp + 1], h0, h1, h2, h3, r2, r3);
+                mma_bf16_16816(acc[jp + 1], l0, l1, l2, l3, r2, r3);
+            }
+        }
+    }
+    cp_async_wait_group<0>();
+
+    // ---- the split's (m, l, o), or the output itself when there is one split ----------
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        l_run[h] += __shfl_xor_sync(kFullMask, l_run[h], 1);
+        l_run[h] += __shfl_xor_sync(kFullMask, l_run[h], 2);
+    }
+    if (a.nsplit == 1) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = h ? r_hi : r_lo;
+            if (r >= a.R) continue;
+            const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+            float* dst = a.out + head_of(r) * D + 2 * t4;
+#pragma unroll
+            for (int j = 0; j < DT; ++j)
+                *reinterpret_cast<float2*>(dst + j * 8) = make_float2(acc[j][2 * h] * inv, acc[j][2 * h + 1] * inv);
+        }
+        return;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int r = h ? r_hi : r_lo;
+        if (r >= a.R) continue;
+        const size_t pr = (size_t(u) * a.R + r) * a.max_splits + sp;
+        float* dst = a.part_o + pr * D + 2 * t4;
+#pragma unroll
+        for (int j = 0; j < DT; ++j)
+            *reinterpret_cast<float2*>(dst + j * 8) = make_float2(acc[j][2 * h], acc[j][2 * h + 1]);
+        if (t4 == 0) {
+            a.part_m[pr] = m_run[h];
+            a.part_l[pr] = l_run[h];
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t before = atomic_add_acq_rel_u32(&a.counters[size_t(u) * a.row_tiles + rt], 1u);
+        s_merge = before + 1 == uint32_t(a.nsplit);
+        if (s_merge) a.counters[size_t(u) * a.row_tiles + rt] = 0u;
+    }
+    __syncthreads();
+    if (!s_merge) return;
+    // merge the splits of this (unit, row tile): weights per (row, split) once into
+    // shared memory, then each output reads its splits' partials, eight outputs at a time
+    __shared__ float s_w[kMqRows][kMqMaxSplits], s_den[kMqRows];
+    const int rows = min(kMqRows, a.R - rt * kMqRows);
+    for (int rr = tid; rr < rows; rr += kMqThreads) {
+        const size_t pr0 = (size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < a.nsplit; ++s2) M = fmaxf(M, __ldcg(a.part_m + pr0 + s2));
+        float den = 0.f;
+        for (int s2 = 0; s2 < a.nsplit; ++s2) {
+            const float ms = __ldcg(a.part_m + pr0 + s2);
+            const float w = (ms == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(ms - M);
+            s_w[rr][s2] = w;
+            den = fmaf(w, __ldcg(a.part_l + pr0 + s2), den);
+        }
+        s_den[rr] = den;
+    }
+    __syncthreads();
+    const int n_out = rows * D;
+    for (int i0 = tid; i0 < n_out; i0 += kMqThreads * 8) {
+        float num[8];
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) num[k2] = 0.f;
+        for (int s2 = 0; s2 < a.nsplit; ++s2) {
+            float v[8];
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                const int i = i0 + k2 * kMqThreads;
+                const int rr = i / D, d = i - (i / D) * D;
+                v[k2] = (i < n_out && s_w[min(rr, kMqRows - 1)][s2] > 0.f)
+                            ? __ldcg(a.part_o + ((size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits + s2) * D + d)
+                            : 0.f;
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                const int i = i0 + k2 * kMqThreads;
+                if (i < n_out) num[k2] = fmaf(s_w[i / D][s2], v[k2], num[k2]);
+            }
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) {
+            const int i = i0 + k2 * kMqThreads;
+            if (i >= n_out) continue;
+            const int rr = i / D, d = i - (i / D) * D;
+            const float den = s_den[rr];
+            a.out[head_of(rt * kMqRows + rr) * D + d] = den > 0.f ? num[k2] / den : 0.f;
+        }
+    }
+}
+
+template <int D, bool QSPLIT>
+cudaError_t launch_mq_t(const MqArgs& a, int units, cudaStream_t s)
+{
+    constexpr int STAGE_BYTES = 2 * (D / 64) * kMqTile * kRowB;
+    constexpr size_t smem = 1024 + size_t(kMqStages) * STAGE_BYTES + size_t(2) * kMqMaxBlocks * sizeof(int);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mq_kernel<D, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const unsigned grid = unsigned(size_t(units) * a.row_tiles * a.nsplit);
+    return launch_after_previous(decode_mq_kernel<D, QSPLIT>, dim3(grid), dim3(kMqThreads), smem, s, a);
+}
+
+}  // namespace
+
+int mq_row_tiles(int Q, int G) { return (Q * G + kMqRows - 1) / kMqRows; }
+
+cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
+                             const void* k_pages, const void* v_pages, const int32_t* block_table,
+                             const int32_t* sel_ids, const int32_t* sel_count, float* out, cudaStream_t s)
+{
+    const int units = g.units();
+    if (units == 0) return cudaSuccess;
+    MqArgs a{};
+    a.q = q;
+    a.q_bf16 = g.q_bf16;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.block_table = block_table;
+    a.sel_ids = sel_ids;
+    a.sel_count = sel_count;
+    a.out = out;
+    a.Hq = g.Hq;
+    a.Hkv = g.Hkv;
+    a.G = g.G;
+    a.Q = g.Q;
+    a.R = g.Q * g.G;
+    a.nb = g.nb;
+    a.bs = g.bs;
+    a.N = g.N;
+    a.num_pages = g.num_pages;
+    a.sel_stride = g.sel_stride;
+    a.row_tiles = mq_row_tiles(g.Q, g.G);
+    a.max_splits = L.max_splits;
+    // splits of the selected tokens: about two CTAs per SM, at least enough for each
+    // split's blocks to fit the page cache, at most the workspace's partial slots
+    const int tiles = (g.sel_stride * g.bs + kMqTile - 1) / kMqTile;
+    const long long cells = (long long)units * a.row_tiles;
+    long long ns = (2LL * num_sms() + cells - 1) / cells;   // about one wave at two CTAs per SM
+    const long long ns_min = (g.sel_stride + (kMqMaxBlocks - 16) - 1) / (kMqMaxBlocks - 16);
+    if (ns < ns_min) ns = ns_min;
+    if (ns > tiles) ns = tiles > 0 ? tiles : 1;
+    if (ns > L.max_splits) ns = L.max_splits;
+    if (ns > kMqMaxSplits) ns = kMqMaxSplits;
+    if (ns < ns_min) return cudaErrorInvalidValue;   // the workspace cannot hold enough splits
+    a.nsplit = int(ns);
+    a.scale_log2 = g.scale_log2;
+    a.part_m = reinterpret_cast<float*>(ws + L.part_m);
+    a.part_l = reinterpret_cast<float*>(ws + L.part_l);
+    a.part_o = reinterpret_cast<float*>(ws + L.part_o);
+    a.counters = reinterpret_cast<uint32_t*>(ws + L.dec_counters);
+    a.err = reinterpret_cast<uint32_t*>(ws + L.err);
+    if (g.D == 128) return g.q_bf16 ? launch_mq_t<128, false>(a, units, s) : launch_mq_t<128, true>(a, units, s);
+    return g.q_bf16 ? launch_mq_t<64, false>(a, units, s) : launch_mq_t<64, true>(a, units, s);
+}
+
+}  // namespace sa

@@ -23,6 +23,7 @@ struct Geometry {
     int mean_block, n_mean;        // kmean rows per unit
     int topk;
     int n_reserve;                 // reserve block ids per unit (0: none)
+    int Q;                         // query vectors per sequence sharing a selection (>= 1)
     int score_kind;
     float scale_log2;              // softmax_scale * log2(e)
     int units() const { return B * Hkv; }
@@ -74,6 +75,11 @@ cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws,
                           const void* k_pages, const void* v_pages, const int32_t* block_table,
                           const int32_t* sel_ids, const int32_t* sel_count, float* out,
                           const int32_t* sel_slot, int slot_C, cudaStream_t s);
+// Multi-query attention (sa_decode_mq.cu): Q query vectors per sequence, one selection.
+int mq_row_tiles(int Q, int G);
+cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
+                             const void* k_pages, const void* v_pages, const int32_t* block_table,
+                             const int32_t* sel_ids, const int32_t* sel_count, float* out, cudaStream_t s);
 // Slot pool (sa_io.cu): the misses' K/V tiles from a host-resident page-first store
 // into their slots, and each selected block's slot.
 cudaError_t launch_load_misses(const Geometry& g, const void* host_k, const void* host_v,

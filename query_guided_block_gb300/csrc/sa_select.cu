@@ -46,6 +46,7 @@ struct SelectArgs {
     int rows;            // metadata rows per unit
     int Hkv, G;
     int Hq;
+    int Q;               // query vectors per sequence; the coefficients sum over all of them
     // candidates: c in [0, n_cand); direct (c is the row) or via level-1 survivors
     int via_survivors;
     const int32_t* surv;     // [units, surv_stride], ascending coarse ids
@@ -401,6 +402,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem + stages * kStageBytes);
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ int s_topk_unit, s_nvalid;
+    __shared__ float s_coef[2][kSelThreads];   // per-thread partial sums of the query coefficients
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sub = lane % LPR, rsub = lane / LPR;
@@ -450,22 +452,40 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
         const uint32_t parity = uint32_t(k / stages) & 1u;
         const ChunkInfo c = chunk_info(a, cid, ROWS);
         if (c.u != cur_u) {   // query coefficients of this unit (uniform across the CTA)
+            // The CTA sums the unit's Q x G query rows per channel together: thread t takes
+            // channel t mod D of rows t / D, t / D + 256 / D, ... (coalesced loads), the
+            // 256 / D partial sums of a channel meet in shared memory.
             cur_u = c.u;
             const int b = c.u / a.Hkv, kvh = c.u - (c.u / a.Hkv) * a.Hkv;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) { cp[e] = 0.f; cn[e] = 0.f; }
-            for (int g = 0; g < a.G; ++g) {
-                const size_t qrow = (size_t(b) * a.Hq + size_t(kvh) * a.G + g) * D + d0;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    const float x = load_q(a.q, qrow + e, a.q_bf16 != 0);
-                    if constexpr (KIND == KIND_QUEST) {
-                        cp[e] += fmaxf(x, 0.f);
-                        cn[e] += fminf(x, 0.f);
-                    } else {
-                        cp[e] += x;
-                    }
+            constexpr int RSTEP = kSelThreads / D;
+            const int dch = tid % D;
+            const int rows = a.Q * a.G;
+            float pp = 0.f, nn = 0.f;
+#pragma unroll 8
+            for (int r = tid / D; r < rows; r += RSTEP) {
+                const int t = r / a.G, g = r - t * a.G;
+                const float x = load_q(a.q, ((size_t(b) * a.Q + t) * a.Hq + size_t(kvh) * a.G + g) * D + dch,
+                                       a.q_bf16 != 0);
+                if constexpr (KIND == KIND_QUEST) {
+                    pp += fmaxf(x, 0.f);
+                    nn += fminf(x, 0.f);
+                } else {
+                    pp += x;
                 }
+            }
+            s_coef[0][tid] = pp;
+            s_coef[1][tid] = nn;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                float sp = 0.f, sn = 0.f;
+#pragma unroll
+                for (int k2 = 0; k2 < RSTEP; ++k2) {
+                    sp += s_coef[0][d0 + e + k2 * D];
+                    sn += s_coef[1][d0 + e + k2 * D];
+                }
+                cp[e] = sp;
+                cn[e] = sn;
             }
         }
         if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
@@ -543,7 +563,7 @@ cudaError_t launch_select_t(const SelectArgs& a0, int units, cudaStream_t s)
     const size_t keys_bytes = size_t(a.n_cand) * sizeof(uint32_t);
     // two CTAs per SM when they fit: dynamic stages + keys, plus static (histogram) and
     // the per-CTA reservation
-    constexpr size_t kStatic = 10 * 1024;
+    constexpr size_t kStatic = 13 * 1024;
     a.stages = (2 * (3 * size_t(kStageBytes) + keys_bytes + kStatic) <= size_t(kSmemPerSm)) ? 3 : 2;
     const size_t smem = size_t(a.stages) * kStageBytes + keys_bytes;
     static bool configured = false;   // once per instantiation, before any graph capture
@@ -593,6 +613,7 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.Hkv = g.Hkv;
     a.G = g.G;
     a.Hq = g.Hq;
+    a.Q = g.Q;
     a.err = reinterpret_cast<uint32_t*>(ws + L.err);
     a.scores = reinterpret_cast<float*>(ws + L.scores);
     a.counters = reinterpret_cast<uint32_t*>(ws + L.sel_counters);

@@ -41,7 +41,10 @@ class SparseDecoder:
         self.sel_ids = torch.empty(p.batch, p.num_kv_heads, self.sel_stride, dtype=torch.int32,
                                    device=dev)
         self.sel_count = torch.empty(p.batch, p.num_kv_heads, dtype=torch.int32, device=dev)
-        self.out = torch.empty(p.batch, p.num_q_heads, p.head_dim, dtype=torch.float32, device=dev)
+        self.Q = max(1, p.num_queries)
+        out_shape = ((p.batch, self.Q, p.num_q_heads, p.head_dim) if self.Q > 1
+                     else (p.batch, p.num_q_heads, p.head_dim))
+        self.out = torch.empty(out_shape, dtype=torch.float32, device=dev)
 
     def metadata_bytes(self) -> int:
         n = self.kmin.numel() * self.kmin.element_size() * 2

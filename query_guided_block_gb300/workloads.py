@@ -61,6 +61,7 @@ class Workload:
     q_drift: float = 0.15            # q_t = normalise(q_{t-1} + drift*N(0,I)) * |q_0|
     cache_slots: int = 0             # LRU slots per (sequence, KV head); 0 = no diff
     num_reserve: int = 0             # random reserve blocks per (sequence, KV head)
+    num_queries: int = 1             # query vectors per sequence sharing one selection
     seed: int = 0
     description: str = ""
 
@@ -111,6 +112,10 @@ WORKLOADS: Dict[str, Workload] = {
            n_tokens=131072, block_size=32, window_tokens=512, topk=64,
            planted_per_unit=41, num_reserve=41,
            description="gqa_128k plus a 1% random reserve set (41 blocks) per KV head"),
+        _w(name="mq_128k", batch=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+           n_tokens=131072, block_size=32, window_tokens=512, topk=64,
+           planted_per_unit=41, num_queries=16,
+           description="gqa_128k with 16 queries per sequence sharing each KV head's selection"),
         _w(name="lru_64k", batch=32, num_q_heads=32, num_kv_heads=8, head_dim=128,
            n_tokens=65536, block_size=64, window_tokens=512, topk=32,
            steps=64, q_drift=0.15, cache_slots=128,
@@ -151,7 +156,8 @@ def make_inputs(w: Workload, device="cpu", planted_blocks: Optional[torch.Tensor
 
     Returns a dict of tensors on ``device``:
 
-    * ``q``            [B, Hq, D] (``steps == 1``) or [steps, B, Hq, D]; dtype ``q_dtype``
+    * ``q``            [B, Hq, D] (``steps == 1``), [steps, B, Hq, D], or [B, Q, Hq, D] when
+                       ``num_queries`` Q > 1 (then ``queries_per_seq`` = Q); dtype ``q_dtype``
     * ``k_pages``, ``v_pages``  [num_pages, Hkv, block_size, D]; dtype ``kv_dtype``
     * ``block_table``  [B, num_blocks] int32, a seeded permutation of the page pool
     * ``planted``      [B, Hkv, P] int64 logical block ids of planted blocks (P may be 0)
@@ -164,8 +170,16 @@ def make_inputs(w: Workload, device="cpu", planted_blocks: Optional[torch.Tensor
 
     # --- queries first (planted keys point along them) -------------------
     gq = _gen(w, "q", device)
+    Qn = max(1, w.num_queries)
     q0 = torch.randn(B, Hq, D, generator=gq, device=device, dtype=torch.float32)
-    if w.steps > 1:
+    if Qn > 1:
+        if w.steps > 1:
+            raise ValueError("num_queries > 1 with several steps is not a workload here")
+        # queries 1.. of a sequence lie near query 0 (nearby positions of one chunk)
+        rest = q0.unsqueeze(1) + 0.3 * torch.randn(B, Qn - 1, Hq, D, generator=gq, device=device,
+                                                   dtype=torch.float32)
+        q_f32 = torch.cat([q0.unsqueeze(1), rest], 1)          # [B, Q, Hq, D]
+    elif w.steps > 1:
         qs = [q0]
         norm0 = q0.norm(dim=-1, keepdim=True)
         for _ in range(1, w.steps):
@@ -208,7 +222,7 @@ def make_inputs(w: Workload, device="cpu", planted_blocks: Optional[torch.Tensor
         planted = torch.zeros(B, Hkv, 0, dtype=torch.int64, device=device)
 
     if P > 0:
-        q_first = q_f32[0] if w.steps > 1 else q_f32          # [B, Hq, D]
+        q_first = q_f32[0] if w.steps > 1 else (q_f32[:, 0] if Qn > 1 else q_f32)   # [B, Hq, D]
         direction = q_first.view(B, Hkv, w.group, D).sum(dim=2)
         direction = direction / direction.norm(dim=-1, keepdim=True)   # [B, Hkv, D]
         shift = (w.planted_scale * math.sqrt(D)) * direction
@@ -222,6 +236,8 @@ def make_inputs(w: Workload, device="cpu", planted_blocks: Optional[torch.Tensor
 
     out = {"q": q, "k_pages": k_pages, "v_pages": v_pages,
            "block_table": block_table, "planted": planted}
+    if Qn > 1:
+        out["queries_per_seq"] = Qn
     if w.num_reserve > 0:
         gr = _gen(w, "reserve", device)
         keys = torch.rand(B * Hkv, nb, generator=gr, device=device)
@@ -237,8 +253,10 @@ def gather_sequences(inp: dict, seqs, device="cpu") -> dict:
     bt = inp["block_table"][seqs].long()
     pages = bt.reshape(-1)
     q = inp["q"]
-    q = q[:, seqs] if q.dim() == 4 else q[seqs]
+    q = q[seqs] if inp.get("queries_per_seq", 1) > 1 or q.dim() == 3 else q[:, seqs]
     extra = {}
+    if "queries_per_seq" in inp:
+        extra["queries_per_seq"] = inp["queries_per_seq"]
     if "reserve_ids" in inp:
         extra["reserve_ids"] = inp["reserve_ids"][seqs].to(device)
     return {**extra, "k_pages": inp["k_pages"][pages].to(device),

@@ -2,6 +2,8 @@
 exports every entry point the header declares, and rejects bad arguments on the host
 before any CUDA call."""
 import ctypes as C
+
+import torch
 import os
 import re
 
@@ -35,7 +37,8 @@ def test_header_and_binding_agree(L):
 
 def test_sizes_for_the_five_workloads(L):
     expect_stride = {"tiny_fp32_4k": 8 + 2, "mha_32k": 32 + 8, "gqa_128k": 64 + 16,
-                     "two_level_256k": 48 + 8, "lru_64k": 32 + 8, "reserve_128k": 64 + 41 + 16}
+                     "two_level_256k": 48 + 8, "lru_64k": 32 + 8, "reserve_128k": 64 + 41 + 16,
+                    "mq_128k": 64 + 16}
     for name, w in WORKLOADS.items():
         p = B.params_for(w)
         assert B.sparse_attn_num_blocks(p) == w.num_blocks
@@ -56,7 +59,10 @@ def test_bad_parameters_are_rejected(L):
                          (dict(two_level=True, coarse_block=1000), B.INVALID_ARG),
                          (dict(softmax_scale=float("nan")), B.INVALID_ARG),
                          (dict(num_pages=0), B.INVALID_ARG),
-                         (dict(num_reserve=-1), B.INVALID_ARG)]:
+                         (dict(num_reserve=-1), B.INVALID_ARG),
+                         (dict(num_queries=-1), B.INVALID_ARG),
+                         (dict(num_queries=4, kv_dtype=torch.float32), B.UNSUPPORTED),
+                         (dict(num_queries=4, two_level=True), B.UNSUPPORTED)]:
         p = B.params_for(w, **change)
         assert L.sparse_attn_workspace_size(C.byref(p), C.byref(n)) == want, change
     assert L.sparse_attn_workspace_size(None, C.byref(n)) == B.INVALID_ARG
