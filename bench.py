@@ -264,6 +264,22 @@ def run_gpu_arm(args):
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    # one appended token per sequence (a decode step's metadata upkeep), L2 flushed before each
+    app_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+    for a_, b_ in app_ev:
+        flush.zero_()
+        a_.record(stream)
+        dec.append_meta(w.n_tokens - 1, kp, bt)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    append_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in app_ev[3:])
+    # rows holding the new token are rebuilt with the other rows of their build run
+    run_blocks = (w.coarse_block // w.block_size if w.two_level else 1) if dec.kmean is not None else 4
+    nb_all = -(-w.n_tokens // w.block_size)
+    run_start = ((w.n_tokens - 1) // w.block_size) // run_blocks * run_blocks
+    reread = w.batch * w.num_kv_heads * (min(nb_all, run_start + run_blocks) - run_start)
+    append_bytes = reread * w.block_size * w.head_dim * esz * (1 + 2 / w.block_size)
     launches_per_step = (3 if w.two_level else 2) + (1 if cache else 0) + (2 if io else 0)
     step_counter = [0]
 
@@ -434,6 +450,9 @@ def run_gpu_arm(args):
         "roofline": roofline,
         "kernels": kern,
         "build_meta": {"ms": meta_ms, "gbs": meta_bytes / meta_ms / 1e6, "bytes": meta_bytes},
+        "append_meta": {"ms": append_ms, "tokens_appended_per_sequence": 1, "blocks_rebuilt": reread,
+                        "bytes": append_bytes,
+                        "note": "sparse_attn_append_meta(n-1 -> n); launch-latency bound"},
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,

@@ -29,20 +29,26 @@
  *      q           [B, Hq, D]                      q_dtype
  *      k_pages,
  *      v_pages     [num_pages, Hkv, block_size, D] kv_dtype  (one page = one block)
- *      block_table [B, nb] int32   logical block j of sequence b -> physical page
- *      kmin, kmax  [B, Hkv, nb, D] kv_dtype  (min/max of stored values: exact)
- *      kmean       [B, Hkv, n_mean, D] float  (mean over mean_block tokens)
+ *      block_table [B, nb_cap] int32  logical block j of sequence b -> physical page;
+ *                  nb_cap = ceil(capacity_tokens / block_size), = nb when capacity is 0
+ *      kmin, kmax  [B, Hkv, nb_cap, D] kv_dtype  (min/max of stored values: exact)
+ *      kmean       [B, Hkv, n_mean_cap, D] float  (mean over mean_block tokens)
  *      sel_ids     [B, Hkv, sel_stride] int32 ascending; sel_count [B, Hkv] int32
  *      out         [B, Hq, D] float
  *    with nb = ceil(n_tokens / block_size), sel_stride = sparse_attn_sel_stride(p),
- *    mean_block = two_level ? coarse_block : block_size, n_mean = ceil(n_tokens/mean_block).
+ *    mean_block = two_level ? coarse_block : block_size, n_mean = ceil(n_tokens/mean_block);
+ *    with capacity = capacity_tokens (or n_tokens when it is 0), nb_cap = ceil(capacity /
+ *    block_size) and n_mean_cap = ceil(capacity / mean_block) are the rows allocated per
+ *    sequence / unit, of which the first nb (n_mean) hold the current context.
  *    The last block may be partial (n_tokens not a multiple of block_size); its
  *    missing tokens are never read into any result.
  *  * Inputs must be finite.  Every pointer must be 16-byte aligned.
  *  * The workspace (`ws`, `ws_bytes` >= sparse_attn_workspace_size) holds scores,
  *    split-K partials, per-unit completion counters and a device error word.  Run
  *    sparse_attn_workspace_init once after allocating it.  Calls that share one
- *    workspace must be ordered on one stream.
+ *    workspace must be ordered on one stream.  sparse_attn_build_meta and
+ *    sparse_attn_append_meta use only its first 256 bytes (the error word), so one
+ *    workspace sized for any length serves them at every length.
  *
  * Status codes: 0 OK, 1 INVALID_ARG (null/misaligned pointer, bad size), 2 UNSUPPORTED
  * (a dtype / head_dim / block_size / group combination without a kernel), 3 CUDA_ERROR
@@ -109,6 +115,11 @@ typedef struct sparse_attn_params {
                                [B, Q, Hq, D] (query t of sequence b at row b * Q + t), the
                                selection scores are summed over the Q queries, and the KV
                                dtype must be bf16, single level */
+    int32_t capacity_tokens;  /* 0, or >= n_tokens: kmin / kmax / kmean are allocated for a
+                               context of this many tokens, [B, Hkv, ceil(capacity /
+                               block_size), D] and [B, Hkv, ceil(capacity / mean block), D],
+                               so the context can grow (sparse_attn_append_meta) without
+                               moving them; 0 means capacity = n_tokens */
 } sparse_attn_params;
 
 /* Human-readable name of a status code (static storage). */
@@ -129,7 +140,9 @@ int32_t sparse_attn_sel_stride(const sparse_attn_params* p);
  * listed points takes the next point's ratio).  Host-only; -1 on a bad argument. */
 int32_t sparse_attn_topk_for_length(int32_t n_tokens, int32_t block_size);
 
-/* Bytes of workspace the calls below need for this problem. */
+/* Bytes of workspace the calls below need for this problem.  When capacity_tokens >
+ * n_tokens the size covers every context length up to capacity_tokens, so one
+ * workspace serves a growing context. */
 int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes);
 
 /* Zero the workspace's counters and error word (stream-ordered).  Call once after
@@ -148,6 +161,17 @@ int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream str
 int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
                            const int32_t* block_table, void* kmin, void* kmax, float* kmean,
                            void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
+/* Metadata after tokens were appended to the cache (SGLang page §2.2, the block
+ * representation is kept current as the context grows; §3.1.1, incremental update
+ * instead of a rebuild).  p describes the context after the append (n_tokens = N_new);
+ * tokens [n_old, N_new) of every sequence are new and already in the pages.  Only the
+ * rows holding new tokens are rebuilt from their tokens (with the rows sharing a
+ * build run), so the result equals sparse_attn_build_meta at N_new bit for bit; the
+ * other rows are left as they are.  0 <= n_old <= n_tokens. */
+int sparse_attn_append_meta(const sparse_attn_params* p, int32_t n_old, const void* k_pages,
+                            const int32_t* block_table, void* kmin, void* kmax, float* kmean,
+                            void* ws, size_t ws_bytes, sparse_attn_stream stream);
 
 /* Block selection for one decode query per query head.
  * Single level (SGLang page §3.1.2; SparDA page §3.2 fixed top-k):

@@ -37,13 +37,13 @@ class sparse_attn_params(C.Structure):
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "n_tokens", "block_size",
         "num_pages", "window_tokens", "topk", "two_level", "coarse_block", "topk_coarse",
         "score_kind", "kv_dtype", "q_dtype")] + [("softmax_scale", C.c_float), ("num_reserve", C.c_int32),
-                                                 ("num_queries", C.c_int32)]
+                                                 ("num_queries", C.c_int32), ("capacity_tokens", C.c_int32)]
 
 
 def make_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size, num_pages,
                 window_tokens, topk, two_level=False, coarse_block=1024, topk_coarse=48,
                 score_kind=SCORE_QUEST, kv_dtype=torch.bfloat16, q_dtype=torch.bfloat16,
-                softmax_scale=0.0, num_reserve=0, num_queries=1) -> sparse_attn_params:
+                softmax_scale=0.0, num_reserve=0, num_queries=1, capacity_tokens=0) -> sparse_attn_params:
     def code(dt):
         if dt in (torch.bfloat16, BF16):
             return BF16
@@ -55,7 +55,7 @@ def make_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size
     return sparse_attn_params(batch, num_q_heads, num_kv_heads, head_dim, n_tokens, block_size,
                               num_pages, window_tokens, topk, int(bool(two_level)), coarse_block,
                               topk_coarse, int(score_kind), code(kv_dtype), code(q_dtype),
-                              float(softmax_scale), int(num_reserve), int(num_queries))
+                              float(softmax_scale), int(num_reserve), int(num_queries), int(capacity_tokens))
 
 
 def params_for(w, **over) -> sparse_attn_params:
@@ -90,6 +90,7 @@ def lib():
             "sparse_attn_workspace_size": ([P, C.POINTER(C.c_size_t)], C.c_int),
             "sparse_attn_workspace_init": ([vp, sz, vp], C.c_int),
             "sparse_attn_build_meta": ([P, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
+            "sparse_attn_append_meta": ([P, i32, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_select": ([P, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_decode": ([P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_diff": ([P, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -116,7 +117,8 @@ def exported_symbols():
             "sparse_attn_select", "sparse_attn_decode", "sparse_attn_diff",
             "sparse_attn_get_device_error", "sparse_attn_select_noalloc",
             "sparse_attn_select_reserved", "sparse_attn_topk_for_length",
-            "sparse_attn_slot_map", "sparse_attn_load_misses", "sparse_attn_decode_slots"]
+            "sparse_attn_slot_map", "sparse_attn_load_misses", "sparse_attn_decode_slots",
+            "sparse_attn_append_meta"]
 
 
 def _status_string(status: int) -> str:
@@ -182,6 +184,20 @@ def sparse_attn_build_meta(p, k_pages, block_table, kmin, kmax, kmean, ws, strea
     _check("sparse_attn_build_meta", lib().sparse_attn_build_meta(
         C.byref(p), _ptr(k_pages), _ptr(block_table), _ptr(kmin), _ptr(kmax), _ptr(kmean),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_append_meta(p, n_old, k_pages, block_table, kmin, kmax, kmean, ws, stream=None) -> None:
+    _check("sparse_attn_append_meta", lib().sparse_attn_append_meta(
+        C.byref(p), int(n_old), _ptr(k_pages), _ptr(block_table), _ptr(kmin), _ptr(kmax), _ptr(kmean),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def meta_rows(p) -> tuple:
+    """(block rows, mean rows) allocated per unit in kmin / kmax and kmean: the capacity
+    (capacity_tokens, or n_tokens when it is 0) in blocks and in mean rows."""
+    cap = p.capacity_tokens if p.capacity_tokens > 0 else p.n_tokens
+    mean_block = p.coarse_block if p.two_level else p.block_size
+    return -(-cap // p.block_size), -(-cap // mean_block)
 
 
 def sparse_attn_select(p, q, kmin, kmax, kmean, sel_ids, sel_count, ws, stream=None) -> None:

@@ -21,7 +21,8 @@ int make_geometry(const sparse_attn_params* p, Geometry* g)
     memset(g, 0, sizeof *g);
     if (p->batch < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->head_dim < 1 ||
         p->n_tokens < 0 || p->block_size < 1 || p->num_pages < 0 || p->window_tokens < 0 ||
-        p->topk < 0 || p->topk_coarse < 0 || p->num_reserve < 0 || p->num_queries < 0)
+        p->topk < 0 || p->topk_coarse < 0 || p->num_reserve < 0 || p->num_queries < 0 ||
+        (p->capacity_tokens != 0 && p->capacity_tokens < p->n_tokens))
         return SPARSE_ATTN_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return SPARSE_ATTN_INVALID_ARG;
     if (p->two_level != 0 && p->two_level != 1) return SPARSE_ATTN_INVALID_ARG;
@@ -86,6 +87,9 @@ int make_geometry(const sparse_attn_params* p, Geometry* g)
         g->mean_block = bs;
     }
     g->n_mean = (p->n_tokens + g->mean_block - 1) / g->mean_block;
+    const long long cap = p->capacity_tokens > 0 ? p->capacity_tokens : p->n_tokens;
+    g->nb_cap = int((cap + bs - 1) / bs);
+    g->n_mean_cap = int((cap + g->mean_block - 1) / g->mean_block);
     const float scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf(float(p->head_dim));
     g->scale_log2 = scale * 1.4426950408889634f;
     return SPARSE_ATTN_OK;
@@ -181,7 +185,27 @@ int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes)
     Geometry g;
     int st = make_geometry(p, &g);
     if (st) return st;
-    *bytes = workspace_layout(g).total;
+    size_t total = workspace_layout(g).total;
+    if (p->capacity_tokens > p->n_tokens) {
+        // Every length up to the capacity: each term of the layout grows with the
+        // length except the window's block count, which alternates between two values
+        // as the window slides over block boundaries; bound that one separately.
+        sparse_attn_params pc = *p;
+        pc.n_tokens = p->capacity_tokens;
+        Geometry gc;
+        st = make_geometry(&pc, &gc);
+        if (st) return st;
+        if (p->window_tokens > 0) {
+            int win_max = (p->window_tokens + gc.bs - 1) / gc.bs + 1;
+            if (win_max > gc.nb) win_max = gc.nb;
+            const int k_max = gc.topk < gc.n_cand ? gc.topk : gc.n_cand;
+            const int r_max = gc.n_reserve < gc.n_cand ? gc.n_reserve : gc.n_cand;
+            if (k_max + r_max + win_max > gc.sel_stride) gc.sel_stride = k_max + r_max + win_max;
+        }
+        const size_t tc = workspace_layout(gc).total;
+        if (tc > total) total = tc;
+    }
+    *bytes = total;
     return SPARSE_ATTN_OK;
 }
 
@@ -191,15 +215,17 @@ int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream str
     return status_of(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
-                           const int32_t* block_table, void* kmin, void* kmax, float* kmean,
-                           void* ws, size_t ws_bytes, sparse_attn_stream stream)
+static int meta_common(const sparse_attn_params* p, int32_t first_token, const void* k_pages,
+                       const int32_t* block_table, void* kmin, void* kmax, float* kmean, void* ws,
+                       size_t ws_bytes, sparse_attn_stream stream)
 {
     Geometry g;
     int st = make_geometry(p, &g);
     if (st) return st;
+    if (first_token < 0 || first_token > g.N) return SPARSE_ATTN_INVALID_ARG;
     const WorkspaceLayout L = workspace_layout(g);
-    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    // the metadata kernels touch only the header's error word
+    if (!ws || !aligned(ws, 256) || ws_bytes < 256) return SPARSE_ATTN_INVALID_ARG;
     const bool need_mean = g.two_level || g.score_kind == SPARSE_ATTN_SCORE_MEAN;
     if (need_mean && !kmean) return SPARSE_ATTN_INVALID_ARG;
     if (g.units() > 0 && g.nb > 0) {
@@ -208,10 +234,25 @@ int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
             !aligned(block_table, 4) || (kmean && !aligned(kmean, 16)))
             return SPARSE_ATTN_INVALID_ARG;
     }
+    if (first_token == g.N && first_token > 0) return SPARSE_ATTN_OK;   // nothing appended
     char* w = static_cast<char*>(ws);
     return status_of(launch_build_meta(g, k_pages, block_table, kmin, kmax, need_mean ? kmean : nullptr,
-                                       reinterpret_cast<uint32_t*>(w + L.err),
+                                       reinterpret_cast<uint32_t*>(w + L.err), first_token,
                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_build_meta(const sparse_attn_params* p, const void* k_pages,
+                           const int32_t* block_table, void* kmin, void* kmax, float* kmean,
+                           void* ws, size_t ws_bytes, sparse_attn_stream stream)
+{
+    return meta_common(p, 0, k_pages, block_table, kmin, kmax, kmean, ws, ws_bytes, stream);
+}
+
+int sparse_attn_append_meta(const sparse_attn_params* p, int32_t n_old, const void* k_pages,
+                            const int32_t* block_table, void* kmin, void* kmax, float* kmean,
+                            void* ws, size_t ws_bytes, sparse_attn_stream stream)
+{
+    return meta_common(p, n_old, k_pages, block_table, kmin, kmax, kmean, ws, ws_bytes, stream);
 }
 
 static int select_common(const sparse_attn_params* p, const void* q, const void* kmin,

@@ -41,6 +41,7 @@ struct DecodeArgs {
     const int32_t* sel_count;
     float* out;
     int Hq, Hkv, nb, bs, N, num_pages, sel_stride;
+    int bt_stride;           // block_table row length (capacity in blocks)
     // slot mode (slot_C > 0): K/V come from a per-unit slot pool [units * slot_C, bs, D]
     // through sel_slot [units, sel_stride] instead of block_table and the page pools
     const int32_t* sel_slot;
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
                 }
             } else {
                 const int b = u / a.Hkv;
-                const int p = a.block_table[size_t(b) * a.nb + j];
+                const int p = a.block_table[size_t(b) * a.bt_stride + j];
                 if (p < 0 || p >= a.num_pages) {
                     raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
                 } else {
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a
                     valid = min(a.bs, a.N - j * a.bs);
                 }
             } else {
-                const int p = a.block_table[size_t(u / a.Hkv) * a.nb + j];
+                const int p = a.block_table[size_t(u / a.Hkv) * a.bt_stride + j];
                 if (p < 0 || p >= a.num_pages) {
                     raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
                 } else {
@@ -914,6 +915,7 @@ cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws,
     a.bs = g.bs;
     a.N = g.N;
     a.num_pages = g.num_pages;
+    a.bt_stride = g.nb_cap;
     a.sel_stride = g.sel_stride;
     a.blocks_per_item = L.blocks_per_split;
     a.items_per_unit = L.max_splits;

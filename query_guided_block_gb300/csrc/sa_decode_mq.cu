@@ -42,6 +42,7 @@ struct MqArgs {
     const int32_t* sel_count;
     float* out;
     int Hq, Hkv, G, Q, R, nb, bs, N, num_pages, sel_stride;
+    int bt_stride;       // block_table row length (capacity in blocks)
     int row_tiles, nsplit, max_splits;
     float scale_log2;
     float* part_m;    // [units * R, max_splits]
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kMqThreads, 2) decode_mq_kernel(MqArgs a)
         if (j < 0 || j >= a.nb) {
             raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
         } else {
-            const int p = a.block_table[size_t(b) * a.nb + j];
+            const int p = a.block_table[size_t(b) * a.bt_stride + j];
             if (p < 0 || p >= a.num_pages) {
                 raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
             } else {
@@ -414,6 +415,7 @@ cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* 
     a.bs = g.bs;
     a.N = g.N;
     a.num_pages = g.num_pages;
+    a.bt_stride = g.nb_cap;
     a.sel_stride = g.sel_stride;
     a.row_tiles = mq_row_tiles(g.Q, g.G);
     a.max_splits = L.max_splits;

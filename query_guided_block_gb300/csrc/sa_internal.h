@@ -21,6 +21,7 @@ struct Geometry {
     bool two_level;
     int coarse_block, per_coarse, n_coarse, topk_coarse;
     int mean_block, n_mean;        // kmean rows per unit
+    int nb_cap, n_mean_cap;        // metadata rows allocated per unit (capacity_tokens)
     int topk;
     int n_reserve;                 // reserve block ids per unit (0: none)
     int Q;                         // query vectors per sequence sharing a selection (>= 1)
@@ -63,7 +64,7 @@ int decode_blocks_per_item(int D, bool kv_bf16, int block_size);
 bool decode_supported(int D, bool kv_bf16, int block_size, int G);
 
 cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int32_t* block_table,
-                              void* kmin, void* kmax, float* kmean, uint32_t* err,
+                              void* kmin, void* kmax, float* kmean, uint32_t* err, int first_token,
                               cudaStream_t s);
 
 cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,

@@ -30,6 +30,7 @@ struct IoArgs {
     char* pool_k;                // [units, C, bs, D]
     char* pool_v;
     int units, Hkv, nb, num_pages, stride, C;
+    int bt_stride;               // block_table row length (capacity in blocks)
     size_t tile_bytes;           // bs * D * element size
     uint32_t* err;
 };
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kIoThreads) load_misses_kernel(IoArgs a)
         if (j < 0 || j >= a.nb || s < 0 || s >= a.C) {
             if (t == 0) raise_error(a.err, j < 0 || j >= a.nb ? SPARSE_ATTN_ERR_SEL_ID : SPARSE_ATTN_ERR_SLOT);
         } else {
-            const int page = a.block_table[size_t(b) * a.nb + j];
+            const int page = a.block_table[size_t(b) * a.bt_stride + j];
             if (page < 0 || page >= a.num_pages) {
                 if (t == 0) raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
             } else {
@@ -169,6 +170,7 @@ cudaError_t launch_load_misses(const Geometry& g, const void* host_k, const void
     a.Hkv = g.Hkv;
     a.nb = g.nb;
     a.num_pages = g.num_pages;
+    a.bt_stride = g.nb_cap;
     a.stride = g.sel_stride;
     a.C = cache_slots;
     a.tile_bytes = size_t(g.bs) * g.D * (g.kv_bf16 ? 2 : 4);

@@ -28,9 +28,13 @@ struct MetaArgs {
     float* kmean;
     uint32_t* err;
     int Hkv, bs, N, nb, num_pages, D;
+    int bt_stride;        // block_table row length (capacity in blocks)
     int run_blocks;       // logical blocks per warp run (= mean row when kmean is built)
-    int runs_per_unit;
-    long long total_runs;
+    int runs_per_unit;    // runs of the context
+    int run_first;        // first run to (re)build: 0, or the run holding the first appended token
+    int row_stride;       // kmin / kmax rows per unit (capacity)
+    int mean_stride;      // kmean rows per unit (capacity)
+    long long total_runs; // units * (runs_per_unit - run_first)
 };
 
 template <int D, bool BF16>
@@ -45,8 +49,11 @@ __global__ void __launch_bounds__(kMetaWarps * 32) build_meta_kernel(MetaArgs a)
     const int lane = threadIdx.x & 31;
     const long long run = (long long)blockIdx.x * kMetaWarps + (threadIdx.x >> 5);
     if (run >= a.total_runs) return;
-    const int u = int(run / a.runs_per_unit);
-    const int r = int(run % a.runs_per_unit);
+    allow_dependents_early();
+    grid_dependency_wait();   // K pages (e.g. just appended) may come from the previous kernel
+    const int live = a.runs_per_unit - a.run_first;
+    const int u = int(run / live);
+    const int r = a.run_first + int(run % live);
     const int b = u / a.Hkv, kvh = u % a.Hkv;
     const int sub = lane % LPR, rsub = lane / LPR;
 
@@ -61,7 +68,7 @@ __global__ void __launch_bounds__(kMetaWarps * 32) build_meta_kernel(MetaArgs a)
     const int j0 = r * a.run_blocks;
     const int j1 = min(a.nb, j0 + a.run_blocks);
     for (int j = j0; j < j1; ++j) {
-        const int page = a.block_table[size_t(b) * a.nb + j];
+        const int page = a.block_table[size_t(b) * a.bt_stride + j];
         if (page < 0 || page >= a.num_pages) {
             if (lane == 0) raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
             continue;
@@ -112,7 +119,7 @@ __global__ void __launch_bounds__(kMetaWarps * 32) build_meta_kernel(MetaArgs a)
             }
         }
         if (rsub == 0) {
-            const size_t row = (size_t(u) * a.nb + j) * D + sub * EPL;
+            const size_t row = (size_t(u) * a.row_stride + j) * D + sub * EPL;
             uint4 wlo, whi;
             if constexpr (BF16) {
                 wlo.x = f32_to_bf16_bits_exact(lo[0]) | (f32_to_bf16_bits_exact(lo[1]) << 16);
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(kMetaWarps * 32) build_meta_kernel(MetaArgs a)
         }
         if (rsub == 0 && tokens > 0) {
             const float inv = 1.0f / float(tokens);
-            float* dst = a.kmean + (size_t(u) * a.runs_per_unit + r) * D + sub * EPL;
+            float* dst = a.kmean + (size_t(u) * a.mean_stride + r) * D + sub * EPL;
 #pragma unroll
             for (int e = 0; e < EPL; e += 4)
                 *reinterpret_cast<float4*>(dst + e) =
@@ -158,14 +165,13 @@ cudaError_t launch_meta_t(const MetaArgs& a, cudaStream_t s)
 {
     const long long ctas = (a.total_runs + kMetaWarps - 1) / kMetaWarps;
     if (ctas == 0) return cudaSuccess;
-    build_meta_kernel<D, BF16><<<dim3(unsigned(ctas)), kMetaWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_after_previous(build_meta_kernel<D, BF16>, dim3(unsigned(ctas)), dim3(kMetaWarps * 32), 0, s, a);
 }
 
 }  // namespace
 
 cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int32_t* block_table,
-                              void* kmin, void* kmax, float* kmean, uint32_t* err,
+                              void* kmin, void* kmax, float* kmean, uint32_t* err, int first_token,
                               cudaStream_t s)
 {
     MetaArgs a{};
@@ -180,11 +186,17 @@ cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int3
     a.N = g.N;
     a.nb = g.nb;
     a.num_pages = g.num_pages;
+    a.bt_stride = g.nb_cap;
     a.D = g.D;
     // A mean row is a whole number of blocks: one warp owns exactly one mean row.
     a.run_blocks = kmean ? g.mean_block / g.bs : kMetaRunNoMean;
     a.runs_per_unit = (g.nb + a.run_blocks - 1) / a.run_blocks;
-    a.total_runs = (long long)g.units() * a.runs_per_unit;
+    // rows holding tokens >= first_token are rebuilt from their tokens; earlier rows keep
+    // their values (their tokens have not changed)
+    a.run_first = min(a.runs_per_unit, (first_token / g.bs) / a.run_blocks);
+    a.row_stride = g.nb_cap;
+    a.mean_stride = g.n_mean_cap;
+    a.total_runs = (long long)g.units() * (a.runs_per_unit - a.run_first);
     if (g.D == 128) return g.kv_bf16 ? launch_meta_t<128, true>(a, s) : launch_meta_t<128, false>(a, s);
     return g.kv_bf16 ? launch_meta_t<64, true>(a, s) : launch_meta_t<64, false>(a, s);
 }

@@ -43,7 +43,8 @@ struct SelectArgs {
     const void* kmin;    // QUEST: [units, rows, D] metadata dtype
     const void* kmax;
     const float* kmean;  // MEAN:  [units, rows, D] fp32
-    int rows;            // metadata rows per unit
+    int rows;            // metadata rows per unit (the context's)
+    int row_stride;      // metadata rows allocated per unit (capacity)
     int Hkv, G;
     int Hq;
     int Q;               // query vectors per sequence; the coefficients sum over all of them
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a)
         const uint32_t bytes = uint32_t(c.nrows) * SS::ROW_BYTES;
         if (array == 0) mbar_arrive_expect_tx(&full[s], bytes * SS::ARRAYS);
         if (bytes) {
-            const size_t off = (size_t(c.u) * a.rows + c.row0) * SS::ROW_BYTES;
+            const size_t off = (size_t(c.u) * a.row_stride + c.row0) * SS::ROW_BYTES;
             unsigned char* dst = smem + s * kStageBytes;
             if (array == 0) bulk_copy_g2s(dst, hi_src + off, bytes, &full[s]);
             else bulk_copy_g2s(dst + ROWS * SS::ROW_BYTES, lo_src + off, bytes, &full[s]);
@@ -620,6 +621,7 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
 
     if (!g.two_level) {
         a.rows = g.nb;
+        a.row_stride = g.score_kind == SPARSE_ATTN_SCORE_MEAN ? g.n_mean_cap : g.nb_cap;
         a.via_survivors = 0;
         a.row_limit = g.win_first;
         a.n_cand = g.n_cand;
@@ -648,6 +650,7 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     int32_t* n_surv = reinterpret_cast<int32_t*>(ws + L.n_survivors);
     SelectArgs l1 = a;
     l1.rows = g.n_coarse;
+    l1.row_stride = g.n_mean_cap;
     l1.via_survivors = 0;
     l1.row_limit = g.n_coarse;
     l1.n_cand = g.n_coarse;
@@ -669,6 +672,7 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     // ---- level 2: Quest bound over the survivors' slices, plus the window ----
     SelectArgs l2 = a;
     l2.rows = g.nb;
+    l2.row_stride = g.nb_cap;
     l2.via_survivors = 1;
     l2.surv = surv;
     l2.n_surv = n_surv;

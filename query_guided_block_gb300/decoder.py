@@ -26,14 +26,13 @@ class SparseDecoder:
         kv = torch.bfloat16 if p.kv_dtype == B.BF16 else torch.float32
         self.kv_dtype = kv
         dev = self.device
-        self.kmin = torch.empty(p.batch, p.num_kv_heads, self.nb, p.head_dim, dtype=kv, device=dev)
+        rows_blk, rows_mean = B.meta_rows(p)             # capacity, >= the context's rows
+        self.kmin = torch.empty(p.batch, p.num_kv_heads, rows_blk, p.head_dim, dtype=kv, device=dev)
         self.kmax = torch.empty_like(self.kmin)
         self.needs_mean = bool(p.two_level) or p.score_kind == B.SCORE_MEAN
         self.kmean = None
         if self.needs_mean:
-            mb = p.coarse_block if p.two_level else p.block_size
-            rows = -(-p.n_tokens // mb)
-            self.kmean = torch.empty(p.batch, p.num_kv_heads, rows, p.head_dim, dtype=torch.float32,
+            self.kmean = torch.empty(p.batch, p.num_kv_heads, rows_mean, p.head_dim, dtype=torch.float32,
                                      device=dev)
         self.ws_bytes = B.sparse_attn_workspace_size(p)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
@@ -55,6 +54,11 @@ class SparseDecoder:
     def build_meta(self, k_pages, block_table, stream=None):
         B.sparse_attn_build_meta(self.p, k_pages, block_table, self.kmin, self.kmax, self.kmean,
                                  self.ws, stream)
+
+    def append_meta(self, n_old, k_pages, block_table, stream=None):
+        """Metadata after tokens [n_old, p.n_tokens) were appended to the pages."""
+        B.sparse_attn_append_meta(self.p, n_old, k_pages, block_table, self.kmin, self.kmax,
+                                  self.kmean, self.ws, stream)
 
     def select(self, q, reserve_ids=None, stream=None):
         """Selection; with ``reserve_ids`` [B, Hkv, num_reserve] int32 (drawn by the caller)

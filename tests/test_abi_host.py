@@ -62,7 +62,8 @@ def test_bad_parameters_are_rejected(L):
                          (dict(num_reserve=-1), B.INVALID_ARG),
                          (dict(num_queries=-1), B.INVALID_ARG),
                          (dict(num_queries=4, kv_dtype=torch.float32), B.UNSUPPORTED),
-                         (dict(num_queries=4, two_level=True), B.UNSUPPORTED)]:
+                         (dict(num_queries=4, two_level=True), B.UNSUPPORTED),
+                         (dict(capacity_tokens=1000), B.INVALID_ARG)]:         # below n_tokens
         p = B.params_for(w, **change)
         assert L.sparse_attn_workspace_size(C.byref(p), C.byref(n)) == want, change
     assert L.sparse_attn_workspace_size(None, C.byref(n)) == B.INVALID_ARG
@@ -115,3 +116,23 @@ def test_plain_select_refuses_a_reserve_count(L):
     p = B.params_for(WORKLOADS["reserve_128k"])
     rc = L.sparse_attn_select(C.byref(p), None, None, None, None, None, None, None, 0, None)
     assert rc == B.INVALID_ARG
+
+
+def test_append_rejects_bad_lengths(L):
+    """n_old outside [0, n_tokens] is refused on the host, before any launch."""
+    p = B.params_for(WORKLOADS["gqa_128k"], capacity_tokens=200000)
+    for n_old in (-1, p.n_tokens + 1):
+        rc = L.sparse_attn_append_meta(C.byref(p), n_old, None, None, None, None, None, None, 0, None)
+        assert rc == B.INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["gqa_128k", "reserve_128k", "two_level_256k", "lru_64k"])
+def test_capacity_workspace_covers_every_length(name):
+    """A workspace sized with capacity_tokens serves select / decode at every length up
+    to the capacity (the window's block count alternates as it slides over block
+    boundaries, so the size at the capacity alone is not always enough)."""
+    w = WORKLOADS[name]
+    cap = w.n_tokens + 5 * w.block_size + 3
+    big = B.sparse_attn_workspace_size(B.params_for(w, capacity_tokens=cap))
+    for n in range(w.n_tokens - 3 * w.block_size, cap + 1):
+        assert B.sparse_attn_workspace_size(B.params_for(w, n_tokens=n)) <= big, n
