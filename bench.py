@@ -275,7 +275,7 @@ def run_gpu_arm(args):
     torch.cuda.synchronize()
     append_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in app_ev[3:])
     # rows holding the new token are rebuilt with the other rows of their build run
-    run_blocks = (w.coarse_block // w.block_size if w.two_level else 1) if dec.kmean is not None else 4
+    run_blocks = (w.coarse_block // w.block_size if w.two_level else 1) if dec.kmean is not None else 1
     nb_all = -(-w.n_tokens // w.block_size)
     run_start = ((w.n_tokens - 1) // w.block_size) // run_blocks * run_blocks
     reread = w.batch * w.num_kv_heads * (min(nb_all, run_start + run_blocks) - run_start)

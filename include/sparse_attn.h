@@ -214,6 +214,20 @@ int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k
                        const int32_t* sel_count, float* out, void* ws, size_t ws_bytes,
                        sparse_attn_stream stream);
 
+/* One decode step in a single launch: sparse_attn_select_reserved (num_reserve = 0
+ * allowed, reserve_ids may then be NULL) followed by sparse_attn_decode, with the same
+ * results bit for bit (SGLang page §1.2, select-then-compute as one step).  The
+ * attention of a (sequence, KV head) unit starts as soon as that unit's selection is
+ * written, not after the whole batch's.  sel_ids / sel_count are written as by the
+ * select call.  Single-level selection, bf16 K/V and one query per sequence only
+ * (SPARSE_ATTN_UNSUPPORTED otherwise, or when one CTA per SM cannot hold the problem:
+ * then call the two entry points).  The launch is cooperative; a workspace must not be
+ * shared by two concurrent steps. */
+int sparse_attn_step(const sparse_attn_params* p, const void* q, const void* kmin, const void* kmax,
+                     const float* kmean, const int32_t* reserve_ids, const void* k_pages,
+                     const void* v_pages, const int32_t* block_table, int32_t* sel_ids,
+                     int32_t* sel_count, float* out, void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
 /* Step-to-step diff and LRU slot cache (SGLang page §3.2: cache 2-4x top-k, LRU
  * eviction; steps a-d: diff against the previous step, find what is resident, load
  * the misses, update the index).  For each unit, with S = sel_ids row (ascending,

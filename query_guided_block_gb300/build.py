@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libsparse_attn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["sa_api.cu", "sa_meta.cu", "sa_select.cu", "sa_decode.cu", "sa_diff.cu", "sa_io.cu", "sa_decode_mq.cu"]
+SOURCES = ["sa_api.cu", "sa_meta.cu", "sa_select.cu", "sa_decode.cu", "sa_diff.cu", "sa_io.cu", "sa_decode_mq.cu", "sa_step.cu", "sa_step_d64.cu"]
 
 
 def nvcc() -> str:

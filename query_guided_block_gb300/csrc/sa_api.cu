@@ -139,6 +139,7 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     L.sel_counters = off;     off = align256(off + units * sizeof(uint32_t));
     L.dec_counters = off;     off = align256(off + dec_cells * sizeof(uint32_t));
     L.l1_counters = off;      off = align256(off + units * sizeof(uint32_t));
+    L.ready = off;            off = align256(off + units * sizeof(uint32_t));
     L.scores = off;           off = align256(off + units * L.score_cols * sizeof(float));
     L.survivors = off;        off = align256(off + units * size_t(g.topk_coarse > 0 ? g.topk_coarse : 1) * sizeof(int32_t));
     L.n_survivors = off;      off = align256(off + units * sizeof(int32_t));
@@ -332,6 +333,40 @@ int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k
                                           sel_ids, sel_count, out, reinterpret_cast<cudaStream_t>(stream)));
     return status_of(launch_decode(g, L, static_cast<char*>(ws), q, k_pages, v_pages, block_table,
                                    sel_ids, sel_count, out, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_step(const sparse_attn_params* p, const void* q, const void* kmin, const void* kmax,
+                     const float* kmean, const int32_t* reserve_ids, const void* k_pages,
+                     const void* v_pages, const int32_t* block_table, int32_t* sel_ids,
+                     int32_t* sel_count, float* out, void* ws, size_t ws_bytes, sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    if (!step_supported(g)) return SPARSE_ATTN_UNSUPPORTED;
+    if (g.n_reserve > 0 && g.units() > 0 && (!reserve_ids || !aligned(reserve_ids, 4)))
+        return SPARSE_ATTN_INVALID_ARG;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (g.units() > 0) {
+        if (!q || !out || !sel_ids || !sel_count || !aligned(q, 16) || !aligned(out, 16) ||
+            !aligned(sel_ids, 4) || !aligned(sel_count, 4))
+            return SPARSE_ATTN_INVALID_ARG;
+        if (g.nb > 0) {
+            const bool mean = g.score_kind == SPARSE_ATTN_SCORE_MEAN;
+            if (mean && (!kmean || !aligned(kmean, 16))) return SPARSE_ATTN_INVALID_ARG;
+            if (!mean && (!kmin || !kmax || !aligned(kmin, 16) || !aligned(kmax, 16)))
+                return SPARSE_ATTN_INVALID_ARG;
+            if (!k_pages || !v_pages || !block_table || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+                !aligned(block_table, 4))
+                return SPARSE_ATTN_INVALID_ARG;
+        }
+    }
+    const cudaError_t e = launch_step(g, L, static_cast<char*>(ws), q, kmin, kmax, kmean, reserve_ids, k_pages,
+                                      v_pages, block_table, sel_ids, sel_count, out,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return SPARSE_ATTN_UNSUPPORTED;
+    return status_of(e);
 }
 
 int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,

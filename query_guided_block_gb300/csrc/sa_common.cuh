@@ -54,6 +54,32 @@ __device__ __forceinline__ float load_q(const void* q, size_t idx, bool bf16)
     return reinterpret_cast<const float*>(q)[idx];
 }
 
+// N consecutive query elements from element idx (16-byte aligned for N = 8 bf16 or
+// 4 fp32; 8-byte for 4 bf16), widened to fp32.
+template <int N>
+__device__ __forceinline__ void load_q_vec(const void* q, size_t idx, bool bf16, float* out)
+{
+    static_assert(N == 4 || N == 8, "4 or 8 elements");
+    if (bf16) {
+        const uint16_t* p = reinterpret_cast<const uint16_t*>(q) + idx;
+        if constexpr (N == 8) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+            unpack16<true>(v, out);
+        } else {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+            out[0] = bf16_lo(v.x); out[1] = bf16_hi(v.x);
+            out[2] = bf16_lo(v.y); out[3] = bf16_hi(v.y);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(q) + idx);
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            const float4 v = __ldg(p + i);
+            out[4 * i] = v.x; out[4 * i + 1] = v.y; out[4 * i + 2] = v.z; out[4 * i + 3] = v.w;
+        }
+    }
+}
+
 // Round-trip of a float that holds a bf16 value back to its 16-bit pattern (exact).
 __device__ __forceinline__ uint32_t f32_to_bf16_bits_exact(float x) { return __float_as_uint(x) >> 16; }
 
@@ -306,6 +332,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 // About one second at GB300 clocks: far beyond any legitimate copy latency.
 constexpr long long kWaitCycles = 2000000000LL;
+
+// Device-scope flag hand-off between CTAs of one grid: the writer publishes with a
+// release store (after a fence that covers its CTA's writes), the reader polls with
+// acquire loads.
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *flag == want, giving up after about `max_cycles` SM clocks (false).
+__device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t want, long long max_cycles)
+{
+    if (ld_acquire_gpu(flag) == want) return true;
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(flag) != want) {
+        if (clock64() - t0 > max_cycles) return false;
+        __nanosleep(32);
+    }
+    return true;
+}
 
 // exp2 on the special-function unit (PTX ex2.approx.ftz.f32; about 2 ulp).
 __device__ __forceinline__ float fast_exp2(float x)

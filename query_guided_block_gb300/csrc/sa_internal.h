@@ -40,6 +40,7 @@ struct WorkspaceLayout {
     size_t sel_counters;   // uint32 [units]
     size_t dec_counters;   // uint32 [units]
     size_t l1_counters;    // uint32 [units] (two-level, level 1)
+    size_t ready;          // uint32 [units] (fused step: unit's selection published)
     size_t scores;         // float [units, score_cols]
     size_t survivors;      // int32 [units, topk_coarse] (two-level)
     size_t n_survivors;    // int32 [units]
@@ -70,12 +71,13 @@ cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int3
 cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* kmin, const void* kmax, const float* kmean,
                           const int32_t* reserve_ids, int32_t* sel_ids, int32_t* sel_count,
-                          cudaStream_t s);
+                          cudaStream_t s, uint32_t* ready = nullptr);   // publish ready[u] per unit
 
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* k_pages, const void* v_pages, const int32_t* block_table,
                           const int32_t* sel_ids, const int32_t* sel_count, float* out,
-                          const int32_t* sel_slot, int slot_C, cudaStream_t s);
+                          const int32_t* sel_slot, int slot_C, cudaStream_t s,
+                          uint32_t* ready = nullptr);   // bf16 K/V only: wait per unit on ready[]
 // Multi-query attention (sa_decode_mq.cu): Q query vectors per sequence, one selection.
 int mq_row_tiles(int Q, int G);
 cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
@@ -90,6 +92,21 @@ cudaError_t launch_load_misses(const Geometry& g, const void* host_k, const void
 cudaError_t launch_slot_map(const Geometry& g, const int32_t* sel_ids, const int32_t* sel_count,
                             const int32_t* slot_block, int cache_slots, int32_t* sel_slot,
                             uint32_t* err, cudaStream_t s);
+
+// Fused step (sa_step.cu): select then decode in one cooperative persistent launch,
+// single-level selection, bf16 K/V, one query per sequence.  cudaErrorNotSupported
+// when the problem does not fit one CTA per SM.
+bool step_supported(const Geometry& g);
+cudaError_t launch_step(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
+                        const void* kmin, const void* kmax, const float* kmean,
+                        const int32_t* reserve_ids, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, int32_t* sel_ids, int32_t* sel_count, float* out,
+                        cudaStream_t s);
+cudaError_t launch_step_d64(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
+                            const void* kmin, const void* kmax, const float* kmean,
+                            const int32_t* reserve_ids, const void* k_pages, const void* v_pages,
+                            const int32_t* block_table, int32_t* sel_ids, int32_t* sel_count, float* out,
+                            cudaStream_t s);
 
 cudaError_t launch_diff(const Geometry& g, int step, const int32_t* sel_ids,
                         const int32_t* sel_count, const int32_t* prev_ids,

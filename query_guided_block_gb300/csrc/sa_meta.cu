@@ -189,7 +189,9 @@ cudaError_t launch_build_meta(const Geometry& g, const void* k_pages, const int3
     a.bt_stride = g.nb_cap;
     a.D = g.D;
     // A mean row is a whole number of blocks: one warp owns exactly one mean row.
-    a.run_blocks = kmean ? g.mean_block / g.bs : kMetaRunNoMean;
+    // Without means an append rebuilds single blocks (min / max are exact, so the
+    // grouping of blocks into runs does not change a bit of the result).
+    a.run_blocks = kmean ? g.mean_block / g.bs : (first_token > 0 ? 1 : kMetaRunNoMean);
     a.runs_per_unit = (g.nb + a.run_blocks - 1) / a.run_blocks;
     // rows holding tokens >= first_token are rebuilt from their tokens; earlier rows keep
     // their values (their tokens have not changed)

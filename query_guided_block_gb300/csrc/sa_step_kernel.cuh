@@ -1,0 +1,118 @@
+// The fused step kernel (select phase, then decode phase, in one cooperative grid)
+// and its launcher, instantiated per head dimension by sa_step.cu (D = 128) and
+// sa_step_d64.cu (D = 64).  The design notes are in sa_step.cu.
+#pragma once
+
+#include "sa_decode_body.cuh"
+#include "sa_select_body.cuh"
+
+namespace sa {
+namespace {
+
+static_assert(kSelThreads == kDecThreads, "both phases run on the same CTA shape");
+
+template <int KIND, int D, int G, bool QSPLIT>
+__global__ void __launch_bounds__(kDecThreads, 1) step_kernel(SelectArgs sa_args, DecodeArgs da, uint32_t* ready)
+{
+    select_body_warps<KIND, KIND == KIND_QUEST, D>(sa_args, ready);
+    __syncthreads();   // select's rings and keys are reused as the decode rings
+    decode_mma_body<D, G, QSPLIT>(da, ready);
+}
+
+template <int KIND, int D, int G, bool QSPLIT>
+cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, uint32_t* ready, int ctas,
+                          cudaStream_t s)
+{
+    constexpr size_t smem = slab_smem_bytes<D>();
+    static_assert(smem >= SlabSelShape<KIND, KIND == KIND_QUEST, D>::RING_BYTES &&
+                      smem >= kMaxSelectKeys * sizeof(uint32_t),
+                  "select rings and keys must fit the decode rings");
+    auto kernel = step_kernel<KIND, D, G, QSPLIT>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDecThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorNotSupported;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(ctas));
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: the decode waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, sa_args, da, ready);
+}
+
+template <int KIND, int D, bool QSPLIT>
+cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, uint32_t* ready, int ctas, int G,
+                            cudaStream_t s)
+{
+    switch (G) {
+        case 1: return launch_step_t<KIND, D, 1, QSPLIT>(sa_args, da, ready, ctas, s);
+        case 2: return launch_step_t<KIND, D, 2, QSPLIT>(sa_args, da, ready, ctas, s);
+        case 4: return launch_step_t<KIND, D, 4, QSPLIT>(sa_args, da, ready, ctas, s);
+        case 8: return launch_step_t<KIND, D, 8, QSPLIT>(sa_args, da, ready, ctas, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// CTAs of the fused grid: one per SM, fewer when there are fewer decode items; 0 when
+// a CTA's item range would overflow its page cache or touch too many units.
+int step_ctas(const Geometry& g, const WorkspaceLayout& L)
+{
+    const long long items = (long long)g.units() * L.max_splits;
+    long long ctas = num_sms();
+    if (ctas > items) ctas = items;
+    if (ctas < 1) return 0;
+    const long long min_ctas = (items * L.blocks_per_split + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
+    const long long min_ctas_units = (g.units() + 61) / 62;
+    if (ctas < min_ctas || ctas < min_ctas_units) return 0;
+    return int(ctas);
+}
+
+template <int D>
+cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
+                             const void* kmin, const void* kmax, const float* kmean,
+                             const int32_t* reserve_ids, const void* k_pages, const void* v_pages,
+                             const int32_t* block_table, int32_t* sel_ids, int32_t* sel_count,
+                             float* out, cudaStream_t s)
+{
+    const int units = g.units();
+    if (units == 0) return cudaSuccess;
+    const int ctas = step_ctas(g, L);
+    if (ctas == 0) return cudaErrorNotSupported;
+    const bool mean = g.score_kind == SPARSE_ATTN_SCORE_MEAN;
+
+    SelectArgs sa_args = select_args_base(g, L, ws, q, kmin, kmax, kmean);
+    set_single_level(sa_args, g, reserve_ids, sel_ids, sel_count);
+    if (mean) set_slab_chunking<KIND_MEAN, false, D>(sa_args, units);
+    else set_slab_chunking<KIND_QUEST, true, D>(sa_args, units);
+    // a CTA records the units it completes in a fixed list: its chunk range may touch
+    // at most kSlabSelMaxUnits units
+    const long long per_cta = ((long long)sa_args.total_chunks + ctas - 1) / ctas;
+    if (per_cta / sa_args.chunks_per_unit + 2 > kSlabSelMaxUnits) return cudaErrorNotSupported;
+    // A CTA runs the top-ks of the units it completes one after another; with more
+    // units than CTAs those queue up, while the select kernel (two CTAs per SM) runs
+    // them side by side: leave such problems to the two-kernel form.
+    if (units > ctas) return cudaErrorNotSupported;
+    DecodeArgs da = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out, nullptr, 0);
+    uint32_t* ready = reinterpret_cast<uint32_t*>(ws + L.ready);
+
+    const bool qs = !g.q_bf16;
+    if (mean)
+        return qs ? dispatch_step_g<KIND_MEAN, D, true>(sa_args, da, ready, ctas, g.G, s)
+                  : dispatch_step_g<KIND_MEAN, D, false>(sa_args, da, ready, ctas, g.G, s);
+    return qs ? dispatch_step_g<KIND_QUEST, D, true>(sa_args, da, ready, ctas, g.G, s)
+              : dispatch_step_g<KIND_QUEST, D, false>(sa_args, da, ready, ctas, g.G, s);
+}
+
+}  // namespace
+}  // namespace sa

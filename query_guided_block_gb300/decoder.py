@@ -80,9 +80,19 @@ class SparseDecoder:
                              self.out if out is None else out, self.ws, stream)
 
     def step(self, q, k_pages, v_pages, block_table, reserve_ids=None, stream=None):
-        """select + decode for one query batch; returns the output tensor."""
+        """select + decode for one query batch (two launches); returns the output tensor."""
         self.select(q, reserve_ids, stream)
         self.decode(q, k_pages, v_pages, block_table, stream=stream)
+        return self.out
+
+    def step_fused(self, q, k_pages, v_pages, block_table, reserve_ids=None, stream=None):
+        """select + decode for one query batch in one launch (sparse_attn_step); the same
+        results as ``step``.  Raises SparseAttnError (unsupported) for two-level
+        selection, fp32 K/V or several queries per sequence."""
+        if self.p.num_reserve > 0 and reserve_ids is None:
+            raise ValueError("this problem has num_reserve > 0: pass reserve_ids")
+        B.sparse_attn_step(self.p, q, self.kmin, self.kmax, self.kmean, reserve_ids, k_pages, v_pages,
+                           block_table, self.sel_ids, self.sel_count, self.out, self.ws, stream)
         return self.out
 
     def device_error(self, stream=None) -> int:
