@@ -84,9 +84,12 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
+_CSRC = "query_guided_block_gb300/csrc/"
 KERNEL_SOURCES = {
-    "select": ["query_guided_block_gb300/csrc/sa_select.cu", "query_guided_block_gb300/csrc/sa_common.cuh"],
-    "decode": ["query_guided_block_gb300/csrc/sa_decode.cu", "query_guided_block_gb300/csrc/sa_common.cuh"],
+    "select": [_CSRC + f for f in ("sa_select.cu", "sa_select_body.cuh", "sa_common.cuh")],
+    "decode": [_CSRC + f for f in ("sa_decode.cu", "sa_decode_body.cuh", "sa_common.cuh")],
+    "step": [_CSRC + f for f in ("sa_step.cu", "sa_step_kernel.cuh", "sa_select_body.cuh", "sa_decode_body.cuh",
+                                 "sa_common.cuh")],
 }
 
 
@@ -280,10 +283,16 @@ def run_gpu_arm(args):
     run_start = ((w.n_tokens - 1) // w.block_size) // run_blocks * run_blocks
     reread = w.batch * w.num_kv_heads * (min(nb_all, run_start + run_blocks) - run_start)
     append_bytes = reread * w.block_size * w.head_dim * esz * (1 + 2 / w.block_size)
-    launches_per_step = (3 if w.two_level else 2) + (1 if cache else 0) + (2 if io else 0)
     step_counter = [0]
 
     reserve = inp.get("reserve_ids")   # random reserve set, drawn with the inputs
+    # The step as a user calls it: sparse_attn_step (one cooperative launch, or select
+    # followed by a decode that waits per unit) where it covers the problem, else the
+    # select and decode calls.
+    step_launches = -1 if (io or args.two_launch) else Bn.sparse_attn_step_launches(p)
+    use_step = step_launches > 0
+    launches_per_step = ((step_launches if use_step else (3 if w.two_level else 2)) + (1 if cache else 0)
+                         + (2 if io else 0))
 
     def io_phase():   # diff, misses in from the host store, slot map
         cache.diff(step_counter[0])
@@ -291,14 +300,19 @@ def run_gpu_arm(args):
         pool.slot_map()
 
     def one_step(q):
-        dec.select(q, reserve)
-        if io:
-            io_phase()
-            pool.decode(q)
-        else:
-            dec.decode(q, kp, vp, bt)
+        if use_step:
+            dec.step_fused(q, kp, vp, bt, reserve)
             if cache:
                 cache.diff(step_counter[0])
+        else:
+            dec.select(q, reserve)
+            if io:
+                io_phase()
+                pool.decode(q)
+            else:
+                dec.decode(q, kp, vp, bt)
+                if cache:
+                    cache.diff(step_counter[0])
         if cache:
             cache.advance()
             step_counter[0] += 1
@@ -322,6 +336,15 @@ def run_gpu_arm(args):
         q = q_all[(args.warmup + i) % q_all.shape[0]] if cache else q_static
         a, b, c, d = ev[i]
         a.record(stream)
+        if use_step:                 # a step b [diff d]: no event between kernels that has no work to time
+            dec.step_fused(q, kp, vp, bt, reserve)
+            b.record(stream)
+            if cache:
+                cache.diff(step_counter[0])
+                d.record(stream)
+                cache.advance()
+                step_counter[0] += 1
+            continue
         dec.select(q, reserve)
         b.record(stream)
         if io:                       # a select b diff + misses + map c decode d
@@ -349,9 +372,25 @@ def run_gpu_arm(args):
     if flags:
         raise RuntimeError(f"device error flags 0x{flags:x}")
 
-    sel_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    dec_ms = [e[2].elapsed_time(e[3]) if io else e[1].elapsed_time(e[2]) for e in ev]
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[3] if (cache or not use_step) else e[1]) for e in ev]
+    if use_step:
+        fused_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        # breakdown: the select and decode calls timed on their own after the timed region
+        bk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(min(K, 100))]
+        for a, b, c in bk:
+            flush.zero_()
+            a.record(stream)
+            dec.select(q_static if not cache else q_all[0], reserve)
+            b.record(stream)
+            dec.decode(q_static if not cache else q_all[0], kp, vp, bt)
+            c.record(stream)
+        torch.cuda.synchronize()
+        sel_ms = [a.elapsed_time(b) for a, b, c in bk]
+        dec_ms = [b.elapsed_time(c) for a, b, c in bk]
+    else:
+        sel_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        dec_ms = [e[2].elapsed_time(e[3]) if io else e[1].elapsed_time(e[2]) for e in ev]
     total_ms_local = sum(step_ms)
     total_ms = aggregate_max(total_ms_local, world, dev)
     queries = w.batch * w.num_q_heads * max(1, w.num_queries)
@@ -374,11 +413,19 @@ def run_gpu_arm(args):
                            "launches_per_step": 3,
                            "note": "diff + miss tiles read from pinned host memory + slot map"}
     elif cache:
-        kern["diff"] = {"ms": statistics.mean([e[2].elapsed_time(e[3]) for e in ev]),
+        kern["diff"] = {"ms": statistics.mean([(e[1] if use_step else e[2]).elapsed_time(e[3]) for e in ev]),
                         "launches_per_step": 1}
-    dominant = "select" if sel_avg >= dec_avg else "decode"
-    dk = kern[dominant]
     step_bytes = nbytes["select"] + nbytes["decode"]
+    if use_step:
+        st_avg = statistics.mean(fused_ms)
+        kern["step"] = {"ms": st_avg, "bytes": step_bytes, "gbs": step_bytes / st_avg / 1e6,
+                        "launches_per_step": step_launches,
+                        "note": "sparse_attn_step: " + ("one cooperative launch (select phase, then decode "
+                                "phase waiting per unit)" if step_launches == 1 else
+                                "select kernel, then decode as its dependent waiting per unit")}
+        kern["select"]["note"] = kern["decode"]["note"] = "separate call, timed after the timed region"
+    dominant = "step" if use_step else ("select" if sel_avg >= dec_avg else "decode")
+    dk = kern[dominant]
     step_gbs = step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9
     traffic = recorded_traffic(dominant, w.name)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak,
@@ -401,6 +448,11 @@ def run_gpu_arm(args):
         q_dev.copy_(q_host, non_blocking=True)
         if reserve is not None:
             res_dev.copy_(res_host, non_blocking=True)
+        if use_step:
+            dec.step_fused(q_dev, kp, vp, bt, res_dev if reserve is not None else None)
+            out_host.copy_(dec.out, non_blocking=True)
+            b.record(stream)
+            continue
         dec.select(q_dev, res_dev if reserve is not None else None)
         if io:
             io_phase()
@@ -442,7 +494,9 @@ def run_gpu_arm(args):
                    "window_tokens": w.window_tokens, "two_level": w.two_level,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed before every step ({flush.numel() >> 20} MB write, outside the step events)",
-                   "timing": "CUDA events per kernel on the launching stream"},
+                   "step": (f"sparse_attn_step ({step_launches} launch{'es' if step_launches > 1 else ''})"
+                            if use_step else "sparse_attn_select + sparse_attn_decode"),
+                   "timing": "CUDA events per call on the launching stream"},
         "hbm_gbs": step_gbs,
         "hbm_frac_of_measured": step_gbs / peak,
         "hbm_frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS,
@@ -582,6 +636,8 @@ def main():
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--two-launch", action="store_true",
+                    help="time the separate select and decode calls instead of sparse_attn_step")
     ap.add_argument("--io", action="store_true",
                     help="LRU workloads: K/V read through the slot pool, misses loaded each step "
                          "from a pinned host store")

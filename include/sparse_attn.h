@@ -228,6 +228,13 @@ int sparse_attn_step(const sparse_attn_params* p, const void* q, const void* kmi
                      const void* v_pages, const int32_t* block_table, int32_t* sel_ids,
                      int32_t* sel_count, float* out, void* ws, size_t ws_bytes, sparse_attn_stream stream);
 
+/* Kernels one sparse_attn_step call launches on the current device: 1 (the single
+ * cooperative launch), 2 (select, then decode as its programmatic dependent waiting per
+ * unit; chosen when there are more (sequence, KV head) units than SMs or a CTA's share
+ * would not fit), 0 (B = 0), or -1 when the problem is invalid or not supported by
+ * sparse_attn_step.  Host-only. */
+int32_t sparse_attn_step_launches(const sparse_attn_params* p);
+
 /* Step-to-step diff and LRU slot cache (SGLang page §3.2: cache 2-4x top-k, LRU
  * eviction; steps a-d: diff against the previous step, find what is resident, load
  * the misses, update the index).  For each unit, with S = sel_ids row (ascending,

@@ -94,6 +94,7 @@ def lib():
             "sparse_attn_select": ([P, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_decode": ([P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_step": ([P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
+            "sparse_attn_step_launches": ([P], C.c_int32),
             "sparse_attn_diff": ([P, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                   vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_get_device_error": ([vp, sz, vp, u32p], C.c_int),
@@ -119,7 +120,7 @@ def exported_symbols():
             "sparse_attn_get_device_error", "sparse_attn_select_noalloc",
             "sparse_attn_select_reserved", "sparse_attn_topk_for_length",
             "sparse_attn_slot_map", "sparse_attn_load_misses", "sparse_attn_decode_slots",
-            "sparse_attn_append_meta", "sparse_attn_step"]
+            "sparse_attn_append_meta", "sparse_attn_step", "sparse_attn_step_launches"]
 
 
 def _status_string(status: int) -> str:
@@ -234,6 +235,12 @@ def sparse_attn_step(p, q, kmin, kmax, kmean, reserve_ids, k_pages, v_pages, blo
         C.byref(p), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(kmean), _ptr(reserve_ids), _ptr(k_pages),
         _ptr(v_pages), _ptr(block_table), _ptr(sel_ids), _ptr(sel_count), _ptr(out), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_step_launches(p) -> int:
+    """Kernels a sparse_attn_step call launches (1 or 2), 0 for an empty batch, -1 when
+    the problem is not supported by sparse_attn_step."""
+    return int(lib().sparse_attn_step_launches(C.byref(p)))
 
 
 def sparse_attn_diff(p, step, sel_ids, sel_count, prev_ids, prev_count, cache_slots, slot_block,

@@ -335,6 +335,13 @@ int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k
                                    sel_ids, sel_count, out, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int32_t sparse_attn_step_launches(const sparse_attn_params* p)
+{
+    Geometry g;
+    if (make_geometry(p, &g) != SPARSE_ATTN_OK || !step_supported(g)) return -1;
+    return step_launches(g, workspace_layout(g));
+}
+
 int sparse_attn_step(const sparse_attn_params* p, const void* q, const void* kmin, const void* kmax,
                      const float* kmean, const int32_t* reserve_ids, const void* k_pages,
                      const void* v_pages, const int32_t* block_table, int32_t* sel_ids,

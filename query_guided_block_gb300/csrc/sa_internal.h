@@ -97,6 +97,7 @@ cudaError_t launch_slot_map(const Geometry& g, const int32_t* sel_ids, const int
 // single-level selection, bf16 K/V, one query per sequence.  cudaErrorNotSupported
 // when the problem does not fit one CTA per SM.
 bool step_supported(const Geometry& g);
+int step_launches(const Geometry& g, const WorkspaceLayout& L);   // kernels one step launches
 cudaError_t launch_step(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                         const void* kmin, const void* kmax, const float* kmean,
                         const int32_t* reserve_ids, const void* k_pages, const void* v_pages,

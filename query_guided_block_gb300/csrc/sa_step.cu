@@ -25,6 +25,13 @@ bool step_supported(const Geometry& g)
     return g.kv_bf16 && !g.two_level && g.Q == 1 && decode_supported(g.D, g.kv_bf16, g.bs, g.G);
 }
 
+int step_launches(const Geometry& g, const WorkspaceLayout& L)
+{
+    if (g.units() == 0) return 0;
+    const int single = g.D == 64 ? step_single_ctas<64>(g, L) : step_single_ctas<128>(g, L);
+    return single > 0 ? 1 : 2;
+}
+
 // Select and decode for one step.  The single cooperative launch when its grid holds
 // the problem (one CTA per SM); otherwise the two kernels, the decode launched behind
 // the select and waiting per unit on the published selections.

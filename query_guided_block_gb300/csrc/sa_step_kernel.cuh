@@ -78,6 +78,25 @@ int step_ctas(const Geometry& g, const WorkspaceLayout& L)
     return int(ctas);
 }
 
+// CTAs of the single-launch step, or 0 when the problem runs as two kernels: the grid
+// must hold every decode range (step_ctas), each CTA may complete at most
+// kSlabSelMaxUnits units, and there must be no more units than CTAs (a CTA runs the
+// top-ks of the units it completes one after another, while the select kernel, two
+// CTAs per SM, runs them side by side).
+template <int D>
+int step_single_ctas(const Geometry& g, const WorkspaceLayout& L)
+{
+    const int units = g.units();
+    const int ctas = step_ctas(g, L);
+    if (ctas == 0 || units > ctas) return 0;
+    const int rows = g.score_kind == SPARSE_ATTN_SCORE_MEAN ? SlabSelShape<KIND_MEAN, false, D>::ROWS
+                                                           : SlabSelShape<KIND_QUEST, true, D>::ROWS;
+    const long long chunks_per_unit = ((g.n_cand > 0 ? g.n_cand : 1) + rows - 1) / rows;
+    const long long per_cta = (units * chunks_per_unit + ctas - 1) / ctas;
+    if (per_cta / chunks_per_unit + 2 > kSlabSelMaxUnits) return 0;
+    return ctas;
+}
+
 template <int D>
 cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                              const void* kmin, const void* kmax, const float* kmean,
@@ -87,7 +106,7 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
 {
     const int units = g.units();
     if (units == 0) return cudaSuccess;
-    const int ctas = step_ctas(g, L);
+    const int ctas = step_single_ctas<D>(g, L);
     if (ctas == 0) return cudaErrorNotSupported;
     const bool mean = g.score_kind == SPARSE_ATTN_SCORE_MEAN;
 
@@ -95,14 +114,6 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
     set_single_level(sa_args, g, reserve_ids, sel_ids, sel_count);
     if (mean) set_slab_chunking<KIND_MEAN, false, D>(sa_args, units);
     else set_slab_chunking<KIND_QUEST, true, D>(sa_args, units);
-    // a CTA records the units it completes in a fixed list: its chunk range may touch
-    // at most kSlabSelMaxUnits units
-    const long long per_cta = ((long long)sa_args.total_chunks + ctas - 1) / ctas;
-    if (per_cta / sa_args.chunks_per_unit + 2 > kSlabSelMaxUnits) return cudaErrorNotSupported;
-    // A CTA runs the top-ks of the units it completes one after another; with more
-    // units than CTAs those queue up, while the select kernel (two CTAs per SM) runs
-    // them side by side: leave such problems to the two-kernel form.
-    if (units > ctas) return cudaErrorNotSupported;
     DecodeArgs da = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out, nullptr, 0);
     uint32_t* ready = reinterpret_cast<uint32_t*>(ws + L.ready);
 

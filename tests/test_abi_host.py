@@ -136,3 +136,18 @@ def test_capacity_workspace_covers_every_length(name):
     big = B.sparse_attn_workspace_size(B.params_for(w, capacity_tokens=cap))
     for n in range(w.n_tokens - 3 * w.block_size, cap + 1):
         assert B.sparse_attn_workspace_size(B.params_for(w, n_tokens=n)) <= big, n
+
+
+def test_step_launch_plan():
+    """sparse_attn_step's plan, decided on the host: one cooperative launch while the
+    units fit one CTA per SM, select + dependent decode beyond that, refused for
+    problems it does not cover."""
+    import dataclasses
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["gqa_128k"])) == 1      # 128 units
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["reserve_128k"])) == 1
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["mha_32k"])) == 2       # 256 units
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["two_level_256k"])) == -1
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["tiny_fp32_4k"])) == -1  # fp32 K/V
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["mq_128k"])) == -1       # Q > 1
+    empty = dataclasses.replace(WORKLOADS["gqa_128k"], batch=0)
+    assert B.sparse_attn_step_launches(B.params_for(empty)) == 0
