@@ -39,7 +39,7 @@ cudaError_t launch_select_t(const SelectArgs& a0, int units, uint32_t* ready, cu
 {
     SelectArgs a = a0;
     set_chunking<KIND, MBF16, D>(a, units);
-    const size_t keys_bytes = size_t(a.n_cand) * sizeof(uint32_t);
+    const size_t keys_bytes = size_t(kSelThreads) * key_tile(a.n_cand) * sizeof(uint32_t);
     // two CTAs per SM when they fit: dynamic stages + keys, plus static (histogram) and
     // the per-CTA reservation
     constexpr size_t kStatic = 13 * 1024;

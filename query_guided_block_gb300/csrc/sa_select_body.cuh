@@ -64,6 +64,14 @@ __device__ __forceinline__ int candidate_row(const SelectArgs& a, int u, int c)
 }
 
 // ------------------------------------------------------------- top-k ----
+// Keys per thread in the top-k passes: thread t owns keys [t * key_tile(n), (t + 1) *
+// key_tile(n)) and reads them four at a time; the key array is zero-padded to
+// kSelThreads * key_tile(n) entries.
+__host__ __device__ constexpr int key_tile(int n)
+{
+    return ((n + kSelThreads * 4 - 1) / (kSelThreads * 4)) * 4;
+}
+
 // Runs in one CTA.  keys[0..n) hold order keys (0 = not a candidate); candidate order
 // is block-id order.  Finds the k-th candidate (T, cT) in (key desc, index asc) order;
 // the selection is then {c : key > T, or key == T and c <= cT}.
@@ -89,6 +97,8 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k_eff = min(a.k, n_valid);
     int32_t* out = a.out_ids + size_t(u) * a.out_stride;
+    const int kpt = key_tile(n);
+    const uint32_t* my_keys = keys + tid * kpt;      // 16-byte aligned: kpt is a multiple of 4
 
     // mode 0: none / all candidates; 1: (key & mask) >= prefix; 2: threshold (T, cT)
     int mode = 0;
@@ -109,10 +119,12 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
 #pragma unroll
             for (int i = 0; i < kBinsPerThread; ++i) hist[tid + i * kSelThreads] = 0u;
             __syncthreads();
-#pragma unroll 4
-            for (int c = tid; c < n; c += kSelThreads) {
-                const uint32_t key = keys[c];
-                if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+            for (int i = 0; i < kpt; i += 4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(my_keys + i);
+                const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (kk[e] != 0u && (kk[e] & mask) == prefix) atomicAdd(&hist[(kk[e] >> shift) & dmask], 1u);
             }
             __syncthreads();
             // thread t owns bins 2047-8t .. 2040-8t (descending); scan from the top
@@ -159,13 +171,16 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
             // gather the boundary candidates and rank them by (key desc, index asc)
             if (tid == 0) s_ng = 0;
             __syncthreads();
-#pragma unroll 4
-            for (int c = tid; c < n; c += kSelThreads) {
-                const uint32_t key = keys[c];
-                if (key != 0u && (key & mask) == prefix) {
-                    const int slot = atomicAdd(&s_ng, 1);
-                    g_key[slot] = key;
-                    g_idx[slot] = c;
+            for (int i = 0; i < kpt; i += 4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(my_keys + i);
+                const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (kk[e] != 0u && (kk[e] & mask) == prefix) {
+                        const int slot = atomicAdd(&s_ng, 1);
+                        g_key[slot] = kk[e];
+                        g_idx[slot] = tid * kpt + i + e;
+                    }
                 }
             }
             __syncthreads();
@@ -259,48 +274,45 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
         if (tid == 0) a.out_count[u] = total + a.win_count;
         return;
     }
-    // Each warp owns a contiguous chunk of candidates, read lane-interleaved, so ballot
-    // order is candidate order.  The count pass loads its keys eight rows at a time and
-    // keeps each row's ballot (in the histogram's storage, free now), so the write pass
-    // reads no key again.
-    const int chunk = ((n + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;
-    const int c0 = warp * chunk, c1 = min(n, c0 + chunk);
-    const int iters = chunk / 32;                      // <= kBins / kSelWarps
-    uint32_t* wmask = hist + warp * (kBins / kSelWarps);
+    // Thread t owns candidates [t * kpt, (t + 1) * kpt): count its selected ones, find
+    // its offset by a scan over the threads (thread order is candidate order), then
+    // write their rows in order.  Each pass reads its keys four at a time.
     int cnt = 0;
-    for (int it0 = 0; it0 < iters; it0 += 8) {
-        uint32_t kv[8];
+    for (int i = 0; i < kpt; i += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(my_keys + i);
+        const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int c = c0 + (it0 + j) * 32 + lane;
-            kv[j] = (it0 + j < iters && c < c1) ? keys[c] : 0u;
-        }
+        for (int e = 0; e < 4; ++e) cnt += selected_key(kk[e], tid * kpt + i + e);
+    }
+    int inc = cnt;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (it0 + j < iters) {
-                const int c = c0 + (it0 + j) * 32 + lane;
-                const uint32_t m = __ballot_sync(kFullMask, c < c1 && selected_key(kv[j], c));
-                if (lane == 0) wmask[it0 + j] = m;
-                cnt += __popc(m);
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(kFullMask, inc, off);
+        if (lane >= off) inc += t;
+    }
+    if (lane == 31) s_wtot[warp] = inc;
+    __syncthreads();
+    int pos = inc - cnt;
+    for (int wv = 0; wv < warp; ++wv) pos += s_wtot[wv];
+    for (int i = 0; i < kpt && cnt > 0; i += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(my_keys + i);
+        const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = tid * kpt + i + e;
+            if (selected_key(kk[e], c)) {
+                out[pos++] = candidate_row(a, u, c);
+                --cnt;
             }
         }
-    }
-    if (lane == 0) s_wtot[warp] = cnt;
-    __syncthreads();
-    int pos = 0;
-    for (int wv = 0; wv < warp; ++wv) pos += s_wtot[wv];
-#pragma unroll 4
-    for (int it = 0; it < iters; ++it) {
-        const uint32_t m = wmask[it];
-        if ((m >> lane) & 1u) out[pos + __popc(m & lanemask_lt())] = candidate_row(a, u, c0 + it * 32 + lane);
-        pos += __popc(m);
     }
     for (int i = tid; i < a.win_count; i += kSelThreads) out[k_eff + i] = a.win_first + i;
     if (tid == 0) a.out_count[u] = k_eff + a.win_count;
 }
 
 // Unit u's scores -> order keys in shared memory (0 for slots that are not
-// candidates); returns the number of candidates and the smallest and largest key.  Loads are issued in batches of
+// candidates, and for the padding up to kSelThreads * key_tile(n_cand) entries);
+// returns the number of candidates and the smallest and largest key.  Loads are issued in batches of
 // independent requests so the L2 latency is paid once per batch, not per element.
 __device__ int load_keys(const SelectArgs& a, int u, uint32_t* keys, uint32_t& key_lo, uint32_t& key_hi)
 {
@@ -337,6 +349,7 @@ __device__ int load_keys(const SelectArgs& a, int u, uint32_t* keys, uint32_t& k
             mine += ok[i];
         }
     }
+    for (int c = a.n_cand + threadIdx.x; c < kSelThreads * key_tile(a.n_cand); c += kSelThreads) keys[c] = 0u;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         mine += __shfl_xor_sync(kFullMask, mine, off);
