@@ -75,6 +75,220 @@ cudaError_t dispatch_select(const SelectArgs& a, int kind, bool mbf16, int D, in
                  : launch_select_t<KIND_QUEST, false, 64>(a, units, ready, s);
 }
 
+// ------------------------------------------------------ two-level, per unit ---
+// Both levels of one (sequence, KV head) unit in one CTA (HiSparse->QSA page §2.2 and
+// §3.1: coarse-block mean scores, top K1 coarse blocks, Quest bound over their slices,
+// top K2 slices plus the window).  A unit's two levels are a short dependent chain over
+// little data (the 256K workload reads 128 KB of means and 384 KB of slice bounds per
+// unit), so one CTA per unit runs the chain without any cross-CTA hand-off: the
+// scores go straight into shared-memory keys (no score row in global memory), and the
+// rows are read with 16-byte loads, kRowsInFlight rows per lane group in flight.  The
+// per-row arithmetic (each lane's fma chain over its channels, then the same xor
+// butterfly over the row's lanes) and the query-coefficient sums are those of the
+// streaming select kernel, so the scores are the same bits.
+constexpr int kRowsInFlight = 8;
+
+// Score `nrows` candidate rows into keys[0, nrows): row_of(c) gives the metadata row of
+// candidate c or -1.  Returns (via shared memory, after a barrier) the valid count and
+// the key range.
+template <int KIND, bool MBF16, int D, typename RowOf>
+__device__ __forceinline__ int score_rows_to_keys(const SelectArgs& a, int u, uint32_t* keys, int nrows,
+                                                  const float (&cp)[SelectShape<KIND, MBF16, D>::EPL],
+                                                  const float (&cn)[SelectShape<KIND, MBF16, D>::EPL],
+                                                  RowOf row_of, uint32_t& key_lo, uint32_t& key_hi)
+{
+    using SS = SelectShape<KIND, MBF16, D>;
+    constexpr int EPL = SS::EPL, LPR = SS::LPR, RPW = SS::RPW, R = kRowsInFlight;
+    constexpr int ROWS_PER_WARP = RPW * R;
+    __shared__ int s_count;
+    __shared__ uint32_t s_lo, s_hi;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sub = lane % LPR, rsub = lane / LPR;
+    if (tid == 0) {
+        s_count = 0;
+        s_lo = 0xffffffffu;
+        s_hi = 0u;
+    }
+    __syncthreads();
+    const char* hi_src = reinterpret_cast<const char*>(KIND == KIND_QUEST ? a.kmax : (const void*)a.kmean);
+    const char* lo_src = reinterpret_cast<const char*>(a.kmin);
+    const size_t unit_off = size_t(u) * a.row_stride;
+    int mine = 0;
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int base = warp * ROWS_PER_WARP; base < nrows; base += kSelWarps * ROWS_PER_WARP) {
+        int row[R];
+        uint4 vh[R], vl[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int c = base + rsub * R + r;
+            row[r] = c < nrows ? row_of(c) : -1;
+            if (row[r] >= 0) {
+                const size_t off = (unit_off + row[r]) * SS::ROW_BYTES + sub * 16;
+                vh[r] = ld_stream16(hi_src + off);
+                if constexpr (KIND == KIND_QUEST) vl[r] = ld_stream16(lo_src + off);
+            }
+        }
+        float part[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float acc = 0.f;
+            if (row[r] >= 0) {
+                float fh[EPL];
+                unpack16<SS::ESZ == 2>(vh[r], fh);
+                if constexpr (KIND == KIND_QUEST) {
+                    float fl[EPL];
+                    unpack16<SS::ESZ == 2>(vl[r], fl);
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], fmaf(cn[e], fl[e], acc));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], acc);
+                }
+            }
+            part[r] = acc;
+        }
+        group_reduce_transposed<R, LPR>(part, lane);
+        constexpr int OUT = R >= LPR ? R / LPR : 1;
+        constexpr int SPREAD = R >= LPR ? 1 : LPR / R;
+        if (sub % SPREAD == 0) {
+#pragma unroll
+            for (int i = 0; i < OUT; ++i) {
+                const int r = R >= LPR ? sub * (R / LPR) + i : sub / SPREAD;
+                const int c = base + rsub * R + r;
+                if (c < nrows) {
+                    const bool ok = row_of(c) >= 0;
+                    const uint32_t key = order_key(part[i]);
+                    keys[c] = ok ? key : 0u;
+                    if (ok) {
+                        lo = min(lo, key);
+                        hi = max(hi, key);
+                        ++mine;
+                    }
+                }
+            }
+        }
+    }
+    for (int c = nrows + tid; c < kSelThreads * key_tile(nrows); c += kSelThreads) keys[c] = 0u;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        mine += __shfl_xor_sync(kFullMask, mine, off);
+        lo = min(lo, __shfl_xor_sync(kFullMask, lo, off));
+        hi = max(hi, __shfl_xor_sync(kFullMask, hi, off));
+    }
+    if (lane == 0) {
+        atomicAdd(&s_count, mine);
+        atomicMin(&s_lo, lo);
+        atomicMax(&s_hi, hi);
+    }
+    __syncthreads();
+    key_lo = s_lo;
+    key_hi = s_hi;
+    return s_count;
+}
+
+// Query coefficients of unit u in the streaming kernel's order: thread t sums channel
+// t mod D over rows t / D, t / D + 256 / D, ... (quest: max(q, 0) and min(q, 0); mean: q),
+// the partials go through shared memory and each lane adds its channels' partials.
+template <int KIND, int EPL, int D>
+__device__ __forceinline__ void unit_coefficients(const SelectArgs& a, int u, int d0, float (&cp)[EPL],
+                                                  float (&cn)[EPL])
+{
+    constexpr int RSTEP = kSelThreads / D;
+    __shared__ float s_part[2][kSelThreads];
+    const int tid = threadIdx.x;
+    const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+    const int dch = tid % D;
+    const int rows = a.Q * a.G;
+    float pp = 0.f, nn = 0.f;
+    for (int r = tid / D; r < rows; r += RSTEP) {
+        const int t = r / a.G, g = r - t * a.G;
+        const float x = load_q(a.q, ((size_t(b) * a.Q + t) * a.Hq + size_t(kvh) * a.G + g) * D + dch, a.q_bf16 != 0);
+        if constexpr (KIND == KIND_QUEST) {
+            pp += fmaxf(x, 0.f);
+            nn += fminf(x, 0.f);
+        } else {
+            pp += x;
+        }
+    }
+    __syncthreads();   // a previous call's partials have been read
+    s_part[0][tid] = pp;
+    s_part[1][tid] = nn;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        float sp = 0.f, sn = 0.f;
+#pragma unroll
+        for (int k2 = 0; k2 < RSTEP; ++k2) {
+            sp += s_part[0][d0 + e + k2 * D];
+            sn += s_part[1][d0 + e + k2 * D];
+        }
+        cp[e] = sp;
+        cn[e] = sn;
+    }
+}
+
+template <bool MBF16, int D>
+__global__ void __launch_bounds__(kSelThreads) select_two_level_kernel(SelectArgs l1, SelectArgs l2)
+{
+    using S1 = SelectShape<KIND_MEAN, false, D>;
+    using S2 = SelectShape<KIND_QUEST, MBF16, D>;
+    extern __shared__ __align__(16) uint32_t keys[];
+    __shared__ int s_surv[kSelThreads];
+    __shared__ int s_nsurv;
+    const int u = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+    allow_dependents_early();
+
+    // ---- level 1: mean score of every coarse block, top K1 ----
+    {
+        float cp[S1::EPL], cn[S1::EPL];
+        unit_coefficients<KIND_MEAN, S1::EPL, D>(l1, u, (lane % S1::LPR) * S1::EPL, cp, cn);
+        uint32_t klo, khi;
+        const int n_valid = score_rows_to_keys<KIND_MEAN, false, D>(
+            l1, u, keys, l1.n_cand, cp, cn, [&](int c) { return c < l1.row_limit ? c : -1; }, klo, khi);
+        topk_and_emit(l1, u, keys, l1.n_cand, n_valid, klo, khi);
+    }
+    __syncthreads();   // survivors written (global, this CTA)
+    if (threadIdx.x == 0) s_nsurv = min(l1.out_count[u], l2.groups);
+    for (int i = threadIdx.x; i < l2.groups; i += kSelThreads)
+        s_surv[i] = l1.out_ids[size_t(u) * l1.out_stride + i];
+    __syncthreads();
+
+    // ---- level 2: Quest bound over the survivors' slices, top K2 plus the window ----
+    {
+        float cp[S2::EPL], cn[S2::EPL];
+        unit_coefficients<KIND_QUEST, S2::EPL, D>(l2, u, (lane % S2::LPR) * S2::EPL, cp, cn);
+        const int nsurv = s_nsurv, per = l2.per_coarse, limit = l2.row_limit;
+        auto row_of = [&](int c) -> int {
+            const int i = c / per;
+            if (i >= nsurv) return -1;
+            const int row = s_surv[i] * per + (c - i * per);
+            return row < limit ? row : -1;
+        };
+        uint32_t klo, khi;
+        const int n_valid = score_rows_to_keys<KIND_QUEST, MBF16, D>(l2, u, keys, l2.n_cand, cp, cn, row_of, klo, khi);
+        topk_and_emit(l2, u, keys, l2.n_cand, n_valid, klo, khi);
+    }
+}
+
+template <bool MBF16, int D>
+cudaError_t launch_two_level_t(const SelectArgs& l1, const SelectArgs& l2, int units, cudaStream_t s)
+{
+    const int n = l1.n_cand > l2.n_cand ? l1.n_cand : l2.n_cand;
+    const size_t smem = size_t(kSelThreads) * key_tile(n) * sizeof(uint32_t);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(select_two_level_kernel<MBF16, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(kMaxSelectKeys * sizeof(uint32_t)));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_after_previous(select_two_level_kernel<MBF16, D>, dim3(unsigned(units)), dim3(kSelThreads), smem,
+                                 s, l1, l2);
+}
+
 }  // namespace
 
 cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
@@ -112,8 +326,6 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     l1.out_count = n_surv;
     l1.counters = reinterpret_cast<uint32_t*>(ws + L.l1_counters);
     if (l1.n_cand == 0) { l1.n_cand = 1; l1.group_rows = 1; l1.row_limit = 0; }
-    cudaError_t e = dispatch_select(l1, KIND_MEAN, false, g.D, units, s);
-    if (e != cudaSuccess) return e;
 
     // ---- level 2: Quest bound over the survivors' slices, plus the window ----
     SelectArgs l2 = a;
@@ -139,6 +351,16 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
     if (l2.n_cand == 0) {
         l2.groups = 1; l2.group_rows = 1; l2.n_cand = 1; l2.row_limit = 0; l2.via_survivors = 0;
     }
+    if (l2.groups <= kSelThreads) {   // both levels of a unit in one CTA
+        if (g.D == 128)
+            return g.kv_bf16 ? launch_two_level_t<true, 128>(l1, l2, units, s)
+                             : launch_two_level_t<false, 128>(l1, l2, units, s);
+        return g.kv_bf16 ? launch_two_level_t<true, 64>(l1, l2, units, s)
+                         : launch_two_level_t<false, 64>(l1, l2, units, s);
+    }
+    // more survivors than a CTA holds: the streaming kernel, one launch per level
+    cudaError_t e = dispatch_select(l1, KIND_MEAN, false, g.D, units, s);
+    if (e != cudaSuccess) return e;
     return dispatch_select(l2, KIND_QUEST, g.kv_bf16, g.D, units, s);
 }
 
