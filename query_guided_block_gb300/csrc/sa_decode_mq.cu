@@ -19,6 +19,7 @@
 //     the splits (log-sum-exp).  One split writes the output directly.
 #include "sa_common.cuh"
 #include "sa_internal.h"
+#include "sa_tcgen05.cuh"
 
 namespace sa {
 namespace {
@@ -55,6 +56,66 @@ struct MqArgs {
 __device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk)
 {
     return half_base + uint32_t(token) * kRowB + uint32_t((chunk ^ (token & 7)) << 4);
+}
+
+// The CTA completing a (unit, row tile) merges its splits' (m, l, o) into the output:
+// weights per (row, split) once into shared memory, then each output reads its splits'
+// partials, eight outputs at a time.
+template <int D>
+__device__ void mq_merge(const MqArgs& a, int u, int rt)
+{
+    const int tid = threadIdx.x;
+    const int b = u / a.Hkv, kvh = u - b * a.Hkv;
+    auto head_of = [&](int r) -> size_t {   // q / out row of unit row r
+        const int t = r / a.G, g = r - (r / a.G) * a.G;
+        return (size_t(b) * a.Q + t) * a.Hq + size_t(kvh) * a.G + g;
+    };
+    __shared__ float s_w[kMqRows][kMqMaxSplits], s_den[kMqRows];
+    const int rows = min(kMqRows, a.R - rt * kMqRows);
+    for (int rr = tid; rr < rows; rr += kMqThreads) {
+        const size_t pr0 = (size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < a.nsplit; ++s2) M = fmaxf(M, __ldcg(a.part_m + pr0 + s2));
+        float den = 0.f;
+        for (int s2 = 0; s2 < a.nsplit; ++s2) {
+            const float ms = __ldcg(a.part_m + pr0 + s2);
+            const float w = (ms == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(ms - M);
+            s_w[rr][s2] = w;
+            den = fmaf(w, __ldcg(a.part_l + pr0 + s2), den);
+        }
+        s_den[rr] = den;
+    }
+    __syncthreads();
+    const int n_out = rows * D;
+    for (int i0 = tid; i0 < n_out; i0 += kMqThreads * 8) {
+        float num[8];
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) num[k2] = 0.f;
+        for (int s2 = 0; s2 < a.nsplit; ++s2) {
+            float v[8];
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                const int i = i0 + k2 * kMqThreads;
+                const int rr = i / D, d = i - (i / D) * D;
+                v[k2] = (i < n_out && s_w[min(rr, kMqRows - 1)][s2] > 0.f)
+                            ? __ldcg(a.part_o + ((size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits + s2) * D + d)
+                            : 0.f;
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                const int i = i0 + k2 * kMqThreads;
+                if (i < n_out) num[k2] = fmaf(s_w[i / D][s2], v[k2], num[k2]);
+            }
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) {
+            const int i = i0 + k2 * kMqThreads;
+            if (i >= n_out) continue;
+            const int rr = i / D, d = i - (i / D) * D;
+            const float den = s_den[rr];
+            a.out[head_of(rt * kMqRows + rr) * D + d] = den > 0.f ? num[k2] / den : 0.f;
+        }
+    }
 }
 
 template <int D, bool QSPLIT>
@@ -321,54 +382,371 @@ __global__ void __launch_bounds__(kMqThreads, 2) decode_mq_kernel(MqArgs a)
     }
     __syncthreads();
     if (!s_merge) return;
-    // merge the splits of this (unit, row tile): weights per (row, split) once into
-    // shared memory, then each output reads its splits' partials, eight outputs at a time
-    __shared__ float s_w[kMqRows][kMqMaxSplits], s_den[kMqRows];
-    const int rows = min(kMqRows, a.R - rt * kMqRows);
-    for (int rr = tid; rr < rows; rr += kMqThreads) {
-        const size_t pr0 = (size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits;
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < a.nsplit; ++s2) M = fmaxf(M, __ldcg(a.part_m + pr0 + s2));
-        float den = 0.f;
-        for (int s2 = 0; s2 < a.nsplit; ++s2) {
-            const float ms = __ldcg(a.part_m + pr0 + s2);
-            const float w = (ms == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(ms - M);
-            s_w[rr][s2] = w;
-            den = fmaf(w, __ldcg(a.part_l + pr0 + s2), den);
+    mq_merge<D>(a, u, rt);
+}
+
+// ------------------------------------------------------------------ tcgen05 ---
+// The same attention on the fifth-generation tensor cores (bf16 queries).  One
+// warpgroup per CTA; per 64-token tile k of the split:
+//   S(k) = Q K^T  one thread issues tcgen05.mma (M = 128, N = 64, K = D) from shared
+//                 memory into tensor memory (two S buffers): A = the 64 query rows (rows
+//                 64..127 zero), B = the K tile, both K-major with the 128-byte swizzle
+//                 the staging ring already writes;
+//   softmax       warps 0-1 read their row of S from tensor memory (thread = row) and
+//                 apply the online softmax with a lazy reference: the row maximum used
+//                 for exp2 moves (and O is rescaled in tensor memory) only when the
+//                 running maximum grows by more than kLazy, so P <= 2^kLazy; P goes to
+//                 shared memory as bf16 hi and its remainder lo (two A tiles);
+//   O += P V      tcgen05.mma (M = 128, N = D, K = 64) for hi and for lo, B = the V tile
+//                 read MN-major.
+// Issue order per tile: S(k + 2), then O += P(k) V(k): S runs two tiles ahead (three S
+// buffers, one mbarrier each, so no barrier can complete twice before it is waited
+// on), and the softmax of a tile never waits for its own Q K^T.  Each group completes
+// on an mbarrier (tcgen05.commit), every wait on it is bounded, and the CTA meets once
+// per tile.  Warps 2-3 compute each tile's token-validity mask two tiles ahead.
+constexpr float kLazy = 8.f;   // log2 growth of the row maximum before O is rescaled
+
+template <int D>
+struct MqTcShape {
+    static constexpr int T = 64;                            // tokens per tile
+    static constexpr int HALVES = D / 64;
+    static constexpr int KV_HALF = T * kRowB;               // 8 KB: 64 tokens x 128 B
+    static constexpr int KV_TENSOR = HALVES * KV_HALF;
+    static constexpr int STAGE_BYTES = 2 * KV_TENSOR;       // K then V
+    static constexpr int STAGES = 4;
+    static constexpr int Q_HALF = 128 * kRowB;              // 128 rows x 128 B
+    static constexpr int Q_BYTES = HALVES * Q_HALF;
+    static constexpr int P_BYTES = 128 * kRowB;             // 128 rows x 64 tokens bf16
+    static constexpr int OFF_Q = 0, OFF_PH = Q_BYTES, OFF_PL = OFF_PH + P_BYTES;
+    static constexpr int OFF_KV = OFF_PL + P_BYTES;
+    static constexpr int OFF_BLK = OFF_KV + STAGES * STAGE_BYTES;
+    static constexpr size_t SMEM = 1024 + size_t(OFF_BLK) + size_t(2) * kMqMaxBlocks * sizeof(int);
+};
+
+template <int D>
+__global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
+{
+    using SH = MqTcShape<D>;
+    constexpr int T = SH::T, STAGES = SH::STAGES;
+    constexpr int CPR = D / 8;                              // 16-byte chunks per token row
+    constexpr int CP_PER_THREAD = T * CPR / kMqThreads;
+    constexpr uint32_t S_COL = 0, O_COL = 256, TMEM_COLS = 512;   // S buffers at 0, 64, 128
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, T, false);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
+    static_assert(O_COL + D <= TMEM_COLS, "S and O must fit the allocation");
+    static_assert(T * CPR % kMqThreads == 0, "tile copy must split over the threads");
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sp = blockIdx.x % a.nsplit;
+    const int rt = (blockIdx.x / a.nsplit) % a.row_tiles;
+    const int u = blockIdx.x / (a.nsplit * a.row_tiles);
+    const int b = u / a.Hkv, kvh = u - b * a.Hkv;
+    const int bs_shift = __ffs(a.bs) - 1;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;           // swizzle atoms: 1024-byte aligned
+    unsigned char* smem = smem_raw + (base - raw);
+    int* blk_page = reinterpret_cast<int*>(smem + SH::OFF_BLK);
+    int* blk_valid = blk_page + kMqMaxBlocks;
+    __shared__ __align__(8) uint64_t bar_s[3], bar_o;
+    __shared__ uint32_t s_tmem;
+    __shared__ uint32_t s_mask[3][2];                        // valid tokens of a tile (64 bits)
+    __shared__ int s_merge;
+
+    allow_dependents_early();
+    grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar_s[0], 1);
+        mbar_init(&bar_s[1], 1);
+        mbar_init(&bar_s[2], 1);
+        mbar_init(&bar_o, 1);
+        fence_mbar_init();
+    }
+
+    // ---- the split's tiles and the blocks they touch --------------------------
+    int count = a.sel_count[u];
+    if (count < 0 || count > a.sel_stride) {
+        if (tid == 0) raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
+        count = count < 0 ? 0 : a.sel_stride;
+    }
+    const int ntok = count * a.bs;
+    const int tiles = (ntok + T - 1) / T;
+    const int t0 = int((long long)tiles * sp / a.nsplit), t1 = int((long long)tiles * (sp + 1) / a.nsplit);
+    const int blk0 = (t0 * T) >> bs_shift;
+    const int blk1 = min(count, ((t1 * T - 1) >> bs_shift) + 1);
+    const int nblk = t1 > t0 ? blk1 - blk0 : 0;
+    for (int e = tid; e < nblk; e += kMqThreads) {
+        const int slot = blk0 + e;
+        int page = -1, valid = 0;
+        const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
+        if (j < 0 || j >= a.nb) {
+            raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
+        } else {
+            const int p = a.block_table[size_t(b) * a.bt_stride + j];
+            if (p < 0 || p >= a.num_pages) {
+                raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
+            } else {
+                page = p;
+                valid = min(a.bs, a.N - j * a.bs);
+            }
         }
-        s_den[rr] = den;
+        if (e < kMqMaxBlocks) {
+            blk_page[e] = page;
+            blk_valid[e] = valid;
+        }
+    }
+
+    // ---- query rows 0..63 of the tile (zero past R), zero rows 64..127 of Q and P ----
+    auto head_of = [&](int r) -> size_t {   // q / out row of unit row r
+        const int t = r / a.G, g = r - (r / a.G) * a.G;
+        return (size_t(b) * a.Q + t) * a.Hq + size_t(kvh) * a.G + g;
+    };
+    for (int i = tid; i < 128 * CPR; i += kMqThreads) {
+        const int row = i / CPR, c = i - (i / CPR) * CPR;
+        const int r = rt * kMqRows + row;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < 64 && r < a.R)
+            v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + head_of(r) * D) + c);
+        *reinterpret_cast<uint4*>(smem + SH::OFF_Q + (c >> 3) * SH::Q_HALF + row * kRowB + (((c & 7) ^ (row & 7)) << 4)) = v;
+    }
+    for (int i = tid; i < 64 * 8; i += kMqThreads) {   // rows 64..127 of both P tiles
+        const int off = (64 + i / 8) * kRowB + (i % 8) * 16;
+        *reinterpret_cast<uint4*>(smem + SH::OFF_PH + off) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + SH::OFF_PL + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();   // page lookups ready
+
+    // ---- staging ring: thread copies chunk cp_c of tile rows cp_r + i * (128 / CPR) ----
+    const char* kbase = reinterpret_cast<const char*>(a.k_pages);
+    const char* vbase = reinterpret_cast<const char*>(a.v_pages);
+    const int cp_c = tid % CPR, cp_r = tid / CPR;
+    constexpr int ROWS_PER_PASS = kMqThreads / CPR;
+    auto token_ok = [&](int gi) -> bool {
+        const int e = (gi >> bs_shift) - blk0, r = gi & (a.bs - 1);
+        return gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && r < blk_valid[max(0, min(e, kMqMaxBlocks - 1))];
+    };
+    auto issue_tile = [&](int tile, int st) {
+        const uint32_t kd = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES + uint32_t(cp_c >> 3) * SH::KV_HALF;
+        const uint32_t vd = kd + SH::KV_TENSOR;
+#pragma unroll
+        for (int i = 0; i < CP_PER_THREAD; ++i) {
+            const int tr = cp_r + i * ROWS_PER_PASS;
+            const int gi = tile * T + tr;
+            const bool ok = token_ok(gi);
+            const int e = ok ? (gi >> bs_shift) - blk0 : 0, r = gi & (a.bs - 1);
+            const size_t off = ok ? ((size_t(blk_page[e]) * a.Hkv * a.bs + size_t(kvh) * a.bs + r) * (D * 2) + cp_c * 16) : 0;
+            const uint32_t so = uint32_t(tr) * kRowB + uint32_t(((cp_c & 7) ^ (tr & 7)) << 4);
+            cp_async_16_zfill(kd + so, kbase + off, ok ? 16u : 0u);
+            cp_async_16_zfill(vd + so, vbase + off, ok ? 16u : 0u);
+        }
+    };
+    // warps 2-3: 64-bit validity mask of a tile (one token per thread)
+    auto write_mask = [&](int tile) {
+        if (warp >= 2) {
+            const uint32_t m = __ballot_sync(kFullMask, token_ok(tile * T + (warp - 2) * 32 + lane));
+            if (lane == 0) s_mask[(tile - t0) % 3][warp - 2] = m;
+        }
+    };
+    auto issue_s = [&](int tile, int st) {   // S(tile) = Q K^T into S buffer (tile - t0) mod 3
+        const uint32_t kst = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = uint32_t(ks & 3) * 32;
+            const uint64_t ad = smem_desc_sw128(base + SH::OFF_Q + uint32_t(ks >> 2) * SH::Q_HALF + off, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kst + uint32_t(ks >> 2) * SH::KV_HALF + off, 16, 1024);
+            umma_bf16(s_tmem + S_COL + uint32_t((tile - t0) % 3) * T, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar_s[(tile - t0) % 3]);
+    };
+    auto issue_o = [&](int k, int st) {      // O += P(k) V(k): hi then lo
+        const uint32_t vst = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES + SH::KV_TENSOR;
+#pragma unroll
+        for (int kk = 0; kk < T / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(vst + uint32_t(kk) * 16 * kRowB, SH::KV_HALF, 1024);
+            const uint64_t ah = smem_desc_sw128(base + SH::OFF_PH + uint32_t(kk) * 32, 16, 1024);
+            const uint64_t al = smem_desc_sw128(base + SH::OFF_PL + uint32_t(kk) * 32, 16, 1024);
+            umma_bf16(s_tmem + O_COL, ah, bd, IDESC_O, (k > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(s_tmem + O_COL, al, bd, IDESC_O, 1u);
+        }
+        umma_commit(&bar_o);
+    };
+
+    const int ntiles = t1 - t0;
+#pragma unroll
+    for (int kk = 0; kk < STAGES - 1; ++kk) {
+        if (kk < ntiles) issue_tile(t0 + kk, kk);
+        cp_async_commit();
+    }
+    if (ntiles > 0) write_mask(t0);
+    if (ntiles > 1) write_mask(t0 + 1);
+    cp_async_wait_group<STAGES - 3>();   // tiles 0 and 1 of this thread
+    fence_proxy_async_smem();            // Q, P zeros and tiles 0, 1, before the tensor core
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    const uint32_t lane_base = uint32_t(32 * warp) << 16;   // this warp's tensor-memory lanes
+    const int row = 32 * warp + lane;                      // warps 0-1: the tile's query row
+    if (tid == 0 && ntiles > 0) issue_s(t0, 0);
+    if (tid == 0 && ntiles > 1) issue_s(t0 + 1, 1);
+
+    float m_ref = -INFINITY, l_run = 0.f;                  // reference maximum, row sum
+    for (int k = 0; k < ntiles; ++k) {
+        const int tile = t0 + k;
+        float x[64];
+        bool rescale = false;
+        float alpha = 1.f, m_new = m_ref;
+        if (warp < 2) {   // S(k): scale, mask, row maximum
+            if (!mbar_wait_bounded(&bar_s[k % 3], uint32_t(k / 3) & 1u, kWaitCycles))
+                raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+            tc_fence_after_sync();
+            uint32_t sv[2][32];
+            tmem_ld32(tmem + lane_base + S_COL + uint32_t(k % 3) * T, sv[0]);
+            tmem_ld32(tmem + lane_base + S_COL + uint32_t(k % 3) * T + 32, sv[1]);
+            tmem_wait_ld();
+            const uint32_t mk0 = s_mask[k % 3][0], mk1 = s_mask[k % 3][1];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const bool ok = ((j < 32 ? mk0 : mk1) >> (j & 31)) & 1u;
+                x[j] = ok ? __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[j]);
+            }
+            if (mx > m_ref + kLazy || (m_ref == -INFINITY && mx != -INFINITY)) {
+                m_new = mx;
+                alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mx);
+                rescale = true;
+            }
+        }
+        // O += P(k - 1) V(k - 1) is done: P, O and its stage are free
+        if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, kWaitCycles))
+            raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+        if (k + STAGES - 1 < ntiles) issue_tile(tile + STAGES - 1, (k + STAGES - 1) % STAGES);
+        cp_async_commit();
+        if (k + 2 < ntiles) write_mask(tile + 2);
+        if (warp < 2) {
+            tc_fence_after_sync();
+            if (k > 0 && __any_sync(kFullMask, rescale)) {   // O rows of this warp (lazy)
+                const float al = rescale ? alpha : 1.f;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tmem + lane_base + O_COL + c0, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
+                    tmem_st32(tmem + lane_base + O_COL + c0, ov);
+                }
+                tmem_wait_st();
+            }
+            if (rescale) {
+                l_run *= alpha;
+                m_ref = m_new;
+            }
+            float psum = 0.f;
+            unsigned char* ph = smem + SH::OFF_PH + row * kRowB;
+            unsigned char* pl = smem + SH::OFF_PL + row * kRowB;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const int j = c * 8 + 2 * e2;
+                    const float p0 = x[j] == -INFINITY ? 0.f : fast_exp2(x[j] - m_ref);
+                    const float p1 = x[j + 1] == -INFINITY ? 0.f : fast_exp2(x[j + 1] - m_ref);
+                    psum += p0 + p1;
+                    hw[e2] = pack_bf16x2(p0, p1);
+                    lw[e2] = pack_bf16x2(p0 - bf16_lo(hw[e2]), p1 - bf16_hi(hw[e2]));
+                }
+                const int slot = (c ^ (row & 7)) << 4;
+                *reinterpret_cast<uint4*>(ph + slot) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(pl + slot) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            l_run += psum;
+        }
+        cp_async_wait_group<STAGES - 3>();   // tile k + 2 of this thread
+        fence_proxy_async_smem();            // P(k) and tile k + 2, before the tensor core
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        if (tid == 0) {
+            if (k + 2 < ntiles) issue_s(tile + 2, (k + 2) % STAGES);
+            issue_o(k, k % STAGES);
+        }
+    }
+    cp_async_wait_group<0>();
+    if (ntiles > 0 && !mbar_wait_bounded(&bar_o, uint32_t(ntiles - 1) & 1u, kWaitCycles))
+        raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+    tc_fence_after_sync();
+
+    // ---- epilogue: rows 0..63 (warps 0-1) ----
+    const int r_unit = rt * kMqRows + row;
+    if (warp < 2) {
+        const bool have = r_unit < a.R;
+        float* dst = nullptr;
+        float inv = 1.f;
+        if (have) {
+            if (a.nsplit == 1) {
+                dst = a.out + head_of(r_unit) * D;
+                inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            } else {
+                const size_t pr = (size_t(u) * a.R + r_unit) * a.max_splits + sp;
+                dst = a.part_o + pr * D;
+                a.part_m[pr] = m_ref;
+                a.part_l[pr] = l_run;
+            }
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ov[32];
+            if (ntiles > 0) {
+                tmem_ld32(tmem + lane_base + O_COL + c0, ov);
+                tmem_wait_ld();
+            }
+            if (have) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float o4[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) o4[e2] = ntiles > 0 ? __uint_as_float(ov[j + e2]) * inv : 0.f;
+                    *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    if (a.nsplit == 1) return;
+    if (tid == 0) {
+        const uint32_t before = atomic_add_acq_rel_u32(&a.counters[size_t(u) * a.row_tiles + rt], 1u);
+        s_merge = before + 1 == uint32_t(a.nsplit);
+        if (s_merge) a.counters[size_t(u) * a.row_tiles + rt] = 0u;
     }
     __syncthreads();
-    const int n_out = rows * D;
-    for (int i0 = tid; i0 < n_out; i0 += kMqThreads * 8) {
-        float num[8];
-#pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) num[k2] = 0.f;
-        for (int s2 = 0; s2 < a.nsplit; ++s2) {
-            float v[8];
-#pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-                const int i = i0 + k2 * kMqThreads;
-                const int rr = i / D, d = i - (i / D) * D;
-                v[k2] = (i < n_out && s_w[min(rr, kMqRows - 1)][s2] > 0.f)
-                            ? __ldcg(a.part_o + ((size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits + s2) * D + d)
-                            : 0.f;
-            }
-#pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-                const int i = i0 + k2 * kMqThreads;
-                if (i < n_out) num[k2] = fmaf(s_w[i / D][s2], v[k2], num[k2]);
-            }
-        }
-#pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) {
-            const int i = i0 + k2 * kMqThreads;
-            if (i >= n_out) continue;
-            const int rr = i / D, d = i - (i / D) * D;
-            const float den = s_den[rr];
-            a.out[head_of(rt * kMqRows + rr) * D + d] = den > 0.f ? num[k2] / den : 0.f;
-        }
+    if (!s_merge) return;
+    mq_merge<D>(a, u, rt);
+}
+
+template <int D>
+cudaError_t launch_mq_tc_t(const MqArgs& a, int units, cudaStream_t s)
+{
+    const size_t smem = MqTcShape<D>::SMEM;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
     }
+    const unsigned grid = unsigned(size_t(units) * a.row_tiles * a.nsplit);
+    return launch_after_previous(decode_mq_tc_kernel<D>, dim3(grid), dim3(kMqThreads), smem, s, a);
 }
 
 template <int D, bool QSPLIT>
@@ -423,7 +801,10 @@ cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* 
     // split's blocks to fit the page cache, at most the workspace's partial slots
     const int tiles = (g.sel_stride * g.bs + kMqTile - 1) / kMqTile;
     const long long cells = (long long)units * a.row_tiles;
-    long long ns = (2LL * num_sms() + cells - 1) / cells;   // about one wave at two CTAs per SM
+    // bf16 queries run on tcgen05 (one CTA per SM: at most one wave of splits); fp32
+    // queries on mma.sync (two CTAs per SM)
+    const bool tc = g.q_bf16 != 0;
+    long long ns = tc ? (num_sms() >= cells ? num_sms() / cells : 1) : (2LL * num_sms() + cells - 1) / cells;
     const long long ns_min = (g.sel_stride + (kMqMaxBlocks - 16) - 1) / (kMqMaxBlocks - 16);
     if (ns < ns_min) ns = ns_min;
     if (ns > tiles) ns = tiles > 0 ? tiles : 1;
@@ -437,8 +818,8 @@ cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* 
     a.part_o = reinterpret_cast<float*>(ws + L.part_o);
     a.counters = reinterpret_cast<uint32_t*>(ws + L.dec_counters);
     a.err = reinterpret_cast<uint32_t*>(ws + L.err);
-    if (g.D == 128) return g.q_bf16 ? launch_mq_t<128, false>(a, units, s) : launch_mq_t<128, true>(a, units, s);
-    return g.q_bf16 ? launch_mq_t<64, false>(a, units, s) : launch_mq_t<64, true>(a, units, s);
+    if (tc) return g.D == 128 ? launch_mq_tc_t<128>(a, units, s) : launch_mq_tc_t<64>(a, units, s);
+    return g.D == 128 ? launch_mq_t<128, true>(a, units, s) : launch_mq_t<64, true>(a, units, s);
 }
 
 }  // namespace sa
