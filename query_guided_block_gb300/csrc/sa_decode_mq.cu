@@ -21,6 +21,9 @@
 #include "sa_internal.h"
 #include "sa_tcgen05.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 namespace sa {
 namespace {
 
@@ -387,23 +390,24 @@ __global__ void __launch_bounds__(kMqThreads, 2) decode_mq_kernel(MqArgs a)
 
 // ------------------------------------------------------------------ tcgen05 ---
 // The same attention on the fifth-generation tensor cores (bf16 queries).  One
-// warpgroup per CTA; per 64-token tile k of the split:
-//   S(k) = Q K^T  one thread issues tcgen05.mma (M = 128, N = 64, K = D) from shared
-//                 memory into tensor memory (two S buffers): A = the 64 query rows (rows
-//                 64..127 zero), B = the K tile, both K-major with the 128-byte swizzle
-//                 the staging ring already writes;
-//   softmax       warps 0-1 read their row of S from tensor memory (thread = row) and
-//                 apply the online softmax with a lazy reference: the row maximum used
-//                 for exp2 moves (and O is rescaled in tensor memory) only when the
-//                 running maximum grows by more than kLazy, so P <= 2^kLazy; P goes to
-//                 shared memory as bf16 hi and its remainder lo (two A tiles);
-//   O += P V      tcgen05.mma (M = 128, N = D, K = 64) for hi and for lo, B = the V tile
-//                 read MN-major.
-// Issue order per tile: S(k + 2), then O += P(k) V(k): S runs two tiles ahead (three S
-// buffers, one mbarrier each, so no barrier can complete twice before it is waited
-// on), and the softmax of a tile never waits for its own Q K^T.  Each group completes
-// on an mbarrier (tcgen05.commit), every wait on it is bounded, and the CTA meets once
-// per tile.  Warps 2-3 compute each tile's token-validity mask two tiles ahead.
+// warpgroup per CTA, with fixed roles; per 64-token tile k of the split:
+//   load (warp 2, one thread)   the tile's K and V arrive by TMA: one 2-D box (64
+//       channels x up to 64 tokens of one KV head of one page) per selected block and
+//       64-channel half, written with the 128-byte swizzle by the tensor map, completing
+//       on the stage's mbarrier (transaction bytes);
+//   S(k) = Q K^T (warp 3, one thread)  tcgen05.mma (M = 128, N = 64, K = D) into tensor
+//       memory (three S buffers, issued two tiles ahead): A = the 64 query rows (rows
+//       64..127 zero), B = the K tile, both K-major;
+//   softmax (warps 0-1)         thread = query row: S from tensor memory, the online
+//       softmax with a lazy reference (the row maximum used for exp2 moves, and O is
+//       rescaled in tensor memory, only when the running maximum grows by more than
+//       kLazy, so P <= 2^kLazy), P to shared memory as bf16 hi and its remainder lo;
+//   O += P V (warp 3)           tcgen05.mma (M = 128, N = D, K = 64) for hi and lo,
+//       B = the V tile read MN-major.
+// Warps 2-3 also build each tile's token-validity mask two tiles ahead and zero the V
+// rows of tokens that are not selected (a box reads whole blocks) before O += P V reads
+// them.  Every group completes on an mbarrier and every wait is bounded; the CTA meets
+// once per tile.
 constexpr float kLazy = 8.f;   // log2 growth of the row maximum before O is rescaled
 
 template <int D>
@@ -424,17 +428,17 @@ struct MqTcShape {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
+__global__ void __launch_bounds__(kMqThreads, 1)
+    decode_mq_tc_kernel(MqArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        int box_rows)
 {
     using SH = MqTcShape<D>;
     constexpr int T = SH::T, STAGES = SH::STAGES;
     constexpr int CPR = D / 8;                              // 16-byte chunks per token row
-    constexpr int CP_PER_THREAD = T * CPR / kMqThreads;
     constexpr uint32_t S_COL = 0, O_COL = 256, TMEM_COLS = 512;   // S buffers at 0, 64, 128
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, T, false);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
     static_assert(O_COL + D <= TMEM_COLS, "S and O must fit the allocation");
-    static_assert(T * CPR % kMqThreads == 0, "tile copy must split over the threads");
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sp = blockIdx.x % a.nsplit;
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
     unsigned char* smem = smem_raw + (base - raw);
     int* blk_page = reinterpret_cast<int*>(smem + SH::OFF_BLK);
     int* blk_valid = blk_page + kMqMaxBlocks;
-    __shared__ __align__(8) uint64_t bar_s[3], bar_o;
+    __shared__ __align__(8) uint64_t bar_s[3], bar_o, bar_kv[STAGES];
     __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_mask[3][2];                        // valid tokens of a tile (64 bits)
     __shared__ int s_merge;
@@ -462,10 +466,9 @@ __global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&bar_s[0], 1);
-        mbar_init(&bar_s[1], 1);
-        mbar_init(&bar_s[2], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&bar_s[i], 1);
         mbar_init(&bar_o, 1);
+        for (int i = 0; i < STAGES; ++i) mbar_init(&bar_kv[i], 1);
         fence_mbar_init();
     }
 
@@ -520,89 +523,96 @@ __global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
         *reinterpret_cast<uint4*>(smem + SH::OFF_PH + off) = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(smem + SH::OFF_PL + off) = make_uint4(0u, 0u, 0u, 0u);
     }
-    __syncthreads();   // page lookups ready
+    fence_proxy_async_smem();   // Q and the P zeros, before the tensor core reads them
+    tc_fence_before_sync();
+    __syncthreads();            // page lookups, barriers and tensor memory ready
+    tc_fence_after_sync();
+    const uint32_t tmem = s_tmem;
 
-    // ---- staging ring: thread copies chunk cp_c of tile rows cp_r + i * (128 / CPR) ----
-    const char* kbase = reinterpret_cast<const char*>(a.k_pages);
-    const char* vbase = reinterpret_cast<const char*>(a.v_pages);
-    const int cp_c = tid % CPR, cp_r = tid / CPR;
-    constexpr int ROWS_PER_PASS = kMqThreads / CPR;
     auto token_ok = [&](int gi) -> bool {
         const int e = (gi >> bs_shift) - blk0, r = gi & (a.bs - 1);
         return gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && r < blk_valid[max(0, min(e, kMqMaxBlocks - 1))];
     };
-    auto issue_tile = [&](int tile, int st) {
-        const uint32_t kd = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES + uint32_t(cp_c >> 3) * SH::KV_HALF;
-        const uint32_t vd = kd + SH::KV_TENSOR;
+    // warp 2, one thread: the tile's boxes into stage st, counted on bar_kv[st]
+    auto load_tile = [&](int tile, int st) {
+        const uint32_t kst = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES;
+        const int g0 = tile * T;
+        uint32_t bytes = 0;
+        for (int r0 = 0; r0 < T; r0 += box_rows) {
+            const int gi = g0 + r0;
+            const int e = (gi >> bs_shift) - blk0;
+            if (gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && blk_page[e] >= 0) bytes += uint32_t(box_rows) * kRowB * D / 64 * 2;
+        }
+        mbar_arrive_expect_tx(&bar_kv[st], bytes);
+        for (int r0 = 0; r0 < T; r0 += box_rows) {
+            const int gi = g0 + r0;
+            const int e = (gi >> bs_shift) - blk0;
+            if (!(gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && blk_page[e] >= 0)) continue;
+            const int y = (blk_page[e] * a.Hkv + kvh) * a.bs + (gi & (a.bs - 1));
 #pragma unroll
-        for (int i = 0; i < CP_PER_THREAD; ++i) {
-            const int tr = cp_r + i * ROWS_PER_PASS;
-            const int gi = tile * T + tr;
-            const bool ok = token_ok(gi);
-            const int e = ok ? (gi >> bs_shift) - blk0 : 0, r = gi & (a.bs - 1);
-            const size_t off = ok ? ((size_t(blk_page[e]) * a.Hkv * a.bs + size_t(kvh) * a.bs + r) * (D * 2) + cp_c * 16) : 0;
-            const uint32_t so = uint32_t(tr) * kRowB + uint32_t(((cp_c & 7) ^ (tr & 7)) << 4);
-            cp_async_16_zfill(kd + so, kbase + off, ok ? 16u : 0u);
-            cp_async_16_zfill(vd + so, vbase + off, ok ? 16u : 0u);
+            for (int h = 0; h < SH::HALVES; ++h) {
+                const uint32_t off = uint32_t(h) * SH::KV_HALF + uint32_t(r0) * kRowB;
+                tma_load_2d(smem + (kst - base) + off, &kmap, h * 64, y, &bar_kv[st]);
+                tma_load_2d(smem + (kst - base) + SH::KV_TENSOR + off, &vmap, h * 64, y, &bar_kv[st]);
+            }
         }
     };
     // warps 2-3: 64-bit validity mask of a tile (one token per thread)
-    auto write_mask = [&](int tile) {
-        if (warp >= 2) {
-            const uint32_t m = __ballot_sync(kFullMask, token_ok(tile * T + (warp - 2) * 32 + lane));
-            if (lane == 0) s_mask[(tile - t0) % 3][warp - 2] = m;
-        }
+    auto write_mask = [&](int k) {
+        const uint32_t m = __ballot_sync(kFullMask, token_ok((t0 + k) * T + (warp - 2) * 32 + lane));
+        if (lane == 0) s_mask[k % 3][warp - 2] = m;
     };
-    auto issue_s = [&](int tile, int st) {   // S(tile) = Q K^T into S buffer (tile - t0) mod 3
-        const uint32_t kst = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES;
+    auto issue_s = [&](int k) {   // S(k) = Q K^T into S buffer k mod 3 (warp 3, one thread)
+        const uint32_t kst = base + SH::OFF_KV + uint32_t(k % STAGES) * SH::STAGE_BYTES;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = uint32_t(ks & 3) * 32;
             const uint64_t ad = smem_desc_sw128(base + SH::OFF_Q + uint32_t(ks >> 2) * SH::Q_HALF + off, 16, 1024);
             const uint64_t bd = smem_desc_sw128(kst + uint32_t(ks >> 2) * SH::KV_HALF + off, 16, 1024);
-            umma_bf16(s_tmem + S_COL + uint32_t((tile - t0) % 3) * T, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+            umma_bf16(tmem + S_COL + uint32_t(k % 3) * T, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
         }
-        umma_commit(&bar_s[(tile - t0) % 3]);
+        umma_commit(&bar_s[k % 3]);
     };
-    auto issue_o = [&](int k, int st) {      // O += P(k) V(k): hi then lo
-        const uint32_t vst = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES + SH::KV_TENSOR;
+    auto issue_o = [&](int k) {   // O += P(k) V(k): hi then lo (warp 3, one thread)
+        const uint32_t vst = base + SH::OFF_KV + uint32_t(k % STAGES) * SH::STAGE_BYTES + SH::KV_TENSOR;
 #pragma unroll
         for (int kk = 0; kk < T / 16; ++kk) {
             const uint64_t bd = smem_desc_sw128(vst + uint32_t(kk) * 16 * kRowB, SH::KV_HALF, 1024);
             const uint64_t ah = smem_desc_sw128(base + SH::OFF_PH + uint32_t(kk) * 32, 16, 1024);
             const uint64_t al = smem_desc_sw128(base + SH::OFF_PL + uint32_t(kk) * 32, 16, 1024);
-            umma_bf16(s_tmem + O_COL, ah, bd, IDESC_O, (k > 0 || kk > 0) ? 1u : 0u);
-            umma_bf16(s_tmem + O_COL, al, bd, IDESC_O, 1u);
+            umma_bf16(tmem + O_COL, ah, bd, IDESC_O, (k > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(tmem + O_COL, al, bd, IDESC_O, 1u);
         }
         umma_commit(&bar_o);
     };
+    auto wait_kv = [&](int k) {   // tile k's boxes have landed
+        if (!mbar_wait_bounded(&bar_kv[k % STAGES], uint32_t(k / STAGES) & 1u, kWaitCycles))
+            raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+    };
 
     const int ntiles = t1 - t0;
-#pragma unroll
-    for (int kk = 0; kk < STAGES - 1; ++kk) {
-        if (kk < ntiles) issue_tile(t0 + kk, kk);
-        cp_async_commit();
+    if (tid == 64)
+        for (int k = 0; k < STAGES - 1 && k < ntiles; ++k) load_tile(t0 + k, k);
+    if (warp >= 2) {
+        if (ntiles > 0) write_mask(0);
+        if (ntiles > 1) write_mask(1);
     }
-    if (ntiles > 0) write_mask(t0);
-    if (ntiles > 1) write_mask(t0 + 1);
-    cp_async_wait_group<STAGES - 3>();   // tiles 0 and 1 of this thread
-    fence_proxy_async_smem();            // Q, P zeros and tiles 0, 1, before the tensor core
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem = s_tmem;
+    if (tid == 96) {
+        for (int k = 0; k < 2 && k < ntiles; ++k) {
+            wait_kv(k);
+            issue_s(k);
+        }
+    }
+    __syncthreads();   // masks of tiles 0 and 1
+
     const uint32_t lane_base = uint32_t(32 * warp) << 16;   // this warp's tensor-memory lanes
     const int row = 32 * warp + lane;                      // warps 0-1: the tile's query row
-    if (tid == 0 && ntiles > 0) issue_s(t0, 0);
-    if (tid == 0 && ntiles > 1) issue_s(t0 + 1, 1);
-
     float m_ref = -INFINITY, l_run = 0.f;                  // reference maximum, row sum
     for (int k = 0; k < ntiles; ++k) {
-        const int tile = t0 + k;
-        float x[64];
-        bool rescale = false;
-        float alpha = 1.f, m_new = m_ref;
-        if (warp < 2) {   // S(k): scale, mask, row maximum
+        if (warp < 2) {
+            float x[64];
+            bool rescale = false;
+            float alpha = 1.f, m_new = m_ref;
             if (!mbar_wait_bounded(&bar_s[k % 3], uint32_t(k / 3) & 1u, kWaitCycles))
                 raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
             tc_fence_after_sync();
@@ -623,14 +633,9 @@ __global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
                 alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mx);
                 rescale = true;
             }
-        }
-        // O += P(k - 1) V(k - 1) is done: P, O and its stage are free
-        if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, kWaitCycles))
-            raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
-        if (k + STAGES - 1 < ntiles) issue_tile(tile + STAGES - 1, (k + STAGES - 1) % STAGES);
-        cp_async_commit();
-        if (k + 2 < ntiles) write_mask(tile + 2);
-        if (warp < 2) {
+            // O += P(k - 1) V(k - 1) is done: P and O are free
+            if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, kWaitCycles))
+                raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
             tc_fence_after_sync();
             if (k > 0 && __any_sync(kFullMask, rescale)) {   // O rows of this warp (lazy)
                 const float al = rescale ? alpha : 1.f;
@@ -669,18 +674,41 @@ __global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
                 *reinterpret_cast<uint4*>(pl + slot) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             l_run += psum;
+            fence_proxy_async_smem();   // P(k), before the tensor core reads it
+        } else {
+            // O += P(k - 1) V(k - 1) done: its stage is free for tile k + 3
+            if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, kWaitCycles))
+                raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+            if (tid == 64 && k + STAGES - 1 < ntiles) load_tile(t0 + k + STAGES - 1, (k + STAGES - 1) % STAGES);
+            if (k + 2 < ntiles) write_mask(k + 2);
+            // zero V rows of tile k whose token is not selected (boxes read whole blocks)
+            const uint32_t mk = s_mask[k % 3][warp - 2];
+            if (__any_sync(kFullMask, ((mk >> lane) & 1u) == 0u)) {
+                wait_kv(k);
+                if (((mk >> lane) & 1u) == 0u) {
+                    const int tr = (warp - 2) * 32 + lane;
+#pragma unroll
+                    for (int h = 0; h < SH::HALVES; ++h)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4*>(smem + SH::OFF_KV + (k % STAGES) * SH::STAGE_BYTES + SH::KV_TENSOR +
+                                                      h * SH::KV_HALF + tr * kRowB + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
         }
-        cp_async_wait_group<STAGES - 3>();   // tile k + 2 of this thread
-        fence_proxy_async_smem();            // P(k) and tile k + 2, before the tensor core
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
-        if (tid == 0) {
-            if (k + 2 < ntiles) issue_s(tile + 2, (k + 2) % STAGES);
-            issue_o(k, k % STAGES);
+        if (tid == 96) {
+            if (k + 2 < ntiles) {
+                wait_kv(k + 2);
+                issue_s(k + 2);
+            }
+            wait_kv(k);   // already complete: the tensor core reads V(k) after this thread saw it land
+            issue_o(k);
         }
     }
-    cp_async_wait_group<0>();
     if (ntiles > 0 && !mbar_wait_bounded(&bar_o, uint32_t(ntiles - 1) & 1u, kWaitCycles))
         raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
     tc_fence_after_sync();
@@ -734,8 +762,31 @@ __global__ void __launch_bounds__(kMqThreads, 1) decode_mq_tc_kernel(MqArgs a)
     mq_merge<D>(a, u, rt);
 }
 
+// A 2-D tensor map over a page pool viewed as [num_pages * Hkv * bs rows, D bf16]: boxes
+// of 64 channels x box_rows tokens, 128-byte swizzle (the layout the MMAs read).
+inline cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, int D, long long rows, int box_rows)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return cudaErrorNotSupported;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+    const cuuint32_t box[2] = {64u, cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D>
-cudaError_t launch_mq_tc_t(const MqArgs& a, int units, cudaStream_t s)
+cudaError_t launch_mq_tc_t(const MqArgs& a, int units, int num_pages, cudaStream_t s)
 {
     const size_t smem = MqTcShape<D>::SMEM;
     static bool configured = false;
@@ -745,8 +796,15 @@ cudaError_t launch_mq_tc_t(const MqArgs& a, int units, cudaStream_t s)
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    const int box_rows = a.bs < MqTcShape<D>::T ? a.bs : MqTcShape<D>::T;
+    const long long rows = (long long)num_pages * a.Hkv * a.bs;
+    CUtensorMap kmap, vmap;
+    cudaError_t e = encode_pool_map(&kmap, a.k_pages, D, rows, box_rows);
+    if (e != cudaSuccess) return e;
+    e = encode_pool_map(&vmap, a.v_pages, D, rows, box_rows);
+    if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(size_t(units) * a.row_tiles * a.nsplit);
-    return launch_after_previous(decode_mq_tc_kernel<D>, dim3(grid), dim3(kMqThreads), smem, s, a);
+    return launch_after_previous(decode_mq_tc_kernel<D>, dim3(grid), dim3(kMqThreads), smem, s, a, kmap, vmap, box_rows);
 }
 
 template <int D, bool QSPLIT>
@@ -818,7 +876,7 @@ cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* 
     a.part_o = reinterpret_cast<float*>(ws + L.part_o);
     a.counters = reinterpret_cast<uint32_t*>(ws + L.dec_counters);
     a.err = reinterpret_cast<uint32_t*>(ws + L.err);
-    if (tc) return g.D == 128 ? launch_mq_tc_t<128>(a, units, s) : launch_mq_tc_t<64>(a, units, s);
+    if (tc) return g.D == 128 ? launch_mq_tc_t<128>(a, units, g.num_pages, s) : launch_mq_tc_t<64>(a, units, g.num_pages, s);
     return g.D == 128 ? launch_mq_t<128, true>(a, units, s) : launch_mq_t<64, true>(a, units, s);
 }
 
