@@ -700,13 +700,13 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
-        if (tid == 96) {
+        if (tid == 96) {   // O += P(k) V(k) first: the next softmax waits for it, S(k + 2) is not due yet
+            wait_kv(k);    // already complete: the tensor core reads V(k) after this thread saw it land
+            issue_o(k);
             if (k + 2 < ntiles) {
                 wait_kv(k + 2);
                 issue_s(k + 2);
             }
-            wait_kv(k);   // already complete: the tensor core reads V(k) after this thread saw it land
-            issue_o(k);
         }
     }
     if (ntiles > 0 && !mbar_wait_bounded(&bar_o, uint32_t(ntiles - 1) & 1u, kWaitCycles))
