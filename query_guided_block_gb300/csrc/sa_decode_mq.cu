@@ -67,7 +67,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t half_base, int token, int chunk
 template <int D>
 __device__ void mq_merge(const MqArgs& a, int u, int rt)
 {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, nthr = blockDim.x;
     const int b = u / a.Hkv, kvh = u - b * a.Hkv;
     auto head_of = [&](int r) -> size_t {   // q / out row of unit row r
         const int t = r / a.G, g = r - (r / a.G) * a.G;
@@ -75,7 +75,7 @@ __device__ void mq_merge(const MqArgs& a, int u, int rt)
     };
     __shared__ float s_w[kMqRows][kMqMaxSplits], s_den[kMqRows];
     const int rows = min(kMqRows, a.R - rt * kMqRows);
-    for (int rr = tid; rr < rows; rr += kMqThreads) {
+    for (int rr = tid; rr < rows; rr += nthr) {
         const size_t pr0 = (size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits;
         float M = -INFINITY;
         for (int s2 = 0; s2 < a.nsplit; ++s2) M = fmaxf(M, __ldcg(a.part_m + pr0 + s2));
@@ -90,7 +90,7 @@ __device__ void mq_merge(const MqArgs& a, int u, int rt)
     }
     __syncthreads();
     const int n_out = rows * D;
-    for (int i0 = tid; i0 < n_out; i0 += kMqThreads * 8) {
+    for (int i0 = tid; i0 < n_out; i0 += nthr * 8) {
         float num[8];
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) num[k2] = 0.f;
@@ -98,7 +98,7 @@ __device__ void mq_merge(const MqArgs& a, int u, int rt)
             float v[8];
 #pragma unroll
             for (int k2 = 0; k2 < 8; ++k2) {
-                const int i = i0 + k2 * kMqThreads;
+                const int i = i0 + k2 * nthr;
                 const int rr = i / D, d = i - (i / D) * D;
                 v[k2] = (i < n_out && s_w[min(rr, kMqRows - 1)][s2] > 0.f)
                             ? __ldcg(a.part_o + ((size_t(u) * a.R + rt * kMqRows + rr) * a.max_splits + s2) * D + d)
@@ -106,13 +106,13 @@ __device__ void mq_merge(const MqArgs& a, int u, int rt)
             }
 #pragma unroll
             for (int k2 = 0; k2 < 8; ++k2) {
-                const int i = i0 + k2 * kMqThreads;
+                const int i = i0 + k2 * nthr;
                 if (i < n_out) num[k2] = fmaf(s_w[i / D][s2], v[k2], num[k2]);
             }
         }
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) {
-            const int i = i0 + k2 * kMqThreads;
+            const int i = i0 + k2 * nthr;
             if (i >= n_out) continue;
             const int rr = i / D, d = i - (i / D) * D;
             const float den = s_den[rr];
@@ -389,26 +389,33 @@ __global__ void __launch_bounds__(kMqThreads, 2) decode_mq_kernel(MqArgs a)
 }
 
 // ------------------------------------------------------------------ tcgen05 ---
-// The same attention on the fifth-generation tensor cores (bf16 queries).  One
-// warpgroup per CTA, with fixed roles; per 64-token tile k of the split:
-//   load (warp 2, one thread)   the tile's K and V arrive by TMA: one 2-D box (64
-//       channels x up to 64 tokens of one KV head of one page) per selected block and
-//       64-channel half, written with the 128-byte swizzle by the tensor map, completing
-//       on the stage's mbarrier (transaction bytes);
-//   S(k) = Q K^T (warp 3, one thread)  tcgen05.mma (M = 128, N = 64, K = D) into tensor
-//       memory (three S buffers, issued two tiles ahead): A = the 64 query rows (rows
-//       64..127 zero), B = the K tile, both K-major;
-//   softmax (warps 0-1)         thread = query row: S from tensor memory, the online
-//       softmax with a lazy reference (the row maximum used for exp2 moves, and O is
-//       rescaled in tensor memory, only when the running maximum grows by more than
-//       kLazy, so P <= 2^kLazy), P to shared memory as bf16 hi and its remainder lo;
-//   O += P V (warp 3)           tcgen05.mma (M = 128, N = D, K = 64) for hi and lo,
-//       B = the V tile read MN-major.
-// Warps 2-3 also build each tile's token-validity mask two tiles ahead and zero the V
-// rows of tokens that are not selected (a box reads whole blocks) before O += P V reads
-// them.  Every group completes on an mbarrier and every wait is bounded; the CTA meets
-// once per tile.
+// The same attention on the fifth-generation tensor cores (bf16 queries).  Six warps
+// with fixed roles; per 64-token tile k of the split:
+//   load (warp 4, one thread, running ahead on its own)  the tile's K and V arrive by
+//       TMA: one 2-D box (64 channels x up to 64 tokens of one KV head of one page) per
+//       selected block and 64-channel half, written with the 128-byte swizzle by the
+//       tensor map and counted on the stage's mbarrier; a stage is refilled once the
+//       MMAs that read it have completed (a per-stage mbarrier);
+//   S(k) = Q K^T (warp 5, one thread)  tcgen05.mma (M = 128, N = 64, K = D) into tensor
+//       memory, three S buffers, issued two tiles ahead; A holds the 64 query rows twice
+//       (rows r and r + 64), so S lanes 64..127 repeat lanes 0..63;
+//   softmax (warps 0-3)  thread = (query row, half of the tile's columns): warps 0-1 take
+//       columns 0..31 from lanes 0..63, warps 2-3 columns 32..63 from lanes 64..127; the
+//       two halves of a row exchange their maxima through a named barrier, then apply
+//       the online softmax with a lazy reference (the maximum used for exp2 moves, and O
+//       is rescaled in tensor memory, only when the running maximum grows by more than
+//       kLazy, so P <= 2^kLazy) and write P as bf16: hi in row r, the remainder lo in
+//       row r + 64 of one 128-row A tile;
+//   O += P V (warp 5)  tcgen05.mma (M = 128, N = D, K = 64), B = the V tile read
+//       MN-major; O rows r and r + 64 hold the hi and lo products and add up at the end.
+//       Warp 5 also builds each tile's token-validity mask two tiles ahead and zeroes
+//       the V rows of tokens that are not selected (a box reads whole blocks).
+// Issue order per tile: O += P(k) V(k), then S(k + 2).  Every group completes on an
+// mbarrier (three for S, one for O, one per staging stage for loaded and for free) and
+// every wait is bounded; warps 0-3 and 5 meet once per tile, the loader never waits on
+// them.
 constexpr float kLazy = 8.f;   // log2 growth of the row maximum before O is rescaled
+constexpr int kTcThreads = 192;
 
 template <int D>
 struct MqTcShape {
@@ -421,14 +428,19 @@ struct MqTcShape {
     static constexpr int Q_HALF = 128 * kRowB;              // 128 rows x 128 B
     static constexpr int Q_BYTES = HALVES * Q_HALF;
     static constexpr int P_BYTES = 128 * kRowB;             // 128 rows x 64 tokens bf16
-    static constexpr int OFF_Q = 0, OFF_PH = Q_BYTES, OFF_PL = OFF_PH + P_BYTES;
-    static constexpr int OFF_KV = OFF_PL + P_BYTES;
+    static constexpr int OFF_Q = 0, OFF_P = Q_BYTES;
+    static constexpr int OFF_KV = OFF_P + P_BYTES;
     static constexpr int OFF_BLK = OFF_KV + STAGES * STAGE_BYTES;
     static constexpr size_t SMEM = 1024 + size_t(OFF_BLK) + size_t(2) * kMqMaxBlocks * sizeof(int);
 };
 
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(kMqThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     decode_mq_tc_kernel(MqArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         int box_rows)
 {
@@ -439,6 +451,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, T, false);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
     static_assert(O_COL + D <= TMEM_COLS, "S and O must fit the allocation");
+    constexpr int LOADER = 4 * 32, ISSUER = 5 * 32;         // the two single-thread roles
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sp = blockIdx.x % a.nsplit;
@@ -453,9 +466,11 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     unsigned char* smem = smem_raw + (base - raw);
     int* blk_page = reinterpret_cast<int*>(smem + SH::OFF_BLK);
     int* blk_valid = blk_page + kMqMaxBlocks;
-    __shared__ __align__(8) uint64_t bar_s[3], bar_o, bar_kv[STAGES];
+    __shared__ __align__(8) uint64_t bar_s[3], bar_o, bar_kv[STAGES], bar_free[STAGES];
     __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_mask[3][2];                        // valid tokens of a tile (64 bits)
+    __shared__ float s_mx[2][64];                            // per-half row maxima
+    __shared__ float s_l[64];                                // row sums of the second half
     __shared__ int s_merge;
 
     allow_dependents_early();
@@ -468,7 +483,10 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bar_s[i], 1);
         mbar_init(&bar_o, 1);
-        for (int i = 0; i < STAGES; ++i) mbar_init(&bar_kv[i], 1);
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&bar_kv[i], 1);
+            mbar_init(&bar_free[i], 1);
+        }
         fence_mbar_init();
     }
 
@@ -484,7 +502,7 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     const int blk0 = (t0 * T) >> bs_shift;
     const int blk1 = min(count, ((t1 * T - 1) >> bs_shift) + 1);
     const int nblk = t1 > t0 ? blk1 - blk0 : 0;
-    for (int e = tid; e < nblk; e += kMqThreads) {
+    for (int e = tid; e < nblk; e += kTcThreads) {
         const int slot = blk0 + e;
         int page = -1, valid = 0;
         const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
@@ -505,25 +523,21 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         }
     }
 
-    // ---- query rows 0..63 of the tile (zero past R), zero rows 64..127 of Q and P ----
+    // ---- query rows 0..63 of the tile (zero past R), repeated in rows 64..127 --------
     auto head_of = [&](int r) -> size_t {   // q / out row of unit row r
         const int t = r / a.G, g = r - (r / a.G) * a.G;
         return (size_t(b) * a.Q + t) * a.Hq + size_t(kvh) * a.G + g;
     };
-    for (int i = tid; i < 128 * CPR; i += kMqThreads) {
+    for (int i = tid; i < 64 * CPR; i += kTcThreads) {
         const int row = i / CPR, c = i - (i / CPR) * CPR;
         const int r = rt * kMqRows + row;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row < 64 && r < a.R)
-            v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + head_of(r) * D) + c);
-        *reinterpret_cast<uint4*>(smem + SH::OFF_Q + (c >> 3) * SH::Q_HALF + row * kRowB + (((c & 7) ^ (row & 7)) << 4)) = v;
+        if (r < a.R) v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + head_of(r) * D) + c);
+        const int off = (c >> 3) * SH::Q_HALF + (((c & 7) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + SH::OFF_Q + off + row * kRowB) = v;
+        *reinterpret_cast<uint4*>(smem + SH::OFF_Q + off + (row + 64) * kRowB) = v;
     }
-    for (int i = tid; i < 64 * 8; i += kMqThreads) {   // rows 64..127 of both P tiles
-        const int off = (64 + i / 8) * kRowB + (i % 8) * 16;
-        *reinterpret_cast<uint4*>(smem + SH::OFF_PH + off) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(smem + SH::OFF_PL + off) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();   // Q and the P zeros, before the tensor core reads them
+    fence_proxy_async_smem();   // Q, before the tensor core reads it
     tc_fence_before_sync();
     __syncthreads();            // page lookups, barriers and tensor memory ready
     tc_fence_after_sync();
@@ -533,21 +547,22 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         const int e = (gi >> bs_shift) - blk0, r = gi & (a.bs - 1);
         return gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && r < blk_valid[max(0, min(e, kMqMaxBlocks - 1))];
     };
-    // warp 2, one thread: the tile's boxes into stage st, counted on bar_kv[st]
+    auto box_ok = [&](int gi) -> bool {
+        const int e = (gi >> bs_shift) - blk0;
+        return gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && blk_page[e] >= 0;
+    };
+    // the loader thread: the tile's boxes into stage st, counted on bar_kv[st]
     auto load_tile = [&](int tile, int st) {
         const uint32_t kst = base + SH::OFF_KV + uint32_t(st) * SH::STAGE_BYTES;
         const int g0 = tile * T;
         uint32_t bytes = 0;
-        for (int r0 = 0; r0 < T; r0 += box_rows) {
-            const int gi = g0 + r0;
-            const int e = (gi >> bs_shift) - blk0;
-            if (gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && blk_page[e] >= 0) bytes += uint32_t(box_rows) * kRowB * D / 64 * 2;
-        }
+        for (int r0 = 0; r0 < T; r0 += box_rows)
+            if (box_ok(g0 + r0)) bytes += uint32_t(box_rows) * kRowB * SH::HALVES * 2;
         mbar_arrive_expect_tx(&bar_kv[st], bytes);
         for (int r0 = 0; r0 < T; r0 += box_rows) {
             const int gi = g0 + r0;
+            if (!box_ok(gi)) continue;
             const int e = (gi >> bs_shift) - blk0;
-            if (!(gi < ntok && e >= 0 && e < min(nblk, kMqMaxBlocks) && blk_page[e] >= 0)) continue;
             const int y = (blk_page[e] * a.Hkv + kvh) * a.bs + (gi & (a.bs - 1));
 #pragma unroll
             for (int h = 0; h < SH::HALVES; ++h) {
@@ -557,12 +572,17 @@ __global__ void __launch_bounds__(kMqThreads, 1)
             }
         }
     };
-    // warps 2-3: 64-bit validity mask of a tile (one token per thread)
+    // warp 5: 64-bit validity mask of a tile (two tokens per lane)
     auto write_mask = [&](int k) {
-        const uint32_t m = __ballot_sync(kFullMask, token_ok((t0 + k) * T + (warp - 2) * 32 + lane));
-        if (lane == 0) s_mask[k % 3][warp - 2] = m;
+        const int g0 = (t0 + k) * T;
+        const uint32_t m0 = __ballot_sync(kFullMask, token_ok(g0 + lane));
+        const uint32_t m1 = __ballot_sync(kFullMask, token_ok(g0 + 32 + lane));
+        if (lane == 0) {
+            s_mask[k % 3][0] = m0;
+            s_mask[k % 3][1] = m1;
+        }
     };
-    auto issue_s = [&](int k) {   // S(k) = Q K^T into S buffer k mod 3 (warp 3, one thread)
+    auto issue_s = [&](int k) {   // S(k) = Q K^T into S buffer k mod 3
         const uint32_t kst = base + SH::OFF_KV + uint32_t(k % STAGES) * SH::STAGE_BYTES;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -573,17 +593,16 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         }
         umma_commit(&bar_s[k % 3]);
     };
-    auto issue_o = [&](int k) {   // O += P(k) V(k): hi then lo (warp 3, one thread)
+    auto issue_o = [&](int k) {   // O += P(k) V(k), P hi in rows 0..63 and lo in rows 64..127
         const uint32_t vst = base + SH::OFF_KV + uint32_t(k % STAGES) * SH::STAGE_BYTES + SH::KV_TENSOR;
 #pragma unroll
         for (int kk = 0; kk < T / 16; ++kk) {
             const uint64_t bd = smem_desc_sw128(vst + uint32_t(kk) * 16 * kRowB, SH::KV_HALF, 1024);
-            const uint64_t ah = smem_desc_sw128(base + SH::OFF_PH + uint32_t(kk) * 32, 16, 1024);
-            const uint64_t al = smem_desc_sw128(base + SH::OFF_PL + uint32_t(kk) * 32, 16, 1024);
-            umma_bf16(tmem + O_COL, ah, bd, IDESC_O, (k > 0 || kk > 0) ? 1u : 0u);
-            umma_bf16(tmem + O_COL, al, bd, IDESC_O, 1u);
+            const uint64_t ad = smem_desc_sw128(base + SH::OFF_P + uint32_t(kk) * 32, 16, 1024);
+            umma_bf16(tmem + O_COL, ad, bd, IDESC_O, (k > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bar_o);
+        umma_commit(&bar_free[k % STAGES]);   // stage k mod STAGES may be refilled
     };
     auto wait_kv = [&](int k) {   // tile k's boxes have landed
         if (!mbar_wait_bounded(&bar_kv[k % STAGES], uint32_t(k / STAGES) & 1u, kWaitCycles))
@@ -591,13 +610,13 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     };
 
     const int ntiles = t1 - t0;
-    if (tid == 64)
+    if (tid == LOADER)
         for (int k = 0; k < STAGES - 1 && k < ntiles; ++k) load_tile(t0 + k, k);
-    if (warp >= 2) {
+    if (warp == 5) {
         if (ntiles > 0) write_mask(0);
         if (ntiles > 1) write_mask(1);
     }
-    if (tid == 96) {
+    if (tid == ISSUER) {
         for (int k = 0; k < 2 && k < ntiles; ++k) {
             wait_kv(k);
             issue_s(k);
@@ -605,39 +624,41 @@ __global__ void __launch_bounds__(kMqThreads, 1)
     }
     __syncthreads();   // masks of tiles 0 and 1
 
-    const uint32_t lane_base = uint32_t(32 * warp) << 16;   // this warp's tensor-memory lanes
-    const int row = 32 * warp + lane;                      // warps 0-1: the tile's query row
-    float m_ref = -INFINITY, l_run = 0.f;                  // reference maximum, row sum
+    const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;   // this warp's tensor-memory lanes
+    const int row = (32 * warp + lane) & 63;                      // softmax warps: the query row
+    const int half = warp >> 1;                                  // softmax warps: column half
+    float m_ref = -INFINITY, l_run = 0.f;                        // reference maximum, half-row sum
     for (int k = 0; k < ntiles; ++k) {
-        if (warp < 2) {
-            float x[64];
-            bool rescale = false;
-            float alpha = 1.f, m_new = m_ref;
+        if (warp < 4) {
             if (!mbar_wait_bounded(&bar_s[k % 3], uint32_t(k / 3) & 1u, kWaitCycles))
                 raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
             tc_fence_after_sync();
-            uint32_t sv[2][32];
-            tmem_ld32(tmem + lane_base + S_COL + uint32_t(k % 3) * T, sv[0]);
-            tmem_ld32(tmem + lane_base + S_COL + uint32_t(k % 3) * T + 32, sv[1]);
+            uint32_t sv[32];
+            tmem_ld32(tmem + lane_base + S_COL + uint32_t(k % 3) * T + uint32_t(half) * 32, sv);
             tmem_wait_ld();
-            const uint32_t mk0 = s_mask[k % 3][0], mk1 = s_mask[k % 3][1];
+            const uint32_t mk = s_mask[k % 3][half];
+            float x[32];
             float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const bool ok = ((j < 32 ? mk0 : mk1) >> (j & 31)) & 1u;
-                x[j] = ok ? __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2 : -INFINITY;
+            for (int j = 0; j < 32; ++j) {
+                x[j] = ((mk >> j) & 1u) ? __uint_as_float(sv[j]) * a.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, x[j]);
             }
+            s_mx[half][row] = mx;
+            named_barrier(1 + (warp & 1), 64);   // the other half of these rows
+            mx = fmaxf(s_mx[0][row], s_mx[1][row]);
+            bool rescale = false;
+            float alpha = 1.f;
             if (mx > m_ref + kLazy || (m_ref == -INFINITY && mx != -INFINITY)) {
-                m_new = mx;
                 alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mx);
+                m_ref = mx;
                 rescale = true;
             }
             // O += P(k - 1) V(k - 1) is done: P and O are free
             if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, kWaitCycles))
                 raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
             tc_fence_after_sync();
-            if (k > 0 && __any_sync(kFullMask, rescale)) {   // O rows of this warp (lazy)
+            if (k > 0 && __any_sync(kFullMask, rescale)) {   // this warp's O rows (lazy)
                 const float al = rescale ? alpha : 1.f;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -650,15 +671,12 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 }
                 tmem_wait_st();
             }
-            if (rescale) {
-                l_run *= alpha;
-                m_ref = m_new;
-            }
+            if (rescale) l_run *= alpha;
             float psum = 0.f;
-            unsigned char* ph = smem + SH::OFF_PH + row * kRowB;
-            unsigned char* pl = smem + SH::OFF_PL + row * kRowB;
+            unsigned char* ph = smem + SH::OFF_P + row * kRowB;
+            unsigned char* pl = smem + SH::OFF_P + (row + 64) * kRowB;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
@@ -669,24 +687,22 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                     hw[e2] = pack_bf16x2(p0, p1);
                     lw[e2] = pack_bf16x2(p0 - bf16_lo(hw[e2]), p1 - bf16_hi(hw[e2]));
                 }
-                const int slot = (c ^ (row & 7)) << 4;
+                const int slot = ((half * 4 + c) ^ (row & 7)) << 4;   // row and row + 64 share row & 7
                 *reinterpret_cast<uint4*>(ph + slot) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(pl + slot) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             l_run += psum;
             fence_proxy_async_smem();   // P(k), before the tensor core reads it
-        } else {
-            // O += P(k - 1) V(k - 1) done: its stage is free for tile k + 3
-            if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, kWaitCycles))
-                raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
-            if (tid == 64 && k + STAGES - 1 < ntiles) load_tile(t0 + k + STAGES - 1, (k + STAGES - 1) % STAGES);
+        } else if (warp == 5) {
             if (k + 2 < ntiles) write_mask(k + 2);
             // zero V rows of tile k whose token is not selected (boxes read whole blocks)
-            const uint32_t mk = s_mask[k % 3][warp - 2];
-            if (__any_sync(kFullMask, ((mk >> lane) & 1u) == 0u)) {
+            const uint32_t m0 = s_mask[k % 3][0], m1 = s_mask[k % 3][1];
+            if ((m0 & m1) != 0xffffffffu) {
                 wait_kv(k);
-                if (((mk >> lane) & 1u) == 0u) {
-                    const int tr = (warp - 2) * 32 + lane;
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    if (((hr ? m1 : m0) >> lane) & 1u) continue;
+                    const int tr = hr * 32 + lane;
 #pragma unroll
                     for (int h = 0; h < SH::HALVES; ++h)
 #pragma unroll
@@ -696,12 +712,21 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 }
                 fence_proxy_async_smem();
             }
+        } else {
+            // the loader: tile k + STAGES - 1 into the stage tile k - 1 used, once the
+            // MMAs reading it are done
+            if (tid == LOADER && k + STAGES - 1 < ntiles) {
+                if (k > 0 && !mbar_wait_bounded(&bar_free[(k - 1) % STAGES], uint32_t((k - 1) / STAGES) & 1u, kWaitCycles))
+                    raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+                load_tile(t0 + k + STAGES - 1, (k + STAGES - 1) % STAGES);
+            }
+            continue;   // the loader does not meet the others
         }
         tc_fence_before_sync();
-        __syncthreads();
+        named_barrier(3, kTcThreads - 32);   // warps 0-3 and 5
         tc_fence_after_sync();
-        if (tid == 96) {   // O += P(k) V(k) first: the next softmax waits for it, S(k + 2) is not due yet
-            wait_kv(k);    // already complete: the tensor core reads V(k) after this thread saw it land
+        if (tid == ISSUER) {   // O += P(k) V(k) first: the next softmax waits for it
+            wait_kv(k);        // already complete: the tensor core reads V(k) after this thread saw it land
             issue_o(k);
             if (k + 2 < ntiles) {
                 wait_kv(k + 2);
@@ -713,21 +738,37 @@ __global__ void __launch_bounds__(kMqThreads, 1)
         raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
     tc_fence_after_sync();
 
-    // ---- epilogue: rows 0..63 (warps 0-1) ----
+    // ---- epilogue: O[r] + O[r + 64], the lo rows and second-half sums via shared memory ----
+    float* lo_rows = reinterpret_cast<float*>(smem + SH::OFF_KV);   // [64][D], the free ring
+    if (warp == 2 || warp == 3) {
+        s_l[row] = l_run;
+        if (ntiles > 0) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld32(tmem + lane_base + O_COL + c0, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) lo_rows[row * D + ((c0 + j + lane) & (D - 1))] = __uint_as_float(ov[j]);
+            }
+        }
+    }
+    __syncthreads();
     const int r_unit = rt * kMqRows + row;
     if (warp < 2) {
+        const float lsum = l_run + s_l[row];
         const bool have = r_unit < a.R;
         float* dst = nullptr;
         float inv = 1.f;
         if (have) {
             if (a.nsplit == 1) {
                 dst = a.out + head_of(r_unit) * D;
-                inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                inv = lsum > 0.f ? 1.f / lsum : 0.f;
             } else {
                 const size_t pr = (size_t(u) * a.R + r_unit) * a.max_splits + sp;
                 dst = a.part_o + pr * D;
                 a.part_m[pr] = m_ref;
-                a.part_l[pr] = l_run;
+                a.part_l[pr] = lsum;
             }
         }
 #pragma unroll
@@ -742,7 +783,11 @@ __global__ void __launch_bounds__(kMqThreads, 1)
                 for (int j = 0; j < 32; j += 4) {
                     float o4[4];
 #pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) o4[e2] = ntiles > 0 ? __uint_as_float(ov[j + e2]) * inv : 0.f;
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const int d = c0 + j + e2;
+                        o4[e2] = ntiles > 0 ? (__uint_as_float(ov[j + e2]) + lo_rows[row * D + ((d + lane) & (D - 1))]) * inv
+                                            : 0.f;
+                    }
                     *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(o4[0], o4[1], o4[2], o4[3]);
                 }
             }
@@ -804,7 +849,7 @@ cudaError_t launch_mq_tc_t(const MqArgs& a, int units, int num_pages, cudaStream
     e = encode_pool_map(&vmap, a.v_pages, D, rows, box_rows);
     if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(size_t(units) * a.row_tiles * a.nsplit);
-    return launch_after_previous(decode_mq_tc_kernel<D>, dim3(grid), dim3(kMqThreads), smem, s, a, kmap, vmap, box_rows);
+    return launch_after_previous(decode_mq_tc_kernel<D>, dim3(grid), dim3(kTcThreads), smem, s, a, kmap, vmap, box_rows);
 }
 
 template <int D, bool QSPLIT>

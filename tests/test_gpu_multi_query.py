@@ -69,7 +69,10 @@ def run_and_compare(w, seqs=None):
     dict(num_queries=3, q_dtype=torch.float32, block_size=16),      # fp32 query (hi + lo)
     dict(num_queries=8, head_dim=64, num_q_heads=16, num_kv_heads=2, block_size=128, n_tokens=7000),
     dict(num_queries=5, n_tokens=700, topk=3, window_tokens=64),    # one tile: one split
-], ids=["q4", "q16", "q20", "fp32q", "d64", "short"])
+    dict(num_queries=16, batch=1, num_kv_heads=1, num_q_heads=4, n_tokens=60000, topk=100),  # many splits
+    dict(num_queries=16, n_tokens=20000, block_size=16, topk=200, window_tokens=100),       # bs 16 boxes
+    dict(num_queries=12, n_tokens=30000, block_size=128, topk=20),                          # bs 128 boxes
+], ids=["q4", "q16", "q20", "fp32q", "d64", "short", "splits", "bs16", "bs128"])
 def test_multi_query_small(cfg):
     run_and_compare(_w(**cfg))
 
