@@ -90,12 +90,14 @@ KERNEL_SOURCES = {
     "decode": [_CSRC + f for f in ("sa_decode.cu", "sa_decode_body.cuh", "sa_common.cuh")],
     "step": [_CSRC + f for f in ("sa_step.cu", "sa_step_kernel.cuh", "sa_select_body.cuh", "sa_decode_body.cuh",
                                  "sa_common.cuh")],
+    "decode_mq": [_CSRC + f for f in ("sa_decode_mq.cu", "sa_tcgen05.cuh", "sa_common.cuh")],
 }
 
 
-def recorded_traffic(kernel: str, workload: str):
+def recorded_traffic(kernel: str, workload: str, sources: str = ""):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+    current kernel source (else None).  `sources` names the kernel's source files when
+    they differ from `kernel`'s (the multi-query decode)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
@@ -104,7 +106,7 @@ def recorded_traffic(kernel: str, workload: str):
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source_sha:\s*([0-9a-f]+)", text)
     if not m:
         return None
-    if m.group(2) != source_digest(KERNEL_SOURCES[kernel]):
+    if m.group(2) != source_digest(KERNEL_SOURCES[sources or kernel]):
         return None
     return float(m.group(1))
 
@@ -427,7 +429,7 @@ def run_gpu_arm(args):
     dominant = "step" if use_step else ("select" if sel_avg >= dec_avg else "decode")
     dk = kern[dominant]
     step_gbs = step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9
-    traffic = recorded_traffic(dominant, w.name)
+    traffic = recorded_traffic(dominant, w.name, "decode_mq" if (multi_q and dominant == "decode") else "")
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dk["gbs"] / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
