@@ -2,7 +2,7 @@
  * sparse_attn.h -- C ABI of the GB300 (sm_103a) query-guided block-sparse decode
  * attention library (libsparse_attn.so).
  *
- * One decode step ("select-then-compute", SGLang分层稀疏注意力技术解析与优化实践 §1.2, §2.2):
+ * One decode step (select, then compute: SGLang分层稀疏注意力技术解析与优化实践 §1.2, §2.2):
  *
  *   sparse_attn_build_meta   once per context: per-block key bounding box (min/max per
  *                            channel) and, when asked for, per-block key means.
@@ -84,8 +84,12 @@ enum {
     SPARSE_ATTN_ERR_PAGE = 1u << 0,      /* block_table entry outside [0, num_pages) */
     SPARSE_ATTN_ERR_SEL_ID = 1u << 1,    /* sel_ids / prev_ids entry outside [0, nb) */
     SPARSE_ATTN_ERR_SEL_COUNT = 1u << 2, /* sel_count outside [0, sel_stride] */
-    SPARSE_ATTN_ERR_TIMEOUT = 1u << 3,   /* a bounded wait on an async copy gave up */
-    SPARSE_ATTN_ERR_SLOT = 1u << 4       /* LRU state holds an id outside [-1, nb) */
+    SPARSE_ATTN_ERR_TIMEOUT = 1u << 3,   /* a bounded wait (async copy, tensor-core MMA
+                                            completion, a selection published by another
+                                            CTA) gave up after about a second */
+    SPARSE_ATTN_ERR_SLOT = 1u << 4,      /* LRU state holds an id outside [-1, nb) */
+    SPARSE_ATTN_ERR_CAPACITY = 1u << 5   /* a per-CTA work list overflowed (the host's
+                                            launch limits exclude it; a set bit is a bug) */
 };
 
 /* Problem description.  Passed by pointer, read during the call, never retained.
@@ -152,7 +156,7 @@ int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream str
 /* Per-block metadata from the paged keys.
  * Defines: Quest key bounding box -- for each unit, block j and channel d,
  *   kmin[j][d] = min_t K[t][d], kmax[j][d] = max_t K[t][d] over the block's tokens
- *   (SGLang分层稀疏注意力技术解析与优化实践 §3.1.2, "Key Bounding Box");
+ *   (SGLang分层稀疏注意力技术解析与优化实践 §3.1.2, the key bounding box);
  * and, when kmean != NULL, kmean[r][d] = mean of K[t][d] over the tokens of mean row r
  *   (SparDA page www.2kiu.com/news/4656707 §3.1, mean pooling; 从HiSparse到QSA的移植实战
  *   §2.2, the coarse-block summary).  kmean is required when two_level or score_kind ==
@@ -204,11 +208,16 @@ int sparse_attn_select_reserved(const sparse_attn_params* p, const void* q, cons
                                 sparse_attn_stream stream);
 
 /* Sparse decode attention (从HiSparse到QSA的移植实战 §3.3: iterate only the selected
- * blocks given as a compact index array; SGLang page §2.2, "finally the sparse attention").
+ * blocks given as a compact index array; SGLang page §2.2, the attention stage that
+ * follows the selection).
  *   out[b][h] = sum over tokens t of the selected blocks of unit (b, h / G) of
  *               softmax_t(softmax_scale * q_h . k_t) * v_t,
  * exactly, over those tokens only; an empty selection gives a zero row.
- * Out-of-range sel_ids / block_table entries set a device error bit and are skipped. */
+ * Out-of-range sel_ids / block_table entries set a device error bit and are skipped.
+ * With num_queries > 1 every query row of a unit attends over the unit's selection:
+ * bf16 queries run on the fifth-generation tensor cores with K/V loaded by the tensor
+ * memory accelerator from the page pools (viewed as [num_pages * Hkv * block_size, D]
+ * bf16 rows), fp32 queries on the warp-level tensor-core path. */
 int sparse_attn_decode(const sparse_attn_params* p, const void* q, const void* k_pages,
                        const void* v_pages, const int32_t* block_table, const int32_t* sel_ids,
                        const int32_t* sel_count, float* out, void* ws, size_t ws_bytes,

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libsparse_attn.so")
 OK, INVALID_ARG, UNSUPPORTED, CUDA_ERROR, DEVICE_BOUNDS = range(5)
 F32, BF16 = 0, 1
 SCORE_QUEST, SCORE_MEAN = 0, 1
-ERR_PAGE, ERR_SEL_ID, ERR_SEL_COUNT, ERR_TIMEOUT, ERR_SLOT = 1, 2, 4, 8, 16
+ERR_PAGE, ERR_SEL_ID, ERR_SEL_COUNT, ERR_TIMEOUT, ERR_SLOT, ERR_CAPACITY = 1, 2, 4, 8, 16, 32
 
 
 class SparseAttnError(RuntimeError):

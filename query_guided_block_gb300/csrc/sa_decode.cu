@@ -4,7 +4,7 @@
 // block indices and never reads unselected KV; HBM bandwidth is the bound.  SparDA page
 // (www.2kiu.com/news/4656707) §5.3: skip unselected pages inside the kernel rather than
 // gathering them into a temporary buffer first.  The softmax is exact over the union of
-// the selected tokens (SGLang page §1.2 "select-then-compute").
+// the selected tokens (SGLang page §1.2: select, then compute).
 //
 // Design: a persistent grid over "items" (a few selected blocks, 64-128 tokens, of one
 // (sequence, KV head) unit), numbered unit-major; CTA i owns an equal contiguous range,

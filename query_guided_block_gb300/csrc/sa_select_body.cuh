@@ -763,7 +763,7 @@ __device__ __forceinline__ void select_body_warps(const SelectArgs& a, uint32_t*
                 a.counters[u] = 0u;   // every slot of this unit is scored
                 const int i = atomicAdd(&s_ndone, 1);
                 if (i < kSlabSelMaxUnits) s_done[i] = u;
-                else raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+                else raise_error(a.err, SPARSE_ATTN_ERR_CAPACITY);
             }
         }
         __syncwarp();

@@ -83,3 +83,39 @@ def test_diff_rejects_corrupt_state_and_leaves_it_untouched():
     assert dec.device_error() & B.ERR_SEL_ID
     cache.diff(0)
     assert dec.device_error() == 0
+
+
+def test_fused_step_reports_bad_pages_and_stays_usable():
+    """The fused step's decode phase checks the page table like the decode call."""
+    w, inp, dec = _case()
+    bt = inp["block_table"].clone()
+    j = int(dec.sel_ids[1, 0, 0])
+    bt[1, j] = w.num_pages + 1
+    dec.step_fused(inp["q"], inp["k_pages"], inp["v_pages"], bt)
+    assert dec.device_error() & B.ERR_PAGE
+    dec.step_fused(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"])
+    assert dec.device_error() == 0
+    assert torch.isfinite(dec.out).all()
+
+
+def test_tensor_core_multi_query_decode_reports_bad_inputs():
+    """The tcgen05 multi-query decode skips (and reports) a page outside the pool and a
+    selection id outside the context; its tensor-map loads never see them."""
+    w = Workload(name="err_mq", batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                 n_tokens=6000, block_size=32, window_tokens=256, topk=10, num_queries=8)
+    inp = make_inputs(w, "cuda")
+    dec = SparseDecoder(B.params_for(w))
+    dec.build_meta(inp["k_pages"], inp["block_table"])
+    dec.select(inp["q"])
+    assert dec.device_error() == 0
+    bt = inp["block_table"].clone()
+    bt[0, int(dec.sel_ids[0, 1, 2])] = -3
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], bt)
+    assert dec.device_error() & B.ERR_PAGE
+    ids = dec.sel_ids.clone()
+    ids[1, 0, 1] = w.num_blocks + 2
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"], sel_ids=ids)
+    assert dec.device_error() & B.ERR_SEL_ID
+    dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"])
+    assert dec.device_error() == 0
+    assert torch.isfinite(dec.out).all()
