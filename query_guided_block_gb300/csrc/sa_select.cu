@@ -34,9 +34,49 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a, uint3
     select_body<KIND, MBF16, D>(a, ready);
 }
 
+// The warp-slab streaming of the fused step as a select kernel of its own (one CTA per
+// SM, the CTA's query coefficients summed before any copy is in flight).
+template <int KIND, bool MBF16, int D>
+__global__ void __launch_bounds__(kSelThreads, 1) select_warps_kernel(SelectArgs a, uint32_t* ready)
+{
+    select_body_warps<KIND, MBF16, D>(a, ready);
+}
+
+template <int KIND, bool MBF16, int D>
+cudaError_t launch_select_warps_t(const SelectArgs& a0, int units, uint32_t* ready, cudaStream_t s)
+{
+    using WS = SlabSelShape<KIND, MBF16, D>;
+    SelectArgs a = a0;
+    set_slab_chunking<KIND, MBF16, D>(a, units);
+    const size_t keys = size_t(kSelThreads) * key_tile(a.n_cand) * sizeof(uint32_t);
+    const size_t smem = WS::RING_BYTES > keys ? WS::RING_BYTES : keys;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(select_warps_kernel<KIND, MBF16, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(WS::RING_BYTES));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    int ctas = num_sms();
+    if (ctas > a.total_chunks) ctas = a.total_chunks;
+    // a CTA records the units it completes in a fixed list
+    const long long per_cta = ((long long)a.total_chunks + ctas - 1) / ctas;
+    if (per_cta / a.chunks_per_unit + 2 > kSlabSelMaxUnits) return cudaErrorNotSupported;
+    return launch_after_previous(select_warps_kernel<KIND, MBF16, D>, dim3(unsigned(ctas)), dim3(kSelThreads), smem, s,
+                                 a, ready);
+}
+
+// Several queries per sequence (many query rows per unit, one coefficient sum per unit
+// change) with no more units than SMs: the warp-slab kernel, whose CTAs sum their
+// units' coefficients before streaming (mq_128k select 86.5 -> 76.6 us); otherwise the
+// two-CTA-per-SM streaming kernel, which ranks the units two CTAs at a time.
 template <int KIND, bool MBF16, int D>
 cudaError_t launch_select_t(const SelectArgs& a0, int units, uint32_t* ready, cudaStream_t s)
 {
+    if (a0.Q > 1 && units <= num_sms()) {
+        const cudaError_t e = launch_select_warps_t<KIND, MBF16, D>(a0, units, ready, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     SelectArgs a = a0;
     set_chunking<KIND, MBF16, D>(a, units);
     const size_t keys_bytes = size_t(kSelThreads) * key_tile(a.n_cand) * sizeof(uint32_t);
