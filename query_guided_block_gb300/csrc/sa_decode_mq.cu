@@ -582,25 +582,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             s_mask[k % 3][1] = m1;
         }
     };
+    // Descriptors differ from their operand's base only in the start-address field
+    // (bits 0-13, in 16-byte units); every operand lies in this CTA's shared memory, so
+    // adding an offset >> 4 never carries out of the field.
+    const uint64_t q_desc = smem_desc_sw128(base + SH::OFF_Q, 16, 1024);
+    const uint64_t p_desc = smem_desc_sw128(base + SH::OFF_P, 16, 1024);
+    const uint64_t k_desc0 = smem_desc_sw128(base + SH::OFF_KV, 16, 1024);
+    const uint64_t v_desc0 = smem_desc_sw128(base + SH::OFF_KV + SH::KV_TENSOR, SH::KV_HALF, 1024);
     auto issue_s = [&](int k) {   // S(k) = Q K^T into S buffer k mod 3
-        const uint32_t kst = base + SH::OFF_KV + uint32_t(k % STAGES) * SH::STAGE_BYTES;
+        const uint64_t kd = k_desc0 + uint64_t((uint32_t(k % STAGES) * SH::STAGE_BYTES) >> 4);
+        const uint32_t d_tmem = tmem + S_COL + uint32_t(k % 3) * T;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = uint32_t(ks & 3) * 32;
-            const uint64_t ad = smem_desc_sw128(base + SH::OFF_Q + uint32_t(ks >> 2) * SH::Q_HALF + off, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kst + uint32_t(ks >> 2) * SH::KV_HALF + off, 16, 1024);
-            umma_bf16(tmem + S_COL + uint32_t(k % 3) * T, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+            umma_bf16(d_tmem, q_desc + ((uint32_t(ks >> 2) * SH::Q_HALF + off) >> 4),
+                      kd + ((uint32_t(ks >> 2) * SH::KV_HALF + off) >> 4), IDESC_S, ks > 0 ? 1u : 0u);
         }
         umma_commit(&bar_s[k % 3]);
     };
     auto issue_o = [&](int k) {   // O += P(k) V(k), P hi in rows 0..63 and lo in rows 64..127
-        const uint32_t vst = base + SH::OFF_KV + uint32_t(k % STAGES) * SH::STAGE_BYTES + SH::KV_TENSOR;
+        const uint64_t vd = v_desc0 + uint64_t((uint32_t(k % STAGES) * SH::STAGE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < T / 16; ++kk) {
-            const uint64_t bd = smem_desc_sw128(vst + uint32_t(kk) * 16 * kRowB, SH::KV_HALF, 1024);
-            const uint64_t ad = smem_desc_sw128(base + SH::OFF_P + uint32_t(kk) * 32, 16, 1024);
-            umma_bf16(tmem + O_COL, ad, bd, IDESC_O, (k > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < T / 16; ++kk)
+            umma_bf16(tmem + O_COL, p_desc + ((uint32_t(kk) * 32) >> 4), vd + ((uint32_t(kk) * 16 * kRowB) >> 4), IDESC_O,
+                      (k > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar_o);
         umma_commit(&bar_free[k % STAGES]);   // stage k mod STAGES may be refilled
     };
