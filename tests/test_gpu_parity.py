@@ -133,6 +133,16 @@ def test_two_level_small(n_tokens, topk, window):
     compare_all(w, inp, dec)
 
 
+def test_two_level_many_survivors():
+    """More level-1 survivors than one CTA keeps (300 > 256 coarse blocks): the two levels
+    run as two launches of the streaming select kernel."""
+    w = _w(n_tokens=40000, block_size=32, window_tokens=300, topk=20, two_level=True,
+           coarse_block=64, topk_coarse=300, planted_per_unit=6)
+    inp = make_inputs(w, "cuda")
+    dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+
+
 @pytest.mark.parametrize("cfg", [
     dict(n_tokens=20000, block_size=32, topk=10, num_reserve=7, planted_per_unit=4),
     dict(n_tokens=9001, block_size=64, topk=3, num_reserve=40, window_tokens=700),
