@@ -87,6 +87,7 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
     constexpr int kBins = 2048;
     constexpr int kBinsPerThread = kBins / kSelThreads;
     constexpr int kGather = kSelThreads;
+    constexpr int kGatherDirect = 64;   // ranked directly without a radix pass
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t s_bin, s_above, s_binc, s_T;
     __shared__ int s_cT, s_ng;
@@ -111,8 +112,13 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
         mask = low_bits >= 32 ? 0u : ~((1u << low_bits) - 1u);
         prefix = hi & mask;
         uint32_t binc = uint32_t(n_valid);   // candidates matching the current prefix
+        // Gather the boundary candidates once they fit the gather buffer, but take at
+        // least one radix pass first unless they are few: ranking a full buffer is
+        // quadratic in the candidates.
+        int passes = 0;
         while (true) {
-            if (binc <= uint32_t(kGather) || low_bits == 0) break;
+            if (low_bits == 0 || (binc <= uint32_t(kGather) && (passes > 0 || binc <= uint32_t(kGatherDirect)))) break;
+            ++passes;
             const int w = min(11, low_bits);
             const int shift = low_bits - w;
             const uint32_t dmask = (1u << w) - 1u;
@@ -189,6 +195,7 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
                 const uint32_t mk = g_key[tid];
                 const int mi = g_idx[tid];
                 int rank = 0;
+#pragma unroll 8
                 for (int j = 0; j < ng; ++j)
                     rank += (g_key[j] > mk) || (g_key[j] == mk && g_idx[j] < mi);
                 if (rank == krem - 1) { s_T = mk; s_cT = mi; }
