@@ -165,3 +165,38 @@ def test_full_size(name):
     compare_all(w, inp, b, seqs=[0, w.batch - 1])
     del inp, a, b
     torch.cuda.empty_cache()
+
+
+def _random_cases(n, seed=11):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        D = int(rng.choice([64, 128]))
+        Hkv = int(rng.choice([1, 2, 4]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        bs = int(rng.choice([16, 32, 64, 128]))
+        N = int(rng.integers(1, 40000))
+        kw = dict(name=f"rand{i}", batch=int(rng.integers(1, 5)), num_kv_heads=Hkv, num_q_heads=Hkv * G,
+                  head_dim=D, block_size=bs, n_tokens=N, window_tokens=int(rng.choice([0, 64, 300, 2000])),
+                  topk=int(rng.integers(0, 80)), q_dtype=torch.bfloat16 if rng.random() < 0.7 else torch.float32,
+                  score="mean" if rng.random() < 0.25 else "quest",
+                  num_reserve=int(rng.choice([0, 0, 3, 17])), planted_per_unit=int(rng.integers(0, 6)))
+        cases.append(kw)
+    return cases
+
+
+RANDOM = _random_cases(20)
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM)))
+def test_random_problems_match_two_launches(i):
+    """Seeded random small problems (group size, head dim, block size, context length,
+    k, window, reserve set, scoring, query dtype): the fused step equals the two calls
+    bit for bit; every fourth is also checked against the oracle."""
+    w = Workload(**RANDOM[i])
+    inp = make_inputs(w, "cuda")
+    a, b = _pair(w, inp)
+    _run_both(w, inp, a, b, _q(inp))
+    _assert_same(a, b)
+    if i % 4 == 0:
+        compare_all(w, inp, b)
