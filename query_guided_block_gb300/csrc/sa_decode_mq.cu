@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kMqThreads, 2) decode_mq_kernel(MqArgs a)
 //       selected block and 64-channel half, written with the 128-byte swizzle by the
 //       tensor map and counted on the stage's mbarrier; a stage is refilled once the
 //       MMAs that read it have completed (a per-stage mbarrier);
-//   S(k) = Q K^T (warp 5, one thread)  tcgen05.mma (M = 128, N = 64, K = D) into tensor
+//   S(k) = Q K^T (warp 6, one thread)  tcgen05.mma (M = 128, N = 64, K = D) into tensor
 //       memory, three S buffers, issued two tiles ahead; A holds the 64 query rows twice
 //       (rows r and r + 64), so S lanes 64..127 repeat lanes 0..63;
 //   softmax (warps 0-3)  thread = (query row, half of the tile's columns): warps 0-1 take
@@ -406,16 +406,18 @@ __global__ void __launch_bounds__(kMqThreads, 2) decode_mq_kernel(MqArgs a)
 //       is rescaled in tensor memory, only when the running maximum grows by more than
 //       kLazy, so P <= 2^kLazy) and write P as bf16: hi in row r, the remainder lo in
 //       row r + 64 of one 128-row A tile;
-//   O += P V (warp 5)  tcgen05.mma (M = 128, N = D, K = 64), B = the V tile read
+//   O += P V (warp 5, one thread)  tcgen05.mma (M = 128, N = D, K = 64), B = the V tile read
 //       MN-major; O rows r and r + 64 hold the hi and lo products and add up at the end.
 //       Warp 5 also builds each tile's token-validity mask two tiles ahead and zeroes
 //       the V rows of tokens that are not selected (a box reads whole blocks).
-// Issue order per tile: O += P(k) V(k), then S(k + 2).  Every group completes on an
-// mbarrier (three for S, one for O, one per staging stage for loaded and for free) and
-// every wait is bounded; warps 0-3 and 5 meet once per tile, the loader never waits on
-// them.
+// The two MMA groups of a tile are issued by two threads at once (each commits its own
+// group): O += P(k) V(k) by warp 5 and S(k + 2) by warp 6; S(k) is complete before O(k)
+// is issued (the softmax waited for it), so O(k)'s completion frees the stage.  Every
+// group completes on an mbarrier (three for S, one for O, one per staging stage for
+// loaded and for free) and every wait is bounded; warps 0-3, 5 and 6 meet once per
+// tile, the loader never waits on them.
 constexpr float kLazy = 8.f;   // log2 growth of the row maximum before O is rescaled
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 
 template <int D>
 struct MqTcShape {
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, T, false);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
     static_assert(O_COL + D <= TMEM_COLS, "S and O must fit the allocation");
-    constexpr int LOADER = 4 * 32, ISSUER = 5 * 32;         // the two single-thread roles
+    constexpr int LOADER = 4 * 32, ISSUER = 5 * 32, ISSUER_S = 6 * 32;   // single-thread roles
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sp = blockIdx.x % a.nsplit;
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ntiles > 0) write_mask(0);
         if (ntiles > 1) write_mask(1);
     }
-    if (tid == ISSUER) {
+    if (tid == ISSUER_S) {
         for (int k = 0; k < 2 && k < ntiles; ++k) {
             wait_kv(k);
             issue_s(k);
@@ -717,7 +719,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 fence_proxy_async_smem();
             }
-        } else {
+        } else if (warp == 4) {
             // the loader: tile k + STAGES - 1 into the stage tile k - 1 used, once the
             // MMAs reading it are done
             if (tid == LOADER && k + STAGES - 1 < ntiles) {
@@ -728,15 +730,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             continue;   // the loader does not meet the others
         }
         tc_fence_before_sync();
-        named_barrier(3, kTcThreads - 32);   // warps 0-3 and 5
+        named_barrier(3, kTcThreads - 32);   // warps 0-3, 5 and 6
         tc_fence_after_sync();
-        if (tid == ISSUER) {   // O += P(k) V(k) first: the next softmax waits for it
+        if (tid == ISSUER) {
             wait_kv(k);        // already complete: the tensor core reads V(k) after this thread saw it land
             issue_o(k);
-            if (k + 2 < ntiles) {
-                wait_kv(k + 2);
-                issue_s(k + 2);
-            }
+        } else if (tid == ISSUER_S && k + 2 < ntiles) {
+            wait_kv(k + 2);
+            issue_s(k + 2);
         }
     }
     if (ntiles > 0 && !mbar_wait_bounded(&bar_o, uint32_t(ntiles - 1) & 1u, kWaitCycles))
