@@ -200,3 +200,31 @@ def test_random_problems_match_two_launches(i):
     _assert_same(a, b)
     if i % 4 == 0:
         compare_all(w, inp, b)
+
+
+def test_wide_candidate_set():
+    """6240 candidate blocks per unit (a 200K-token context of 32-token blocks): the
+    ranking's keys span 28 per thread; the step equals the two calls and the oracle."""
+    w = _w(batch=1, n_tokens=200000, block_size=32, window_tokens=300, topk=20, planted_per_unit=6)
+    inp = make_inputs(w, "cuda")
+    a, b = _pair(w, inp)
+    _run_both(w, inp, a, b, _q(inp))
+    _assert_same(a, b)
+    compare_all(w, inp, b)
+
+
+@pytest.mark.parametrize("levels", [1, 3], ids=["one_value", "three_values"])
+@pytest.mark.parametrize("score", ["quest", "mean"])
+def test_tied_scores_break_by_block_id(levels, score):
+    """Keys quantised to one or three values: many blocks share one bound or mean, and
+    the top-k takes the lowest block ids among equal scores (the ranking's tie and
+    gather paths), as the oracle does."""
+    w = _w(n_tokens=20000, block_size=32, topk=40, planted_per_unit=0, score=score)
+    inp = make_inputs(w, "cuda")
+    k = inp["k_pages"].float()
+    k = torch.full_like(k, 0.5) if levels == 1 else torch.clamp(torch.round(k), -1.0, 1.0)
+    inp["k_pages"] = k.to(inp["k_pages"].dtype)
+    a, b = _pair(w, inp)
+    _run_both(w, inp, a, b, _q(inp))
+    _assert_same(a, b)
+    compare_all(w, inp, b)
