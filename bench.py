@@ -23,7 +23,6 @@ import concurrent.futures as cf
 import dataclasses
 import hashlib
 import json
-import math
 import os
 import re
 import statistics

@@ -4,7 +4,6 @@ The oracle's LRU is fed the GPU's own selections, so a waived near-tie swap in o
 step cannot cascade into the cache comparison; every diff list, every count and the
 whole slot state are then compared bit for bit at every step.
 """
-import dataclasses
 
 import numpy as np
 import pytest

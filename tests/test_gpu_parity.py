@@ -16,8 +16,7 @@ import oracle
 from query_guided_block_gb300 import binding as B
 from query_guided_block_gb300.build import build
 from query_guided_block_gb300.decoder import SparseDecoder
-from query_guided_block_gb300.workloads import WORKLOADS, Workload, make_inputs, scaled
-from tests.conftest import oracle_problem_for
+from query_guided_block_gb300.workloads import WORKLOADS, Workload, make_inputs
 from tests.parity import (ATOL, as_np, bf16_bits_to_f64, check_selection, check_two_level,
                           oracle_meta, sub_problem, sub_workload)
 

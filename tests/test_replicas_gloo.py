@@ -4,7 +4,6 @@ an independent replica, so only the timing aggregation crosses ranks."""
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
