@@ -331,12 +331,22 @@ int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream s
  *   call (stream-ordered), but calls whose execution overlaps on the GPU -- on
  *   different streams, or from different host threads -- race on it and must be
  *   serialised by the caller.
- * - Device-side error bits of this call stay in the private array (select has no
- *   data-dependent indexing; only a timed-out copy wait could set one). */
+ * - Device-side error bits of a call stay in the private array (select has no
+ *   data-dependent indexing; only a timed-out copy wait could set one); read them
+ *   with sparse_attn_select_noalloc_device_error.
+ * - The cached address belongs to the device's context: after a cudaDeviceReset of
+ *   that device the process must not call this entry point again. */
 #define SPARSE_ATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
 int sparse_attn_select_noalloc(const sparse_attn_params* p, const void* q, const void* kmin,
                                const void* kmax, const float* kmean, int32_t* sel_ids,
                                int32_t* sel_count, sparse_attn_stream stream);
+
+/* Error word of sparse_attn_select_noalloc's private scratch on the current device:
+ * synchronise `stream`, copy the word to *flags (SPARSE_ATTN_ERR_* bits set by the
+ * noalloc calls since the last one started) and clear it.  Returns
+ * SPARSE_ATTN_DEVICE_BOUNDS when any bit was set.  Allocates nothing; the same
+ * first-call and no-overlap rules as sparse_attn_select_noalloc apply. */
+int sparse_attn_select_noalloc_device_error(sparse_attn_stream stream, uint32_t* flags);
 
 #ifdef __cplusplus
 }

@@ -99,6 +99,7 @@ def lib():
                                   vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_get_device_error": ([vp, sz, vp, u32p], C.c_int),
             "sparse_attn_select_noalloc": ([P, vp, vp, vp, vp, vp, vp, vp], C.c_int),
+            "sparse_attn_select_noalloc_device_error": ([vp, u32p], C.c_int),
             "sparse_attn_select_reserved": ([P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_topk_for_length": ([i32, i32], C.c_int32),
             "sparse_attn_slot_map": ([P, vp, vp, vp, i32, vp, vp, sz, vp], C.c_int),
@@ -120,7 +121,8 @@ def exported_symbols():
             "sparse_attn_get_device_error", "sparse_attn_select_noalloc",
             "sparse_attn_select_reserved", "sparse_attn_topk_for_length",
             "sparse_attn_slot_map", "sparse_attn_load_misses", "sparse_attn_decode_slots",
-            "sparse_attn_append_meta", "sparse_attn_step", "sparse_attn_step_launches"]
+            "sparse_attn_append_meta", "sparse_attn_step", "sparse_attn_step_launches",
+            "sparse_attn_select_noalloc_device_error"]
 
 
 def _status_string(status: int) -> str:
@@ -259,6 +261,16 @@ def sparse_attn_select_noalloc(p, q, kmin, kmax, kmean, sel_ids, sel_count, stre
     _check("sparse_attn_select_noalloc", lib().sparse_attn_select_noalloc(
         C.byref(p), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(kmean), _ptr(sel_ids), _ptr(sel_count),
         _stream(stream)))
+
+
+def sparse_attn_select_noalloc_device_error(stream=None) -> int:
+    """Error bits left in the noalloc scratch of the current device (synchronises the
+    stream, clears them); 0 = clean."""
+    flags = C.c_uint32(0)
+    st = lib().sparse_attn_select_noalloc_device_error(_stream(stream), C.byref(flags))
+    if st not in (OK, DEVICE_BOUNDS):
+        raise SparseAttnError("sparse_attn_select_noalloc_device_error", st)
+    return int(flags.value)
 
 
 def _host_or_cuda_ptr(t: torch.Tensor):

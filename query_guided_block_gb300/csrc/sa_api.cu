@@ -101,15 +101,15 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? SPARSE_ATTN_OK : SPARSE
 
 int num_sms()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];   // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 WorkspaceLayout workspace_layout(const Geometry& g)
@@ -505,24 +505,28 @@ int sparse_attn_decode_slots(const sparse_attn_params* p, const void* q, const v
 // looked up once per device (cudaGetSymbolAddress) with that device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SPARSE_ATTN_NOALLOC_SCRATCH_BYTES];
 
+// Two host threads making the first call on a device at once both look the address up
+// and store the same value (atomic slots, no data race).  The address belongs to the
+// device's current context: after a cudaDeviceReset the cached value is stale, so a
+// process that resets a device must not call sparse_attn_select_noalloc on it again.
 static void* noalloc_scratch_address(int* status)
 {
-    static void* cached[64] = {nullptr};
+    static std::atomic<void*> cached[64];   // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         *status = SPARSE_ATTN_CUDA_ERROR;
         return nullptr;
     }
-    if (cached[dev] == nullptr) {
-        void* ptr = nullptr;
+    void* ptr = cached[dev].load(std::memory_order_acquire);
+    if (ptr == nullptr) {
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
             *status = SPARSE_ATTN_CUDA_ERROR;
             return nullptr;
         }
-        cached[dev] = ptr;
+        cached[dev].store(ptr, std::memory_order_release);
     }
     *status = SPARSE_ATTN_OK;
-    return cached[dev];
+    return ptr;
 }
 
 int sparse_attn_select_noalloc(const sparse_attn_params* p, const void* q, const void* kmin,
@@ -554,6 +558,22 @@ int sparse_attn_select_noalloc(const sparse_attn_params* p, const void* q, const
     // error word and completion counters must start at zero; scores need no clearing
     if (cudaMemsetAsync(ws, 0, L.scores, s) != cudaSuccess) return SPARSE_ATTN_CUDA_ERROR;
     return status_of(launch_select(g, L, ws, q, kmin, kmax, kmean, nullptr, sel_ids, sel_count, s));
+}
+
+int sparse_attn_select_noalloc_device_error(sparse_attn_stream stream, uint32_t* flags)
+{
+    if (!flags) return SPARSE_ATTN_INVALID_ARG;
+    int st = SPARSE_ATTN_OK;
+    void* ws = noalloc_scratch_address(&st);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof word, s);
+    if (e != cudaSuccess) return SPARSE_ATTN_CUDA_ERROR;
+    *flags = word;
+    return word ? SPARSE_ATTN_DEVICE_BOUNDS : SPARSE_ATTN_OK;
 }
 
 }  // extern "C"

@@ -351,13 +351,12 @@ cudaError_t launch_decode_t(DecodeArgs a, cudaStream_t s)
     const size_t fixed = decode_fixed_smem(G, item_tokens);
     a.stages = (2 * (3 * stage + fixed + 1024) <= size_t(kSmemPerSm)) ? 3 : 2;
     const size_t smem = a.stages * stage + fixed;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, G>,
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(decode_kernel<D, BF16, G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemLimit);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    });
+    if (cfg != cudaSuccess) return cfg;
     const int per_sm = (2 * (smem + 1024) <= size_t(kSmemPerSm)) ? 2 : 1;
     long long ctas = (long long)num_sms() * per_sm;
     // every CTA's range must fit its shared-memory page cache
@@ -399,13 +398,12 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, uint32_t* ready, cudaStream_t s)
 {
     constexpr size_t smem = slab_smem_bytes<D>();
     static_assert(smem <= size_t(kDecSmemLimit), "slab rings must fit a CTA");
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kDecSmemLimit);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    });
+    if (cfg != cudaSuccess) return cfg;
     long long ctas = num_sms();                    // one CTA (8 independent warps) per SM
     const long long min_ctas = ((long long)a.total_items * a.blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
     if (ctas < min_ctas) ctas = min_ctas;

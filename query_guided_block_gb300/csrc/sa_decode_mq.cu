@@ -840,13 +840,12 @@ template <int D>
 cudaError_t launch_mq_tc_t(const MqArgs& a, int units, int num_pages, cudaStream_t s)
 {
     const size_t smem = MqTcShape<D>::SMEM;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(decode_mq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    });
+    if (cfg != cudaSuccess) return cfg;
     const int box_rows = a.bs < MqTcShape<D>::T ? a.bs : MqTcShape<D>::T;
     const long long rows = (long long)num_pages * a.Hkv * a.bs;
     CUtensorMap kmap, vmap;
@@ -863,13 +862,12 @@ cudaError_t launch_mq_t(const MqArgs& a, int units, cudaStream_t s)
 {
     constexpr int STAGE_BYTES = 2 * (D / 64) * kMqTile * kRowB;
     constexpr size_t smem = 1024 + size_t(kMqStages) * STAGE_BYTES + size_t(2) * kMqMaxBlocks * sizeof(int);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mq_kernel<D, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(decode_mq_kernel<D, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    });
+    if (cfg != cudaSuccess) return cfg;
     const unsigned grid = unsigned(size_t(units) * a.row_tiles * a.nsplit);
     return launch_after_previous(decode_mq_kernel<D, QSPLIT>, dim3(grid), dim3(kMqThreads), smem, s, a);
 }

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "sparse_attn.h"
 
 namespace sa {
@@ -57,6 +59,27 @@ WorkspaceLayout workspace_layout(const Geometry& g);
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
+
+// Runs a kernel's one-time host set-up (function attributes such as its dynamic
+// shared-memory limit) once for each device it is launched on: the attributes belong to
+// that device's context, so a process driving several GPUs sets each one up.  `done` is
+// a bit mask over device ordinals 0..63 (beyond that the set-up runs on every call).
+// Two host threads may both run `setup` for one device; it only sets attributes, so
+// that is harmless.  A cudaDeviceReset discards the attributes but not this mask: a
+// process that resets a device and then calls the library again gets launch errors.
+template <typename Setup>
+inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, Setup setup)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool tracked = dev >= 0 && dev < 64;
+    const unsigned long long bit = tracked ? (1ull << dev) : 0ull;
+    if (tracked && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess && tracked) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 constexpr int kSmemPerSm = 228 * 1024;
 
 // Selected blocks per decode work item, and whether a (D, dtype, block, group)

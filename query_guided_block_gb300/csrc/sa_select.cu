@@ -50,13 +50,12 @@ cudaError_t launch_select_warps_t(const SelectArgs& a0, int units, uint32_t* rea
     set_slab_chunking<KIND, MBF16, D>(a, units);
     const size_t keys = size_t(kSelThreads) * key_tile(a.n_cand) * sizeof(uint32_t);
     const size_t smem = WS::RING_BYTES > keys ? WS::RING_BYTES : keys;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(select_warps_kernel<KIND, MBF16, D>,
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(select_warps_kernel<KIND, MBF16, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(WS::RING_BYTES));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    });
+    if (cfg != cudaSuccess) return cfg;
     int ctas = num_sms();
     if (ctas > a.total_chunks) ctas = a.total_chunks;
     // a CTA records the units it completes in a fixed list
@@ -85,14 +84,13 @@ cudaError_t launch_select_t(const SelectArgs& a0, int units, uint32_t* ready, cu
     constexpr size_t kStatic = 13 * 1024;
     a.stages = (2 * (3 * size_t(kStageBytes) + keys_bytes + kStatic) <= size_t(kSmemPerSm)) ? 3 : 2;
     const size_t smem = size_t(a.stages) * kStageBytes + keys_bytes;
-    static bool configured = false;   // once per instantiation, before any graph capture
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(select_kernel<KIND, MBF16, D>,
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(select_kernel<KIND, MBF16, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(2 * kStageBytes + kMaxSelectKeys * sizeof(uint32_t)));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    });
+    if (cfg != cudaSuccess) return cfg;
     const int per_sm = (2 * (smem + kStatic) <= size_t(kSmemPerSm)) ? 2 : 1;
     int ctas = num_sms() * per_sm;
     if (ctas > a.total_chunks) ctas = a.total_chunks;
@@ -317,14 +315,13 @@ cudaError_t launch_two_level_t(const SelectArgs& l1, const SelectArgs& l2, int u
 {
     const int n = l1.n_cand > l2.n_cand ? l1.n_cand : l2.n_cand;
     const size_t smem = size_t(kSelThreads) * key_tile(n) * sizeof(uint32_t);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(select_two_level_kernel<MBF16, D>,
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(select_two_level_kernel<MBF16, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(kMaxSelectKeys * sizeof(uint32_t)));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    });
+    if (cfg != cudaSuccess) return cfg;
     return launch_after_previous(select_two_level_kernel<MBF16, D>, dim3(unsigned(units)), dim3(kSelThreads), smem,
                                  s, l1, l2);
 }

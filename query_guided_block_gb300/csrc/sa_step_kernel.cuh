@@ -28,16 +28,17 @@ cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, uint3
                       smem >= kMaxSelectKeys * sizeof(uint32_t),
                   "select rings and keys must fit the decode rings");
     auto kernel = step_kernel<KIND, D, G, QSPLIT>;
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t set_up = once_per_device(configured, [&]() -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDecThreads, smem);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorNotSupported;
-        configured = true;
-    }
+        return cudaSuccess;
+    });
+    if (set_up != cudaSuccess) return set_up;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(ctas));
     cfg.blockDim = dim3(kDecThreads);

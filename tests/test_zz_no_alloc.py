@@ -57,6 +57,8 @@ def test_noalloc_select_matches_workspace_select_twice(name, batch):
         for u in range(w.units):
             n = int(cnt.view(-1)[u])
             assert torch.equal(ids.view(w.units, -1)[u, :n], dec.sel_ids.view(w.units, -1)[u, :n])
+        # the private scratch's error word: clean calls leave no bit set
+        assert B.sparse_attn_select_noalloc_device_error() == 0
 
 
 def test_noalloc_select_rejects_what_does_not_fit():
