@@ -476,6 +476,17 @@ def run_gpu_arm(args):
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inp, dev, args.cpu_seconds)
 
+    # the other single-GPU workloads, measured in this process after the headline
+    other = None
+    if args.other_workloads and args.workload == DEFAULT_WORKLOAD and not args.batch and not io:
+        del inp, dec, cache
+        kp = vp = bt = q_all = q_static = None
+        torch.cuda.empty_cache()
+        other = {}
+        for name in OTHER_WORKLOADS:
+            other[name] = measure_other_workload(name, dev, args.other_steps, max(3, min(args.warmup, 10)),
+                                                 flush, peak)
+
     result = {
         "metric": METRIC,
         "value": value,
@@ -512,11 +523,83 @@ def run_gpu_arm(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "other_workloads": other,
     }
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------- other workloads --
+
+OTHER_WORKLOADS = ("mha_32k", "two_level_256k", "lru_64k")
+
+
+def measure_other_workload(name, dev, steps, warmup, flush, peak):
+    """One more workload timed the way the headline is (L2 flushed before every step,
+    CUDA events around the step on the launching stream): the step a user calls
+    (sparse_attn_step where it covers the problem, else select + decode), plus the
+    diff against the LRU slot cache for the multi-step workload."""
+    from query_guided_block_gb300 import binding as Bn
+    from query_guided_block_gb300.decoder import SlotCache, SparseDecoder
+    from query_guided_block_gb300.workloads import WORKLOADS, make_inputs
+
+    w = WORKLOADS[name]
+    inp = make_inputs(w, dev)
+    p = Bn.params_for(w)
+    dec = SparseDecoder(p, dev)
+    kp, vp, bt = inp["k_pages"], inp["v_pages"], inp["block_table"]
+    dec.build_meta(kp, bt)
+    cache = SlotCache(dec, w.cache_slots) if w.cache_slots else None
+    q_all = inp["q"] if inp["q"].dim() == 4 else inp["q"].unsqueeze(0)
+    launches = Bn.sparse_attn_step_launches(p)
+    use_step = launches > 0
+    stream = torch.cuda.current_stream()
+    counter = [0]
+
+    def one_step(q):
+        if use_step:
+            dec.step_fused(q, kp, vp, bt)
+        else:
+            dec.select(q)
+            dec.decode(q, kp, vp, bt)
+        if cache:
+            cache.diff(counter[0])
+            cache.advance()
+        counter[0] += 1
+
+    for i in range(warmup):
+        one_step(q_all[i % q_all.shape[0]])
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (a, b) in enumerate(ev):
+        flush.zero_()
+        a.record(stream)
+        one_step(q_all[(warmup + i) % q_all.shape[0]])
+        b.record(stream)
+    torch.cuda.synchronize()
+    flags = dec.device_error()
+    if flags:
+        raise RuntimeError(f"{name}: device error flags 0x{flags:x}")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = algorithmic_bytes(w, dec.sel_count, dec.sel_ids)
+    step_bytes = nbytes["select"] + nbytes["decode"]
+    gbs = step_bytes / ms / 1e6
+    per_step = (f"sparse_attn_step ({launches} launch{'es' if launches > 1 else ''})" if use_step
+                else "sparse_attn_select + sparse_attn_decode") + (" + sparse_attn_diff" if cache else "")
+    out = {"ms_per_step": ms, "value": w.batch * w.num_q_heads / (ms / 1e3), "unit": "queries/s",
+           "steps": steps, "warmup": warmup, "step": per_step, "step_bytes": step_bytes,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
+           "config": {"batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                      "head_dim": w.head_dim, "context": w.n_tokens, "block_size": w.block_size,
+                      "topk_blocks": w.topk, "window_tokens": w.window_tokens, "two_level": w.two_level,
+                      "cache_slots": w.cache_slots},
+           "gpu_launches": (launches if use_step else (3 if w.two_level else 2)) * steps +
+                           (steps if cache else 0)}
+    del inp, dec, cache
+    torch.cuda.empty_cache()
+    return out
 
 
 # -------------------------------------------------------------- CPU arms --
@@ -643,6 +726,9 @@ def main():
                     help="LRU workloads: K/V read through the slot pool, misses loaded each step "
                          "from a pinned host store")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
+                    help="skip timing mha_32k, two_level_256k and lru_64k after the headline")
+    ap.add_argument("--other-steps", type=int, default=200)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

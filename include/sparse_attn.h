@@ -153,6 +153,18 @@ int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes);
  * allocating a workspace, before its first use. */
 int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream stream);
 
+/* Limit, in SM clock cycles, of every bounded wait of the kernels run on this
+ * workspace: the copy and tensor-core completion waits and the fused step's wait for
+ * a unit's published selection.  0 (the value sparse_attn_workspace_init leaves)
+ * selects the default of 2e9 cycles, about one second at GB300 clocks; larger values
+ * are capped at it.  A wait that runs out sets SPARSE_ATTN_ERR_TIMEOUT in the error
+ * word and the kernel goes on and returns, so the context stays usable; results of
+ * that call are then unspecified (finite), and later calls are unaffected.
+ * Stream-ordered; copies 8 bytes from host memory, so it cannot be captured into a
+ * CUDA graph.  No counterpart in the pages: it exists to bound and to test the waits. */
+int sparse_attn_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t cycles,
+                                         sparse_attn_stream stream);
+
 /* Per-block metadata from the paged keys.
  * Defines: Quest key bounding box -- for each unit, block j and channel d,
  *   kmin[j][d] = min_t K[t][d], kmax[j][d] = max_t K[t][d] over the block's tokens

@@ -12,6 +12,6 @@ from .binding import (SparseAttnError, make_params, params_for,  # noqa: F401
                       sparse_attn_select_noalloc, sparse_attn_select_noalloc_device_error,
                       sparse_attn_select_reserved, sparse_attn_sel_stride,
                       sparse_attn_slot_map, sparse_attn_step, sparse_attn_step_launches,
-                      sparse_attn_topk_for_length, sparse_attn_workspace_init,
+                      sparse_attn_topk_for_length, sparse_attn_workspace_init, sparse_attn_workspace_set_wait_limit,
                       sparse_attn_workspace_size)
 from .decoder import SlotCache, SparseDecoder  # noqa: F401

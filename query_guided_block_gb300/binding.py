@@ -89,6 +89,7 @@ def lib():
             "sparse_attn_sel_stride": ([P], C.c_int32),
             "sparse_attn_workspace_size": ([P, C.POINTER(C.c_size_t)], C.c_int),
             "sparse_attn_workspace_init": ([vp, sz, vp], C.c_int),
+            "sparse_attn_workspace_set_wait_limit": ([vp, sz, C.c_uint64, vp], C.c_int),
             "sparse_attn_build_meta": ([P, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_append_meta": ([P, i32, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_select": ([P, vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
@@ -122,7 +123,7 @@ def exported_symbols():
             "sparse_attn_select_reserved", "sparse_attn_topk_for_length",
             "sparse_attn_slot_map", "sparse_attn_load_misses", "sparse_attn_decode_slots",
             "sparse_attn_append_meta", "sparse_attn_step", "sparse_attn_step_launches",
-            "sparse_attn_select_noalloc_device_error"]
+            "sparse_attn_select_noalloc_device_error", "sparse_attn_workspace_set_wait_limit"]
 
 
 def _status_string(status: int) -> str:
@@ -182,6 +183,13 @@ def sparse_attn_workspace_size(p: sparse_attn_params) -> int:
 def sparse_attn_workspace_init(ws: torch.Tensor, stream=None) -> None:
     _check("sparse_attn_workspace_init",
            lib().sparse_attn_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sparse_attn_workspace_set_wait_limit(ws: torch.Tensor, cycles: int, stream=None) -> None:
+    """Limit (SM clock cycles) of the bounded waits of kernels run on `ws`; 0 = default."""
+    _check("sparse_attn_workspace_set_wait_limit",
+           lib().sparse_attn_workspace_set_wait_limit(_ptr(ws), ws.numel() * ws.element_size(), int(cycles),
+                                                      _stream(stream)))
 
 
 def sparse_attn_build_meta(p, k_pages, block_table, kmin, kmax, kmean, ws, stream=None) -> None:

@@ -129,7 +129,8 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     const size_t dec_cells = units * size_t(g.Q > 1 ? mq_row_tiles(g.Q, g.G) : 1);
 
     size_t off = 0;
-    // one 256-byte header: error word and the persistent kernels' work counters
+    // one 256-byte header: error word, the persistent kernels' work counters, the wait
+    // limit (bytes 24-31) and the fused step's epoch and completion count (32-39)
     L.err = 0;
     L.sel_work = 4;
     L.sel_done = 8;
@@ -214,6 +215,15 @@ int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream str
 {
     if (!ws || !aligned(ws, 256) || ws_bytes < 256) return SPARSE_ATTN_INVALID_ARG;
     return status_of(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sparse_attn_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t cycles, sparse_attn_stream stream)
+{
+    if (!ws || !aligned(ws, 256) || ws_bytes < 256) return SPARSE_ATTN_INVALID_ARG;
+    // pageable source: the runtime stages the 8 bytes before returning
+    const unsigned long long v = cycles;
+    return status_of(cudaMemcpyAsync(static_cast<char*>(ws) + kHdrWaitLimitByte, &v, sizeof v,
+                                     cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 static int meta_common(const sparse_attn_params* p, int32_t first_token, const void* k_pages,

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sa_internal.h"
 #include "sparse_attn.h"
 
 namespace sa {
@@ -333,6 +334,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 // About one second at GB300 clocks: far beyond any legitimate copy latency.
 constexpr long long kWaitCycles = 2000000000LL;
 
+
 // Device-scope flag hand-off between CTAs of one grid: the writer publishes with a
 // release store (after a fence that covers its CTA's writes), the reader polls with
 // acquire loads.
@@ -358,6 +360,51 @@ __device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t
         __nanosleep(32);
     }
     return true;
+}
+
+// Workspace header words (byte offsets from the workspace base; the error word is at 0).
+constexpr int kHdrWaitLimit = int(kHdrWaitLimitByte);   // uint64: wait limit in SM clocks, 0 = kWaitCycles
+constexpr int kHdrStepEpoch = 32;   // uint32: fused steps completed on this workspace
+constexpr int kHdrStepDone = 36;    // uint32: CTAs of the running step that have finished
+
+__device__ __forceinline__ uint32_t* header_word(uint32_t* err, int byte)
+{
+    return reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(err) + byte);
+}
+
+// The wait limit of every bounded wait of a kernel, read once from the workspace header
+// (`err` is the workspace base).  0 selects kWaitCycles; larger values are capped at it.
+__device__ __forceinline__ long long wait_limit(const uint32_t* err)
+{
+    const unsigned long long v =
+        __ldcg(reinterpret_cast<const unsigned long long*>(reinterpret_cast<const char*>(err) + kHdrWaitLimit));
+    return (v == 0 || v > (unsigned long long)kWaitCycles) ? kWaitCycles : (long long)v;
+}
+
+// Per-unit hand-off of the fused step.  A step numbered E + 1 (E = the epoch word when
+// it starts) publishes unit u's selection by storing E + 1 in ready[u]; its decode waits
+// for that value.  Flags left by an earlier step (E or less, even one written late by a
+// step whose waits ran out) never match, so no flag ever needs clearing.  The value 0
+// (a fresh workspace) is skipped when the counter wraps.
+__device__ __forceinline__ uint32_t step_flag_value(uint32_t* err)
+{
+    const uint32_t next = ld_acquire_gpu(header_word(err, kHdrStepEpoch)) + 1u;
+    return next == 0u ? 1u : next;
+}
+
+// The end of one CTA's share of a step: the last CTA of the grid to finish stores the
+// step's number as the new epoch (after a kernel boundary every later step sees it).
+__device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        uint32_t* done = header_word(err, kHdrStepDone);
+        if (atomic_add_acq_rel_u32(done, 1u) + 1u == gridDim.x) {
+            *done = 0u;
+            st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
+        }
+    }
 }
 
 // exp2 on the special-function unit (PTX ex2.approx.ftz.f32; about 2 ulp).

@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
     const int u_hi = (i_end - 1) / a.items_per_unit;
     allow_dependents_early();
     grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+    const long long wait_cycles = wait_limit(a.err);
 
     // ---- resolve the range: counts, selected ids -> pages ---------------------
     for (int u = u_lo + tid; u <= u_hi; u += kDecThreads) {
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
         }
         const unsigned char* ks = smem + s * stage_bytes;
         const unsigned char* vs = ks + size_t(item_tokens) * S::ROW_BYTES;
-        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+        if (!mbar_wait_bounded(&full[s], parity, wait_cycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
 
         // ---- S = q K^T over the item's tokens -------------------------------
         for (int t_base = 0; t_base < item_tokens; t_base += S::ROWS_PER_BATCH) {
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
             bool mine = false;
             for (int i = 0; i < 2 * bpi; ++i) mine |= (s * 2 * bpi + i) % kDecWarps == warp;
             if (nxt < i_end && mine) {
-                if (!mbar_wait_bounded(&empty[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+                if (!mbar_wait_bounded(&empty[s], parity, wait_cycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
                 issue_mine(nxt);
             }
         }
@@ -389,8 +390,15 @@ template <int D, int G, bool QSPLIT>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a, uint32_t* ready)
 {
     allow_dependents_early();
-    if (ready == nullptr) grid_dependency_wait();   // inputs and workspace may come from the previous kernel
-    decode_mma_body<D, G, QSPLIT>(a, ready);
+    if (ready == nullptr) {
+        grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+        decode_mma_body<D, G, QSPLIT>(a, nullptr, 0u);
+        return;
+    }
+    // behind the step's select kernel: the same flag value as it publishes
+    const uint32_t flag_value = step_flag_value(a.err);
+    decode_mma_body<D, G, QSPLIT>(a, ready, flag_value);
+    finish_step(a.err, flag_value);
 }
 
 template <int D, int G, bool QSPLIT>

@@ -185,11 +185,11 @@ constexpr size_t slab_smem_bytes()
 }
 
 // One CTA's share of a decode launch (CTA blockIdx.x of gridDim.x).  With `ready`
-// set, the CTA first waits (bounded) until ready[u] == 1 for every unit of its range
-// (the selection may still be running in this grid or in the select kernel before
-// this one), and the CTA merging a unit clears ready[u] afterwards.
+// set, the CTA first waits (bounded) until ready[u] == flag_value for every unit of its
+// range (the selection may still be running in this grid or in the select kernel
+// before this one).
 template <int D, int G, bool QSPLIT>
-__device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* ready)
+__device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* ready, uint32_t flag_value)
 {
     using SS = SlabShape<D>;
     constexpr int S = SS::STAGES;
@@ -248,8 +248,9 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
         }
     };
     if (ready != nullptr) {   // selections published by other CTAs (acquire)
+        const long long wait_cycles = wait_limit(a.err);
         for (int u = u_lo + tid; u <= u_hi; u += kDecThreads)
-            if (!wait_flag_bounded(ready + u, 1u, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+            if (!wait_flag_bounded(ready + u, flag_value, wait_cycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
         __threadfence();
         __syncthreads();
     }
@@ -469,7 +470,6 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
         __syncthreads();
         if (s_merge_unit >= 0) {
             merge_unit(a, u, G, D);
-            if (ready != nullptr && tid == 0) ready[u] = 0u;   // every reader of it has reported
             __syncthreads();
         }
     }

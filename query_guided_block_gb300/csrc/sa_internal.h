@@ -34,7 +34,7 @@ struct Geometry {
 
 // Workspace carve-up (byte offsets from the workspace base, each 256-byte aligned).
 struct WorkspaceLayout {
-    size_t err;            // uint32 error word
+    size_t err;            // uint32 error word (header words: see sa_common.cuh kHdr*)
     size_t sel_work;       // uint32 next chunk id (select kernels)
     size_t sel_done;       // uint32 finished CTAs (select kernels)
     size_t dec_work;       // uint32 next work item (decode)
@@ -56,6 +56,10 @@ struct WorkspaceLayout {
 };
 
 WorkspaceLayout workspace_layout(const Geometry& g);
+
+// Byte offset of the wait-limit word in the workspace header (kHdrWaitLimit on the
+// device side).
+constexpr size_t kHdrWaitLimitByte = 24;
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();

@@ -426,10 +426,11 @@ __device__ __forceinline__ ChunkInfo chunk_info(const SelectArgs& a, int cid, in
 
 // One CTA's share of a select launch: CTA blockIdx.x of gridDim.x streams its
 // contiguous range of chunks; the CTA completing a unit ranks and emits it.  With
-// `ready` set, that CTA then publishes ready[u] = 1 (release) once the unit's ids and
-// count are written, for consumers in the same grid.
+// `ready` set, that CTA then publishes the step's flag value in ready[u] (release) once
+// the unit's ids and count are written, for a decode in the same grid or in the kernel
+// launched after this one.  Returns that value (0 without `ready`).
 template <int KIND, bool MBF16, int D>
-__device__ __forceinline__ void select_body(const SelectArgs& a, uint32_t* ready)
+__device__ __forceinline__ uint32_t select_body(const SelectArgs& a, uint32_t* ready)
 {
     using SS = SelectShape<KIND, MBF16, D>;
     constexpr int EPL = SS::EPL, LPR = SS::LPR, RPW = SS::RPW, ROWS = SS::ROWS, R = SS::R;
@@ -474,6 +475,10 @@ __device__ __forceinline__ void select_body(const SelectArgs& a, uint32_t* ready
         fence_mbar_init();
     }
     grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+    // the step's flag value, read before any dependent kernel may start (that kernel
+    // reads the same epoch word, which only a finishing step changes)
+    const uint32_t flag_value = ready != nullptr ? step_flag_value(a.err) : 0u;
+    const long long wait_cycles = wait_limit(a.err);
     // Only now may a dependent kernel start: whatever ran before this one has finished,
     // so a dependent that skips its own wait (waiting on ready flags instead) still
     // sees every earlier write.
@@ -527,7 +532,7 @@ __device__ __forceinline__ void select_body(const SelectArgs& a, uint32_t* ready
                 cn[e] = sn;
             }
         }
-        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+        if (!mbar_wait_bounded(&full[s], parity, wait_cycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
 
         // R rows per lane group, partial dots summed over the group's LPR lanes at once
         const unsigned char* hi = smem + s * kStageBytes + d0 * SS::ESZ;
@@ -585,11 +590,12 @@ __device__ __forceinline__ void select_body(const SelectArgs& a, uint32_t* ready
                 __syncthreads();
                 if (ready != nullptr && tid == 0) {
                     __threadfence();
-                    st_release_gpu(&ready[tu], 1u);
+                    st_release_gpu(&ready[tu], flag_value);
                 }
             }
         }
     }
+    return flag_value;
 }
 
 
@@ -620,7 +626,7 @@ struct SlabSelShape {
 };
 
 template <int KIND, bool MBF16, int D>
-__device__ __forceinline__ void select_body_warps(const SelectArgs& a, uint32_t* ready)
+__device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint32_t* ready)
 {
     using SS = SelectShape<KIND, MBF16, D>;
     using WS = SlabSelShape<KIND, MBF16, D>;
@@ -643,6 +649,7 @@ __device__ __forceinline__ void select_body_warps(const SelectArgs& a, uint32_t*
 
     if (tid == 0) s_ndone = 0;
     grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+    const uint32_t flag_value = ready != nullptr ? step_flag_value(a.err) : 0u;   // see select_body
     allow_dependents_early();
 
     // Query coefficients of the first kSlabSelCoefUnits units of the range, summed by
@@ -844,9 +851,10 @@ __device__ __forceinline__ void select_body_warps(const SelectArgs& a, uint32_t*
         __syncthreads();
         if (ready != nullptr && tid == 0) {
             __threadfence();
-            st_release_gpu(&ready[u], 1u);
+            st_release_gpu(&ready[u], flag_value);
         }
     }
+    return flag_value;
 }
 
 // Arguments common to every select launch of a problem.

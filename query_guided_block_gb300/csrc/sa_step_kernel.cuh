@@ -14,9 +14,10 @@ static_assert(kSelThreads == kDecThreads, "both phases run on the same CTA shape
 template <int KIND, int D, int G, bool QSPLIT>
 __global__ void __launch_bounds__(kDecThreads, 1) step_kernel(SelectArgs sa_args, DecodeArgs da, uint32_t* ready)
 {
-    select_body_warps<KIND, KIND == KIND_QUEST, D>(sa_args, ready);
+    const uint32_t flag_value = select_body_warps<KIND, KIND == KIND_QUEST, D>(sa_args, ready);
     __syncthreads();   // select's rings and keys are reused as the decode rings
-    decode_mma_body<D, G, QSPLIT>(da, ready);
+    decode_mma_body<D, G, QSPLIT>(da, ready, flag_value);
+    finish_step(da.err, flag_value);
 }
 
 template <int KIND, int D, int G, bool QSPLIT>

@@ -98,6 +98,10 @@ class SparseDecoder:
     def device_error(self, stream=None) -> int:
         return B.sparse_attn_get_device_error(self.ws, stream)
 
+    def set_wait_limit(self, cycles: int, stream=None):
+        """Bounded-wait limit of this decoder's kernels (SM clocks; 0 = the default)."""
+        B.sparse_attn_workspace_set_wait_limit(self.ws, cycles, stream)
+
 
 class SlotCache:
     """LRU slot-cache state and per-step diff outputs for ``sparse_attn_diff``."""

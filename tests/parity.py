@@ -95,6 +95,60 @@ def check_two_level(w, p, host_q, kmin, kmax, kmean, gpu_ids, gpu_cnt, units, re
         assert ok, f"unit {u}: {last_err}"
 
 
+U32 = 2.0 ** -24          # unit roundoff of IEEE binary32 (round to nearest)
+
+
+def _gamma(m):
+    """gamma_m = m u / (1 - m u): the classical bound on the relative error of m
+    chained fp32 roundings (Higham, Accuracy and Stability of Numerical Algorithms,
+    ch. 3)."""
+    m = np.asarray(m, np.float64)
+    return m * U32 / (1.0 - m * U32)
+
+
+def abs_row_sums(host, w, mean_block):
+    """Per (sequence, KV head, mean row, channel): the number of tokens n_r of the row
+    and sum_t |k_t,d| over them, from the host keys of a gathered instance (pages in
+    logical order).  Returned as float64 arrays [S, Hkv, rows, D] and [rows]."""
+    bt = host["block_table"]
+    S, nb = bt.shape
+    Hkv, bs, D, N = w.num_kv_heads, w.block_size, w.head_dim, w.n_tokens
+    rows = -(-N // mean_block)
+    out = np.empty((S, Hkv, rows, D), np.float64)
+    for s in range(S):   # one sequence at a time keeps the temporaries small
+        k = host["k_pages"][s * nb:(s + 1) * nb].float().abs()          # [nb, Hkv, bs, D]
+        k = k.permute(1, 0, 2, 3).reshape(Hkv, nb * bs, D)[:, :N]
+        pad = rows * mean_block - N
+        if pad:
+            k = torch.cat([k, k.new_zeros(Hkv, pad, D)], 1)
+        out[s] = k.view(Hkv, rows, mean_block, D).double().sum(2).numpy()
+    n = np.minimum(mean_block, N - np.arange(rows) * mean_block).astype(np.float64)
+    return out, n
+
+
+def check_means(gpu_mean, ora_mean, host, w, mean_block):
+    """Block means from fp32 accumulation against the fp64 oracle, within the bound
+    that fp32 arithmetic guarantees.  The kernel forms s = fl(sum_t k_t) over the n
+    tokens of a row in some order of n - 1 additions, then fl(s * fl(1/n)).  Whatever
+    the summation tree, each key passes through at most n - 1 roundings, so
+    |s - S| <= gamma_{n-1} sum_t |k_t| (Higham, ch. 4), and the
+    reciprocal and the product add one rounding each, so
+        |mean_gpu - S/n| <= (1+u)^2 gamma_{n-1} sum|k| / n + (2u + u^2) |S/n|.
+    The bound is taken from the actual keys of each row and channel (x 1.001 for the
+    fp64 evaluation of the bound itself).  For N(0,1) keys and n = 1024 it is about
+    5e-5 per element, against the 1e-4 that a fixed tolerance allowed."""
+    sabs, n = abs_row_sums(host, w, mean_block)
+    ora = np.asarray(ora_mean, np.float64)
+    gpu = np.asarray(gpu_mean, np.float64)[:, :, : ora.shape[2]]
+    tol = ((1 + U32) ** 2 * _gamma(n - 1)[None, None, :, None] * sabs / n[None, None, :, None]
+           + (2 * U32 + U32 * U32) * np.abs(ora)) * 1.001
+    err = np.abs(gpu - ora)
+    bad = err > tol
+    assert not bad.any(), (f"{int(bad.sum())} block means outside the fp32 bound; worst excess "
+                           f"{float((err - tol).max()):.3e} at {np.unravel_index(np.argmax(err - tol), err.shape)}")
+    return float(err.max())
+
+
 def as_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
 

@@ -2,6 +2,8 @@
 checks: the access is skipped, a bit is set in the workspace error word, and the
 context stays usable.  Every input here is one the kernels check before use; nothing
 is expected to fault."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -119,3 +121,48 @@ def test_tensor_core_multi_query_decode_reports_bad_inputs():
     dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"])
     assert dec.device_error() == 0
     assert torch.isfinite(dec.out).all()
+
+
+def test_bounded_wait_runs_out_and_the_next_step_is_clean():
+    """The fused step's decode phase waits, per unit, for the selection another CTA
+    publishes.  With a limit of 64 cycles the CTAs that rank nothing poll their units
+    while the rankers are still at work, so the wait runs out: the call returns
+    promptly, the error word holds SPARSE_ATTN_ERR_TIMEOUT and the output is finite.
+    With the default limit restored, the next step on the same workspace (new queries)
+    equals the two-call result bit for bit: a selection published late by the
+    timed-out step is never taken for the next step's."""
+    from tests.test_gpu_step import _assert_same
+    w = Workload(name="timeout", batch=4, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                 n_tokens=65536, block_size=32, window_tokens=512, topk=64, planted_per_unit=8)
+    inp = make_inputs(w, "cuda")
+    p = B.params_for(w)
+    assert B.sparse_attn_step_launches(p) == 1
+    two, fused = SparseDecoder(p), SparseDecoder(p)
+    for d in (two, fused):
+        d.build_meta(inp["k_pages"], inp["block_table"])
+    kv = (inp["k_pages"], inp["v_pages"], inp["block_table"])
+    fused.step_fused(inp["q"], *kv)
+    assert fused.device_error() == 0              # valid selections in place
+    fused.set_wait_limit(64)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    new_q = lambda: torch.randn(inp["q"].shape, generator=g, device="cuda").to(w.q_dtype)
+    timed_out = False
+    for _ in range(4):
+        fused.out.fill_(float("nan"))
+        t0 = time.time()
+        fused.step_fused(new_q(), *kv)
+        flags = fused.device_error()               # synchronises
+        assert time.time() - t0 < 2.0
+        assert flags & ~B.ERR_TIMEOUT == 0, f"flags 0x{flags:x}"
+        assert torch.isfinite(fused.out).all()
+        if flags & B.ERR_TIMEOUT:
+            timed_out = True
+            break
+    assert timed_out, "no wait ran out with a 64-cycle limit"
+    fused.set_wait_limit(0)
+    for _ in range(2):
+        q = new_q()
+        two.step(q, *kv)
+        fused.step_fused(q, *kv)
+        assert two.device_error() == 0 and fused.device_error() == 0
+        _assert_same(two, fused)

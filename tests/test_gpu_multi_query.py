@@ -13,6 +13,7 @@ from query_guided_block_gb300.build import build
 from query_guided_block_gb300.decoder import SparseDecoder
 from query_guided_block_gb300.workloads import WORKLOADS, Workload, make_inputs
 from tests.parity import ATOL, as_np, check_selection, oracle_meta, sub_problem, sub_workload
+from tests.test_gpu_parity import compare_every_unit
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +33,7 @@ def _w(**kw):
     return Workload(**base)
 
 
-def run_and_compare(w, seqs=None):
+def run_and_compare(w, every_unit_threads=False):
     inp = make_inputs(w, "cuda")
     dec = SparseDecoder(B.params_for(w))
     dec.build_meta(inp["k_pages"], inp["block_table"])
@@ -40,7 +41,16 @@ def run_and_compare(w, seqs=None):
     dec.decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["block_table"])
     assert dec.device_error() == 0
     assert tuple(dec.out.shape) == (w.batch, w.num_queries, w.num_q_heads, w.head_dim)
+    if every_unit_threads:
+        compare_every_unit(w, inp, dec, check=check_sequences)
+    else:
+        check_sequences(w, inp, dec)
+    return dec
 
+
+def check_sequences(w, inp, dec, seqs=None):
+    """Selection and every query's attention output of sequences `seqs` (all by
+    default) against the oracle.  Returns the worst attention error."""
     seqs = list(range(w.batch)) if seqs is None else list(seqs)
     host = sub_problem(w, inp, seqs)
     ws = sub_workload(w, len(seqs))
@@ -59,7 +69,7 @@ def run_and_compare(w, seqs=None):
                             host["block_table"], gids, gcnt)
         worst = max(worst, float(np.abs(got[:, t] - ref).max()))
     assert worst <= ATOL[w.kv_dtype], f"max abs error {worst}"
-    return dec
+    return worst
 
 
 @pytest.mark.parametrize("cfg", [
@@ -77,9 +87,9 @@ def test_multi_query_small(cfg):
     run_and_compare(_w(**cfg))
 
 
-def test_multi_query_full_size_sampled():
+def test_multi_query_full_size_every_unit():
     """mq_128k (B16, 131072 tokens, 16 queries x 4 heads per KV head) in the launch
-    configuration the benchmark times; first and last sequences checked in full."""
+    configuration the benchmark times; every sequence checked in full."""
     w = WORKLOADS["mq_128k"]
-    run_and_compare(w, seqs=[0, w.batch - 1])
+    run_and_compare(w, every_unit_threads=True)
     torch.cuda.empty_cache()

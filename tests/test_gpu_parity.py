@@ -4,9 +4,12 @@ Tolerances (from the problem statement): selected ids, diff / LRU outputs and th
 min/max bounding box are bit-exact (selection up to swaps among candidates whose
 oracle scores lie within 1e-5 relative of the k-th score); attention output within
 2e-3 max-abs for bf16 KV and 1e-5 for fp32 KV; block means (fp32 accumulation vs fp64)
-within 1e-4.
+within the error bound of fp32 summation over the row's tokens (tests.parity.check_means),
+and exact on keys whose fp32 sums are exact.
 """
+import concurrent.futures as cf
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -17,7 +20,7 @@ from query_guided_block_gb300 import binding as B
 from query_guided_block_gb300.build import build
 from query_guided_block_gb300.decoder import SparseDecoder
 from query_guided_block_gb300.workloads import WORKLOADS, Workload, make_inputs
-from tests.parity import (ATOL, as_np, bf16_bits_to_f64, check_selection, check_two_level,
+from tests.parity import (ATOL, as_np, bf16_bits_to_f64, check_means, check_selection, check_two_level,
                           oracle_meta, sub_problem, sub_workload)
 
 pytestmark = pytest.mark.gpu
@@ -55,7 +58,8 @@ def compare_all(w, inp, dec, seqs=None):
     gmax = bf16_bits_to_f64(dec.kmax[seqs])
     assert np.array_equal(gmin, kmin) and np.array_equal(gmax, kmax)
     if kmean is not None:
-        np.testing.assert_allclose(as_np(dec.kmean[seqs]).astype(np.float64), kmean, rtol=0, atol=1e-4)
+        check_means(as_np(dec.kmean[seqs]), kmean, host, ws,
+                    w.coarse_block if w.two_level else w.block_size)
     gids = as_np(dec.sel_ids).reshape(w.units, -1)[rows]
     gcnt = as_np(dec.sel_count).reshape(-1)[rows]
     hq = host["q"] if host["q"].dim() == 3 else host["q"][0]
@@ -78,6 +82,24 @@ def compare_all(w, inp, dec, seqs=None):
     err = np.abs(got - out).max() if out.size else 0.0
     assert err <= ATOL[w.kv_dtype], f"max abs error {err}"
     return err
+
+
+def seq_chunks(batch, threads=None):
+    """Sequences cut into about four chunks per host thread (at least one sequence each)."""
+    threads = threads or max(1, min(8, (os.cpu_count() or 2) // 2))
+    per = max(1, -(-batch // (4 * threads)))
+    return [list(range(s, min(batch, s + per))) for s in range(0, batch, per)], threads
+
+
+def compare_every_unit(w, inp, dec, threads=None, check=None):
+    """compare_all (or `check`) over every sequence of the instance, a chunk of
+    sequences at a time, the chunks spread over host threads (the oracle's ctypes calls
+    release the interpreter lock).  Returns the worst attention error."""
+    check = check or compare_all
+    chunks, threads = seq_chunks(w.batch, threads)
+    with cf.ThreadPoolExecutor(min(threads, len(chunks))) as ex:
+        errs = list(ex.map(lambda c: check(w, inp, dec, seqs=c), chunks))
+    return max(errs) if errs else 0.0
 
 
 def _w(**kw):
@@ -120,6 +142,37 @@ def test_small_matrix(cfg):
     w = _w(**cfg)
     inp = make_inputs(w, "cuda")
     dec = run_gpu(w, inp)
+    compare_all(w, inp, dec)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(score="mean", block_size=64, n_tokens=5000),
+    dict(score="mean", block_size=32, n_tokens=4097, kv_dtype=torch.float32, q_dtype=torch.float32,
+         head_dim=64, num_q_heads=8),
+    dict(two_level=True, block_size=64, n_tokens=40000, coarse_block=1024, topk_coarse=6, topk=12,
+         window_tokens=512, planted_per_unit=0),
+], ids=["block_means", "fp32_ragged", "coarse_means"])
+def test_block_means_exact_on_quantised_keys(cfg):
+    """Keys on the grid m / 64, |m| <= 128 (exact in bf16): every fp32 partial sum of up
+    to 1024 of them is a multiple of 2^-6 below 2^11 in magnitude (17 significant bits),
+    so the kernel's fp32 sum is exact whatever its order.  A row's mean is then
+    fl(S * fl(1/n)): exact when n is a power of two, within two roundings (2u relative)
+    otherwise.  A wrong divisor (n + 1 for n) is off by about 1/n relative and fails."""
+    w = _w(**cfg)
+    inp = make_inputs(w, "cuda")
+    k = inp["k_pages"].float()
+    inp["k_pages"] = (torch.clamp(torch.round(k * 64), -128, 128) / 64).to(inp["k_pages"].dtype)
+    dec = run_gpu(w, inp)
+    host = sub_problem(w, inp, range(w.batch))
+    _, (_, _, kmean) = oracle_meta(w, host)
+    mb = w.coarse_block if w.two_level else w.block_size
+    n = np.minimum(mb, w.n_tokens - np.arange(kmean.shape[2]) * mb)
+    gm = as_np(dec.kmean).astype(np.float64)[:, :, : kmean.shape[2]]
+    pow2 = (n & (n - 1)) == 0
+    assert pow2.any()
+    assert np.array_equal(gm[:, :, pow2], kmean[:, :, pow2]), "power-of-two rows must be exact"
+    err = np.abs(gm[:, :, ~pow2] - kmean[:, :, ~pow2])
+    assert (err <= 2.0 ** -23 * np.abs(kmean[:, :, ~pow2]) * (1 + 1e-9)).all(), "ragged rows beyond 2u"
     compare_all(w, inp, dec)
 
 
@@ -254,13 +307,13 @@ def test_largest_block_count():
 # ----------------------------------------------------------- full sizes ----
 
 @pytest.mark.parametrize("name", ["mha_32k", "gqa_128k", "two_level_256k", "reserve_128k"])
-def test_full_size_sampled(name):
-    """The full configuration in the launch configuration the benchmark times; the
-    first and last sequences are checked against the oracle in full."""
+def test_full_size_every_unit(name):
+    """The full configuration in the launch configuration the benchmark times; every
+    sequence and KV head is checked against the oracle in full."""
     w = WORKLOADS[name]
     inp = make_inputs(w, "cuda")
     dec = run_gpu(w, inp)
-    compare_all(w, inp, dec, seqs=[0, w.batch - 1])
+    compare_every_unit(w, inp, dec)
     # workload sanity: planted blocks are found (the query points at them)
     if w.planted_per_unit and not w.two_level:
         ids = as_np(dec.sel_ids).reshape(w.units, -1)
