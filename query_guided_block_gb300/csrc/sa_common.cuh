@@ -364,6 +364,7 @@ __device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t
 
 // Workspace header words (byte offsets from the workspace base; the error word is at 0).
 constexpr int kHdrWaitLimit = int(kHdrWaitLimitByte);   // uint64: wait limit in SM clocks, 0 = kWaitCycles
+constexpr int kHdrJobTicket = 12;   // uint32: next decode job (job-based launches)
 constexpr int kHdrStepEpoch = 32;   // uint32: fused steps completed on this workspace
 constexpr int kHdrStepDone = 36;    // uint32: CTAs of the running step that have finished
 
@@ -392,9 +393,11 @@ __device__ __forceinline__ uint32_t step_flag_value(uint32_t* err)
     return next == 0u ? 1u : next;
 }
 
-// The end of one CTA's share of a step: the last CTA of the grid to finish stores the
-// step's number as the new epoch (after a kernel boundary every later step sees it).
-__device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
+// The end of one CTA's share of a job-based launch (decode, or the fused step): the
+// last CTA of the grid to finish resets the job ticket and the completion count for
+// the next launch and, when the launch completes a step, stores the step's number as
+// the new epoch.  After the kernel boundary every later launch sees them.
+__device__ __forceinline__ void finish_jobs(uint32_t* err, bool completes_step, uint32_t step_value)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -402,7 +405,8 @@ __device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
         uint32_t* done = header_word(err, kHdrStepDone);
         if (atomic_add_acq_rel_u32(done, 1u) + 1u == gridDim.x) {
             *done = 0u;
-            st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
+            *header_word(err, kHdrJobTicket) = 0u;
+            if (completes_step) st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
         }
     }
 }

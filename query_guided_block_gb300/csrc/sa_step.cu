@@ -2,20 +2,26 @@
 //
 // "SGLang分层稀疏注意力技术解析与优化实践" §1.2 (select-then-compute) runs selection and
 // the attention over the selected tokens as two stages of one decode step.  Here both
-// stages run in a single cooperative grid of one CTA (8 warps) per SM:
-//   1. select phase: every warp streams its own 8 KB metadata slabs through a private
-//      cp.async ring and scores them (the select kernel's arithmetic, so the scores are
-//      the same bits); the warp completing a unit records it, and once the CTA has
-//      finished streaming it ranks and emits its completed units, publishing
-//      ready[u] = 1 (device-scope release) for each;
-//   2. decode phase: the decode kernel's warp-independent tensor-core attention; each
-//      CTA waits (bounded, acquire) only for the units of its own item range instead of
-//      for the whole selection, and the CTA merging a unit clears ready[u].
-// The select phase never waits on another CTA and a cooperative launch keeps every CTA
-// resident, so each wait of the decode phase ends.  Shared memory: the select rings and
-// keys alias the decode rings (a barrier separates the phases).  Problems whose grid
-// does not fit this shape run as the select kernel followed by the decode kernel,
-// launched as its programmatic dependent and waiting per unit on the same flags.
+// stages run in one cooperative grid, one CTA (eight worker warps and a control warp)
+// per SM, arranged so that HBM stays busy across the hand-off between them:
+//   1. streaming: worker warp W scores metadata slabs W, W + NW, ... of the unit-major
+//      slab list (NW worker warps in the grid), so units complete one after another
+//      through the whole phase rather than all at its end; the warp whose count
+//      completes a unit queues it for its CTA's control warp and keeps streaming;
+//   2. ranking: the control warp ranks each queued unit on its own (warp-level radix
+//      select over the unit's scores, lower block id first on ties), writes the
+//      selection and publishes ready[u] = the step's number (release) -- while the
+//      workers of every CTA go on streaming;
+//   3. decode: from the start the control warp also takes 256-token decode jobs from a
+//      device-wide counter (unit order) and, once a job's unit is published, resolves
+//      its pages into a descriptor ring; when its workers have streamed their slabs they
+//      run the jobs (sa_job_decode.cuh), the early units' jobs first.
+// Only the last units' ranking is on the critical path, and it overlaps the decode of
+// all the others.  Nothing in the grid waits on a CTA that is not resident (cooperative
+// launch), every wait is bounded, and the last CTA to finish advances the step epoch.
+// Problems the control warp cannot rank on chip (more than kRankMaxKeys candidates)
+// run as the select kernel followed by the job decode kernel, launched as its
+// programmatic dependent and waiting per unit on the same flags.
 #include "sa_step_kernel.cuh"
 
 namespace sa {
@@ -27,8 +33,9 @@ bool step_supported(const Geometry& g)
 
 int step_launches(const Geometry& g, const WorkspaceLayout& L)
 {
+    (void)L;
     if (g.units() == 0) return 0;
-    const int single = g.D == 64 ? step_single_ctas<64>(g, L) : step_single_ctas<128>(g, L);
+    const int single = g.D == 64 ? step_single_ctas<64>(g) : step_single_ctas<128>(g);
     return single > 0 ? 1 : 2;
 }
 
