@@ -153,13 +153,15 @@ int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes);
  * allocating a workspace, before its first use. */
 int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream stream);
 
-/* Limit, in SM clock cycles, of every bounded wait of the kernels run on this
- * workspace: the copy and tensor-core completion waits and the fused step's wait for
- * a unit's published selection.  0 (the value sparse_attn_workspace_init leaves)
- * selects the default of 2e9 cycles, about one second at GB300 clocks; larger values
- * are capped at it.  A wait that runs out sets SPARSE_ATTN_ERR_TIMEOUT in the error
- * word and the kernel goes on and returns, so the context stays usable; results of
- * that call are then unspecified (finite), and later calls are unaffected.
+/* Limit, in SM clock cycles, of the fused step's hand-off waits on this workspace:
+ * sparse_attn_step's decode waits, per unit, for the selection that another CTA (or
+ * the select kernel launched just before it) publishes.  0 (the value
+ * sparse_attn_workspace_init leaves) selects the default of 2e9 cycles, about one
+ * second at GB300 clocks; larger values are capped at it.  (Waits inside one CTA's
+ * own pipeline -- copy and tensor-core completions -- always use the default.)  A wait
+ * that runs out sets SPARSE_ATTN_ERR_TIMEOUT in the error word and the step goes on
+ * with the selection as it finds it and returns, so the context stays usable; that
+ * call's results are then unspecified (finite), and later calls are unaffected.
  * Stream-ordered; copies 8 bytes from host memory, so it cannot be captured into a
  * CUDA graph.  No counterpart in the pages: it exists to bound and to test the waits. */
 int sparse_attn_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t cycles,

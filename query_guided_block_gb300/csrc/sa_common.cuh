@@ -367,15 +367,20 @@ constexpr int kHdrWaitLimit = int(kHdrWaitLimitByte);   // uint64: wait limit in
 constexpr int kHdrJobTicket = 12;   // uint32: next decode job (job-based launches)
 constexpr int kHdrStepEpoch = 32;   // uint32: fused steps completed on this workspace
 constexpr int kHdrStepDone = 36;    // uint32: CTAs of the running step that have finished
+constexpr int kHdrRankHead = int(kHdrRankHeadByte);   // uint32: queue positions taken for ranking
+constexpr int kHdrRankTail = int(kHdrRankTailByte);   // uint32: completed units queued
 
 __device__ __forceinline__ uint32_t* header_word(uint32_t* err, int byte)
 {
     return reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(err) + byte);
 }
 
-// The wait limit of every bounded wait of a kernel, read once from the workspace header
-// (`err` is the workspace base).  0 selects kWaitCycles; larger values are capped at it.
-__device__ __forceinline__ long long wait_limit(const uint32_t* err)
+// The limit of the fused step's hand-off waits (a unit's selection published by another
+// CTA, or by the select kernel launched just before), read once from the workspace
+// header (`err` is the workspace base).  0 selects kWaitCycles; larger values are capped
+// at it.  Waits inside a CTA's own pipeline (copy and MMA completions, the workers'
+// wait for their control warp) always use kWaitCycles.
+__device__ __forceinline__ long long handoff_wait_limit(const uint32_t* err)
 {
     const unsigned long long v =
         __ldcg(reinterpret_cast<const unsigned long long*>(reinterpret_cast<const char*>(err) + kHdrWaitLimit));
@@ -406,6 +411,8 @@ __device__ __forceinline__ void finish_jobs(uint32_t* err, bool completes_step, 
         if (atomic_add_acq_rel_u32(done, 1u) + 1u == gridDim.x) {
             *done = 0u;
             *header_word(err, kHdrJobTicket) = 0u;
+            *header_word(err, kHdrRankHead) = 0u;
+            *header_word(err, kHdrRankTail) = 0u;
             if (completes_step) st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
         }
     }

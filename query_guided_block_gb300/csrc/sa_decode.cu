@@ -80,7 +80,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
     const int u_hi = (i_end - 1) / a.items_per_unit;
     allow_dependents_early();
     grid_dependency_wait();   // inputs and workspace may come from the previous kernel
-    const long long wait_cycles = wait_limit(a.err);
 
     // ---- resolve the range: counts, selected ids -> pages ---------------------
     for (int u = u_lo + tid; u <= u_hi; u += kDecThreads) {
@@ -195,7 +194,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
         }
         const unsigned char* ks = smem + s * stage_bytes;
         const unsigned char* vs = ks + size_t(item_tokens) * S::ROW_BYTES;
-        if (!mbar_wait_bounded(&full[s], parity, wait_cycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
 
         // ---- S = q K^T over the item's tokens -------------------------------
         for (int t_base = 0; t_base < item_tokens; t_base += S::ROWS_PER_BATCH) {
@@ -332,7 +331,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a)
             bool mine = false;
             for (int i = 0; i < 2 * bpi; ++i) mine |= (s * 2 * bpi + i) % kDecWarps == warp;
             if (nxt < i_end && mine) {
-                if (!mbar_wait_bounded(&empty[s], parity, wait_cycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+                if (!mbar_wait_bounded(&empty[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
                 issue_mine(nxt);
             }
         }
@@ -416,20 +415,20 @@ __global__ void __launch_bounds__(kJobThreads, 1) decode_jobs_kernel(DecodeArgs 
     if (ready == nullptr) grid_dependency_wait();   // inputs and workspace may come from the previous kernel
     // behind the step's select kernel: the same flag value as it publishes
     const uint32_t flag_value = ready != nullptr ? step_flag_value(a.err) : 0u;
-    const long long wait_cycles = wait_limit(a.err);
+    const long long handoff_cycles = handoff_wait_limit(a.err);
     __syncthreads();
     if (warp == kCtlWarp) {
         JobFeeder f{0, 0, 0, -1, false};
         long long idle_since = -1;   // no progress since then (bounded like every wait)
         while (true) {
-            if (feeder_step<D, G, QSPLIT>(f, a, ja, desc, js, ready, flag_value, wait_cycles)) {
+            if (feeder_step<D, G, QSPLIT>(f, a, ja, desc, js, ready, flag_value, handoff_cycles)) {
                 idle_since = -1;
                 continue;
             }
             if (f.ended || ld_acquire_cta_shared(&js.workers_done) != 0) break;
             const long long now = clock64();
             if (idle_since < 0) idle_since = now;
-            if (now - idle_since > 2 * wait_cycles) {
+            if (now - idle_since > 2 * kWaitCycles) {
                 if ((threadIdx.x & 31) == 0) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
                 break;
             }
@@ -437,7 +436,7 @@ __global__ void __launch_bounds__(kJobThreads, 1) decode_jobs_kernel(DecodeArgs 
         }
     } else {
         worker_decode<D, G, QSPLIT>(a, ja, desc, js, smem, base + uint32_t(warp) * SS::STAGES * SS::SLAB_BYTES,
-                                    wait_cycles);
+                                    kWaitCycles);
     }
     finish_jobs(a.err, ready != nullptr, flag_value);
 }

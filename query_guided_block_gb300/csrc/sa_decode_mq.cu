@@ -477,7 +477,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     allow_dependents_early();
     grid_dependency_wait();   // inputs and workspace may come from the previous kernel
-    const long long wait_cycles = wait_limit(a.err);
 
     if (warp == 0) {
         tmem_alloc(&s_tmem, TMEM_COLS);
@@ -613,7 +612,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         umma_commit(&bar_free[k % STAGES]);   // stage k mod STAGES may be refilled
     };
     auto wait_kv = [&](int k) {   // tile k's boxes have landed
-        if (!mbar_wait_bounded(&bar_kv[k % STAGES], uint32_t(k / STAGES) & 1u, wait_cycles))
+        if (!mbar_wait_bounded(&bar_kv[k % STAGES], uint32_t(k / STAGES) & 1u, kWaitCycles))
             raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
     };
 
@@ -638,7 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float m_ref = -INFINITY, l_run = 0.f;                        // reference maximum, half-row sum
     for (int k = 0; k < ntiles; ++k) {
         if (warp < 4) {
-            if (!mbar_wait_bounded(&bar_s[k % 3], uint32_t(k / 3) & 1u, wait_cycles))
+            if (!mbar_wait_bounded(&bar_s[k % 3], uint32_t(k / 3) & 1u, kWaitCycles))
                 raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
             tc_fence_after_sync();
             uint32_t sv[32];
@@ -663,7 +662,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 rescale = true;
             }
             // O += P(k - 1) V(k - 1) is done: P and O are free
-            if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, wait_cycles))
+            if (k > 0 && !mbar_wait_bounded(&bar_o, uint32_t(k - 1) & 1u, kWaitCycles))
                 raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
             tc_fence_after_sync();
             if (k > 0 && __any_sync(kFullMask, rescale)) {   // this warp's O rows (lazy)
@@ -724,7 +723,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // the loader: tile k + STAGES - 1 into the stage tile k - 1 used, once the
             // MMAs reading it are done
             if (tid == LOADER && k + STAGES - 1 < ntiles) {
-                if (k > 0 && !mbar_wait_bounded(&bar_free[(k - 1) % STAGES], uint32_t((k - 1) / STAGES) & 1u, wait_cycles))
+                if (k > 0 && !mbar_wait_bounded(&bar_free[(k - 1) % STAGES], uint32_t((k - 1) / STAGES) & 1u, kWaitCycles))
                     raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
                 load_tile(t0 + k + STAGES - 1, (k + STAGES - 1) % STAGES);
             }
@@ -741,7 +740,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             issue_s(k + 2);
         }
     }
-    if (ntiles > 0 && !mbar_wait_bounded(&bar_o, uint32_t(ntiles - 1) & 1u, wait_cycles))
+    if (ntiles > 0 && !mbar_wait_bounded(&bar_o, uint32_t(ntiles - 1) & 1u, kWaitCycles))
         raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
     tc_fence_after_sync();
 

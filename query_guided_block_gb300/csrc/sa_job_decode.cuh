@@ -19,8 +19,10 @@
 //     mma.sync m16n8k16 with the softmax on the fragments (the layout notes are in
 //     sa_decode_body.cuh).
 //   * At the end of a job the eight warps combine their (m, l, o) through shared memory
-//     (worker-only named barrier), write the job's partial and count it; the CTA that
-//     counts a unit's last job merges the unit (log-sum-exp over its jobs, slot order).
+//     (two worker-only named barriers per job), write the job's partial and count it;
+//     the count's result is looked at one job later, so its round trip overlaps the next
+//     job, and the CTA that counted a unit's last job merges the unit (log-sum-exp over
+//     its jobs, slot order).
 #pragma once
 
 #include "sa_decode_body.cuh"
@@ -389,6 +391,8 @@ __device__ void worker_decode(const DecodeArgs& a, const JobArgs& ja, JobDesc* d
 
     float acc[DT][4];
     float m_run = -INFINITY, l_run = 0.f;
+    int pend_u = -1;          // thread 0: unit of the last counted job and the count before it
+    uint32_t pend_old = 0u;
     for (int j = 0; j <= avail && j < end_job && !abort; ++j) {
         const JobDesc& d = desc[j % kJobRing];
         load_qfrag(d);
@@ -492,7 +496,13 @@ __device__ void worker_decode(const DecodeArgs& a, const JobArgs& ja, JobDesc* d
             if (lane == 0) js.flush[warp] = free_off;
         }
         const int u = d.unit, k = d.k;
-        worker_barrier();
+        worker_barrier();   // the flushes are written; descriptor j is not read again
+        if (tid == 0) {
+            st_release_cta_shared(&js.consumed, j + 1);
+            // the previous job's count, issued one job ago: did it complete a unit?
+            js.merge_unit = (pend_u >= 0 && pend_old + 1u == uint32_t(ja.jobs_per_unit)) ? pend_u : -1;
+            sync_job_window(a, desc, js, j + 1 + H, wait_cycles);
+        }
         {
             const size_t head0 = size_t(u / a.Hkv) * a.Hq + size_t(u % a.Hkv) * G;
             for (int o = tid; o < G * D; o += kWorkerThreads) {
@@ -517,22 +527,24 @@ __device__ void worker_decode(const DecodeArgs& a, const JobArgs& ja, JobDesc* d
                 }
             }
         }
-        worker_barrier();   // partial written; the flush stages and descriptor j are free again
-        if (tid == 0) {
-            const uint32_t before = atomic_add_acq_rel_u32(&a.counters[u], 1u);
-            js.merge_unit = before + 1u == uint32_t(ja.jobs_per_unit) ? u : -1;
-            st_release_cta_shared(&js.consumed, j + 1);
+        worker_barrier();   // partial written, flush stages free; window and merge decision published
+        if (tid == 0) {     // count the job (release); its result is looked at one job later
+            pend_old = atomic_add_acq_rel_u32(&a.counters[u], 1u);
+            pend_u = u;
         }
-        sync_job_window(a, desc, js, j + 1 + H, wait_cycles);
-        worker_barrier();
         avail = js.avail;
         end_job = js.end_job;
         abort = js.abort != 0;
-        if (js.merge_unit >= 0) {
-            merge_jobs(a, ja, js.merge_unit, G, D);
+        const int mu = js.merge_unit;
+        if (mu >= 0) {
+            merge_jobs(a, ja, mu, G, D);
             worker_barrier();
         }
     }
+    // the last job's count
+    if (tid == 0) js.merge_unit = (pend_u >= 0 && pend_old + 1u == uint32_t(ja.jobs_per_unit)) ? pend_u : -1;
+    worker_barrier();
+    if (js.merge_unit >= 0) merge_jobs(a, ja, js.merge_unit, G, D);
     cp_async_wait_group<0>();
     if (tid == 0) st_release_cta_shared(&js.workers_done, 1);
 }

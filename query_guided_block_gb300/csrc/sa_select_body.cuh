@@ -478,7 +478,6 @@ __device__ __forceinline__ uint32_t select_body(const SelectArgs& a, uint32_t* r
     // the step's flag value, read before any dependent kernel may start (that kernel
     // reads the same epoch word, which only a finishing step changes)
     const uint32_t flag_value = ready != nullptr ? step_flag_value(a.err) : 0u;
-    const long long wait_cycles = wait_limit(a.err);
     // Only now may a dependent kernel start: whatever ran before this one has finished,
     // so a dependent that skips its own wait (waiting on ready flags instead) still
     // sees every earlier write.
@@ -532,7 +531,7 @@ __device__ __forceinline__ uint32_t select_body(const SelectArgs& a, uint32_t* r
                 cn[e] = sn;
             }
         }
-        if (!mbar_wait_bounded(&full[s], parity, wait_cycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+        if (!mbar_wait_bounded(&full[s], parity, kWaitCycles)) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
 
         // R rows per lane group, partial dots summed over the group's LPR lanes at once
         const unsigned char* hi = smem + s * kStageBytes + d0 * SS::ESZ;

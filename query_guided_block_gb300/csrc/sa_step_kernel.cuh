@@ -13,8 +13,8 @@ namespace {
 
 constexpr int kRankMaxKeys = 4096;   // candidates per unit the control warp ranks on chip
 constexpr int kRankMaxRows = 8192;   // blocks per unit its reserve-set bitmap covers
-constexpr int kRankQueue = 256;      // units one CTA's worker warps may complete in a step
-constexpr int kRankBins = 256;       // 8-bit radix digits
+constexpr int kRankList = 256;       // candidates kept once the k-th key is bracketed this tightly
+constexpr int kGroupSlabs = 4;       // consecutive slabs of one unit a worker warp takes per visit
 
 static_assert(kSlabSelStages * kSlabSelBytes == SlabShape<128>::STAGES * SlabShape<128>::SLAB_BYTES &&
                   kSlabSelStages * kSlabSelBytes == SlabShape<64>::STAGES * SlabShape<64>::SLAB_BYTES,
@@ -29,12 +29,19 @@ constexpr size_t step_smem_bytes()
     return 1024 + kStepRingBytes + size_t(kJobRing) * sizeof(JobDesc) + size_t(kRankMaxKeys) * sizeof(uint32_t);
 }
 
-// Worker -> control-warp hand-off of completed units (static shared memory).
+// The control warp's ranking scratch and the workers' streaming count (static shared memory).
 struct RankSync {
-    int q[kRankQueue];        // unit + 1 of each completed unit, in push order (0: not yet stored)
-    int tail;                 // pushes so far
-    int stream_done;          // worker warps that finished streaming
-    uint32_t hist[kRankBins]; // radix histogram; gather list; reserve-set bitmap
+    uint32_t list_key[kRankList];  // bracketed candidates (index order); reserve-set bitmap
+    uint32_t list_idx[kRankList];
+};
+
+// Fused-step arguments beyond select and decode: the step's hand-off in the workspace.
+struct StepArgs {
+    uint32_t* ready;               // [units] flag value once a unit's selection is written
+    unsigned long long* queue;     // [units] completed units: (flag value << 32) | (unit + 1)
+    uint32_t* head;                // queue entries claimed by control warps
+    uint32_t* tail;                // queue entries pushed by worker warps
+    int units;
 };
 
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
@@ -42,18 +49,33 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // ------------------------------------------------------------- streaming ---
-// Worker warp W (of NW = 8 per CTA x the grid) scores the 8 KB metadata slabs W, W + NW,
-// W + 2 NW, ... of the unit-major slab list, so every warp works near the same point of
-// the list and units complete one after another through the whole phase instead of
-// all at its end.  Per slab the warp forms its unit's two coefficient vectors from the
-// query (the same partial-sum order as the select kernel, so the scores are the same
-// bits), scores the rows from its cp.async ring, stores them and adds the slab's slot
-// count to the unit's counter (release); the warp whose count completes a unit resets
-// the counter and queues the unit for the control warp.  A count's result is looked at
-// one slab later, so its round trip overlaps the next slab.
-template <int KIND, int D, int G>
-__device__ void worker_stream(const SelectArgs& a, RankSync& rs, unsigned char* ring_ptr, uint32_t ring)
+// The slab list is unit-major and cut into groups of kGroupSlabs consecutive slabs of
+// one unit.  Worker warp W (of NW = 8 per CTA x the grid) takes groups W, W + NW, ..., so
+// every warp works near the same point of the list and units complete one after
+// another through the whole phase instead of all at its end.  Per group the warp forms
+// its unit's two coefficient vectors (the same partial-sum order as the select kernel,
+// so the scores are the same bits; the query rows of the next group are loaded one group
+// ahead), scores the group's slabs from its cp.async ring (the copy sequence runs
+// across groups), stores the scores and adds the group's slot count to the unit's
+// counter (release).  The warp whose count completes a unit resets the counter and
+// queues the unit device-wide; the count's result is looked at one group later, so its
+// round trip overlaps the next group.
+template <int KIND, int D, int G, bool QSPLIT>
+__device__ void worker_stream(const SelectArgs& a, const StepArgs& st, uint32_t flag_value, unsigned char* ring_ptr,
+                              uint32_t ring)
 {
     using SS = SelectShape<KIND, KIND == KIND_QUEST, D>;
     using WS = SlabSelShape<KIND, KIND == KIND_QUEST, D>;
@@ -67,14 +89,28 @@ __device__ void worker_stream(const SelectArgs& a, RankSync& rs, unsigned char* 
     const char* lo_src = reinterpret_cast<const char*>(a.kmin);
     const int W = blockIdx.x * kWorkerWarps + warp;
     const int NW = gridDim.x * kWorkerWarps;
-    const int n_mine = W < a.total_chunks ? (a.total_chunks - 1 - W) / NW + 1 : 0;
+    const int spu = a.chunks_per_unit;                         // slabs per unit
+    const int gpu = (spu + kGroupSlabs - 1) / kGroupSlabs;      // groups per unit
+    const int total_groups = st.units * gpu;
+    const int n_groups = W < total_groups ? (total_groups - 1 - W) / NW + 1 : 0;
 
-    auto issue = [&](int k, int st) {
-        if (k >= n_mine) return;
-        const ChunkInfo c = chunk_info(a, W + k * NW, ROWS);
+    // this warp's slab sequence: group gi = W + m * NW covers slabs [first, first + n)
+    auto group_slabs = [&](int m, int& cid0, int& n) {
+        const int gi = W + m * NW;
+        const int u = gi / gpu, k = gi - u * gpu;
+        cid0 = u * spu + k * kGroupSlabs;
+        n = min(kGroupSlabs, spu - k * kGroupSlabs);
+    };
+    // copy slab number `i` of the sequence (group m, slab j of it) into stage st_
+    int iss_m = 0, iss_j = 0;                                   // next slab to issue
+    auto issue_next = [&](int st_) {
+        if (iss_m >= n_groups) return;
+        int cid0, n;
+        group_slabs(iss_m, cid0, n);
+        const ChunkInfo c = chunk_info(a, cid0 + iss_j, ROWS);
         const size_t off = (size_t(c.u) * a.row_stride + c.row0) * SS::ROW_BYTES;
         const uint32_t nbytes = uint32_t(c.nrows) * SS::ROW_BYTES;
-        const uint32_t dst = ring + uint32_t(st) * kSlabSelBytes;
+        const uint32_t dst = ring + uint32_t(st_) * kSlabSelBytes;
 #pragma unroll
         for (int arr = 0; arr < SS::ARRAYS; ++arr) {
             const char* src = (arr == 0 ? hi_src : lo_src) + off;
@@ -84,123 +120,143 @@ __device__ void worker_stream(const SelectArgs& a, RankSync& rs, unsigned char* 
                 if (byte < nbytes) cp_async_16_zfill(dst + arr * (ROWS * SS::ROW_BYTES) + byte, src + byte, 16u);
             }
         }
+        if (++iss_j == n) {
+            iss_j = 0;
+            ++iss_m;
+        }
+    };
+    // query rows of a unit for this lane's channels (raw; converted when used)
+    float qx[G][EPL];
+    auto load_q_rows = [&](int m) {
+        if (m >= n_groups) return;
+        int cid0, n;
+        group_slabs(m, cid0, n);
+        const int u = cid0 / spu;
+        const size_t qb = (size_t(u / a.Hkv) * a.Hq + size_t(u % a.Hkv) * G) * D + d0;
+#pragma unroll
+        for (int g = 0; g < G; ++g) load_q_vec<EPL>(a.q, qb + size_t(g) * D, !QSPLIT, qx[g]);
     };
     auto push = [&](int u) {   // lane 0: every slot of unit u is scored
         a.counters[u] = 0u;
-        const int idx = atomicAdd(&rs.tail, 1);
-        if (idx < kRankQueue) st_release_cta_shared(&rs.q[idx], u + 1);
-        else raise_error(a.err, SPARSE_ATTN_ERR_CAPACITY);
+        const uint32_t idx = atomicAdd(st.tail, 1u);
+        if (idx < uint32_t(st.units))
+            st_release_gpu_u64(st.queue + idx, (static_cast<unsigned long long>(flag_value) << 32) | uint32_t(u + 1));
+        else
+            raise_error(a.err, SPARSE_ATTN_ERR_CAPACITY);
     };
 
+    load_q_rows(0);
 #pragma unroll
     for (int k = 0; k < S - 1; ++k) {
-        issue(k, k);
+        issue_next(k);
         cp_async_commit();
     }
     int pend_u = -1;
     uint32_t pend_old = 0, pend_n = 0;
-    for (int k = 0; k < n_mine; ++k) {
-        cp_async_wait_group<S - 2>();   // this lane's copies of slab k are done
-        __syncwarp();                   // ... and every lane's; the stage read last is free
-        issue(k + S - 1, (k + S - 1) % S);
-        cp_async_commit();
-        const ChunkInfo c = chunk_info(a, W + k * NW, ROWS);
-
-        // the unit's coefficient vectors for this lane's channels
+    int slab = 0;   // slabs consumed so far (ring position)
+    for (int m = 0; m < n_groups; ++m) {
+        int cid0, n;
+        group_slabs(m, cid0, n);
+        const int u = cid0 / spu;
+        // the unit's coefficient vectors for this lane's channels, then the next group's rows
         float cp[EPL], cn[EPL];
-        {
-            float x[G][EPL];
-            const size_t qb = (size_t(c.u / a.Hkv) * a.Hq + size_t(c.u % a.Hkv) * G) * D + d0;
 #pragma unroll
-            for (int g = 0; g < G; ++g) load_q_vec<EPL>(a.q, qb + size_t(g) * D, a.q_bf16 != 0, x[g]);
+        for (int e = 0; e < EPL; ++e) {
+            float sp = 0.f, sn = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                float sp = 0.f, sn = 0.f;
+            for (int k2 = 0; k2 < RSTEP; ++k2) {
+                float pp = 0.f, nn = 0.f;
 #pragma unroll
-                for (int k2 = 0; k2 < RSTEP; ++k2) {
-                    float pp = 0.f, nn = 0.f;
-#pragma unroll
-                    for (int r = k2; r < G; r += RSTEP) {
-                        if constexpr (KIND == KIND_QUEST) {
-                            pp += fmaxf(x[r][e], 0.f);
-                            nn += fminf(x[r][e], 0.f);
-                        } else {
-                            pp += x[r][e];
-                        }
+                for (int r = k2; r < G; r += RSTEP) {
+                    if constexpr (KIND == KIND_QUEST) {
+                        pp += fmaxf(qx[r][e], 0.f);
+                        nn += fminf(qx[r][e], 0.f);
+                    } else {
+                        pp += qx[r][e];
                     }
-                    sp += pp;
-                    sn += nn;
                 }
-                cp[e] = sp;
-                cn[e] = sn;
+                sp += pp;
+                sn += nn;
             }
+            cp[e] = sp;
+            cn[e] = sn;
         }
-        const unsigned char* hi = ring_ptr + size_t(k % S) * kSlabSelBytes + d0 * SS::ESZ;
-        const unsigned char* lo = hi + ROWS * SS::ROW_BYTES;
-        float part[R];
+        load_q_rows(m + 1);
+        uint32_t slots = 0;
+        for (int j = 0; j < n; ++j, ++slab) {
+            cp_async_wait_group<S - 2>();   // this lane's copies of this slab are done
+            __syncwarp();                   // ... and every lane's; the stage read last is free
+            issue_next((slab + S - 1) % S);
+            cp_async_commit();
+            const ChunkInfo c = chunk_info(a, cid0 + j, ROWS);
+            const unsigned char* hi = ring_ptr + size_t(slab % S) * kSlabSelBytes + d0 * SS::ESZ;
+            const unsigned char* lo = hi + ROWS * SS::ROW_BYTES;
+            float part[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int row = rsub * R + r;
-            float fh[EPL], acc = 0.f;
-            unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(hi + row * SS::ROW_BYTES), fh);
-            if constexpr (KIND == KIND_QUEST) {
-                float fl[EPL];
-                unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(lo + row * SS::ROW_BYTES), fl);
+            for (int r = 0; r < R; ++r) {
+                const int row = rsub * R + r;
+                float fh[EPL], acc = 0.f;
+                unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(hi + row * SS::ROW_BYTES), fh);
+                if constexpr (KIND == KIND_QUEST) {
+                    float fl[EPL];
+                    unpack16<SS::ESZ == 2>(*reinterpret_cast<const uint4*>(lo + row * SS::ROW_BYTES), fl);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], fmaf(cn[e], fl[e], acc));
-            } else {
+                    for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], fmaf(cn[e], fl[e], acc));
+                } else {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], acc);
+                    for (int e = 0; e < EPL; ++e) acc = fmaf(cp[e], fh[e], acc);
+                }
+                part[r] = acc;
             }
-            part[r] = acc;
-        }
-        group_reduce_transposed<R, LPR>(part, lane);
-        {
-            constexpr int OUT = R >= LPR ? R / LPR : 1;
-            constexpr int SPREAD = R >= LPR ? 1 : LPR / R;
-            float* srow = a.scores + size_t(c.u) * a.n_cand + c.cand0;
-            if (sub % SPREAD == 0) {
+            group_reduce_transposed<R, LPR>(part, lane);
+            {
+                constexpr int OUT = R >= LPR ? R / LPR : 1;
+                constexpr int SPREAD = R >= LPR ? 1 : LPR / R;
+                float* srow = a.scores + size_t(c.u) * a.n_cand + c.cand0;
+                if (sub % SPREAD == 0) {
 #pragma unroll
-                for (int i = 0; i < OUT; ++i) {
-                    const int r = R >= LPR ? sub * (R / LPR) + i : sub / SPREAD;
-                    const int row = rsub * R + r;
-                    if (row < c.nrows) srow[row] = part[i];
+                    for (int i = 0; i < OUT; ++i) {
+                        const int r = R >= LPR ? sub * (R / LPR) + i : sub / SPREAD;
+                        const int row = rsub * R + r;
+                        if (row < c.nrows) srow[row] = part[i];
+                    }
                 }
             }
+            slots += uint32_t(c.nslots);
         }
         __syncwarp();   // every lane's scores before lane 0's release count
         if (lane == 0) {
-            const uint32_t old = atomic_add_acq_rel_u32(&a.counters[c.u], uint32_t(c.nslots));
+            const uint32_t old = atomic_add_acq_rel_u32(&a.counters[u], slots);
             if (pend_u >= 0 && pend_old + pend_n == uint32_t(a.n_cand)) push(pend_u);
-            pend_u = c.u;
+            pend_u = u;
             pend_old = old;
-            pend_n = uint32_t(c.nslots);
+            pend_n = slots;
         }
     }
     if (lane == 0 && pend_u >= 0 && pend_old + pend_n == uint32_t(a.n_cand)) push(pend_u);
     cp_async_wait_group<0>();
     __syncwarp();
-    if (lane == 0) {
-        __threadfence_block();
-        atomicAdd(&rs.stream_done, 1);
-    }
 }
 
 // --------------------------------------------------------------- ranking ---
-// The control warp ranks one completed unit: its scores come from L2 into shared
-// memory as order keys, an 8-bit radix select below the keys' common prefix narrows
-// the k-th key to a bin of at most 32 (gathered and ranked directly) or to exact ties,
-// and the selection {key > T, or key == T and index <= cT} (lower block id first) is
-// emitted in ascending order by ballots, then the window; with a reserve set the top-k
-// rows and the reserve blocks go through a bitmap first.  The unit is then published
-// (fence + release store of the step's flag value).
+// The control warp ranks one completed unit exactly, without shared-memory atomics
+// (scores of a unit cluster, so histogram bins would collide):
+//   * the unit's scores come from L2 into shared memory as order keys (0: none);
+//   * the k-th largest key T is found by bisection over key values, each probe a
+//     count of keys >= t (every lane counts its keys, one warp reduction); once the
+//     keys >= the lower bracket are at most kRankList they are gathered in index order
+//     and the remaining probes count only them;
+//   * the selection is {key > T} plus, among keys == T, the lowest indices up to k
+//     (lower block id first), emitted in ascending order by ballots, then the window;
+//     with a reserve set the top-k rows and the reserve blocks go through a bitmap.
+// The unit is then published (fence + release store of the step's flag value).
 __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& rs, uint32_t* ready,
                           uint32_t flag_value)
 {
     const int lane = threadIdx.x & 31;
     const uint32_t lt = lanemask_lt();
     const int n = a.n_cand;
-    const int n32 = (n + 31) & ~31;
+    const int n128 = (n + 127) & ~127;
     const float* row = a.scores + size_t(u) * a.n_cand;
     for (int c = lane; c < n; c += 32) cp_async_4(smem_u32(keys + c), row + c);
     cp_async_commit();
@@ -208,7 +264,7 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
     __syncwarp();
     uint32_t lo = 0xffffffffu, hi = 0u;
     int nv = 0;
-    for (int c = lane; c < n32; c += 32) {
+    for (int c = lane; c < n128; c += 32) {
         uint32_t key = 0u;
         if (c < n && candidate_row(a, u, c) >= 0) key = order_key(__uint_as_float(keys[c]));
         keys[c] = key;
@@ -218,141 +274,91 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
             ++nv;
         }
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        nv += __shfl_xor_sync(kFullMask, nv, off);
-        lo = min(lo, __shfl_xor_sync(kFullMask, lo, off));
-        hi = max(hi, __shfl_xor_sync(kFullMask, hi, off));
-    }
+    nv = __reduce_add_sync(kFullMask, nv);
+    lo = __reduce_min_sync(kFullMask, lo);
+    hi = __reduce_max_sync(kFullMask, hi);
     __syncwarp();
     const int k_eff = min(a.k, nv);
+    const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
+    auto count_all = [&](uint32_t t) -> int {   // keys >= t (t > 0)
+        int c = 0;
+        for (int i = lane; i < n128 / 4; i += 32) {
+            const uint4 v = keys4[i];
+            c += (v.x >= t) + (v.y >= t) + (v.z >= t) + (v.w >= t);
+        }
+        return __reduce_add_sync(kFullMask, c);
+    };
+    int nl = 0;   // gathered candidates (0: not gathered)
+    auto count_list = [&](uint32_t t) -> int {
+        int c = 0;
+        for (int i = lane; i < nl; i += 32) c += rs.list_key[i] >= t;
+        return __reduce_add_sync(kFullMask, c);
+    };
+    auto gather = [&](uint32_t t) {   // keys >= t into the list, index order
+        int run = 0;
+        for (int c0 = 0; c0 < n128; c0 += 32) {
+            const uint32_t key = keys[c0 + lane];
+            const bool in = key >= t && key != 0u;
+            const uint32_t b = __ballot_sync(kFullMask, in);
+            if (in) {
+                rs.list_key[run + __popc(b & lt)] = key;
+                rs.list_idx[run + __popc(b & lt)] = uint32_t(c0 + lane);
+            }
+            run += __popc(b);
+        }
+        __syncwarp();
+        nl = run;
+    };
 
-    // mode 0: none; 1: (key & mask) >= prefix; 2: threshold (T, cT)
-    int mode = 0;
-    uint32_t prefix = 0u, mask = 0u, T = 0u;
+    bool all = k_eff > 0 && k_eff >= nv;   // every candidate
+    uint32_t T = 0xffffffffu;
     int cT = -1;
-    if (k_eff > 0 && k_eff < nv) {
-        int krem = k_eff;
-        int low_bits = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
-        mask = low_bits >= 32 ? 0u : ~((1u << low_bits) - 1u);
-        prefix = hi & mask;
-        uint32_t binc = uint32_t(nv);   // candidates matching the current prefix
-        while (low_bits > 0 && binc > 32u && int(binc) != krem) {
-            const int w = min(8, low_bits);
-            const int shift = low_bits - w;
-            const uint32_t dmask = (1u << w) - 1u;
-            for (int i = lane; i < kRankBins; i += 32) rs.hist[i] = 0u;
-            __syncwarp();
-            for (int c = lane; c < n32; c += 32) {
-                const uint32_t key = keys[c];
-                if (key != 0u && (key & mask) == prefix) atomicAdd(&rs.hist[(key >> shift) & dmask], 1u);
+    if (k_eff > 0 && !all) {
+        // bisection: count(>= tl) >= k_eff > count(>= th + 1)
+        uint32_t tl = lo, th = hi;
+        int cnt_l = nv;
+        while (tl < th) {
+            const uint32_t mid = tl + ((th - tl) >> 1) + 1u;
+            const int c = nl > 0 ? count_list(mid) : count_all(mid);
+            if (c >= k_eff) {
+                tl = mid;
+                cnt_l = c;
+            } else {
+                th = mid - 1u;
             }
-            __syncwarp();
-            // lane l holds bins 255 - 8l .. 248 - 8l (descending); find the krem-th key
-            uint32_t cnt[8], sum = 0u;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                cnt[r] = rs.hist[kRankBins - 1 - 8 * lane - r];
-                sum += cnt[r];
-            }
-            uint32_t inc = sum;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t t = __shfl_up_sync(kFullMask, inc, off);
-                if (lane >= off) inc += t;
-            }
-            const uint32_t before = inc - sum;
-            const bool mine = before < uint32_t(krem) && inc >= uint32_t(krem);
-            uint32_t bin = 0u, above = 0u, bc = 0u;
-            if (mine) {
-                uint32_t acc = before;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    if (acc + cnt[r] >= uint32_t(krem)) {
-                        bin = uint32_t(kRankBins - 1 - 8 * lane - r);
-                        above = acc;
-                        bc = cnt[r];
-                        break;
-                    }
-                    acc += cnt[r];
-                }
-            }
-            const int src = __ffs(__ballot_sync(kFullMask, mine)) - 1;
-            bin = __shfl_sync(kFullMask, bin, src);
-            above = __shfl_sync(kFullMask, above, src);
-            bc = __shfl_sync(kFullMask, bc, src);
-            krem -= int(above);
-            prefix |= bin << shift;
-            mask |= dmask << shift;
-            low_bits = shift;
-            binc = bc;
-            __syncwarp();   // the histogram is rewritten next pass
+            if (nl == 0 && cnt_l <= kRankList) gather(tl);
         }
-        if (int(binc) == krem) {
-            mode = 1;   // the whole boundary bin is in
-        } else if (binc <= 32u) {
-            // gather the boundary candidates (index order) and rank them by (key desc, index asc)
-            uint32_t* g = rs.hist;   // keys at [0, 32), indices at [32, 64)
-            int ng = 0;
-            for (int c0 = 0; c0 < n32; c0 += 32) {
-                const int c = c0 + lane;
-                const uint32_t key = keys[c];
-                const bool in = key != 0u && (key & mask) == prefix;
-                const uint32_t b = __ballot_sync(kFullMask, in);
-                if (in) {
-                    const int slot = ng + __popc(b & lt);
-                    g[slot] = key;
-                    g[32 + slot] = uint32_t(c);
-                }
-                ng += __popc(b);
-            }
-            __syncwarp();
-            const uint32_t mk = lane < ng ? g[lane] : 0u;
-            const int mi = lane < ng ? int(g[32 + lane]) : INT_MAX;
-            int rank = 0;
-            for (int jj = 0; jj < ng; ++jj) {
-                const uint32_t kj = __shfl_sync(kFullMask, mk, jj);
-                const int ij = __shfl_sync(kFullMask, mi, jj);
-                rank += (kj > mk) || (kj == mk && ij < mi);
-            }
-            const bool kth = lane < ng && rank == krem - 1;
-            const int src = __ffs(__ballot_sync(kFullMask, kth)) - 1;
-            T = __shfl_sync(kFullMask, mk, src);
-            cT = __shfl_sync(kFullMask, mi, src);
-            mode = 2;
-            __syncwarp();
-        } else {
-            // more than 32 candidates share every key bit: the krem lowest indices are in
-            T = prefix;
-            int run = 0, hit = -1;
-            for (int c0 = 0; c0 < n32; c0 += 32) {
-                const int c = c0 + lane;
-                const bool e = keys[c] == prefix;
-                const uint32_t b = __ballot_sync(kFullMask, e);
-                if (e && run + __popc(b & lt) == krem - 1) hit = c;
-                run += __popc(b);
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) hit = max(hit, __shfl_xor_sync(kFullMask, hit, off));
-            cT = hit;
-            mode = 2;
+        T = tl;
+        if (nl == 0 && cnt_l <= kRankList) gather(T);
+        // among keys == T, the lowest indices fill the remaining places
+        const int above = T == 0xffffffffu ? 0 : (nl > 0 ? count_list(T + 1u) : count_all(T + 1u));
+        const int krem = k_eff - above;
+        int run = 0, hit = -1;
+        const int limit = nl > 0 ? nl : n128;
+        for (int c0 = 0; c0 < limit; c0 += 32) {
+            const int p = c0 + lane;
+            const uint32_t key = nl > 0 ? (p < nl ? rs.list_key[p] : 0u) : keys[p];
+            const bool e = key == T;
+            const uint32_t b = __ballot_sync(kFullMask, e);
+            if (e && run + __popc(b & lt) == krem - 1) hit = nl > 0 ? int(rs.list_idx[p]) : p;
+            run += __popc(b);
         }
-    } else if (k_eff > 0) {
-        mode = 1;   // every candidate (mask = prefix = 0)
+        cT = __reduce_max_sync(kFullMask, hit);
     }
-
     auto selected = [&](uint32_t key, int c) -> bool {
-        if (mode == 0 || key == 0u) return false;
-        if (mode == 1) return (key & mask) >= prefix;
+        if (key == 0u || k_eff == 0) return false;
+        if (all) return true;
         return key > T || (key == T && c <= cT);
     };
+
     int32_t* out = a.out_ids + size_t(u) * a.out_stride;
     int total = 0;
     if (a.n_reserve > 0) {
         // Reserve set (SparDA page §3.4): top-k rows and reserve blocks outside the window
         // marked in a bitmap over block ids, emitted in ascending order
-        uint32_t* bits = rs.hist;
-        const int nw = (a.rows + 31) >> 5;   // <= kRankBins words: rows <= kRankMaxRows
+        __syncwarp();   // the gathered list is not used past here; its storage holds the bitmap
+        uint32_t* bits = rs.list_key;        // <= kRankList words: rows <= kRankMaxRows
+        const int nw = (a.rows + 31) >> 5;
         for (int i = lane; i < nw; i += 32) bits[i] = 0u;
         __syncwarp();
         for (int c = lane; c < n; c += 32)
@@ -380,8 +386,16 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
             for (uint32_t mm = m; mm; mm &= mm - 1) out[pos++] = w * 32 + (__ffs(mm) - 1);
             total += __shfl_sync(kFullMask, inc, 31);
         }
+    } else if (nl > 0 && !all) {
+        for (int c0 = 0; c0 < nl; c0 += 32) {   // every selected key is in the list
+            const int p = c0 + lane;
+            const bool sel = p < nl && selected(rs.list_key[p], int(rs.list_idx[p]));
+            const uint32_t b = __ballot_sync(kFullMask, sel);
+            if (sel) out[total + __popc(b & lt)] = candidate_row(a, u, int(rs.list_idx[p]));
+            total += __popc(b);
+        }
     } else {
-        for (int c0 = 0; c0 < n32; c0 += 32) {
+        for (int c0 = 0; c0 < n128; c0 += 32) {
             const int c = c0 + lane;
             const bool sel = c < n && selected(keys[c], c);
             const uint32_t b = __ballot_sync(kFullMask, sel);
@@ -402,7 +416,7 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
 // ----------------------------------------------------------------- kernel ---
 template <int KIND, int D, int G, bool QSPLIT>
 __global__ void __launch_bounds__(kJobThreads, 1)
-    step_kernel(SelectArgs sa_args, DecodeArgs da, JobArgs ja, uint32_t* ready)
+    step_kernel(SelectArgs sa_args, DecodeArgs da, JobArgs ja, StepArgs st)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -413,7 +427,7 @@ __global__ void __launch_bounds__(kJobThreads, 1)
     __shared__ JobSync js;
     __shared__ RankSync rs;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         js.consumed = 0;
         js.merge_unit = -1;
@@ -421,57 +435,65 @@ __global__ void __launch_bounds__(kJobThreads, 1)
         js.end_job = INT_MAX;
         js.abort = 0;
         js.workers_done = 0;
-        rs.tail = 0;
-        rs.stream_done = 0;
     }
-    for (int i = tid; i < kRankQueue; i += kJobThreads) rs.q[i] = 0;
     if (tid < kJobRing) desc[tid].seq = 0;
     grid_dependency_wait();   // inputs and workspace may come from the previous kernel
     const uint32_t flag_value = step_flag_value(sa_args.err);
-    const long long wait_cycles = wait_limit(sa_args.err);
+    const long long handoff_cycles = handoff_wait_limit(sa_args.err);
     __syncthreads();
 
     if (warp == kCtlWarp) {
-        // control warp: rank the units this CTA's workers complete, feed decode jobs
+        // control warp: rank completed units taken from the device-wide queue (whichever
+        // control warp is free takes the next position), and feed this CTA's decode jobs
         JobFeeder f{0, 0, 0, -1, false};
-        int head = 0;
-        long long idle_since = -1;   // no progress since then (bounded like every wait)
+        int claim = -1;               // queue position this warp ranks once it is filled
+        bool claims_done = false;     // every position is taken
+        long long idle_since = -1;    // no progress since then (bounded like every wait)
         while (true) {
-            if (head < kRankQueue) {
-                const int v = ld_acquire_cta_shared(&rs.q[head]);
-                if (v != 0) {
-                    rank_unit(sa_args, v - 1, keys, rs, ready, flag_value);
-                    ++head;
+            if (claim < 0 && !claims_done) {
+                uint32_t h = 0;
+                if (lane == 0) h = atomicAdd(st.head, 1u);
+                h = __shfl_sync(kFullMask, h, 0);
+                if (h < uint32_t(st.units)) claim = int(h);
+                else claims_done = true;
+                idle_since = -1;
+                continue;
+            }
+            if (claim >= 0) {
+                unsigned long long v = 0;
+                if (lane == 0) v = ld_acquire_gpu_u64(st.queue + claim);
+                v = __shfl_sync(kFullMask, v, 0);
+                __syncwarp();
+                if (uint32_t(v >> 32) == flag_value) {
+                    rank_unit(sa_args, int(uint32_t(v)) - 1, keys, rs, st.ready, flag_value);
+                    claim = -1;
                     idle_since = -1;
                     continue;
                 }
             }
-            if (feeder_step<D, G, QSPLIT>(f, da, ja, desc, js, ready, flag_value, wait_cycles)) {
+            if (feeder_step<D, G, QSPLIT>(f, da, ja, desc, js, st.ready, flag_value, handoff_cycles)) {
                 idle_since = -1;
                 continue;
             }
-            if (ld_acquire_cta_shared(&rs.stream_done) == kWorkerWarps &&
-                head >= min(ld_acquire_cta_shared(&rs.tail), kRankQueue) &&
-                (f.ended || ld_acquire_cta_shared(&js.workers_done) != 0))
-                break;
+            if (claims_done && claim < 0 && (f.ended || ld_acquire_cta_shared(&js.workers_done) != 0)) break;
             const long long now = clock64();
             if (idle_since < 0) idle_since = now;
-            if (now - idle_since > 2 * wait_cycles) {
-                if ((threadIdx.x & 31) == 0) raise_error(sa_args.err, SPARSE_ATTN_ERR_TIMEOUT);
+            if (now - idle_since > 2 * kWaitCycles) {
+                if (lane == 0) raise_error(sa_args.err, SPARSE_ATTN_ERR_TIMEOUT);
                 break;
             }
             __nanosleep(64);
         }
     } else {
         const uint32_t ring = base + uint32_t(warp) * kWarpRingBytes;
-        worker_stream<KIND, D, G>(sa_args, rs, smem + size_t(warp) * kWarpRingBytes, ring);
-        worker_decode<D, G, QSPLIT>(da, ja, desc, js, smem, ring, wait_cycles);
+        worker_stream<KIND, D, G, QSPLIT>(sa_args, st, flag_value, smem + size_t(warp) * kWarpRingBytes, ring);
+        worker_decode<D, G, QSPLIT>(da, ja, desc, js, smem, ring, kWaitCycles);
     }
     finish_jobs(sa_args.err, true, flag_value);
 }
 
 template <int KIND, int D, int G, bool QSPLIT>
-cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const JobArgs& ja, uint32_t* ready,
+cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const JobArgs& ja, const StepArgs& st,
                           int ctas, cudaStream_t s)
 {
     constexpr size_t smem = step_smem_bytes();
@@ -497,39 +519,32 @@ cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, sa_args, da, ja, ready);
+    return cudaLaunchKernelEx(&cfg, kernel, sa_args, da, ja, st);
 }
 
 template <int KIND, int D, bool QSPLIT>
-cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, const JobArgs& ja, uint32_t* ready,
+cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, const JobArgs& ja, const StepArgs& st,
                             int ctas, int G, cudaStream_t s)
 {
     switch (G) {
-        case 1: return launch_step_t<KIND, D, 1, QSPLIT>(sa_args, da, ja, ready, ctas, s);
-        case 2: return launch_step_t<KIND, D, 2, QSPLIT>(sa_args, da, ja, ready, ctas, s);
-        case 4: return launch_step_t<KIND, D, 4, QSPLIT>(sa_args, da, ja, ready, ctas, s);
-        case 8: return launch_step_t<KIND, D, 8, QSPLIT>(sa_args, da, ja, ready, ctas, s);
+        case 1: return launch_step_t<KIND, D, 1, QSPLIT>(sa_args, da, ja, st, ctas, s);
+        case 2: return launch_step_t<KIND, D, 2, QSPLIT>(sa_args, da, ja, st, ctas, s);
+        case 4: return launch_step_t<KIND, D, 4, QSPLIT>(sa_args, da, ja, st, ctas, s);
+        case 8: return launch_step_t<KIND, D, 8, QSPLIT>(sa_args, da, ja, st, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 // CTAs of the single-launch step (one per SM), or 0 when the problem runs as two
-// kernels: the control warp holds at most kRankMaxKeys candidate keys of a unit (and
-// a bitmap of kRankMaxRows blocks for a reserve set), and the units a CTA's workers can
-// complete must fit its queue.
+// kernels: the control warp holds at most kRankMaxKeys candidate keys of a unit (and a
+// bitmap of kRankMaxRows blocks for a reserve set).
 template <int D>
 int step_single_ctas(const Geometry& g)
 {
     const int units = g.units();
     if (units == 0 || g.n_cand > kRankMaxKeys) return 0;
     if (g.n_reserve > 0 && g.nb > kRankMaxRows) return 0;
-    const int rows = g.score_kind == SPARSE_ATTN_SCORE_MEAN ? SlabSelShape<KIND_MEAN, false, D>::ROWS
-                                                           : SlabSelShape<KIND_QUEST, true, D>::ROWS;
-    const long long slabs = (long long)units * (((g.n_cand > 0 ? g.n_cand : 1) + rows - 1) / rows);
-    const long long ctas = num_sms();
-    const long long per_warp = (slabs + ctas * kWorkerWarps - 1) / (ctas * kWorkerWarps);
-    if (per_warp * kWorkerWarps > kRankQueue) return 0;
-    return int(ctas);
+    return num_sms();
 }
 
 template <int D>
@@ -551,14 +566,19 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
     else set_slab_chunking<KIND_QUEST, true, D>(sa_args, units);
     DecodeArgs da = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out, nullptr, 0);
     const JobArgs ja = job_args(g, L, ws);
-    uint32_t* ready = reinterpret_cast<uint32_t*>(ws + L.ready);
+    StepArgs st{};
+    st.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
+    st.queue = reinterpret_cast<unsigned long long*>(ws + L.rank_queue);
+    st.head = reinterpret_cast<uint32_t*>(ws + L.err + kHdrRankHeadByte);
+    st.tail = reinterpret_cast<uint32_t*>(ws + L.err + kHdrRankTailByte);
+    st.units = units;
 
     const bool qs = !g.q_bf16;
     if (mean)
-        return qs ? dispatch_step_g<KIND_MEAN, D, true>(sa_args, da, ja, ready, ctas, g.G, s)
-                  : dispatch_step_g<KIND_MEAN, D, false>(sa_args, da, ja, ready, ctas, g.G, s);
-    return qs ? dispatch_step_g<KIND_QUEST, D, true>(sa_args, da, ja, ready, ctas, g.G, s)
-              : dispatch_step_g<KIND_QUEST, D, false>(sa_args, da, ja, ready, ctas, g.G, s);
+        return qs ? dispatch_step_g<KIND_MEAN, D, true>(sa_args, da, ja, st, ctas, g.G, s)
+                  : dispatch_step_g<KIND_MEAN, D, false>(sa_args, da, ja, st, ctas, g.G, s);
+    return qs ? dispatch_step_g<KIND_QUEST, D, true>(sa_args, da, ja, st, ctas, g.G, s)
+              : dispatch_step_g<KIND_QUEST, D, false>(sa_args, da, ja, st, ctas, g.G, s);
 }
 
 }  // namespace
