@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(kJobThreads, 1) decode_jobs_kernel(DecodeArgs 
     const long long handoff_cycles = handoff_wait_limit(a.err);
     __syncthreads();
     if (warp == kCtlWarp) {
-        JobFeeder f{0, 0, 0, -1, false};
+        JobFeeder f = feeder_init();
         long long idle_since = -1;   // no progress since then (bounded like every wait)
         while (true) {
             if (feeder_step<D, G, QSPLIT>(f, a, ja, desc, js, ready, flag_value, handoff_cycles)) {

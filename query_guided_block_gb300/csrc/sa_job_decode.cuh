@@ -37,8 +37,9 @@ constexpr int kWorkerWarps = 8;
 constexpr int kWorkerThreads = kWorkerWarps * 32;
 constexpr int kCtlWarp = kWorkerWarps;                // the control warp follows the workers
 constexpr int kJobThreads = kWorkerThreads + 32;
-constexpr int kJobRing = 4;                           // descriptors resolved ahead of the workers
-constexpr int kJobQWords = 8 * 128 / 2;               // a unit's bf16 query rows, G <= 8, D <= 128
+constexpr int kJobRing = 8;                           // descriptors resolved ahead of the workers
+constexpr int kJobBatch = 4;                          // jobs the feeder resolves side by side
+constexpr int kJobQWords = 256;                       // a unit's bf16 query rows when G * D <= 512
 constexpr int kJobEnd = -1;
 constexpr int kBarWorkers = 1;                        // named barrier of the 256 worker threads
 static_assert(kJobSlabs == 2 * kWorkerWarps, "two slabs per worker warp and job");
@@ -50,8 +51,16 @@ struct JobDesc {
     int pad;
     int page[kJobMaxBlocks];  // page (or pool tile) of each of the job's blocks, -1 if none
     int valid[kJobMaxBlocks]; // tokens of that block (0 for an empty slot)
-    uint32_t q[kJobQWords];   // the unit's query rows (bf16 queries)
+    uint32_t q[kJobQWords];   // the unit's query rows (bf16 queries with G * D <= 512)
 };
+
+// Whether the descriptor carries the unit's query rows (else the workers read them from
+// global memory at the start of each job).
+template <int D, int G, bool QSPLIT>
+__host__ __device__ constexpr bool job_q_in_desc()
+{
+    return !QSPLIT && G * D / 2 <= kJobQWords;
+}
 
 // Bytes of dynamic shared memory the decode part needs: 1 KB alignment slack, the
 // worker rings, the descriptor ring.
@@ -102,30 +111,42 @@ struct JobArgs {
 
 // --------------------------------------------------------------- control warp --
 // Feeder: produces descriptors for the CTA's jobs in order (local job j -> slot
-// j % kJobRing).  step() does one non-blocking piece of work and reports whether it
-// made progress; it never waits on another CTA, so the control warp can interleave it
-// with the selection work of the fused step.
+// j % kJobRing).  Jobs come from the device-wide counter in batches of up to kJobBatch
+// consecutive jobs (the next batch's ticket is taken while the current one resolves);
+// a batch is resolved side by side, one group of 32 / kJobBatch lanes per job, so its
+// chain of dependent loads (counts and ids, then the page table) is paid once per batch.
+// step() does one non-blocking piece of work and reports whether it made progress; it
+// never waits on another CTA, so the control warp can interleave it with the selection
+// work of the fused step.
 struct JobFeeder {
     int produced;             // descriptors filled
-    int state;                // 0: need a ticket, 1: selection not yet published, 2: resolve
-    int ticket;
-    long long t0;             // first time the selection was found unpublished
+    int state;                // 0: need a batch, 1: selections not yet published, 2: resolve
+    int first, count;         // the batch being resolved: jobs [first, first + count)
+    int next;                 // start of the next batch (ticket taken ahead), -1 if none yet
+    long long t0;             // first time a selection was found unpublished
     bool ended;
 };
+
+__device__ __forceinline__ JobFeeder feeder_init() { return JobFeeder{0, 0, 0, 0, -1, -1, false}; }
 
 template <int D, int G, bool QSPLIT>
 __device__ bool feeder_step(JobFeeder& f, const DecodeArgs& a, const JobArgs& ja, JobDesc* desc, const JobSync& js,
                             const uint32_t* ready, uint32_t flag_value, long long wait_cycles)
 {
     const int lane = threadIdx.x & 31;
+    // jobs per batch: one lane group (32 / batch lanes) per job must cover its blocks
+    const int batch = ja.job_blocks <= 32 / kJobBatch ? kJobBatch : (ja.job_blocks <= 16 ? 2 : 1);
     if (f.ended) return false;
-    if (f.produced - *reinterpret_cast<const volatile int*>(&js.consumed) >= kJobRing) return false;
-    JobDesc& d = desc[f.produced % kJobRing];
+    const int room = kJobRing - (f.produced - *reinterpret_cast<const volatile int*>(&js.consumed));
     if (f.state == 0) {
-        int t = 0;
-        if (lane == 0) t = int(atomicAdd(ja.ticket, 1u));
-        t = __shfl_sync(kFullMask, t, 0);
-        if (t >= ja.total_jobs) {
+        if (room < batch) return false;
+        int t = f.next;
+        if (t < 0) {
+            if (lane == 0) t = int(atomicAdd(ja.ticket, uint32_t(batch)));
+            t = __shfl_sync(kFullMask, t, 0);
+        }
+        if (t >= ja.total_jobs) {   // no more jobs: the end marker
+            JobDesc& d = desc[f.produced % kJobRing];
             if (lane == 0) {
                 d.unit = kJobEnd;
                 d.k = 0;
@@ -135,16 +156,20 @@ __device__ bool feeder_step(JobFeeder& f, const DecodeArgs& a, const JobArgs& ja
             f.ended = true;
             return true;
         }
-        f.ticket = t;
+        f.first = t;
+        f.count = min(batch, ja.total_jobs - t);
+        // the next batch's ticket, in flight while this one resolves
+        int nt = 0;
+        if (lane == 0) nt = int(atomicAdd(ja.ticket, uint32_t(batch)));
+        f.next = __shfl_sync(kFullMask, nt, 0);
         f.state = ready != nullptr ? 1 : 2;
         f.t0 = -1;
         return true;
     }
-    const int u = f.ticket / ja.jobs_per_unit;
-    if (f.state == 1) {   // the unit's selection, published by a select of this step
-        int ok = 0;
-        if (lane == 0) ok = ld_acquire_gpu(ready + u) == flag_value;
-        ok = __shfl_sync(kFullMask, ok, 0);
+    if (f.state == 1) {   // the batch's units' selections, published by a select of this step
+        int ok = 1;
+        if (lane < f.count) ok = ld_acquire_gpu(ready + (f.first + lane) / ja.jobs_per_unit) == flag_value;
+        ok = __all_sync(kFullMask, ok);
         __syncwarp();
         if (!ok) {
             const long long now = clock64();
@@ -155,18 +180,22 @@ __device__ bool feeder_step(JobFeeder& f, const DecodeArgs& a, const JobArgs& ja
         f.state = 2;
         return true;
     }
-    // resolve: slots -> selected block -> page; query rows
-    const int k = f.ticket - u * ja.jobs_per_unit;
-    int count = a.sel_count[u];
-    if (count < 0 || count > a.sel_stride) {
-        if (lane == 0) raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
-        count = count < 0 ? 0 : a.sel_stride;
-    }
-    {
-        const int e = lane;   // kJobMaxBlocks == 32 lanes
+    // resolve: lane group g handles job first + g; its lane e, slot k * J + e -> block -> page
+    const int per = 32 / batch;
+    const int g = lane / per, e = lane - g * per;
+    const int t = f.first + g;
+    const bool live = g < f.count;
+    const int u = live ? t / ja.jobs_per_unit : 0;
+    const int k = live ? t - u * ja.jobs_per_unit : 0;
+    int page = -1, valid = 0;
+    if (live && e < ja.job_blocks) {
+        int count = a.sel_count[u];
+        if (count < 0 || count > a.sel_stride) {
+            if (e == 0) raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
+            count = count < 0 ? 0 : a.sel_stride;
+        }
         const int slot = k * ja.job_blocks + e;
-        int page = -1, valid = 0;
-        if (e < ja.job_blocks && slot < count) {
+        if (slot < count) {
             const int j = a.sel_ids[size_t(u) * a.sel_stride + slot];
             if (j < 0 || j >= a.nb) {
                 raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
@@ -188,22 +217,36 @@ __device__ bool feeder_step(JobFeeder& f, const DecodeArgs& a, const JobArgs& ja
                 }
             }
         }
-        d.page[e] = page;
-        d.valid[e] = valid;
     }
-    if constexpr (!QSPLIT) {   // the unit's G query rows are contiguous: [b, kvh * G .. + G)
-        const size_t head0 = size_t(u / a.Hkv) * a.Hq + size_t(u % a.Hkv) * G;
-        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q) + head0 * D / 2;
-        for (int w = lane; w < G * D / 2; w += 32) d.q[w] = __ldg(q32 + w);
+    for (int b = 0; b < f.count; ++b) {   // every descriptor of the batch: all of its block entries
+        JobDesc& d = desc[(f.produced + b) % kJobRing];
+        for (int x = lane; x < kJobMaxBlocks; x += 32) {
+            const int src = b * per + x;   // lane holding entry x of job b (when x < per)
+            const int pg = __shfl_sync(kFullMask, page, src & 31);
+            const int vd = __shfl_sync(kFullMask, valid, src & 31);
+            d.page[x] = x < per ? pg : -1;
+            d.valid[x] = x < per ? vd : 0;
+        }
+        if constexpr (job_q_in_desc<D, G, QSPLIT>()) {   // the unit's G query rows are contiguous
+            const int ub = (f.first + b) / ja.jobs_per_unit;
+            const size_t head0 = size_t(ub / a.Hkv) * a.Hq + size_t(ub % a.Hkv) * G;
+            const uint4* q4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(a.q) + head0 * D / 2);
+            uint4* dq = reinterpret_cast<uint4*>(d.q);
+            for (int w = lane; w < G * D / 8; w += 32) dq[w] = __ldg(q4 + w);
+        }
     }
     __syncwarp();
     if (lane == 0) {
-        d.unit = u;
-        d.k = k;
-        st_release_cta_shared(&d.seq, f.produced + 1);
+        for (int b = 0; b < f.count; ++b) {
+            JobDesc& d = desc[(f.produced + b) % kJobRing];
+            const int tb = f.first + b;
+            d.unit = tb / ja.jobs_per_unit;
+            d.k = tb - d.unit * ja.jobs_per_unit;
+            st_release_cta_shared(&d.seq, f.produced + b + 1);
+        }
     }
     __syncwarp();
-    ++f.produced;
+    f.produced += f.count;
     f.state = 0;
     return true;
 }
@@ -320,7 +363,7 @@ __device__ void worker_decode(const DecodeArgs& a, const JobArgs& ja, JobDesc* d
     constexpr int S = SS::STAGES;
     constexpr int DT = SS::DT;
     constexpr int H = S / 2;   // jobs the copies run ahead of the job being computed
-    static_assert(H + 1 <= kJobRing, "descriptors the copies read ahead must stay in the ring");
+    static_assert(H + 1 + kJobBatch <= kJobRing, "the copies' descriptors and a batch must fit the ring");
     static_assert(G <= 8, "query rows live in the first 8 MMA rows");
     static_assert(8 * D * 4 <= SS::SLAB_BYTES, "a warp's G x D outputs must fit one stage");
 
@@ -364,10 +407,17 @@ __device__ void worker_decode(const DecodeArgs& a, const JobArgs& ja, JobDesc* d
     auto load_qfrag = [&](const JobDesc& d) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            if constexpr (!QSPLIT) {
+            if constexpr (job_q_in_desc<D, G, QSPLIT>()) {
                 const int w = (g4 * D + ks * 16 + 2 * t4) / 2;
                 qa[ks][0] = g4 < G ? d.q[w] : 0u;
                 qa[ks][2] = g4 < G ? d.q[w + 4] : 0u;
+                qa[ks][1] = qa[ks][3] = 0u;
+            } else if constexpr (!QSPLIT) {
+                const size_t head0 = size_t(d.unit / a.Hkv) * a.Hq + size_t(d.unit % a.Hkv) * G;
+                const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q);
+                const size_t qrow = (head0 + g4) * D + ks * 16 + 2 * t4;
+                qa[ks][0] = g4 < G ? __ldg(q32 + qrow / 2) : 0u;
+                qa[ks][2] = g4 < G ? __ldg(q32 + qrow / 2 + 4) : 0u;
                 qa[ks][1] = qa[ks][3] = 0u;
             } else {
                 const size_t head0 = size_t(d.unit / a.Hkv) * a.Hq + size_t(d.unit % a.Hkv) * G;

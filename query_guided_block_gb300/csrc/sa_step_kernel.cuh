@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kJobThreads, 1)
     if (warp == kCtlWarp) {
         // control warp: rank completed units taken from the device-wide queue (whichever
         // control warp is free takes the next position), and feed this CTA's decode jobs
-        JobFeeder f{0, 0, 0, -1, false};
+        JobFeeder f = feeder_init();
         int claim = -1;               // queue position this warp ranks once it is filled
         bool claims_done = false;     // every position is taken
         long long idle_since = -1;    // no progress since then (bounded like every wait)
