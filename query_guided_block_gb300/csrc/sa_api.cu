@@ -125,11 +125,6 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     L.blocks_per_split = decode_blocks_per_item(g.D, g.kv_bf16, g.bs);
     L.max_splits = (g.sel_stride + L.blocks_per_split - 1) / L.blocks_per_split;
     if (L.max_splits < 1) L.max_splits = 1;
-    // bf16 job decode: 256-token jobs, never more than the item slots above
-    L.job_blocks = g.bs <= 256 ? 256 / g.bs : 1;
-    L.jobs_per_unit = (g.sel_stride + L.job_blocks - 1) / L.job_blocks;
-    if (L.jobs_per_unit < 1) L.jobs_per_unit = 1;
-    if (L.jobs_per_unit > L.max_splits) L.max_splits = L.jobs_per_unit;
     const size_t heads = size_t(g.B) * g.Hq * g.Q;   // query rows (Q queries per sequence)
     const size_t dec_cells = units * size_t(g.Q > 1 ? mq_row_tiles(g.Q, g.G) : 1);
 

@@ -364,7 +364,6 @@ __device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t
 
 // Workspace header words (byte offsets from the workspace base; the error word is at 0).
 constexpr int kHdrWaitLimit = int(kHdrWaitLimitByte);   // uint64: wait limit in SM clocks, 0 = kWaitCycles
-constexpr int kHdrJobTicket = 12;   // uint32: next decode job (job-based launches)
 constexpr int kHdrStepEpoch = 32;   // uint32: fused steps completed on this workspace
 constexpr int kHdrStepDone = 36;    // uint32: CTAs of the running step that have finished
 constexpr int kHdrRankHead = int(kHdrRankHeadByte);   // uint32: queue positions taken for ranking
@@ -398,11 +397,12 @@ __device__ __forceinline__ uint32_t step_flag_value(uint32_t* err)
     return next == 0u ? 1u : next;
 }
 
-// The end of one CTA's share of a job-based launch (decode, or the fused step): the
-// last CTA of the grid to finish resets the job ticket and the completion count for
-// the next launch and, when the launch completes a step, stores the step's number as
-// the new epoch.  After the kernel boundary every later launch sees them.
-__device__ __forceinline__ void finish_jobs(uint32_t* err, bool completes_step, uint32_t step_value)
+// The end of one CTA's share of the launch that completes a step (the fused kernel, or
+// the decode kernel behind the step's select kernel): the last CTA of the grid to
+// finish resets the completion count and the rank queue for the next step and stores
+// the step's number as the new epoch.  After the kernel boundary every later launch
+// sees them.
+__device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -410,10 +410,9 @@ __device__ __forceinline__ void finish_jobs(uint32_t* err, bool completes_step, 
         uint32_t* done = header_word(err, kHdrStepDone);
         if (atomic_add_acq_rel_u32(done, 1u) + 1u == gridDim.x) {
             *done = 0u;
-            *header_word(err, kHdrJobTicket) = 0u;
             *header_word(err, kHdrRankHead) = 0u;
             *header_word(err, kHdrRankTail) = 0u;
-            if (completes_step) st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
+            st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
         }
     }
 }

@@ -6,22 +6,20 @@
 // gathering them into a temporary buffer first.  The softmax is exact over the union of
 // the selected tokens (SGLang page §1.2: select, then compute).
 //
-//   * bf16 K/V (the fast path, decode_jobs_kernel below; sa_job_decode.cuh): 256-token
-//     jobs taken from a device-wide counter by one CTA per SM; a control warp resolves
-//     each job's pages ahead, eight worker warps stream 16-token slabs through per-warp
-//     cp.async rings and do QK^T and PV on tensor cores (mma.sync m16n8k16, fp32
-//     accumulate) with the softmax on the fragments; each job writes one (m, l, o)
-//     partial and the CTA counting a unit's last job merges them in job order.
-//   * fp32 K/V (decode_kernel): a persistent grid over "items" (a few selected blocks of
-//     one (sequence, KV head) unit), numbered unit-major; CTA i owns an equal contiguous
-//     range, so it sees one or two unit boundaries and no CTA ever waits on another.  At
-//     start the CTA resolves, for its whole range, selected id -> page through the page
-//     table into shared memory (bounds-checked); items go through a CTA-wide bulk-copy
-//     pipeline, dots on FMA units with the G heads' partial sums reduced across a key
-//     row's lanes.  At the end of its segment of a unit the CTA writes one (m, l, o)
-//     partial; the CTA that completes a unit's item count merges the unit's partials.
+// Design: a persistent grid over "items" (a few selected blocks, 64-128 tokens, of one
+// (sequence, KV head) unit), numbered unit-major; CTA i owns an equal contiguous range,
+// so it sees one or two unit boundaries and no CTA ever waits on another.  At start the
+// CTA resolves, for its whole range, selected id -> page through the page table into
+// shared memory (bounds-checked).  At the end of its segment of a unit the CTA writes
+// one (m, l, o) partial; the CTA that completes a unit's item count merges the unit's
+// partials (log-sum-exp) into fp32 outputs.
+//   * bf16 K/V (the fast path, decode_mma_kernel below): warps stream 16-token slabs
+//     independently through per-warp cp.async rings and do QK^T and PV on tensor cores
+//     (mma.sync m16n8k16, fp32 accumulate) with the softmax on the fragments.
+//   * fp32 K/V (decode_kernel): items through a CTA-wide bulk-copy pipeline, dots on
+//     FMA units with the G heads' partial sums reduced across a key row's lanes.
 
-#include "sa_job_decode.cuh"
+#include "sa_decode_body.cuh"
 
 namespace sa {
 namespace {
@@ -384,89 +382,53 @@ cudaError_t dispatch_group(const DecodeArgs& a, int G, cudaStream_t s)
 }
 
 
-// bf16 K/V: the job-based decode (sa_job_decode.cuh), one CTA of eight worker warps and
-// a control warp per SM.  With `ready` set the kernel runs behind the step's select
-// kernel, which publishes each unit's selection: it skips the grid-wide wait (its CTAs
-// start on SMs as the select kernel's CTAs leave them), the control warp waits per unit,
-// and the last CTA advances the step epoch.
+// With `ready` set the kernel runs behind a select kernel that publishes each unit's
+// selection: it skips the grid-wide wait and waits per unit instead, so its CTAs
+// start on SMs as the select kernel's CTAs leave them.
 template <int D, int G, bool QSPLIT>
-__global__ void __launch_bounds__(kJobThreads, 1) decode_jobs_kernel(DecodeArgs a, JobArgs ja, uint32_t* ready)
+__global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a, uint32_t* ready)
 {
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    using SS = SlabShape<D>;
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;   // the swizzle pattern repeats every 1024 bytes
-    unsigned char* smem = smem_raw + (base - raw);
-    constexpr size_t kRing = size_t(kWorkerWarps) * SS::STAGES * SS::SLAB_BYTES;
-    JobDesc* desc = reinterpret_cast<JobDesc*>(smem + kRing);
-    __shared__ JobSync js;
-
-    const int tid = threadIdx.x, warp = tid >> 5;
-    if (tid == 0) {
-        js.consumed = 0;
-        js.merge_unit = -1;
-        js.avail = -1;
-        js.end_job = 1 << 30;
-        js.abort = 0;
-        js.workers_done = 0;
-    }
-    if (tid < kJobRing) desc[tid].seq = 0;
     allow_dependents_early();
-    if (ready == nullptr) grid_dependency_wait();   // inputs and workspace may come from the previous kernel
-    // behind the step's select kernel: the same flag value as it publishes
-    const uint32_t flag_value = ready != nullptr ? step_flag_value(a.err) : 0u;
-    const long long handoff_cycles = handoff_wait_limit(a.err);
-    __syncthreads();
-    if (warp == kCtlWarp) {
-        JobFeeder f = feeder_init();
-        long long idle_since = -1;   // no progress since then (bounded like every wait)
-        while (true) {
-            if (feeder_step<D, G, QSPLIT>(f, a, ja, desc, js, ready, flag_value, handoff_cycles)) {
-                idle_since = -1;
-                continue;
-            }
-            if (f.ended || ld_acquire_cta_shared(&js.workers_done) != 0) break;
-            const long long now = clock64();
-            if (idle_since < 0) idle_since = now;
-            if (now - idle_since > 2 * kWaitCycles) {
-                if ((threadIdx.x & 31) == 0) raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
-                break;
-            }
-            __nanosleep(64);
-        }
-    } else {
-        worker_decode<D, G, QSPLIT>(a, ja, desc, js, smem, base + uint32_t(warp) * SS::STAGES * SS::SLAB_BYTES,
-                                    kWaitCycles);
+    if (ready == nullptr) {
+        grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+        decode_mma_body<D, G, QSPLIT>(a, nullptr, 0u);
+        return;
     }
-    finish_jobs(a.err, ready != nullptr, flag_value);
+    // behind the step's select kernel: the same flag value as it publishes
+    const uint32_t flag_value = step_flag_value(a.err);
+    decode_mma_body<D, G, QSPLIT>(a, ready, flag_value);
+    finish_step(a.err, flag_value);
 }
 
 template <int D, int G, bool QSPLIT>
-cudaError_t launch_decode_jobs_t(const DecodeArgs& a, const JobArgs& ja, uint32_t* ready, cudaStream_t s)
+cudaError_t launch_decode_mma_t(DecodeArgs a, uint32_t* ready, cudaStream_t s)
 {
-    constexpr size_t smem = job_decode_smem_bytes<D>();
-    static_assert(smem <= size_t(kDecSmemLimit), "worker rings and descriptors must fit a CTA");
+    constexpr size_t smem = slab_smem_bytes<D>();
+    static_assert(smem <= size_t(kDecSmemLimit), "slab rings must fit a CTA");
     static std::atomic<unsigned long long> configured{0};   // devices set up
     const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
-        return cudaFuncSetAttribute(decode_jobs_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    int(smem));
+        return cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kDecSmemLimit);
     });
     if (cfg != cudaSuccess) return cfg;
-    long long ctas = num_sms();   // one CTA per SM; jobs are taken from a device-wide counter
-    if (ctas > ja.total_jobs) ctas = ja.total_jobs;
-    if (ctas < 1) return cudaSuccess;
-    return launch_after_previous(decode_jobs_kernel<D, G, QSPLIT>, dim3(unsigned(ctas)), dim3(kJobThreads), smem, s,
-                                 a, ja, ready);
+    long long ctas = num_sms();                    // one CTA (8 independent warps) per SM
+    const long long min_ctas = ((long long)a.total_items * a.blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
+    if (ctas < min_ctas) ctas = min_ctas;
+    const long long min_ctas_units = (a.units + 61) / 62;
+    if (ctas < min_ctas_units) ctas = min_ctas_units;
+    if (ctas > a.total_items) ctas = a.total_items;
+    return launch_after_previous(decode_mma_kernel<D, G, QSPLIT>, dim3(unsigned(ctas)), dim3(kDecThreads), smem, s, a,
+                                 ready);
 }
 
 template <int D, bool QSPLIT>
-cudaError_t dispatch_jobs(const DecodeArgs& a, const JobArgs& ja, int G, uint32_t* ready, cudaStream_t s)
+cudaError_t dispatch_mma(const DecodeArgs& a, int G, uint32_t* ready, cudaStream_t s)
 {
     switch (G) {
-        case 1: return launch_decode_jobs_t<D, 1, QSPLIT>(a, ja, ready, s);
-        case 2: return launch_decode_jobs_t<D, 2, QSPLIT>(a, ja, ready, s);
-        case 4: return launch_decode_jobs_t<D, 4, QSPLIT>(a, ja, ready, s);
-        case 8: return launch_decode_jobs_t<D, 8, QSPLIT>(a, ja, ready, s);
+        case 1: return launch_decode_mma_t<D, 1, QSPLIT>(a, ready, s);
+        case 2: return launch_decode_mma_t<D, 2, QSPLIT>(a, ready, s);
+        case 4: return launch_decode_mma_t<D, 4, QSPLIT>(a, ready, s);
+        case 8: return launch_decode_mma_t<D, 8, QSPLIT>(a, ready, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -497,12 +459,10 @@ cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws,
     if (units == 0) return cudaSuccess;
     DecodeArgs a = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out,
                                sel_slot, slot_C);
-    if (g.kv_bf16) {   // tensor-core path, job-based
-        const JobArgs ja = job_args(g, L, ws);
+    if (g.kv_bf16) {   // tensor-core path
         if (g.q_bf16)
-            return g.D == 128 ? dispatch_jobs<128, false>(a, ja, g.G, ready, s)
-                              : dispatch_jobs<64, false>(a, ja, g.G, ready, s);
-        return g.D == 128 ? dispatch_jobs<128, true>(a, ja, g.G, ready, s) : dispatch_jobs<64, true>(a, ja, g.G, ready, s);
+            return g.D == 128 ? dispatch_mma<128, false>(a, g.G, ready, s) : dispatch_mma<64, false>(a, g.G, ready, s);
+        return g.D == 128 ? dispatch_mma<128, true>(a, g.G, ready, s) : dispatch_mma<64, true>(a, g.G, ready, s);
     }
     return g.D == 128 ? dispatch_group<128, false>(a, g.G, s) : dispatch_group<64, false>(a, g.G, s);
 }

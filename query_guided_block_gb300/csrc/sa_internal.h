@@ -52,10 +52,8 @@ struct WorkspaceLayout {
     size_t part_o;         // float [B*Hq, max_splits, D]
     size_t total;
     int score_cols;        // candidates per unit row of the score buffer
-    int max_splits;        // decode work items (split-K slices) per unit: partial slots per head
+    int max_splits;        // decode work items (split-K slices) per unit
     int blocks_per_split;  // selected blocks per decode work item
-    int job_blocks;        // selected blocks per job of the bf16 job-based decode (256 tokens)
-    int jobs_per_unit;     // its jobs per unit (<= max_splits)
 };
 
 WorkspaceLayout workspace_layout(const Geometry& g);
@@ -91,9 +89,8 @@ inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, Setup 
 }
 constexpr int kSmemPerSm = 228 * 1024;
 
-// Selected blocks per decode work item (fp32 item-based decode, and the multi-query
-// splits' upper bound), and whether a (D, dtype, block, group) combination fits the
-// decode kernels.
+// Selected blocks per decode work item, and whether a (D, dtype, block, group)
+// combination fits the decode kernel's shared-memory pipeline.
 int decode_blocks_per_item(int D, bool kv_bf16, int block_size);
 bool decode_supported(int D, bool kv_bf16, int block_size, int G);
 

@@ -4,24 +4,24 @@
 // the attention over the selected tokens as two stages of one decode step.  Here both
 // stages run in one cooperative grid, one CTA (eight worker warps and a control warp)
 // per SM, arranged so that HBM stays busy across the hand-off between them:
-//   1. streaming: worker warp W scores metadata slabs W, W + NW, ... of the unit-major
-//      slab list (NW worker warps in the grid), so units complete one after another
-//      through the whole phase rather than all at its end; the warp whose count
-//      completes a unit queues it for its CTA's control warp and keeps streaming;
-//   2. ranking: the control warp ranks each queued unit on its own (warp-level radix
-//      select over the unit's scores, lower block id first on ties), writes the
-//      selection and publishes ready[u] = the step's number (release) -- while the
-//      workers of every CTA go on streaming;
-//   3. decode: from the start the control warp also takes 256-token decode jobs from a
-//      device-wide counter (unit order) and, once a job's unit is published, resolves
-//      its pages into a descriptor ring; when its workers have streamed their slabs they
-//      run the jobs (sa_job_decode.cuh), the early units' jobs first.
-// Only the last units' ranking is on the critical path, and it overlaps the decode of
-// all the others.  Nothing in the grid waits on a CTA that is not resident (cooperative
-// launch), every wait is bounded, and the last CTA to finish advances the step epoch.
-// Problems the control warp cannot rank on chip (more than kRankMaxKeys candidates)
-// run as the select kernel followed by the job decode kernel, launched as its
-// programmatic dependent and waiting per unit on the same flags.
+//   1. streaming: the metadata slabs are listed unit by unit and cut into groups of
+//      four; worker warp W scores groups W, W + NW, ... (NW worker warps in the grid),
+//      so units complete one after another through the whole phase rather than all at
+//      its end; the warp whose count completes a unit puts it on a device-wide queue
+//      and keeps streaming;
+//   2. ranking: control warps take queue positions as they come free and rank each unit
+//      on their own (bisection over the key values, lower block id first on ties),
+//      write the selection and publish ready[u] = the step's number (release) -- while
+//      the workers of every CTA go on streaming, so only the last units' ranking is
+//      exposed;
+//   3. decode: once its workers have streamed their groups, the CTA runs the decode
+//      kernel's warp-slab attention over its own contiguous range of decode items,
+//      waiting (bounded, acquire) only for the units of that range.
+// Nothing in the grid waits on a CTA that is not resident (cooperative launch), every
+// wait is bounded, and the last CTA to finish advances the step epoch.  Problems the
+// control warp cannot rank on chip (more than kRankMaxKeys candidates) or whose decode
+// ranges do not fit one CTA per SM run as the select kernel followed by the decode
+// kernel, launched as its programmatic dependent and waiting per unit on the same flags.
 #include "sa_step_kernel.cuh"
 
 namespace sa {
@@ -33,9 +33,8 @@ bool step_supported(const Geometry& g)
 
 int step_launches(const Geometry& g, const WorkspaceLayout& L)
 {
-    (void)L;
     if (g.units() == 0) return 0;
-    const int single = g.D == 64 ? step_single_ctas<64>(g) : step_single_ctas<128>(g);
+    const int single = g.D == 64 ? step_single_ctas<64>(g, L) : step_single_ctas<128>(g, L);
     return single > 0 ? 1 : 2;
 }
 

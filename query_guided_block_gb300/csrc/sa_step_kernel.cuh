@@ -5,12 +5,15 @@
 
 #include <limits.h>
 
-#include "sa_job_decode.cuh"
+#include "sa_decode_body.cuh"
 #include "sa_select_body.cuh"
 
 namespace sa {
 namespace {
 
+constexpr int kWorkerWarps = kDecWarps;                   // stream, then decode
+constexpr int kCtlWarp = kWorkerWarps;                    // the control warp follows the workers
+constexpr int kStepThreads = (kWorkerWarps + 1) * 32;
 constexpr int kRankMaxKeys = 4096;   // candidates per unit the control warp ranks on chip
 constexpr int kRankMaxRows = 8192;   // blocks per unit its reserve-set bitmap covers
 constexpr int kRankList = 256;       // candidates kept once the k-th key is bracketed this tightly
@@ -23,10 +26,11 @@ constexpr int kWarpRingBytes = kSlabSelStages * kSlabSelBytes;
 constexpr size_t kStepRingBytes = size_t(kWorkerWarps) * kWarpRingBytes;
 
 // Dynamic shared memory of the fused kernel: alignment slack, worker rings, the decode
-// job descriptors and the control warp's key row.
+// range's page cache and the control warp's key row.
+constexpr size_t kStepPageCacheBytes = size_t(2) * kMaxRangeBlocks * sizeof(int);
 constexpr size_t step_smem_bytes()
 {
-    return 1024 + kStepRingBytes + size_t(kJobRing) * sizeof(JobDesc) + size_t(kRankMaxKeys) * sizeof(uint32_t);
+    return 1024 + kStepRingBytes + kStepPageCacheBytes + size_t(kRankMaxKeys) * sizeof(uint32_t);
 }
 
 // The control warp's ranking scratch and the workers' streaming count (static shared memory).
@@ -264,6 +268,7 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
     __syncwarp();
     uint32_t lo = 0xffffffffu, hi = 0u;
     int nv = 0;
+#pragma unroll 8
     for (int c = lane; c < n128; c += 32) {
         uint32_t key = 0u;
         if (c < n && candidate_row(a, u, c) >= 0) key = order_key(__uint_as_float(keys[c]));
@@ -282,6 +287,7 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
     const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
     auto count_all = [&](uint32_t t) -> int {   // keys >= t (t > 0)
         int c = 0;
+#pragma unroll 8
         for (int i = lane; i < n128 / 4; i += 32) {
             const uint4 v = keys4[i];
             c += (v.x >= t) + (v.y >= t) + (v.z >= t) + (v.w >= t);
@@ -291,11 +297,13 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
     int nl = 0;   // gathered candidates (0: not gathered)
     auto count_list = [&](uint32_t t) -> int {
         int c = 0;
+#pragma unroll 8
         for (int i = lane; i < nl; i += 32) c += rs.list_key[i] >= t;
         return __reduce_add_sync(kFullMask, c);
     };
     auto gather = [&](uint32_t t) {   // keys >= t into the list, index order
         int run = 0;
+#pragma unroll 4
         for (int c0 = 0; c0 < n128; c0 += 32) {
             const uint32_t key = keys[c0 + lane];
             const bool in = key >= t && key != 0u;
@@ -415,86 +423,62 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
 
 // ----------------------------------------------------------------- kernel ---
 template <int KIND, int D, int G, bool QSPLIT>
-__global__ void __launch_bounds__(kJobThreads, 1)
-    step_kernel(SelectArgs sa_args, DecodeArgs da, JobArgs ja, StepArgs st)
+__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(SelectArgs sa_args, DecodeArgs da, StepArgs st)
 {
+    static_assert(SlabShape<D>::RING_BYTES == kStepRingBytes, "the decode rings are the streaming rings");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;   // the decode swizzle repeats every 1024 bytes
     unsigned char* smem = smem_raw + (base - raw);
-    JobDesc* desc = reinterpret_cast<JobDesc*>(smem + kStepRingBytes);
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kStepRingBytes + size_t(kJobRing) * sizeof(JobDesc));
-    __shared__ JobSync js;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kStepRingBytes + kStepPageCacheBytes);
     __shared__ RankSync rs;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        js.consumed = 0;
-        js.merge_unit = -1;
-        js.avail = -1;
-        js.end_job = INT_MAX;
-        js.abort = 0;
-        js.workers_done = 0;
-    }
-    if (tid < kJobRing) desc[tid].seq = 0;
     grid_dependency_wait();   // inputs and workspace may come from the previous kernel
     const uint32_t flag_value = step_flag_value(sa_args.err);
-    const long long handoff_cycles = handoff_wait_limit(sa_args.err);
-    __syncthreads();
 
     if (warp == kCtlWarp) {
         // control warp: rank completed units taken from the device-wide queue (whichever
-        // control warp is free takes the next position), and feed this CTA's decode jobs
-        JobFeeder f = feeder_init();
+        // control warp is free takes the next position)
         int claim = -1;               // queue position this warp ranks once it is filled
-        bool claims_done = false;     // every position is taken
         long long idle_since = -1;    // no progress since then (bounded like every wait)
         while (true) {
-            if (claim < 0 && !claims_done) {
+            if (claim < 0) {
                 uint32_t h = 0;
                 if (lane == 0) h = atomicAdd(st.head, 1u);
                 h = __shfl_sync(kFullMask, h, 0);
-                if (h < uint32_t(st.units)) claim = int(h);
-                else claims_done = true;
+                if (h >= uint32_t(st.units)) break;   // every position is taken
+                claim = int(h);
                 idle_since = -1;
+            }
+            unsigned long long v = 0;
+            if (lane == 0) v = ld_acquire_gpu_u64(st.queue + claim);
+            v = __shfl_sync(kFullMask, v, 0);
+            __syncwarp();
+            if (uint32_t(v >> 32) == flag_value) {
+                rank_unit(sa_args, int(uint32_t(v)) - 1, keys, rs, st.ready, flag_value);
+                claim = -1;
                 continue;
             }
-            if (claim >= 0) {
-                unsigned long long v = 0;
-                if (lane == 0) v = ld_acquire_gpu_u64(st.queue + claim);
-                v = __shfl_sync(kFullMask, v, 0);
-                __syncwarp();
-                if (uint32_t(v >> 32) == flag_value) {
-                    rank_unit(sa_args, int(uint32_t(v)) - 1, keys, rs, st.ready, flag_value);
-                    claim = -1;
-                    idle_since = -1;
-                    continue;
-                }
-            }
-            if (feeder_step<D, G, QSPLIT>(f, da, ja, desc, js, st.ready, flag_value, handoff_cycles)) {
-                idle_since = -1;
-                continue;
-            }
-            if (claims_done && claim < 0 && (f.ended || ld_acquire_cta_shared(&js.workers_done) != 0)) break;
             const long long now = clock64();
             if (idle_since < 0) idle_since = now;
-            if (now - idle_since > 2 * kWaitCycles) {
+            if (now - idle_since > kWaitCycles) {
                 if (lane == 0) raise_error(sa_args.err, SPARSE_ATTN_ERR_TIMEOUT);
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(128);
         }
     } else {
         const uint32_t ring = base + uint32_t(warp) * kWarpRingBytes;
         worker_stream<KIND, D, G, QSPLIT>(sa_args, st, flag_value, smem + size_t(warp) * kWarpRingBytes, ring);
-        worker_decode<D, G, QSPLIT>(da, ja, desc, js, smem, ring, kWaitCycles);
+        decode_mma_body<D, G, QSPLIT>(da, st.ready, flag_value);   // waits per unit on the published selections
     }
-    finish_jobs(sa_args.err, true, flag_value);
+    finish_step(sa_args.err, flag_value);
 }
 
 template <int KIND, int D, int G, bool QSPLIT>
-cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const JobArgs& ja, const StepArgs& st,
-                          int ctas, cudaStream_t s)
+cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const StepArgs& st, int ctas,
+                          cudaStream_t s)
 {
     constexpr size_t smem = step_smem_bytes();
     auto kernel = step_kernel<KIND, D, G, QSPLIT>;
@@ -503,7 +487,7 @@ cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kJobThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStepThreads, smem);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorNotSupported;
         return cudaSuccess;
@@ -511,7 +495,7 @@ cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const
     if (set_up != cudaSuccess) return set_up;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(ctas));
-    cfg.blockDim = dim3(kJobThreads);
+    cfg.blockDim = dim3(kStepThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -519,32 +503,41 @@ cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, const
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, sa_args, da, ja, st);
+    return cudaLaunchKernelEx(&cfg, kernel, sa_args, da, st);
 }
 
 template <int KIND, int D, bool QSPLIT>
-cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, const JobArgs& ja, const StepArgs& st,
-                            int ctas, int G, cudaStream_t s)
+cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, const StepArgs& st, int ctas, int G,
+                            cudaStream_t s)
 {
     switch (G) {
-        case 1: return launch_step_t<KIND, D, 1, QSPLIT>(sa_args, da, ja, st, ctas, s);
-        case 2: return launch_step_t<KIND, D, 2, QSPLIT>(sa_args, da, ja, st, ctas, s);
-        case 4: return launch_step_t<KIND, D, 4, QSPLIT>(sa_args, da, ja, st, ctas, s);
-        case 8: return launch_step_t<KIND, D, 8, QSPLIT>(sa_args, da, ja, st, ctas, s);
+        case 1: return launch_step_t<KIND, D, 1, QSPLIT>(sa_args, da, st, ctas, s);
+        case 2: return launch_step_t<KIND, D, 2, QSPLIT>(sa_args, da, st, ctas, s);
+        case 4: return launch_step_t<KIND, D, 4, QSPLIT>(sa_args, da, st, ctas, s);
+        case 8: return launch_step_t<KIND, D, 8, QSPLIT>(sa_args, da, st, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-// CTAs of the single-launch step (one per SM), or 0 when the problem runs as two
-// kernels: the control warp holds at most kRankMaxKeys candidate keys of a unit (and a
-// bitmap of kRankMaxRows blocks for a reserve set).
+// CTAs of the single-launch step (one per SM, fewer when there are fewer decode items),
+// or 0 when the problem runs as two kernels: the control warp holds at most
+// kRankMaxKeys candidate keys of a unit (and a bitmap of kRankMaxRows blocks for a
+// reserve set), and every CTA's decode range must fit its page cache and touch at most
+// 62 units -- the decode kernel's own grid is then the same, so both cut the decode
+// into the same partials and give the same bits.
 template <int D>
-int step_single_ctas(const Geometry& g)
+int step_single_ctas(const Geometry& g, const WorkspaceLayout& L)
 {
     const int units = g.units();
     if (units == 0 || g.n_cand > kRankMaxKeys) return 0;
     if (g.n_reserve > 0 && g.nb > kRankMaxRows) return 0;
-    return num_sms();
+    const long long items = (long long)units * L.max_splits;
+    long long ctas = num_sms();
+    if (ctas > items) ctas = items;
+    const long long min_ctas = (items * L.blocks_per_split + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
+    const long long min_ctas_units = (units + 61) / 62;
+    if (ctas < 1 || ctas < min_ctas || ctas < min_ctas_units) return 0;
+    return int(ctas);
 }
 
 template <int D>
@@ -556,7 +549,7 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
 {
     const int units = g.units();
     if (units == 0) return cudaSuccess;
-    const int ctas = step_single_ctas<D>(g);
+    const int ctas = step_single_ctas<D>(g, L);
     if (ctas == 0) return cudaErrorNotSupported;
     const bool mean = g.score_kind == SPARSE_ATTN_SCORE_MEAN;
 
@@ -565,7 +558,6 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
     if (mean) set_slab_chunking<KIND_MEAN, false, D>(sa_args, units);
     else set_slab_chunking<KIND_QUEST, true, D>(sa_args, units);
     DecodeArgs da = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out, nullptr, 0);
-    const JobArgs ja = job_args(g, L, ws);
     StepArgs st{};
     st.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
     st.queue = reinterpret_cast<unsigned long long*>(ws + L.rank_queue);
@@ -575,10 +567,10 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
 
     const bool qs = !g.q_bf16;
     if (mean)
-        return qs ? dispatch_step_g<KIND_MEAN, D, true>(sa_args, da, ja, st, ctas, g.G, s)
-                  : dispatch_step_g<KIND_MEAN, D, false>(sa_args, da, ja, st, ctas, g.G, s);
-    return qs ? dispatch_step_g<KIND_QUEST, D, true>(sa_args, da, ja, st, ctas, g.G, s)
-              : dispatch_step_g<KIND_QUEST, D, false>(sa_args, da, ja, st, ctas, g.G, s);
+        return qs ? dispatch_step_g<KIND_MEAN, D, true>(sa_args, da, st, ctas, g.G, s)
+                  : dispatch_step_g<KIND_MEAN, D, false>(sa_args, da, st, ctas, g.G, s);
+    return qs ? dispatch_step_g<KIND_QUEST, D, true>(sa_args, da, st, ctas, g.G, s)
+              : dispatch_step_g<KIND_QUEST, D, false>(sa_args, da, st, ctas, g.G, s);
 }
 
 }  // namespace
