@@ -5,8 +5,10 @@ One step = one pass of the hot path over one batch of decode queries:
 select (score every block from its metadata + top-k + window) and decode (exact
 softmax attention over the selected blocks), plus the diff/LRU step for the
 multi-step workload.  Inputs are resident in HBM when the timed region starts;
-the L2 is flushed (a 2x-L2 write) before every timed step, outside the step's
-events.  Each kernel is bracketed by CUDA events on the launching stream.
+the L2 is flushed before every timed step, outside the step's events: a buffer of
+twice the L2 size is written and then read back, so the L2 holds only clean lines of
+unrelated data (a write alone would leave the L2 full of dirty lines, and the timed
+step would pay for writing them back).  Each kernel is bracketed by CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
@@ -267,7 +269,17 @@ def run_gpu_arm(args):
     meta_bytes = kp.numel() * esz + dec.metadata_bytes() + bt.numel() * 4
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_sum = torch.empty((), dtype=torch.int64, device=dev)
+
+    class _Flush:   # write a 2x-L2 buffer, then read it back: the L2 ends clean
+        def zero_(self):
+            flush_buf.zero_()
+            torch.sum(flush_buf.view(torch.int64), out=flush_sum)
+
+        def numel(self):
+            return flush_buf.numel()
+    flush = _Flush()
 
     # one appended token per sequence (a decode step's metadata upkeep), L2 flushed before each
     app_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
@@ -505,7 +517,8 @@ def run_gpu_arm(args):
                    "block_size": w.block_size, "topk_blocks": w.topk,
                    "window_tokens": w.window_tokens, "two_level": w.two_level,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"flushed before every step ({flush.numel() >> 20} MB write, outside the step events)",
+                   "l2": f"flushed before every step ({flush.numel() >> 20} MB written then read back, "
+                         "outside the step events)",
                    "step": (f"sparse_attn_step ({step_launches} launch{'es' if step_launches > 1 else ''})"
                             if use_step else "sparse_attn_select + sparse_attn_decode"),
                    "timing": "CUDA events per call on the launching stream"},

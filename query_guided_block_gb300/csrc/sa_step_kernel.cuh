@@ -78,7 +78,7 @@ __device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsign
 // queues the unit device-wide; the count's result is looked at one group later, so its
 // round trip overlaps the next group.
 template <int KIND, int D, int G, bool QSPLIT>
-__device__ void worker_stream(const SelectArgs& a, const StepArgs& st, uint32_t flag_value, unsigned char* ring_ptr,
+__device__ __forceinline__ void worker_stream(const SelectArgs& a, const StepArgs& st, uint32_t flag_value, unsigned char* ring_ptr,
                               uint32_t ring)
 {
     using SS = SelectShape<KIND, KIND == KIND_QUEST, D>;
@@ -254,13 +254,22 @@ __device__ void worker_stream(const SelectArgs& a, const StepArgs& st, uint32_t 
 //     (lower block id first), emitted in ascending order by ballots, then the window;
 //     with a reserve set the top-k rows and the reserve blocks go through a bitmap.
 // The unit is then published (fence + release store of the step's flag value).
-__device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& rs, uint32_t* ready,
-                          uint32_t flag_value)
+__device__ __forceinline__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& rs,
+                                          uint32_t* ready, uint32_t flag_value)
 {
     const int lane = threadIdx.x & 31;
     const uint32_t lt = lanemask_lt();
+    // single-level selection: candidate c is block row c when c < row_limit (the kernel
+    // parameters are read once, into registers)
     const int n = a.n_cand;
+    const int lim = min(a.n_cand, a.row_limit);
     const int n128 = (n + 127) & ~127;
+    const int k_req = a.k, rows = a.rows, win_first = a.win_first, win_count = a.win_count;
+    const int n_reserve = a.n_reserve;
+    const int32_t* reserve = a.reserve;
+    uint32_t* err = a.err;
+    int32_t* out = a.out_ids + size_t(u) * a.out_stride;
+    int32_t* out_count = a.out_count;
     const float* row = a.scores + size_t(u) * a.n_cand;
     for (int c = lane; c < n; c += 32) cp_async_4(smem_u32(keys + c), row + c);
     cp_async_commit();
@@ -271,7 +280,7 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
 #pragma unroll 8
     for (int c = lane; c < n128; c += 32) {
         uint32_t key = 0u;
-        if (c < n && candidate_row(a, u, c) >= 0) key = order_key(__uint_as_float(keys[c]));
+        if (c < lim) key = order_key(__uint_as_float(keys[c]));
         keys[c] = key;
         if (key) {
             lo = min(lo, key);
@@ -283,7 +292,7 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
     lo = __reduce_min_sync(kFullMask, lo);
     hi = __reduce_max_sync(kFullMask, hi);
     __syncwarp();
-    const int k_eff = min(a.k, nv);
+    const int k_eff = min(k_req, nv);
     const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
     auto count_all = [&](uint32_t t) -> int {   // keys >= t (t > 0)
         int c = 0;
@@ -359,25 +368,21 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
         return key > T || (key == T && c <= cT);
     };
 
-    int32_t* out = a.out_ids + size_t(u) * a.out_stride;
     int total = 0;
-    if (a.n_reserve > 0) {
+    if (n_reserve > 0) {
         // Reserve set (SparDA page §3.4): top-k rows and reserve blocks outside the window
         // marked in a bitmap over block ids, emitted in ascending order
         __syncwarp();   // the gathered list is not used past here; its storage holds the bitmap
         uint32_t* bits = rs.list_key;        // <= kRankList words: rows <= kRankMaxRows
-        const int nw = (a.rows + 31) >> 5;
+        const int nw = (rows + 31) >> 5;
         for (int i = lane; i < nw; i += 32) bits[i] = 0u;
         __syncwarp();
-        for (int c = lane; c < n; c += 32)
-            if (selected(keys[c], c)) {
-                const int r = candidate_row(a, u, c);
-                atomicOr(&bits[r >> 5], 1u << (r & 31));
-            }
-        for (int i = lane; i < a.n_reserve; i += 32) {
-            const int j = a.reserve[size_t(u) * a.n_reserve + i];
-            if (j < 0 || j >= a.rows) raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
-            else if (j < a.win_first) atomicOr(&bits[j >> 5], 1u << (j & 31));
+        for (int c = lane; c < lim; c += 32)
+            if (selected(keys[c], c)) atomicOr(&bits[c >> 5], 1u << (c & 31));
+        for (int i = lane; i < n_reserve; i += 32) {
+            const int j = reserve[size_t(u) * n_reserve + i];
+            if (j < 0 || j >= rows) raise_error(err, SPARSE_ATTN_ERR_SEL_ID);
+            else if (j < win_first) atomicOr(&bits[j >> 5], 1u << (j & 31));
         }
         __syncwarp();
         for (int w0 = 0; w0 < nw; w0 += 32) {
@@ -399,20 +404,20 @@ __device__ void rank_unit(const SelectArgs& a, int u, uint32_t* keys, RankSync& 
             const int p = c0 + lane;
             const bool sel = p < nl && selected(rs.list_key[p], int(rs.list_idx[p]));
             const uint32_t b = __ballot_sync(kFullMask, sel);
-            if (sel) out[total + __popc(b & lt)] = candidate_row(a, u, int(rs.list_idx[p]));
+            if (sel) out[total + __popc(b & lt)] = int(rs.list_idx[p]);
             total += __popc(b);
         }
     } else {
         for (int c0 = 0; c0 < n128; c0 += 32) {
             const int c = c0 + lane;
-            const bool sel = c < n && selected(keys[c], c);
+            const bool sel = c < lim && selected(keys[c], c);
             const uint32_t b = __ballot_sync(kFullMask, sel);
-            if (sel) out[total + __popc(b & lt)] = candidate_row(a, u, c);
+            if (sel) out[total + __popc(b & lt)] = c;
             total += __popc(b);
         }
     }
-    for (int i = lane; i < a.win_count; i += 32) out[total + i] = a.win_first + i;
-    if (lane == 0) a.out_count[u] = total + a.win_count;
+    for (int i = lane; i < win_count; i += 32) out[total + i] = win_first + i;
+    if (lane == 0) out_count[u] = total + win_count;
     __syncwarp();
     if (lane == 0) {
         __threadfence();

@@ -110,12 +110,13 @@ def test_repeated_steps_reset_the_ready_flags():
     compare_all(w, inp, b)
 
 
-def test_many_small_units_in_one_launch():
-    """9600 units of a few blocks each: every CTA's control warp ranks dozens of units
-    while the workers stream; one cooperative launch, equal to the two calls."""
+def test_many_small_units():
+    """9600 units of a few blocks each: more than one CTA per SM's decode ranges can
+    cover, so the step runs as the select kernel followed by the decode kernel waiting
+    per unit on the published selections; equal to the two calls."""
     w = _w(batch=1200, num_q_heads=8, num_kv_heads=8, n_tokens=200, block_size=16, window_tokens=40,
            topk=3, planted_per_unit=0)
-    assert B.sparse_attn_step_launches(B.params_for(w)) == 1
+    assert B.sparse_attn_step_launches(B.params_for(w)) == 2
     inp = make_inputs(w, "cuda")
     a, b = _pair(w, inp)
     for _ in range(2):   # consecutive steps: each waits for its own selections
@@ -126,8 +127,8 @@ def test_many_small_units_in_one_launch():
 
 def test_two_kernel_path_for_wide_candidate_rows():
     """More candidates per unit than the control warp ranks on chip (4096): the step runs
-    as the select kernel followed by the job decode kernel, launched as its dependent
-    and waiting per unit on the published selections."""
+    as the select kernel followed by the decode kernel, launched as its dependent and
+    waiting per unit on the published selections."""
     w = _w(batch=3, num_q_heads=16, num_kv_heads=4, n_tokens=150000, block_size=32, window_tokens=500,
            topk=40, planted_per_unit=6)
     assert B.sparse_attn_step_launches(B.params_for(w)) == 2
