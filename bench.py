@@ -275,7 +275,7 @@ def run_gpu_arm(args):
     class _Flush:   # write a 2x-L2 buffer, then read it back: the L2 ends clean
         def zero_(self):
             flush_buf.zero_()
-            torch.sum(flush_buf.view(torch.int64), out=flush_sum)
+            torch.sum(flush_buf.view(torch.int64), dim=0, out=flush_sum)
 
         def numel(self):
             return flush_buf.numel()
