@@ -130,8 +130,7 @@ WorkspaceLayout workspace_layout(const Geometry& g)
 
     size_t off = 0;
     // one 256-byte header: error word, the persistent kernels' work counters, the wait
-    // limit (bytes 24-31), the fused step's epoch and completion count (32-39) and its
-    // rank-queue head and tail (40-47)
+    // limit (bytes 24-31) and the fused step's epoch and completion count (32-39)
     L.err = 0;
     L.sel_work = 4;
     L.sel_done = 8;
@@ -142,7 +141,6 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     L.dec_counters = off;     off = align256(off + dec_cells * sizeof(uint32_t));
     L.l1_counters = off;      off = align256(off + units * sizeof(uint32_t));
     L.ready = off;            off = align256(off + units * sizeof(uint32_t));
-    L.rank_queue = off;       off = align256(off + units * sizeof(uint64_t));
     L.scores = off;           off = align256(off + units * L.score_cols * sizeof(float));
     L.survivors = off;        off = align256(off + units * size_t(g.topk_coarse > 0 ? g.topk_coarse : 1) * sizeof(int32_t));
     L.n_survivors = off;      off = align256(off + units * sizeof(int32_t));

@@ -366,8 +366,6 @@ __device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t
 constexpr int kHdrWaitLimit = int(kHdrWaitLimitByte);   // uint64: wait limit in SM clocks, 0 = kWaitCycles
 constexpr int kHdrStepEpoch = 32;   // uint32: fused steps completed on this workspace
 constexpr int kHdrStepDone = 36;    // uint32: CTAs of the running step that have finished
-constexpr int kHdrRankHead = int(kHdrRankHeadByte);   // uint32: queue positions taken for ranking
-constexpr int kHdrRankTail = int(kHdrRankTailByte);   // uint32: completed units queued
 
 __device__ __forceinline__ uint32_t* header_word(uint32_t* err, int byte)
 {
@@ -399,9 +397,8 @@ __device__ __forceinline__ uint32_t step_flag_value(uint32_t* err)
 
 // The end of one CTA's share of the launch that completes a step (the fused kernel, or
 // the decode kernel behind the step's select kernel): the last CTA of the grid to
-// finish resets the completion count and the rank queue for the next step and stores
-// the step's number as the new epoch.  After the kernel boundary every later launch
-// sees them.
+// finish resets the completion count for the next step and stores the step's number as
+// the new epoch.  After the kernel boundary every later launch sees them.
 __device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
 {
     __syncthreads();
@@ -410,8 +407,6 @@ __device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
         uint32_t* done = header_word(err, kHdrStepDone);
         if (atomic_add_acq_rel_u32(done, 1u) + 1u == gridDim.x) {
             *done = 0u;
-            *header_word(err, kHdrRankHead) = 0u;
-            *header_word(err, kHdrRankTail) = 0u;
             st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
         }
     }

@@ -43,7 +43,6 @@ struct WorkspaceLayout {
     size_t dec_counters;   // uint32 [units]
     size_t l1_counters;    // uint32 [units] (two-level, level 1)
     size_t ready;          // uint32 [units] (fused step: unit's selection published)
-    size_t rank_queue;     // uint64 [units] (fused step: completed units, in completion order)
     size_t scores;         // float [units, score_cols]
     size_t survivors;      // int32 [units, topk_coarse] (two-level)
     size_t n_survivors;    // int32 [units]
@@ -61,8 +60,6 @@ WorkspaceLayout workspace_layout(const Geometry& g);
 // Byte offset of the wait-limit word in the workspace header (kHdrWaitLimit on the
 // device side).
 constexpr size_t kHdrWaitLimitByte = 24;
-constexpr size_t kHdrRankHeadByte = 40;   // fused step's rank-queue head and tail (uint32 each)
-constexpr size_t kHdrRankTailByte = 44;
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();

@@ -2,26 +2,20 @@
 //
 // "SGLang分层稀疏注意力技术解析与优化实践" §1.2 (select-then-compute) runs selection and
 // the attention over the selected tokens as two stages of one decode step.  Here both
-// stages run in one cooperative grid, one CTA (eight worker warps and a control warp)
-// per SM, arranged so that HBM stays busy across the hand-off between them:
-//   1. streaming: the metadata slabs are listed unit by unit and cut into groups of
-//      four; worker warp W scores groups W, W + NW, ... (NW worker warps in the grid),
-//      so units complete one after another through the whole phase rather than all at
-//      its end; the warp whose count completes a unit puts it on a device-wide queue
-//      and keeps streaming;
-//   2. ranking: control warps take queue positions as they come free and rank each unit
-//      on their own (bisection over the key values, lower block id first on ties),
-//      write the selection and publish ready[u] = the step's number (release) -- while
-//      the workers of every CTA go on streaming, so only the last units' ranking is
-//      exposed;
-//   3. decode: once its workers have streamed their groups, the CTA runs the decode
-//      kernel's warp-slab attention over its own contiguous range of decode items,
-//      waiting (bounded, acquire) only for the units of that range.
-// Nothing in the grid waits on a CTA that is not resident (cooperative launch), every
-// wait is bounded, and the last CTA to finish advances the step epoch.  Problems the
-// control warp cannot rank on chip (more than kRankMaxKeys candidates) or whose decode
-// ranges do not fit one CTA per SM run as the select kernel followed by the decode
-// kernel, launched as its programmatic dependent and waiting per unit on the same flags.
+// stages run in a single cooperative grid of one CTA (8 warps) per SM:
+//   1. select phase: every warp streams its own 8 KB metadata slabs through a private
+//      cp.async ring and scores them (the select kernel's arithmetic, so the scores are
+//      the same bits); the warp completing a unit records it, and once the CTA has
+//      finished streaming it ranks and emits its completed units, publishing
+//      ready[u] = 1 (device-scope release) for each;
+//   2. decode phase: the decode kernel's warp-independent tensor-core attention; each
+//      CTA waits (bounded, acquire) only for the units of its own item range instead of
+//      for the whole selection, and the CTA merging a unit clears ready[u].
+// The select phase never waits on another CTA and a cooperative launch keeps every CTA
+// resident, so each wait of the decode phase ends.  Shared memory: the select rings and
+// keys alias the decode rings (a barrier separates the phases).  Problems whose grid
+// does not fit this shape run as the select kernel followed by the decode kernel,
+// launched as its programmatic dependent and waiting per unit on the same flags.
 #include "sa_step_kernel.cuh"
 
 namespace sa {

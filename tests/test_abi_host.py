@@ -139,16 +139,13 @@ def test_capacity_workspace_covers_every_length(name):
 
 
 def test_step_launch_plan():
-    """sparse_attn_step's plan, decided on the host: one cooperative launch while each
-    unit's candidates fit the control warp's on-chip ranking (4096 keys), select +
-    dependent decode beyond that, refused for problems it does not cover."""
+    """sparse_attn_step's plan, decided on the host: one cooperative launch while the
+    units fit one CTA per SM, select + dependent decode beyond that, refused for
+    problems it does not cover."""
     import dataclasses
-    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["gqa_128k"])) == 1      # 4080 candidates
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["gqa_128k"])) == 1      # 128 units
     assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["reserve_128k"])) == 1
-    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["mha_32k"])) == 1       # 256 units
-    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["lru_64k"])) == 1
-    wide = dataclasses.replace(WORKLOADS["gqa_128k"], n_tokens=200000)              # 6234 candidates
-    assert B.sparse_attn_step_launches(B.params_for(wide)) == 2
+    assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["mha_32k"])) == 2       # 256 units
     assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["two_level_256k"])) == -1
     assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["tiny_fp32_4k"])) == -1  # fp32 K/V
     assert B.sparse_attn_step_launches(B.params_for(WORKLOADS["mq_128k"])) == -1       # Q > 1

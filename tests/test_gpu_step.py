@@ -125,21 +125,6 @@ def test_many_small_units():
     compare_every_unit(w, inp, b)
 
 
-def test_two_kernel_path_for_wide_candidate_rows():
-    """More candidates per unit than the control warp ranks on chip (4096): the step runs
-    as the select kernel followed by the decode kernel, launched as its dependent and
-    waiting per unit on the published selections."""
-    w = _w(batch=3, num_q_heads=16, num_kv_heads=4, n_tokens=150000, block_size=32, window_tokens=500,
-           topk=40, planted_per_unit=6)
-    assert B.sparse_attn_step_launches(B.params_for(w)) == 2
-    inp = make_inputs(w, "cuda")
-    a, b = _pair(w, inp)
-    for _ in range(2):
-        _run_both(w, inp, a, b, _q(inp))
-        _assert_same(a, b)
-    compare_every_unit(w, inp, b)
-
-
 @pytest.mark.parametrize("case", ["two_level", "fp32_kv", "multi_query"])
 def test_unsupported_problems_are_refused(case):
     kw = {"two_level": dict(two_level=True, n_tokens=40000, coarse_block=1024, topk_coarse=4),
