@@ -366,7 +366,9 @@ cudaError_t launch_decode_t(DecodeArgs a, cudaStream_t s)
     const long long min_ctas_units = (a.units + 61) / 62;
     if (ctas < min_ctas_units) ctas = min_ctas_units;
     if (ctas > a.total_items) ctas = a.total_items;
-    return launch_after_previous(decode_kernel<D, BF16, G>, dim3(unsigned(ctas)), dim3(kDecThreads), smem, s, a);
+    DecodeArgs args = a;
+    args.ranges = int(ctas);   // this kernel's ranges: one per CTA of its own grid
+    return launch_after_previous(decode_kernel<D, BF16, G>, dim3(unsigned(ctas)), dim3(kDecThreads), smem, s, args);
 }
 
 template <int D, bool BF16>
@@ -411,13 +413,8 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, uint32_t* ready, cudaStream_t s)
                                              kDecSmemLimit);
     });
     if (cfg != cudaSuccess) return cfg;
-    long long ctas = num_sms();                    // one CTA (8 independent warps) per SM
-    const long long min_ctas = ((long long)a.total_items * a.blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
-    if (ctas < min_ctas) ctas = min_ctas;
-    const long long min_ctas_units = (a.units + 61) / 62;
-    if (ctas < min_ctas_units) ctas = min_ctas_units;
-    if (ctas > a.total_items) ctas = a.total_items;
-    return launch_after_previous(decode_mma_kernel<D, G, QSPLIT>, dim3(unsigned(ctas)), dim3(kDecThreads), smem, s, a,
+    const unsigned ctas = unsigned(a.ranges);       // one CTA (8 independent warps) per range
+    return launch_after_previous(decode_mma_kernel<D, G, QSPLIT>, dim3(ctas), dim3(kDecThreads), smem, s, a,
                                  ready);
 }
 

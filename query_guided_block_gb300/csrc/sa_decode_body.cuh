@@ -41,6 +41,7 @@ struct DecodeArgs {
     int slot_C;
     int page_heads;          // KV heads per page: Hkv, or 1 in slot mode
     int blocks_per_item, items_per_unit, total_items, units;
+    int ranges;              // CTAs 0 .. ranges - 1 own contiguous item ranges (<= the grid)
     int stages;
     float scale_log2;
     float* part_m;   // [B*Hq, items_per_unit]
@@ -51,7 +52,8 @@ struct DecodeArgs {
 };
 
 // The CTA that completed unit u merges the unit's partials.  A unit's segments start
-// at its first item and at every CTA range start inside it; each segment wrote one
+// at its first item and at every range start inside it (range c = items
+// [T c / R, T (c + 1) / R) of the T items, R = a.ranges); each segment wrote one
 // (m, l, o) partial at the slot of its first item, so segment i of a unit whose first
 // item lies in CTA c0 sits at slot max(start(c0 + i), x0) - x0.  Segments are taken
 // kMergeChunk at a time, and within a chunk every load is issued before any is used:
@@ -69,7 +71,7 @@ __device__ void merge_unit(const DecodeArgs& a, int u, int G, int D)
     const size_t head0 = size_t(b) * a.Hq + size_t(kvh) * G;
     const int ipu = a.items_per_unit;
     const long long x0 = (long long)u * ipu, x1 = x0 + ipu;
-    const long long T = a.total_items, C = gridDim.x;
+    const long long T = a.total_items, C = a.ranges;
     if (tid == 0) a.counters[u] = 0u;
     long long c0 = x0 * C / T;                                   // CTA holding item x0
     while (c0 + 1 < C && (T * (c0 + 1)) / C <= x0) ++c0;
@@ -193,7 +195,7 @@ constexpr size_t slab_smem_bytes()
     return 1024 /* alignment slack */ + SlabShape<D>::RING_BYTES + size_t(2) * kMaxRangeBlocks * sizeof(int);
 }
 
-// One CTA's share of a decode launch (CTA blockIdx.x of gridDim.x).  With `ready`
+// One CTA's share of a decode launch (range blockIdx.x of a.ranges; none beyond).  With `ready`
 // set, the CTA first waits (bounded) until ready[u] == flag_value for every unit of its
 // range (the selection may still be running in this grid or in the select kernel
 // before this one).
@@ -225,8 +227,9 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
     __shared__ int s_flush[kDecWarps];             // byte offset of each warp's flushed (o)
     __shared__ int s_merge_unit;
 
-    const int i_begin = int((long long)a.total_items * blockIdx.x / gridDim.x);
-    const int i_end = int((long long)a.total_items * (blockIdx.x + 1) / gridDim.x);
+    const bool ranged = int(blockIdx.x) < a.ranges;
+    const int i_begin = ranged ? int((long long)a.total_items * blockIdx.x / a.ranges) : 0;
+    const int i_end = ranged ? int((long long)a.total_items * (blockIdx.x + 1) / a.ranges) : 0;
     if (i_begin >= i_end) return;
     const int u_lo = i_begin / ipu;
     const int u_hi = (i_end - 1) / ipu;
@@ -448,6 +451,9 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
             if (lane == 0) s_flush[warp] = free_off;
         }
         decoder_barrier();
+        // a segment holding the whole unit is its result: no partial, no merge (the
+        // merge of one partial gives the same bits)
+        const bool whole = seg_i0 == u * ipu && seg_i1 == (u + 1) * ipu;
         const int slot = seg_i0 - u * ipu;
         for (int i = tid; i < G * D; i += kDecThreads) {
             const int g = i / D, d = i - g * D;
@@ -463,6 +469,10 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
                 o = fmaf(wt, reinterpret_cast<const float*>(smem + s_flush[w])[g * D + d], o);
                 l = fmaf(wt, s_l[w][g], l);
             }
+            if (whole) {
+                a.out[head0 * D + i] = l > 0.f ? o / l : 0.f;
+                continue;
+            }
             const size_t ps = (head0 + g) * ipu + slot;
             a.part_o[ps * D + d] = o;
             if (d == 0) {
@@ -471,6 +481,7 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
             }
         }
         decoder_barrier();                           // partials written; flush stages free again
+        if (whole) continue;
         if (tid == 0) {
             const uint32_t n = uint32_t(seg_i1 - seg_i0);
             const uint32_t before = atomic_add_acq_rel_u32(&a.counters[u], n);
@@ -485,6 +496,36 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
     cp_async_wait_group<0>();
 }
 
+
+// Item ranges of a bf16 decode launch (one per CTA).  By default one per SM (more when
+// a range would overflow a CTA's page cache or touch more than 62 units, never more
+// than there are items): the units are then cut across CTA boundaries and merged.
+// When whole units, or equal parts of units, fill at least 80% of the SMs, the ranges
+// follow the unit boundaries instead: with units <= SMs each unit is split into
+// SMs / units equal parts (one part: the segment is the result, no partial and no
+// merge); with more units than SMs each range holds the same number of whole units.
+// An SM streams about as fast as the HBM share of a full grid allows, so leaving a few
+// SMs idle costs less than the split units' partials, merges and segment ends.
+inline int decode_ranges(int units, int items_per_unit, int blocks_per_item, int sms)
+{
+    const long long T = (long long)units * items_per_unit;
+    long long R = sms;
+    const long long min_ctas = (T * blocks_per_item + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
+    const long long min_units = (units + 61) / 62;
+    if (R < min_ctas) R = min_ctas;
+    if (R < min_units) R = min_units;
+    if (R > T) R = T;
+    long long aligned = 0;
+    if (units > 0 && units <= sms) {
+        aligned = (long long)units * (sms / units);
+    } else if (units > sms) {
+        const long long per = (units + sms - 1) / sms;
+        if (units % per == 0) aligned = units / per;
+    }
+    if (aligned > 0 && 5 * aligned >= 4LL * sms && aligned >= min_ctas && aligned >= min_units && aligned <= T)
+        R = aligned;
+    return int(R < 1 ? 1 : R);
+}
 
 // Arguments of a decode launch (split-K partials and counters in the workspace).
 inline DecodeArgs decode_args(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
@@ -516,6 +557,7 @@ inline DecodeArgs decode_args(const Geometry& g, const WorkspaceLayout& L, char*
     a.items_per_unit = L.max_splits;
     a.units = g.units();
     a.total_items = g.units() * L.max_splits;
+    a.ranges = decode_ranges(g.units(), L.max_splits, L.blocks_per_split, num_sms());   // bf16 path
     a.scale_log2 = g.scale_log2;
     a.part_m = reinterpret_cast<float*>(ws + L.part_m);
     a.part_l = reinterpret_cast<float*>(ws + L.part_l);

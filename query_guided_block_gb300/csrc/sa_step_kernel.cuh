@@ -67,17 +67,16 @@ cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, uin
 }
 
 // CTAs of the fused grid: one per SM, fewer when there are fewer decode items; 0 when
-// a CTA's item range would overflow its page cache or touch too many units.
+// the decode ranges (those of the decode kernel, so both give the same bits) need more
+// CTAs than that.
 int step_ctas(const Geometry& g, const WorkspaceLayout& L)
 {
     const long long items = (long long)g.units() * L.max_splits;
     long long ctas = num_sms();
     if (ctas > items) ctas = items;
     if (ctas < 1) return 0;
-    const long long min_ctas = (items * L.blocks_per_split + kMaxRangeBlocks - 1) / kMaxRangeBlocks;
-    const long long min_ctas_units = (g.units() + 61) / 62;
-    if (ctas < min_ctas || ctas < min_ctas_units) return 0;
-    return int(ctas);
+    const int ranges = decode_ranges(g.units(), L.max_splits, L.blocks_per_split, num_sms());
+    return ranges > ctas ? 0 : int(ctas);
 }
 
 // CTAs of the single-launch step, or 0 when the problem runs as two kernels: the grid
