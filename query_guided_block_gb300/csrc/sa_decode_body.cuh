@@ -195,12 +195,12 @@ constexpr size_t slab_smem_bytes()
     return 1024 /* alignment slack */ + SlabShape<D>::RING_BYTES + size_t(2) * kMaxRangeBlocks * sizeof(int);
 }
 
-// One CTA's share of a decode launch (range blockIdx.x of a.ranges; none beyond).  With `ready`
-// set, the CTA first waits (bounded) until ready[u] == flag_value for every unit of its
-// range (the selection may still be running in this grid or in the select kernel
-// before this one).
+// Items [i_begin, i_end) of a decode launch, by one CTA.  With `ready` set, the CTA
+// first waits (bounded) until ready[u] == flag_value for every unit of the range (the
+// selection may still be running in this grid or in the select kernel before this one).
 template <int D, int G, bool QSPLIT>
-__device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* ready, uint32_t flag_value)
+__device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* ready, uint32_t flag_value,
+                                                 int i_begin, int i_end)
 {
     using SS = SlabShape<D>;
     constexpr int S = SS::STAGES;
@@ -227,9 +227,6 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
     __shared__ int s_flush[kDecWarps];             // byte offset of each warp's flushed (o)
     __shared__ int s_merge_unit;
 
-    const bool ranged = int(blockIdx.x) < a.ranges;
-    const int i_begin = ranged ? int((long long)a.total_items * blockIdx.x / a.ranges) : 0;
-    const int i_end = ranged ? int((long long)a.total_items * (blockIdx.x + 1) / a.ranges) : 0;
     if (i_begin >= i_end) return;
     const int u_lo = i_begin / ipu;
     const int u_hi = (i_end - 1) / ipu;
@@ -496,6 +493,16 @@ __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* r
     cp_async_wait_group<0>();
 }
 
+
+// One CTA's share of a decode launch: range blockIdx.x of a.ranges (none beyond).
+template <int D, int G, bool QSPLIT>
+__device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* ready, uint32_t flag_value)
+{
+    if (int(blockIdx.x) >= a.ranges) return;
+    const int i_begin = int((long long)a.total_items * blockIdx.x / a.ranges);
+    const int i_end = int((long long)a.total_items * (blockIdx.x + 1) / a.ranges);
+    decode_mma_items<D, G, QSPLIT>(a, ready, flag_value, i_begin, i_end);
+}
 
 // Item ranges of a bf16 decode launch (one per CTA).  By default one per SM (more when
 // a range would overflow a CTA's page cache or touch more than 62 units, never more

@@ -625,7 +625,8 @@ struct SlabSelShape {
 };
 
 template <int KIND, bool MBF16, int D>
-__device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint32_t* ready)
+__device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint32_t* ready, bool publish = true,
+                                                      int* ranked = nullptr, int* n_ranked = nullptr)
 {
     using SS = SelectShape<KIND, MBF16, D>;
     using WS = SlabSelShape<KIND, MBF16, D>;
@@ -848,11 +849,13 @@ __device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint3
         const int n_valid = load_keys(a, u, keys, klo, khi);
         topk_and_emit(a, u, keys, a.n_cand, n_valid, klo, khi);
         __syncthreads();
-        if (ready != nullptr && tid == 0) {
+        if (publish && ready != nullptr && tid == 0) {
             __threadfence();
             st_release_gpu(&ready[u], flag_value);
         }
+        if (ranked != nullptr && tid == 0) ranked[i] = u;
     }
+    if (n_ranked != nullptr && tid == 0) *n_ranked = nd;
     return flag_value;
 }
 

@@ -11,12 +11,30 @@ namespace {
 
 static_assert(kSelThreads == kDecThreads, "both phases run on the same CTA shape");
 
+// When every decode range is one whole unit, the CTA that ranks a unit decodes it
+// straight after (the selection is its own: no hand-off, no wait) and no flag is
+// published; otherwise CTA c decodes range c once its units are published.  Either way a
+// unit's result comes from the same per-unit code, so the bits do not depend on which
+// CTA computes it.
 template <int KIND, int D, int G, bool QSPLIT>
 __global__ void __launch_bounds__(kDecThreads, 1) step_kernel(SelectArgs sa_args, DecodeArgs da, uint32_t* ready)
 {
-    const uint32_t flag_value = select_body_warps<KIND, KIND == KIND_QUEST, D>(sa_args, ready);
+    __shared__ int s_ranked[kSlabSelMaxUnits];
+    __shared__ int s_nranked;
+    const bool by_ranker = da.ranges == da.units;
+    const uint32_t flag_value =
+        select_body_warps<KIND, KIND == KIND_QUEST, D>(sa_args, ready, !by_ranker, s_ranked, &s_nranked);
     __syncthreads();   // select's rings and keys are reused as the decode rings
-    decode_mma_body<D, G, QSPLIT>(da, ready, flag_value);
+    if (by_ranker) {
+        const int n = s_nranked;
+        for (int i = 0; i < n; ++i) {
+            const int u = s_ranked[i];
+            decode_mma_items<D, G, QSPLIT>(da, nullptr, 0u, u * da.items_per_unit, (u + 1) * da.items_per_unit);
+            __syncthreads();   // the next unit reuses the rings and the page cache
+        }
+    } else {
+        decode_mma_body<D, G, QSPLIT>(da, ready, flag_value);
+    }
     finish_step(da.err, flag_value);
 }
 
