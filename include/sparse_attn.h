@@ -154,14 +154,16 @@ int sparse_attn_workspace_size(const sparse_attn_params* p, size_t* bytes);
 int sparse_attn_workspace_init(void* ws, size_t ws_bytes, sparse_attn_stream stream);
 
 /* Limit, in SM clock cycles, of the fused step's hand-off waits on this workspace:
- * sparse_attn_step's decode waits, per unit, for the selection that another CTA (or
- * the select kernel launched just before it) publishes.  0 (the value
+ * sparse_attn_step's decode waits for the selections that other CTAs (or the select
+ * kernel launched just before it) publish -- per unit of its range, or, when each CTA
+ * decodes whole units, for the next unit in publication order.  0 (the value
  * sparse_attn_workspace_init leaves) selects the default of 2e9 cycles, about one
  * second at GB300 clocks; larger values are capped at it.  (Waits inside one CTA's
  * own pipeline -- copy and tensor-core completions -- always use the default.)  A wait
  * that runs out sets SPARSE_ATTN_ERR_TIMEOUT in the error word and the step goes on
  * with the selection as it finds it and returns, so the context stays usable; that
- * call's results are then unspecified (finite), and later calls are unaffected.
+ * call's results are then unspecified (a unit may keep an earlier call's output), and
+ * later calls are unaffected.
  * Stream-ordered; copies 8 bytes from host memory, so it cannot be captured into a
  * CUDA graph.  No counterpart in the pages: it exists to bound and to test the waits. */
 int sparse_attn_workspace_set_wait_limit(void* ws, size_t ws_bytes, uint64_t cycles,

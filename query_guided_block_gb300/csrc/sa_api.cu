@@ -129,8 +129,9 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     const size_t dec_cells = units * size_t(g.Q > 1 ? mq_row_tiles(g.Q, g.G) : 1);
 
     size_t off = 0;
-    // one 256-byte header: error word, the persistent kernels' work counters, the wait
-    // limit (bytes 24-31) and the fused step's epoch and completion count (32-39)
+    // one 256-byte header: error word, the select kernel's work counters (4-11), the
+    // fused step's publish-queue counters (12-23), the wait limit (24-31) and the fused
+    // step's epoch and completion count (32-39)
     L.err = 0;
     L.sel_work = 4;
     L.sel_done = 8;
@@ -141,6 +142,7 @@ WorkspaceLayout workspace_layout(const Geometry& g)
     L.dec_counters = off;     off = align256(off + dec_cells * sizeof(uint32_t));
     L.l1_counters = off;      off = align256(off + units * sizeof(uint32_t));
     L.ready = off;            off = align256(off + units * sizeof(uint32_t));
+    L.queue = off;            off = align256(off + units * sizeof(uint32_t));
     L.scores = off;           off = align256(off + units * L.score_cols * sizeof(float));
     L.survivors = off;        off = align256(off + units * size_t(g.topk_coarse > 0 ? g.topk_coarse : 1) * sizeof(int32_t));
     L.n_survivors = off;      off = align256(off + units * sizeof(int32_t));

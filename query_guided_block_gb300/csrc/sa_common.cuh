@@ -343,6 +343,13 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Device-scope release reduction (no value returned, so the thread does not wait for
+// it): every earlier memory operation of this thread is ordered before the add.
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p)
 {
     uint32_t v;
@@ -366,6 +373,9 @@ __device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t
 constexpr int kHdrWaitLimit = int(kHdrWaitLimitByte);   // uint64: wait limit in SM clocks, 0 = kWaitCycles
 constexpr int kHdrStepEpoch = 32;   // uint32: fused steps completed on this workspace
 constexpr int kHdrStepDone = 36;    // uint32: CTAs of the running step that have finished
+constexpr int kHdrQueueTail = 12;   // uint32: fused step: selections published to the queue
+constexpr int kHdrQueueHead = 16;   // uint32: fused step: decode tickets taken
+constexpr int kHdrRanked = 20;      // uint32: fused step: units ranked (queued or kept)
 
 __device__ __forceinline__ uint32_t* header_word(uint32_t* err, int byte)
 {
@@ -397,8 +407,9 @@ __device__ __forceinline__ uint32_t step_flag_value(uint32_t* err)
 
 // The end of one CTA's share of the launch that completes a step (the fused kernel, or
 // the decode kernel behind the step's select kernel): the last CTA of the grid to
-// finish resets the completion count for the next step and stores the step's number as
-// the new epoch.  After the kernel boundary every later launch sees them.
+// finish resets the completion count and the publish queue's counters for the next
+// step and stores the step's number as the new epoch.  After the kernel boundary every
+// later launch sees them.
 __device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
 {
     __syncthreads();
@@ -407,6 +418,9 @@ __device__ __forceinline__ void finish_step(uint32_t* err, uint32_t step_value)
         uint32_t* done = header_word(err, kHdrStepDone);
         if (atomic_add_acq_rel_u32(done, 1u) + 1u == gridDim.x) {
             *done = 0u;
+            *header_word(err, kHdrQueueTail) = 0u;   // every CTA is past its publishes and tickets
+            *header_word(err, kHdrQueueHead) = 0u;
+            *header_word(err, kHdrRanked) = 0u;
             st_release_gpu(header_word(err, kHdrStepEpoch), step_value);
         }
     }

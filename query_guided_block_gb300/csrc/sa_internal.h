@@ -37,12 +37,14 @@ struct WorkspaceLayout {
     size_t err;            // uint32 error word (header words: see sa_common.cuh kHdr*)
     size_t sel_work;       // uint32 next chunk id (select kernels)
     size_t sel_done;       // uint32 finished CTAs (select kernels)
-    size_t dec_work;       // uint32 next work item (decode)
-    size_t dec_done;       // uint32 finished CTAs (decode)
+    size_t dec_work;       // uint32 (header) fused step: selections published so far
+    size_t dec_done;       // uint32 (header) fused step: decode tickets taken so far
     size_t sel_counters;   // uint32 [units]
     size_t dec_counters;   // uint32 [units]
     size_t l1_counters;    // uint32 [units] (two-level, level 1)
-    size_t ready;          // uint32 [units] (fused step: unit's selection published)
+    size_t ready;          // uint32 [units] (fused step: unit's selection published, or the
+                           // queue entry at that position filled)
+    size_t queue;          // uint32 [units] (fused step: units in the order they were published)
     size_t scores;         // float [units, score_cols]
     size_t survivors;      // int32 [units, topk_coarse] (two-level)
     size_t n_survivors;    // int32 [units]

@@ -625,8 +625,8 @@ struct SlabSelShape {
 };
 
 template <int KIND, bool MBF16, int D>
-__device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint32_t* ready, bool publish = true,
-                                                      int* ranked = nullptr, int* n_ranked = nullptr)
+__device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint32_t* ready,
+                                                      uint32_t* queue = nullptr, int* kept = nullptr)
 {
     using SS = SelectShape<KIND, MBF16, D>;
     using WS = SlabSelShape<KIND, MBF16, D>;
@@ -849,13 +849,26 @@ __device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint3
         const int n_valid = load_keys(a, u, keys, klo, khi);
         topk_and_emit(a, u, keys, a.n_cand, n_valid, klo, khi);
         __syncthreads();
-        if (publish && ready != nullptr && tid == 0) {
+        if (queue != nullptr) {
+            // queue mode: the CTA keeps its first unit (*kept) and queues the others
+            // (append, publish the position), then counts the unit as ranked (after
+            // its queue entry: a count of every unit means the queue is complete)
+            if (tid == 0) {
+                if (i == 0) {
+                    *kept = u;
+                } else {
+                    const int slot = int(atomicAdd(header_word(a.err, kHdrQueueTail), 1u));
+                    queue[slot] = uint32_t(u);
+                    __threadfence();
+                    st_release_gpu(&ready[slot], flag_value);
+                }
+                red_add_release_gpu(header_word(a.err, kHdrRanked), 1u);
+            }
+        } else if (ready != nullptr && tid == 0) {
             __threadfence();
             st_release_gpu(&ready[u], flag_value);
         }
-        if (ranked != nullptr && tid == 0) ranked[i] = u;
     }
-    if (n_ranked != nullptr && tid == 0) *n_ranked = nd;
     return flag_value;
 }
 

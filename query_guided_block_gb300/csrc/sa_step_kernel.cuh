@@ -12,25 +12,62 @@ namespace {
 static_assert(kSelThreads == kDecThreads, "both phases run on the same CTA shape");
 
 // When every decode range is one whole unit, the CTA that ranks a unit decodes it
-// straight after (the selection is its own: no hand-off, no wait) and no flag is
-// published; otherwise CTA c decodes range c once its units are published.  Either way a
-// unit's result comes from the same per-unit code, so the bits do not depend on which
-// CTA computes it.
+// straight after (the selection is its own: no hand-off, no wait).  A CTA that ranks
+// more than one unit keeps the first and queues the others: it appends each to a queue
+// and publishes the position (ready[position] = the step's flag value, release), and
+// the CTAs that rank nothing take tickets and decode the queued units in order.  A
+// ticket holder waits (bounded) until its position is published, or until every unit
+// is ranked and the queue ends before it.  Otherwise CTA c decodes range c once its
+// units are published.  A unit's result comes from the same per-unit code either way,
+// so the bits do not depend on which CTA computes it.
 template <int KIND, int D, int G, bool QSPLIT>
-__global__ void __launch_bounds__(kDecThreads, 1) step_kernel(SelectArgs sa_args, DecodeArgs da, uint32_t* ready)
+__global__ void __launch_bounds__(kDecThreads, 1) step_kernel(SelectArgs sa_args, DecodeArgs da, uint32_t* ready,
+                                                              uint32_t* queue)
 {
-    __shared__ int s_ranked[kSlabSelMaxUnits];
-    __shared__ int s_nranked;
-    const bool by_ranker = da.ranges == da.units;
+    __shared__ int s_unit;
+    const bool by_queue = da.ranges == da.units;
+    if (threadIdx.x == 0) s_unit = -1;
     const uint32_t flag_value =
-        select_body_warps<KIND, KIND == KIND_QUEST, D>(sa_args, ready, !by_ranker, s_ranked, &s_nranked);
+        select_body_warps<KIND, KIND == KIND_QUEST, D>(sa_args, ready, by_queue ? queue : nullptr, &s_unit);
     __syncthreads();   // select's rings and keys are reused as the decode rings
-    if (by_ranker) {
-        const int n = s_nranked;
-        for (int i = 0; i < n; ++i) {
-            const int u = s_ranked[i];
-            decode_mma_items<D, G, QSPLIT>(da, nullptr, 0u, u * da.items_per_unit, (u + 1) * da.items_per_unit);
-            __syncthreads();   // the next unit reuses the rings and the page cache
+    if (by_queue) {
+        const int kept = s_unit;
+        if (kept >= 0) {
+            decode_mma_items<D, G, QSPLIT>(da, nullptr, 0u, kept * da.items_per_unit, (kept + 1) * da.items_per_unit);
+        } else {
+            const long long wait_cycles = handoff_wait_limit(da.err);
+            uint32_t* tail = header_word(da.err, kHdrQueueTail);
+            uint32_t* ranked = header_word(da.err, kHdrRanked);
+            while (true) {
+                if (threadIdx.x == 0) {
+                    const uint32_t t = atomicAdd(header_word(da.err, kHdrQueueHead), 1u);
+                    int u = -1;
+                    const long long t0 = clock64();
+                    while (true) {
+                        if (ld_acquire_gpu(ready + min(t, uint32_t(da.units - 1))) == flag_value && t < uint32_t(da.units)) {
+                            const int v = int(__ldcg(queue + t));
+                            if (v >= 0 && v < da.units) u = v;
+                            else raise_error(da.err, SPARSE_ATTN_ERR_TIMEOUT);
+                            break;
+                        }
+                        // every unit ranked and the queue ends before t: nothing for this ticket
+                        if (ld_acquire_gpu(ranked) >= uint32_t(da.units) && ld_acquire_gpu(tail) <= t) break;
+                        if (clock64() - t0 > wait_cycles) {
+                            raise_error(da.err, SPARSE_ATTN_ERR_TIMEOUT);
+                            break;
+                        }
+                        __nanosleep(32);
+                    }
+                    s_unit = u;
+                    __threadfence();
+                }
+                __syncthreads();
+                const int u = s_unit;
+                __syncthreads();   // s_unit is rewritten by the next ticket
+                if (u < 0) break;
+                decode_mma_items<D, G, QSPLIT>(da, nullptr, 0u, u * da.items_per_unit, (u + 1) * da.items_per_unit);
+                __syncthreads();   // the next unit reuses the rings and the page cache
+            }
         }
     } else {
         decode_mma_body<D, G, QSPLIT>(da, ready, flag_value);
@@ -39,7 +76,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) step_kernel(SelectArgs sa_args
 }
 
 template <int KIND, int D, int G, bool QSPLIT>
-cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, uint32_t* ready, int ctas,
+cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, uint32_t* ready, uint32_t* queue, int ctas,
                           cudaStream_t s)
 {
     constexpr size_t smem = slab_smem_bytes<D>();
@@ -68,18 +105,18 @@ cudaError_t launch_step_t(const SelectArgs& sa_args, const DecodeArgs& da, uint3
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, sa_args, da, ready);
+    return cudaLaunchKernelEx(&cfg, kernel, sa_args, da, ready, queue);
 }
 
 template <int KIND, int D, bool QSPLIT>
-cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, uint32_t* ready, int ctas, int G,
+cudaError_t dispatch_step_g(const SelectArgs& sa_args, const DecodeArgs& da, uint32_t* ready, uint32_t* queue, int ctas, int G,
                             cudaStream_t s)
 {
     switch (G) {
-        case 1: return launch_step_t<KIND, D, 1, QSPLIT>(sa_args, da, ready, ctas, s);
-        case 2: return launch_step_t<KIND, D, 2, QSPLIT>(sa_args, da, ready, ctas, s);
-        case 4: return launch_step_t<KIND, D, 4, QSPLIT>(sa_args, da, ready, ctas, s);
-        case 8: return launch_step_t<KIND, D, 8, QSPLIT>(sa_args, da, ready, ctas, s);
+        case 1: return launch_step_t<KIND, D, 1, QSPLIT>(sa_args, da, ready, queue, ctas, s);
+        case 2: return launch_step_t<KIND, D, 2, QSPLIT>(sa_args, da, ready, queue, ctas, s);
+        case 4: return launch_step_t<KIND, D, 4, QSPLIT>(sa_args, da, ready, queue, ctas, s);
+        case 8: return launch_step_t<KIND, D, 8, QSPLIT>(sa_args, da, ready, queue, ctas, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -135,13 +172,14 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
     else set_slab_chunking<KIND_QUEST, true, D>(sa_args, units);
     DecodeArgs da = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out, nullptr, 0);
     uint32_t* ready = reinterpret_cast<uint32_t*>(ws + L.ready);
+    uint32_t* queue = reinterpret_cast<uint32_t*>(ws + L.queue);
 
     const bool qs = !g.q_bf16;
     if (mean)
-        return qs ? dispatch_step_g<KIND_MEAN, D, true>(sa_args, da, ready, ctas, g.G, s)
-                  : dispatch_step_g<KIND_MEAN, D, false>(sa_args, da, ready, ctas, g.G, s);
-    return qs ? dispatch_step_g<KIND_QUEST, D, true>(sa_args, da, ready, ctas, g.G, s)
-              : dispatch_step_g<KIND_QUEST, D, false>(sa_args, da, ready, ctas, g.G, s);
+        return qs ? dispatch_step_g<KIND_MEAN, D, true>(sa_args, da, ready, queue, ctas, g.G, s)
+                  : dispatch_step_g<KIND_MEAN, D, false>(sa_args, da, ready, queue, ctas, g.G, s);
+    return qs ? dispatch_step_g<KIND_QUEST, D, true>(sa_args, da, ready, queue, ctas, g.G, s)
+              : dispatch_step_g<KIND_QUEST, D, false>(sa_args, da, ready, queue, ctas, g.G, s);
 }
 
 }  // namespace
