@@ -216,6 +216,12 @@ def algorithmic_bytes(w, sel_count: torch.Tensor, sel_ids: torch.Tensor):
 
 # ------------------------------------------------------------- GPU arm --
 
+def select_launches(w):
+    """Kernel launches of one sparse_attn_select call: one, except a two-level selection
+    with more than 256 level-1 survivors, which runs one launch per level."""
+    return 2 if (w.two_level and w.topk_coarse > 256) else 1
+
+
 def run_gpu_arm(args):
     world, rank, local = dist_env()
     if world > 1:
@@ -304,7 +310,7 @@ def run_gpu_arm(args):
     # select and decode calls.
     step_launches = -1 if (io or args.two_launch) else Bn.sparse_attn_step_launches(p)
     use_step = step_launches > 0
-    launches_per_step = ((step_launches if use_step else (3 if w.two_level else 2)) + (1 if cache else 0)
+    launches_per_step = ((step_launches if use_step else 1 + select_launches(w)) + (1 if cache else 0)
                          + (2 if io else 0))
 
     def io_phase():   # diff, misses in from the host store, slot map
@@ -415,7 +421,7 @@ def run_gpu_arm(args):
     sel_avg, dec_avg = statistics.mean(sel_ms), statistics.mean(dec_ms)
     kern = {
         "select": {"ms": sel_avg, "bytes": nbytes["select"], "gbs": nbytes["select"] / sel_avg / 1e6,
-                   "launches_per_step": 2 if w.two_level else 1},
+                   "launches_per_step": select_launches(w)},
         "decode": {"ms": dec_avg, "bytes": nbytes["decode"], "gbs": nbytes["decode"] / dec_avg / 1e6,
                    "tflops": nbytes["decode_flops"] / dec_avg / 1e9, "launches_per_step": 1},
     }
@@ -608,7 +614,7 @@ def measure_other_workload(name, dev, steps, warmup, flush, peak):
                       "head_dim": w.head_dim, "context": w.n_tokens, "block_size": w.block_size,
                       "topk_blocks": w.topk, "window_tokens": w.window_tokens, "two_level": w.two_level,
                       "cache_slots": w.cache_slots},
-           "gpu_launches": (launches if use_step else (3 if w.two_level else 2)) * steps +
+           "gpu_launches": (launches if use_step else 1 + select_launches(w)) * steps +
                            (steps if cache else 0)}
     del inp, dec, cache
     torch.cuda.empty_cache()

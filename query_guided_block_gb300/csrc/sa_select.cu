@@ -23,6 +23,8 @@
 // passes with warp-aggregated shared-memory histograms, early exit once a digit bin
 // holds exactly the remaining count, then a stable tie rule (lower id first) and an
 // ordered compaction by warp ballots.
+#include <type_traits>
+
 #include "sa_select_body.cuh"
 
 namespace sa {
@@ -306,13 +308,148 @@ __global__ void __launch_bounds__(kSelThreads) select_two_level_kernel(SelectArg
         };
         uint32_t klo, khi;
         const int n_valid = score_rows_to_keys<KIND_QUEST, MBF16, D>(l2, u, keys, l2.n_cand, cp, cn, row_of, klo, khi);
-        topk_and_emit(l2, u, keys, l2.n_cand, n_valid, klo, khi);
+        topk_and_emit(l2, u, keys, l2.n_cand, n_valid, klo, khi, l2.via_survivors ? s_surv : nullptr, nsurv);
     }
+}
+
+// ------------------------------------------- two-level, a cluster per unit ---
+// The same two levels with P CTAs per unit, one thread-block cluster each, when the
+// units alone would leave most SMs idle (the 256K workload has 64 units on 152 SMs).
+// Each CTA scores its 1/P of the unit's coarse rows, then of the survivors' slices,
+// into a scratch area of its own shared memory and stores the keys into CTA 0's key
+// array (distributed shared memory), with its (valid count, key range) in CTA 0's
+// per-rank slots.  After a cluster barrier CTA 0 runs the top-k on the whole key array:
+// level 1's survivors go to global memory, a second barrier makes them visible to the
+// cluster, and level 2's selection is emitted by CTA 0 alone.  Candidate numbering,
+// scores and the top-k are those of the one-CTA kernel, so the selection is the same.
+constexpr int kMaxClusterRanks = 8;
+// keys (up to kMaxSelectKeys) and a share's scratch keys (P >= 2: at most half of them)
+constexpr size_t kTwoLevelSmemMax = (kMaxSelectKeys + kMaxSelectKeys / 2) * sizeof(uint32_t);
+
+template <bool MBF16, int D>
+__global__ void __launch_bounds__(kSelThreads) select_two_level_cluster_kernel(SelectArgs l1, SelectArgs l2, int P,
+                                                                             int scratch_off)
+{
+    using S1 = SelectShape<KIND_MEAN, false, D>;
+    using S2 = SelectShape<KIND_QUEST, MBF16, D>;
+    extern __shared__ __align__(16) uint32_t keys[];
+    uint32_t* scratch = keys + scratch_off;           // this CTA's share, before it moves to CTA 0
+    __shared__ uint32_t s_stat[kMaxClusterRanks][3];  // CTA 0: per rank (valid count, key lo, key hi)
+    __shared__ int s_surv[kSelThreads];
+    __shared__ int s_nsurv;
+    const uint32_t rank = cluster_ctarank();
+    const int u = int(blockIdx.x) / P;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t keys0 = cluster_map(smem_u32(keys), 0);
+    const uint32_t stat0 = cluster_map(smem_u32(&s_stat[0][0]), 0);
+    grid_dependency_wait();   // inputs and workspace may come from the previous kernel
+    allow_dependents_early();
+
+    // this CTA's share [c0, c1) of n candidates: score into scratch, move to CTA 0
+    auto score_share = [&](const SelectArgs& a, auto kind_tag, const auto& cp, const auto& cn, int n, auto row_of) {
+        constexpr int KIND = decltype(kind_tag)::value;
+        const int c0 = int((long long)n * rank / P), c1 = int((long long)n * (rank + 1) / P);
+        constexpr bool MB = KIND == KIND_QUEST ? MBF16 : false;
+        uint32_t lo = 0xffffffffu, hi = 0u;
+        const int nv = score_rows_to_keys<KIND, MB, D>(a, u, scratch, c1 - c0, cp, cn,
+                                                       [&](int i) { return row_of(c0 + i); }, lo, hi);
+        for (int i = tid; i < c1 - c0; i += kSelThreads) st_cluster_u32(keys0 + uint32_t(c0 + i) * 4u, scratch[i]);
+        if (tid == 0) {
+            st_cluster_u32(stat0 + rank * 12u, uint32_t(nv));
+            st_cluster_u32(stat0 + rank * 12u + 4u, lo);
+            st_cluster_u32(stat0 + rank * 12u + 8u, hi);
+        }
+        cluster_sync_all();   // CTA 0 holds every key of the level
+    };
+    // CTA 0: zero the padding past n, combine the ranks' statistics
+    auto gather = [&](int n, int& n_valid, uint32_t& lo, uint32_t& hi) {
+        for (int c = n + tid; c < kSelThreads * key_tile(n); c += kSelThreads) keys[c] = 0u;
+        n_valid = 0;
+        lo = 0xffffffffu;
+        hi = 0u;
+        for (int r = 0; r < P; ++r) {
+            n_valid += int(s_stat[r][0]);
+            if (s_stat[r][0] > 0u) {
+                lo = min(lo, s_stat[r][1]);
+                hi = max(hi, s_stat[r][2]);
+            }
+        }
+        __syncthreads();
+    };
+
+    // ---- level 1: mean score of every coarse block, top K1 ----
+    {
+        float cp[S1::EPL], cn[S1::EPL];
+        unit_coefficients<KIND_MEAN, S1::EPL, D>(l1, u, (lane % S1::LPR) * S1::EPL, cp, cn);
+        score_share(l1, std::integral_constant<int, KIND_MEAN>(), cp, cn, l1.n_cand,
+                    [&](int c) { return c < l1.row_limit ? c : -1; });
+        if (rank == 0) {
+            int n_valid;
+            uint32_t lo, hi;
+            gather(l1.n_cand, n_valid, lo, hi);
+            topk_and_emit(l1, u, keys, l1.n_cand, n_valid, lo, hi);
+        }
+        cluster_sync_all();   // survivors (global, written by CTA 0) visible to the cluster
+    }
+    if (tid == 0) s_nsurv = min(__ldcg(l1.out_count + u), l2.groups);
+    for (int i = tid; i < l2.groups; i += kSelThreads) s_surv[i] = __ldcg(l1.out_ids + size_t(u) * l1.out_stride + i);
+    __syncthreads();
+
+    // ---- level 2: Quest bound over the survivors' slices, top K2 plus the window ----
+    {
+        float cp[S2::EPL], cn[S2::EPL];
+        unit_coefficients<KIND_QUEST, S2::EPL, D>(l2, u, (lane % S2::LPR) * S2::EPL, cp, cn);
+        const int nsurv = s_nsurv, per = l2.per_coarse, limit = l2.row_limit;
+        score_share(l2, std::integral_constant<int, KIND_QUEST>(), cp, cn, l2.n_cand, [&](int c) -> int {
+            const int i = c / per;
+            if (i >= nsurv) return -1;
+            const int row = s_surv[i] * per + (c - i * per);
+            return row < limit ? row : -1;
+        });
+        if (rank == 0) {
+            int n_valid;
+            uint32_t lo, hi;
+            gather(l2.n_cand, n_valid, lo, hi);
+            topk_and_emit(l2, u, keys, l2.n_cand, n_valid, lo, hi, l2.via_survivors ? s_surv : nullptr, nsurv);
+        }
+    }
+}
+
+// CTAs per unit for the cluster kernel: a power of two up to 4 that keeps about two
+// CTAs per SM; 1 selects the one-CTA kernel.
+inline int two_level_ranks(int units)
+{
+    const int sms = num_sms();
+    int P = 1;
+    while (P < 4 && (long long)units * P * 2 <= 2LL * sms) P *= 2;
+    return P;
+}
+
+template <bool MBF16, int D>
+cudaError_t launch_two_level_cluster_t(const SelectArgs& l1, const SelectArgs& l2, int units, int P, cudaStream_t s)
+{
+    const int n = l1.n_cand > l2.n_cand ? l1.n_cand : l2.n_cand;
+    const int keys_n = kSelThreads * key_tile(n);
+    const int share = (n + P - 1) / P;
+    const int scratch_n = kSelThreads * key_tile(share);
+    const size_t smem = size_t(keys_n + scratch_n) * sizeof(uint32_t);
+    if (smem > kTwoLevelSmemMax) return cudaErrorInvalidValue;
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(select_two_level_cluster_kernel<MBF16, D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(kTwoLevelSmemMax));
+    });
+    if (cfg != cudaSuccess) return cfg;
+    return launch_clusters_after_previous(select_two_level_cluster_kernel<MBF16, D>, dim3(unsigned(units * P)),
+                                          dim3(kSelThreads), smem, unsigned(P), s, l1, l2, P, keys_n);
 }
 
 template <bool MBF16, int D>
 cudaError_t launch_two_level_t(const SelectArgs& l1, const SelectArgs& l2, int units, cudaStream_t s)
 {
+    const int P = two_level_ranks(units);
+    if (P > 1) return launch_two_level_cluster_t<MBF16, D>(l1, l2, units, P, s);
     const int n = l1.n_cand > l2.n_cand ? l1.n_cand : l2.n_cand;
     const size_t smem = size_t(kSelThreads) * key_tile(n) * sizeof(uint32_t);
     static std::atomic<unsigned long long> configured{0};   // devices set up

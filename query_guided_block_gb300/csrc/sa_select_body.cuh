@@ -82,8 +82,18 @@ __host__ __device__ constexpr int key_tile(int n)
 // remaining count, every key of that bin is in.  key_lo / key_hi: the smallest and
 // largest key among the n_valid candidates (from load_keys).
 __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n, int n_valid,
-                              uint32_t key_lo, uint32_t key_hi)
+                              uint32_t key_lo, uint32_t key_hi, const int* surv_smem = nullptr, int n_surv_smem = 0)
 {
+    // candidate -> block id; with the level-1 survivors already in shared memory the
+    // emission does not go back to global memory for them (same mapping as candidate_row)
+    auto row_of = [&](int c) -> int {
+        if (surv_smem == nullptr) return candidate_row(a, u, c);
+        if (c >= a.n_cand) return -1;
+        const int i = c / a.per_coarse;
+        if (i >= n_surv_smem) return -1;
+        const int row = surv_smem[i] * a.per_coarse + (c - i * a.per_coarse);
+        return row < a.row_limit ? row : -1;
+    };
     constexpr int kBins = 2048;
     constexpr int kBinsPerThread = kBins / kSelThreads;
     constexpr int kGather = kSelThreads;
@@ -249,7 +259,7 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
         __syncthreads();
         for (int c = tid; c < n; c += kSelThreads)
             if (selected(c)) {
-                const int r = candidate_row(a, u, c);
+                const int r = row_of(c);
                 atomicOr(&bits[r >> 5], 1u << (r & 31));
             }
         for (int i = tid; i < a.n_reserve; i += kSelThreads) {
@@ -308,7 +318,7 @@ __device__ void topk_and_emit(const SelectArgs& a, int u, uint32_t* keys, int n,
         for (int e = 0; e < 4; ++e) {
             const int c = tid * kpt + i + e;
             if (selected_key(kk[e], c)) {
-                out[pos++] = candidate_row(a, u, c);
+                out[pos++] = row_of(c);
                 --cnt;
             }
         }
