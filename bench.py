@@ -310,13 +310,23 @@ def run_gpu_arm(args):
     # select and decode calls.
     step_launches = -1 if (io or args.two_launch) else Bn.sparse_attn_step_launches(p)
     use_step = step_launches > 0
+    serial_io = bool(io and args.io_serial)
     launches_per_step = ((step_launches if use_step else 1 + select_launches(w)) + (1 if cache else 0)
-                         + (2 if io else 0))
+                         + (2 if serial_io else 0))
 
-    def io_phase():   # diff, misses in from the host store, slot map
-        cache.diff(step_counter[0])
-        pool.load_misses(host_k, host_v, bt)
-        pool.slot_map()
+    def io_phase():   # diff, misses in from the host store, slot map (or: diff writing the slot map)
+        if serial_io:
+            cache.diff(step_counter[0])
+            pool.load_misses(host_k, host_v, bt)
+            pool.slot_map()
+        else:
+            cache.diff(step_counter[0], sel_slot=pool.sel_slot)
+
+    def io_decode(q):   # attention through the slot pool; the misses read in the same pass
+        if serial_io:
+            pool.decode(q)
+        else:
+            pool.decode_io(q, host_k, host_v, bt)
 
     def one_step(q):
         if use_step:
@@ -327,7 +337,7 @@ def run_gpu_arm(args):
             dec.select(q, reserve)
             if io:
                 io_phase()
-                pool.decode(q)
+                io_decode(q)
             else:
                 dec.decode(q, kp, vp, bt)
                 if cache:
@@ -366,10 +376,10 @@ def run_gpu_arm(args):
             continue
         dec.select(q, reserve)
         b.record(stream)
-        if io:                       # a select b diff + misses + map c decode d
+        if io:                       # a select b diff (+ misses) + map c decode (+ misses) d
             io_phase()
             c.record(stream)
-            pool.decode(q)
+            io_decode(q)
             d.record(stream)
             miss_total.add_(cache.counts[:, 1].sum())
         else:                        # a select b decode c diff d
@@ -428,9 +438,15 @@ def run_gpu_arm(args):
     if io:
         io_ms = statistics.mean([e[1].elapsed_time(e[2]) for e in ev])
         io_bytes = float(miss_total.item()) * 2 * pool.tile_bytes() / K
-        kern["diff_io"] = {"ms": io_ms, "misses_bytes": io_bytes, "host_read_gbs": io_bytes / io_ms / 1e6,
-                           "launches_per_step": 3,
-                           "note": "diff + miss tiles read from pinned host memory + slot map"}
+        if serial_io:
+            kern["diff_io"] = {"ms": io_ms, "misses_bytes": io_bytes, "host_read_gbs": io_bytes / io_ms / 1e6,
+                               "launches_per_step": 3,
+                               "note": "diff + miss tiles read from pinned host memory + slot map"}
+        else:
+            kern["diff_io"] = {"ms": io_ms, "misses_bytes": io_bytes, "launches_per_step": 1,
+                               "note": "diff writing the slot map (sparse_attn_diff_slots); the miss tiles "
+                                       "are read from pinned host memory inside the decode's launch "
+                                       "(sparse_attn_decode_slots_io)"}
     elif cache:
         kern["diff"] = {"ms": statistics.mean([(e[1] if use_step else e[2]).elapsed_time(e[3]) for e in ev]),
                         "launches_per_step": 1}
@@ -475,7 +491,7 @@ def run_gpu_arm(args):
         dec.select(q_dev, res_dev if reserve is not None else None)
         if io:
             io_phase()
-            pool.decode(q_dev)
+            io_decode(q_dev)
             cache.advance()
             step_counter[0] += 1
         else:
@@ -526,7 +542,11 @@ def run_gpu_arm(args):
                    "l2": f"flushed before every step ({flush.numel() >> 20} MB written then read back, "
                          "outside the step events)",
                    "step": (f"sparse_attn_step ({step_launches} launch{'es' if step_launches > 1 else ''})"
-                            if use_step else "sparse_attn_select + sparse_attn_decode"),
+                            if use_step else
+                            ("sparse_attn_select + diff + load_misses + slot_map + decode_slots" if serial_io else
+                             "sparse_attn_select + diff_slots + decode_slots_io (misses loaded in the decode's "
+                             "launch)")
+                            if io else "sparse_attn_select + sparse_attn_decode"),
                    "timing": "CUDA events per call on the launching stream"},
         "hbm_gbs": step_gbs,
         "hbm_frac_of_measured": step_gbs / peak,
@@ -744,6 +764,8 @@ def main():
     ap.add_argument("--io", action="store_true",
                     help="LRU workloads: K/V read through the slot pool, misses loaded each step "
                          "from a pinned host store")
+    ap.add_argument("--io-serial", action="store_true",
+                    help="with --io: load the misses in their own launch before the decode")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
                     help="skip timing mha_32k, two_level_256k and lru_64k after the headline")

@@ -281,6 +281,20 @@ int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* s
                      int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, void* ws,
                      size_t ws_bytes, sparse_attn_stream stream);
 
+/* sparse_attn_diff that also writes this step's slot map in the same launch:
+ * sel_slot[u][i] = the slot holding sel_ids[u][i] after the step (a hit keeps its slot,
+ * a miss gets the slot it is placed in) -- what sparse_attn_slot_map would compute from
+ * the updated slot_block.  sel_slot: [B*Hkv, sel_stride] int32; other arguments and
+ * outputs as sparse_attn_diff.  When the diff refuses a unit (error bit set) its
+ * sel_slot row is left as it was. */
+int sparse_attn_diff_slots(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
+                           const int32_t* sel_count, const int32_t* prev_ids,
+                           const int32_t* prev_count, int32_t cache_slots, int32_t* slot_block,
+                           int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
+                           int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
+                           int32_t* new_ids, int32_t* dropped_ids, int32_t* counts,
+                           int32_t* sel_slot, void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
 /* ---- Slot pool: misses loaded from a host-resident store ("SGLang分层稀疏注意力技术解析与
  * 优化实践" §3.3 IO transfer: full KV cache page-first in pinned / host-registered
  * memory, zero-copy transfer of a step's misses batched over requests; §3.2 steps c-d:
@@ -316,6 +330,27 @@ int sparse_attn_decode_slots(const sparse_attn_params* p, const void* q, const v
                              const void* pool_v, int32_t cache_slots, const int32_t* sel_ids,
                              const int32_t* sel_slot, const int32_t* sel_count, float* out,
                              void* ws, size_t ws_bytes, sparse_attn_stream stream);
+
+/* sparse_attn_load_misses and sparse_attn_decode_slots in one launch, so that the
+ * miss transfer overlaps the attention over the resident blocks ("SGLang分层稀疏注意力
+ * 技术解析与优化实践" §3.3: the IO is hidden behind compute).  Loader CTAs copy each
+ * unit's misses (miss_ids / miss_slot / counts as written by sparse_attn_diff) from the
+ * host store into the pool exactly as sparse_attn_load_misses does, while the decode
+ * CTAs attend to every unit's resident blocks first and to its missed blocks last, after
+ * waiting (bounded, see sparse_attn_workspace_set_wait_limit) for the unit's loads.
+ * sel_slot must come from sparse_attn_slot_map after this step's diff (miss slots
+ * included).  The pool ends as after sparse_attn_load_misses; the output equals
+ * sparse_attn_load_misses + sparse_attn_decode_slots up to the fp32 rounding of the
+ * changed order (bit for bit for a unit without misses).  When no SM is left for
+ * loaders the misses are loaded first, in their own launch.  bf16 K/V only (else
+ * UNSUPPORTED); host memory rules as sparse_attn_load_misses; other arguments as
+ * sparse_attn_decode_slots. */
+int sparse_attn_decode_slots_io(const sparse_attn_params* p, const void* q, void* pool_k, void* pool_v,
+                                int32_t cache_slots, const int32_t* sel_ids, const int32_t* sel_slot,
+                                const int32_t* sel_count, const void* host_k_pages,
+                                const void* host_v_pages, const int32_t* block_table,
+                                const int32_t* miss_ids, const int32_t* miss_slot, const int32_t* counts,
+                                float* out, void* ws, size_t ws_bytes, sparse_attn_stream stream);
 
 /* Synchronise `stream`, copy the device error word to *flags (SPARSE_ATTN_ERR_* bits)
  * and clear it.  Returns SPARSE_ATTN_DEVICE_BOUNDS when any bit was set. */

@@ -98,6 +98,8 @@ def lib():
             "sparse_attn_step_launches": ([P], C.c_int32),
             "sparse_attn_diff": ([P, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                   vp, vp, vp, sz, vp], C.c_int),
+            "sparse_attn_diff_slots": ([P, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                        vp, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_get_device_error": ([vp, sz, vp, u32p], C.c_int),
             "sparse_attn_select_noalloc": ([P, vp, vp, vp, vp, vp, vp, vp], C.c_int),
             "sparse_attn_select_noalloc_device_error": ([vp, u32p], C.c_int),
@@ -106,6 +108,8 @@ def lib():
             "sparse_attn_slot_map": ([P, vp, vp, vp, i32, vp, vp, sz, vp], C.c_int),
             "sparse_attn_load_misses": ([P, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp], C.c_int),
             "sparse_attn_decode_slots": ([P, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp], C.c_int),
+            "sparse_attn_decode_slots_io": ([P, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                             vp], C.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -123,7 +127,8 @@ def exported_symbols():
             "sparse_attn_select_reserved", "sparse_attn_topk_for_length",
             "sparse_attn_slot_map", "sparse_attn_load_misses", "sparse_attn_decode_slots",
             "sparse_attn_append_meta", "sparse_attn_step", "sparse_attn_step_launches",
-            "sparse_attn_select_noalloc_device_error", "sparse_attn_workspace_set_wait_limit"]
+            "sparse_attn_select_noalloc_device_error", "sparse_attn_workspace_set_wait_limit",
+            "sparse_attn_decode_slots_io", "sparse_attn_diff_slots"]
 
 
 def _status_string(status: int) -> str:
@@ -263,6 +268,16 @@ def sparse_attn_diff(p, step, sel_ids, sel_count, prev_ids, prev_count, cache_sl
         _ptr(counts), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def sparse_attn_diff_slots(p, step, sel_ids, sel_count, prev_ids, prev_count, cache_slots, slot_block,
+                           slot_last_use, hit_ids, miss_ids, miss_slot, evict_ids, evict_slot, new_ids,
+                           dropped_ids, counts, sel_slot, ws, stream=None) -> None:
+    _check("sparse_attn_diff_slots", lib().sparse_attn_diff_slots(
+        C.byref(p), int(step), _ptr(sel_ids), _ptr(sel_count), _ptr(prev_ids), _ptr(prev_count),
+        int(cache_slots), _ptr(slot_block), _ptr(slot_last_use), _ptr(hit_ids), _ptr(miss_ids),
+        _ptr(miss_slot), _ptr(evict_ids), _ptr(evict_slot), _ptr(new_ids), _ptr(dropped_ids),
+        _ptr(counts), _ptr(sel_slot), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def sparse_attn_select_noalloc(p, q, kmin, kmax, kmean, sel_ids, sel_count, stream=None) -> None:
     """sparse_attn_select with the library's fixed scratch instead of a workspace, for
     callers that cannot allocate device memory (see the C header)."""
@@ -312,6 +327,16 @@ def sparse_attn_decode_slots(p, q, pool_k, pool_v, cache_slots, sel_ids, sel_slo
         C.byref(p), _ptr(q), _ptr(pool_k), _ptr(pool_v), int(cache_slots), _ptr(sel_ids),
         _ptr(sel_slot), _ptr(sel_count), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def sparse_attn_decode_slots_io(p, q, pool_k, pool_v, cache_slots, sel_ids, sel_slot, sel_count,
+                                host_k_pages, host_v_pages, block_table, miss_ids, miss_slot, counts, out,
+                                ws, stream=None) -> None:
+    _check("sparse_attn_decode_slots_io", lib().sparse_attn_decode_slots_io(
+        C.byref(p), _ptr(q), _ptr(pool_k), _ptr(pool_v), int(cache_slots), _ptr(sel_ids),
+        _ptr(sel_slot), _ptr(sel_count), _host_or_cuda_ptr(host_k_pages), _host_or_cuda_ptr(host_v_pages),
+        _ptr(block_table), _ptr(miss_ids), _ptr(miss_slot), _ptr(counts), _ptr(out), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def sparse_attn_get_device_error(ws, stream=None) -> int:

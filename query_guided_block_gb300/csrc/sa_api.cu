@@ -388,13 +388,13 @@ int sparse_attn_step(const sparse_attn_params* p, const void* q, const void* kmi
     return status_of(e);
 }
 
-int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
+static int diff_impl(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
                      const int32_t* sel_count, const int32_t* prev_ids,
                      const int32_t* prev_count, int32_t cache_slots, int32_t* slot_block,
                      int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
                      int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
-                     int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, void* ws,
-                     size_t ws_bytes, sparse_attn_stream stream)
+                     int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, int32_t* sel_slot,
+                     void* ws, size_t ws_bytes, sparse_attn_stream stream)
 {
     Geometry g;
     int st = make_geometry(p, &g);
@@ -414,7 +414,33 @@ int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* s
                                  slot_block, slot_last_use, hit_ids, miss_ids, miss_slot, evict_ids,
                                  evict_slot, new_ids, dropped_ids, counts,
                                  reinterpret_cast<uint32_t*>(w + L.err),
-                                 reinterpret_cast<cudaStream_t>(stream)));
+                                 reinterpret_cast<cudaStream_t>(stream), sel_slot));
+}
+
+int sparse_attn_diff(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
+                     const int32_t* sel_count, const int32_t* prev_ids,
+                     const int32_t* prev_count, int32_t cache_slots, int32_t* slot_block,
+                     int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
+                     int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
+                     int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, void* ws,
+                     size_t ws_bytes, sparse_attn_stream stream)
+{
+    return diff_impl(p, step, sel_ids, sel_count, prev_ids, prev_count, cache_slots, slot_block, slot_last_use,
+                     hit_ids, miss_ids, miss_slot, evict_ids, evict_slot, new_ids, dropped_ids, counts, nullptr, ws,
+                     ws_bytes, stream);
+}
+
+int sparse_attn_diff_slots(const sparse_attn_params* p, int32_t step, const int32_t* sel_ids,
+                           const int32_t* sel_count, const int32_t* prev_ids, const int32_t* prev_count,
+                           int32_t cache_slots, int32_t* slot_block, int32_t* slot_last_use, int32_t* hit_ids,
+                           int32_t* miss_ids, int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
+                           int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, int32_t* sel_slot, void* ws,
+                           size_t ws_bytes, sparse_attn_stream stream)
+{
+    if (!sel_slot || !aligned(sel_slot, 4)) return SPARSE_ATTN_INVALID_ARG;
+    return diff_impl(p, step, sel_ids, sel_count, prev_ids, prev_count, cache_slots, slot_block, slot_last_use,
+                     hit_ids, miss_ids, miss_slot, evict_ids, evict_slot, new_ids, dropped_ids, counts, sel_slot, ws,
+                     ws_bytes, stream);
 }
 
 int sparse_attn_get_device_error(void* ws, size_t ws_bytes, sparse_attn_stream stream, uint32_t* flags)
@@ -511,6 +537,38 @@ int sparse_attn_decode_slots(const sparse_attn_params* p, const void* q, const v
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int sparse_attn_decode_slots_io(const sparse_attn_params* p, const void* q, void* pool_k, void* pool_v,
+                                int32_t cache_slots, const int32_t* sel_ids, const int32_t* sel_slot,
+                                const int32_t* sel_count, const void* host_k_pages, const void* host_v_pages,
+                                const int32_t* block_table, const int32_t* miss_ids, const int32_t* miss_slot,
+                                const int32_t* counts, float* out, void* ws, size_t ws_bytes,
+                                sparse_attn_stream stream)
+{
+    Geometry g;
+    int st = make_geometry(p, &g);
+    if (st) return st;
+    const WorkspaceLayout L = workspace_layout(g);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return SPARSE_ATTN_INVALID_ARG;
+    if (cache_slots < 1 || cache_slots > 1024 || g.sel_stride > cache_slots) return SPARSE_ATTN_INVALID_ARG;
+    if (g.Q > 1) return SPARSE_ATTN_UNSUPPORTED;
+    if (!g.kv_bf16) return SPARSE_ATTN_UNSUPPORTED;
+    if (g.units() == 0) return SPARSE_ATTN_OK;
+    if (!q || !out || !sel_ids || !sel_slot || !sel_count || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(sel_ids, 4) || !aligned(sel_slot, 4) || !aligned(sel_count, 4))
+        return SPARSE_ATTN_INVALID_ARG;
+    if (g.nb == 0)   // nothing selected: the plain slot decode writes the zero output
+        return status_of(launch_decode(g, L, static_cast<char*>(ws), q, pool_k, pool_v, nullptr, sel_ids, sel_count,
+                                       out, sel_slot, cache_slots, reinterpret_cast<cudaStream_t>(stream)));
+    const void* hk = host_k_pages ? device_view(host_k_pages) : nullptr;
+    const void* hv = host_v_pages ? device_view(host_v_pages) : nullptr;
+    if (!hk || !hv || !aligned(hk, 16) || !aligned(hv, 16) || !block_table || !miss_ids || !miss_slot || !counts ||
+        !pool_k || !pool_v || !aligned(pool_k, 16) || !aligned(pool_v, 16) || !aligned(block_table, 4) ||
+        !aligned(miss_ids, 4) || !aligned(miss_slot, 4) || !aligned(counts, 4))
+        return SPARSE_ATTN_INVALID_ARG;
+    const SlotIo io{hk, hv, miss_ids, miss_slot, counts};
+    return status_of(launch_decode(g, L, static_cast<char*>(ws), q, pool_k, pool_v, block_table, sel_ids, sel_count,
+                                   out, sel_slot, cache_slots, reinterpret_cast<cudaStream_t>(stream), nullptr, &io));
+}
 
 // ---- selection for callers that cannot allocate device memory ---------------
 // The scratch lives in this file-scope array; host code needs its device address,

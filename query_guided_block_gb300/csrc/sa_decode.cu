@@ -387,34 +387,172 @@ cudaError_t dispatch_group(const DecodeArgs& a, int G, cudaStream_t s)
 // With `ready` set the kernel runs behind a select kernel that publishes each unit's
 // selection: it skips the grid-wide wait and waits per unit instead, so its CTAs
 // start on SMs as the select kernel's CTAs leave them.
-template <int D, int G, bool QSPLIT>
+template <int D, int G, bool QSPLIT, bool IO>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_mma_kernel(DecodeArgs a, uint32_t* ready)
 {
     allow_dependents_early();
     if (ready == nullptr) {
         grid_dependency_wait();   // inputs and workspace may come from the previous kernel
-        decode_mma_body<D, G, QSPLIT>(a, nullptr, 0u);
+        decode_mma_body<D, G, QSPLIT, IO>(a, nullptr, 0u);
         return;
     }
     // behind the step's select kernel: the same flag value as it publishes
     const uint32_t flag_value = step_flag_value(a.err);
-    decode_mma_body<D, G, QSPLIT>(a, ready, flag_value);
+    decode_mma_body<D, G, QSPLIT, IO>(a, ready, flag_value);
     finish_step(a.err, flag_value);
+}
+
+// Loader CTA: copy the misses (K and V tiles) of units [u0, u1) from the host store into
+// their pool slots, then publish io_flags[u] for each.  The whole share is one batch --
+// miss counts, then every miss's ids and pages, then every tile, each step with all its
+// loads in flight -- so the latency is paid a few times per CTA, not per unit.
+// `scratch`: dynamic shared memory for (u1 - u0) + 1 counts and 2 offsets per miss.
+__device__ void load_misses_for_units(const DecodeArgs& a, int u0, int u1, int D, uint32_t flag_value,
+                                      unsigned char* scratch, size_t scratch_bytes)
+{
+    constexpr int kInFlight = 8;
+    __shared__ int s_total;
+    const int tid = threadIdx.x;
+    const int nu = u1 - u0;
+    int* first = reinterpret_cast<int*>(scratch);                        // [nu + 1] prefix of counts
+    long long* offs = reinterpret_cast<long long*>(scratch + ((size_t(nu + 1) * sizeof(int) + 15) & ~size_t(15)));
+    const long long max_misses = (long long)((scratch + scratch_bytes) - reinterpret_cast<unsigned char*>(offs)) / 16;
+    const size_t tile = size_t(a.bs) * D * 2;
+    if (nu <= 0) return;
+    for (int i = tid; i < nu; i += kDecThreads) {
+        int n = a.io_counts[size_t(u0 + i) * 5 + 1];
+        if (n < 0 || n > a.sel_stride) {
+            raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
+            n = n < 0 ? 0 : a.sel_stride;
+        }
+        first[i + 1] = n;
+    }
+    __syncthreads();
+    if (tid == 0) {   // a few hundred units at most: a serial prefix is cheap
+        first[0] = 0;
+        for (int i = 0; i < nu; ++i) first[i + 1] += first[i];
+        if (first[nu] > max_misses) raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);   // host sizing prevents it
+        s_total = int(min((long long)first[nu], max_misses));
+    }
+    __syncthreads();
+    const int total = s_total;
+    for (int m = tid; m < total; m += kDecThreads) {
+        int lo = 0, hi = nu;   // the unit holding miss m: first[lo] <= m < first[lo + 1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (first[mid] <= m) lo = mid;
+            else hi = mid;
+        }
+        const int u = u0 + lo, i = m - first[lo];
+        const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+        const int j = a.io_miss_ids[size_t(u) * a.sel_stride + i];
+        const int sl = a.io_miss_slot[size_t(u) * a.sel_stride + i];
+        long long so = -1, dst = 0;
+        if (j < 0 || j >= a.nb || sl < 0 || sl >= a.slot_C) {
+            raise_error(a.err, j < 0 || j >= a.nb ? SPARSE_ATTN_ERR_SEL_ID : SPARSE_ATTN_ERR_SLOT);
+        } else {
+            const int p = a.block_table[size_t(b) * a.bt_stride + j];
+            if (p < 0 || p >= a.num_pages) {
+                raise_error(a.err, SPARSE_ATTN_ERR_PAGE);
+            } else {
+                so = (long long)((size_t(p) * a.Hkv + kvh) * tile);
+                dst = (long long)((size_t(u) * a.slot_C + sl) * tile);
+            }
+        }
+        offs[2 * m] = so;
+        offs[2 * m + 1] = dst;
+    }
+    __syncthreads();
+    const long long n16 = (long long)(tile / 16);
+    const long long elems = n16 * total;                    // per tensor
+    char* pk = const_cast<char*>(static_cast<const char*>(a.k_pages));
+    char* pv = const_cast<char*>(static_cast<const char*>(a.v_pages));
+    for (long long base = 0; base < 2 * elems; base += (long long)kDecThreads * kInFlight) {
+        uint4 v[kInFlight];
+#pragma unroll
+        for (int r = 0; r < kInFlight; ++r) {
+            const long long f = base + (long long)r * kDecThreads + tid;
+            if (f < 2 * elems) {
+                const long long g = f < elems ? f : f - elems;
+                const int m = int(g / n16);
+                if (offs[2 * m] >= 0) v[r] = ld_stream16((f < elems ? a.io_host_k : a.io_host_v) + offs[2 * m] + (g - m * n16) * 16);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kInFlight; ++r) {
+            const long long f = base + (long long)r * kDecThreads + tid;
+            if (f < 2 * elems) {
+                const long long g = f < elems ? f : f - elems;
+                const int m = int(g / n16);
+                if (offs[2 * m] >= 0)
+                    *reinterpret_cast<uint4*>((f < elems ? pk : pv) + offs[2 * m + 1] + (g - m * n16) * 16) = v[r];
+            }
+        }
+    }
+    __syncthreads();   // every tile of the share is written
+    for (int i = tid; i < nu; i += kDecThreads) {
+        __threadfence();
+        st_release_gpu(a.io_flags + u0 + i, flag_value);
+    }
+}
+
+// The slot decode with the step's misses loaded in the same cooperative grid: CTAs
+// below a.ranges decode (a unit's missed blocks last), the others load the misses of an
+// equal share of the units.  Every CTA is resident, the loaders wait on nothing, so each
+// wait ends.
+template <int D, int G, bool QSPLIT>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_io_kernel(DecodeArgs a)
+{
+    const uint32_t flag_value = step_flag_value(a.err);
+    if (int(blockIdx.x) < a.ranges) {
+        decode_mma_body<D, G, QSPLIT, true>(a, nullptr, flag_value);
+    } else {
+        extern __shared__ __align__(16) unsigned char io_scratch[];   // the rings this CTA does not use
+        const int L = int(blockIdx.x) - a.ranges;
+        const int u0 = int((long long)a.units * L / a.io_loaders), u1 = int((long long)a.units * (L + 1) / a.io_loaders);
+        load_misses_for_units(a, u0, u1, D, flag_value, io_scratch, slab_smem_bytes_io<D>());
+    }
+    finish_step(a.err, flag_value);
+}
+
+template <int D, int G, bool QSPLIT>
+cudaError_t launch_decode_io_t(DecodeArgs a, cudaStream_t s)
+{
+    constexpr size_t smem = slab_smem_bytes_io<D>();
+    static_assert(smem <= size_t(kDecSmemLimit), "slab rings must fit a CTA");
+    static std::atomic<unsigned long long> configured{0};   // devices set up
+    const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
+        return cudaFuncSetAttribute(decode_io_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kDecSmemLimit);
+    });
+    if (cfg != cudaSuccess) return cfg;
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3(unsigned(a.ranges + a.io_loaders));
+    c.blockDim = dim3(kDecThreads);
+    c.dynamicSmemBytes = smem;
+    c.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: the decode's waits end
+    attr[0].val.cooperative = 1;
+    c.attrs = attr;
+    c.numAttrs = 1;
+    return cudaLaunchKernelEx(&c, decode_io_kernel<D, G, QSPLIT>, a);
 }
 
 template <int D, int G, bool QSPLIT>
 cudaError_t launch_decode_mma_t(DecodeArgs a, uint32_t* ready, cudaStream_t s)
 {
+    if (a.io_host_k != nullptr) return launch_decode_io_t<D, G, QSPLIT>(a, s);
+    static_assert(slab_smem_bytes<D>() <= size_t(kDecSmemLimit), "slab rings must fit a CTA");
     constexpr size_t smem = slab_smem_bytes<D>();
-    static_assert(smem <= size_t(kDecSmemLimit), "slab rings must fit a CTA");
     static std::atomic<unsigned long long> configured{0};   // devices set up
     const cudaError_t cfg = once_per_device(configured, [&]() -> cudaError_t {
-        return cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kDecSmemLimit);
+        return cudaFuncSetAttribute(decode_mma_kernel<D, G, QSPLIT, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemLimit);
     });
     if (cfg != cudaSuccess) return cfg;
     const unsigned ctas = unsigned(a.ranges);       // one CTA (8 independent warps) per range
-    return launch_after_previous(decode_mma_kernel<D, G, QSPLIT>, dim3(ctas), dim3(kDecThreads), smem, s, a,
+    return launch_after_previous(decode_mma_kernel<D, G, QSPLIT, false>, dim3(ctas), dim3(kDecThreads), smem, s, a,
                                  ready);
 }
 
@@ -450,12 +588,35 @@ bool decode_supported(int D, bool kv_bf16, int block_size, int G)
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* k_pages, const void* v_pages, const int32_t* block_table,
                           const int32_t* sel_ids, const int32_t* sel_count, float* out,
-                          const int32_t* sel_slot, int slot_C, cudaStream_t s, uint32_t* ready)
+                          const int32_t* sel_slot, int slot_C, cudaStream_t s, uint32_t* ready,
+                          const SlotIo* io)
 {
     const int units = g.units();
     if (units == 0) return cudaSuccess;
     DecodeArgs a = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out,
                                sel_slot, slot_C);
+    if (io != nullptr) {
+        if (!g.kv_bf16 || slot_C < 1) return cudaErrorNotSupported;
+        const int loaders = num_sms() - a.ranges < 32 ? num_sms() - a.ranges : 32;
+        // a loader's share must fit its shared memory: counts, then two offsets per miss
+        const long long per = loaders > 0 ? (units + loaders - 1) / loaders : 0;
+        const size_t need = size_t(per + 1) * sizeof(int) + 16 + size_t(per) * g.sel_stride * 16;
+        const size_t have = g.D == 128 ? slab_smem_bytes_io<128>() : slab_smem_bytes_io<64>();
+        if (loaders < 1 || need > have) {   // the misses first, in their own launch
+            const cudaError_t e = launch_load_misses(g, io->host_k, io->host_v, block_table, io->miss_ids,
+                                                     io->miss_slot, io->counts, slot_C, const_cast<void*>(k_pages),
+                                                     const_cast<void*>(v_pages), a.err, s);
+            if (e != cudaSuccess) return e;
+        } else {
+            a.io_host_k = static_cast<const char*>(io->host_k);
+            a.io_host_v = static_cast<const char*>(io->host_v);
+            a.io_miss_ids = io->miss_ids;
+            a.io_miss_slot = io->miss_slot;
+            a.io_counts = io->counts;
+            a.io_flags = reinterpret_cast<uint32_t*>(ws + L.ready);
+            a.io_loaders = loaders;
+        }
+    }
     if (g.kv_bf16) {   // tensor-core path
         if (g.q_bf16)
             return g.D == 128 ? dispatch_mma<128, false>(a, g.G, ready, s) : dispatch_mma<64, false>(a, g.G, ready, s);

@@ -40,6 +40,18 @@ struct DecodeArgs {
     const int32_t* sel_slot;
     int slot_C;
     int page_heads;          // KV heads per page: Hkv, or 1 in slot mode
+    // slot mode with the step's misses loaded in the same launch (io_host_k != null):
+    // loader CTAs copy unit u's misses (io_miss_ids[u][0 .. io_counts[u][1]), ascending,
+    // into pool slots io_miss_slot[u][...]) from the host store -- page block_table[b][j],
+    // KV head u % Hkv -- and publish io_flags[u] = the launch's flag value; the decode
+    // takes a unit's missed blocks last and waits (bounded) for that flag before them
+    const char* io_host_k;
+    const char* io_host_v;
+    const int32_t* io_miss_ids;
+    const int32_t* io_miss_slot;
+    const int32_t* io_counts;
+    uint32_t* io_flags;
+    int io_loaders;          // CTAs ranges .. ranges + io_loaders - 1 load misses
     int blocks_per_item, items_per_unit, total_items, units;
     int ranges;              // CTAs 0 .. ranges - 1 own contiguous item ranges (<= the grid)
     int stages;
@@ -195,10 +207,18 @@ constexpr size_t slab_smem_bytes()
     return 1024 /* alignment slack */ + SlabShape<D>::RING_BYTES + size_t(2) * kMaxRangeBlocks * sizeof(int);
 }
 
+// With misses read from the host in the same pass: one more int per cached block (its
+// host page, or -1).
+template <int D>
+constexpr size_t slab_smem_bytes_io()
+{
+    return slab_smem_bytes<D>() + size_t(kMaxRangeBlocks) * sizeof(int);
+}
+
 // Items [i_begin, i_end) of a decode launch, by one CTA.  With `ready` set, the CTA
 // first waits (bounded) until ready[u] == flag_value for every unit of the range (the
 // selection may still be running in this grid or in the select kernel before this one).
-template <int D, int G, bool QSPLIT>
+template <int D, int G, bool QSPLIT, bool IO = false>
 __device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* ready, uint32_t flag_value,
                                                  int i_begin, int i_end)
 {
@@ -223,6 +243,8 @@ __device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* 
     const uint32_t ring = base + uint32_t(warp) * (S * SS::SLAB_BYTES);
     int* blk_page = reinterpret_cast<int*>(smem + SS::RING_BYTES);
     int* blk_valid = blk_page + kMaxRangeBlocks;
+    int* blk_host = blk_valid + kMaxRangeBlocks;   // only with IO (slab_smem_bytes_io)
+    constexpr bool io = IO;
     __shared__ float s_m[kDecWarps][8], s_l[kDecWarps][8];
     __shared__ int s_flush[kDecWarps];             // byte offset of each warp's flushed (o)
     __shared__ int s_merge_unit;
@@ -277,7 +299,7 @@ __device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* 
             raise_error(a.err, SPARSE_ATTN_ERR_SEL_COUNT);
             count = count < 0 ? 0 : a.sel_stride;
         }
-        int page = -1, valid = 0;
+        int page = -1, valid = 0, host = -1;
         if (slot < count) {
             if (j < 0 || j >= a.nb) {
                 raise_error(a.err, SPARSE_ATTN_ERR_SEL_ID);
@@ -288,6 +310,18 @@ __device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* 
                 } else {
                     page = u * a.slot_C + sl;
                     valid = min(a.bs, a.N - j * a.bs);
+                    if (io) {   // a miss of this step: its host page
+                        int n_miss = a.io_counts[size_t(u) * 5 + 1];
+                        n_miss = n_miss < 0 ? 0 : min(n_miss, a.sel_stride);
+                        const int32_t* mids = a.io_miss_ids + size_t(u) * a.sel_stride;
+                        int lo = 0, hi = n_miss;   // first index with mids[index] >= j
+                        while (lo < hi) {
+                            const int mid = (lo + hi) >> 1;
+                            if (mids[mid] < j) lo = mid + 1;
+                            else hi = mid;
+                        }
+                        if (lo < n_miss && mids[lo] == j) host = 1;
+                    }
                 }
             } else {
                 const int p = a.block_table[size_t(u / a.Hkv) * a.bt_stride + j];
@@ -301,11 +335,44 @@ __device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* 
         }
         blk_page[e] = page;
         blk_valid[e] = valid;
+        if (io) blk_host[e] = host;
     }
     decoder_barrier();
+    if constexpr (IO) {
+        // a unit's missed blocks last (stable within hits and within misses), so their
+        // load overlaps the attention over the unit's resident blocks; the rings are
+        // free yet and hold the copy
+        int* tmp = reinterpret_cast<int*>(smem);
+        for (int e = tid; e < n_range_blocks; e += kDecThreads) {
+            tmp[3 * e] = blk_page[e];
+            tmp[3 * e + 1] = blk_valid[e];
+            tmp[3 * e + 2] = blk_host[e];
+        }
+        decoder_barrier();
+        for (int e = tid; e < n_range_blocks; e += kDecThreads) {
+            const int u = (i_begin + e / bpi) / ipu;
+            const int e0 = max(0, u * ipu - i_begin) * bpi;                  // the unit's first block here
+            const int e1 = min(n_range_blocks, ((u + 1) * ipu - i_begin) * bpi);
+            int before = 0, total = 0;                                      // misses before e / in all
+            for (int f = e0; f < e1; ++f) {
+                const int m = tmp[3 * f + 2] >= 0;
+                total += m;
+                before += (f < e) & m;
+            }
+            const bool miss = tmp[3 * e + 2] >= 0;
+            const int pos = e0 + (miss ? (e1 - e0 - total) + before : (e - e0) - before);
+            blk_page[pos] = tmp[3 * e];
+            blk_valid[pos] = tmp[3 * e + 1];
+            blk_host[pos] = tmp[3 * e + 2];
+        }
+        decoder_barrier();
+    }
 
     // Stage slab s of the range into this warp's stage st: lane copies chunk cp_c of
     // slab rows cp_r, cp_r + RPI, ...; a warp instruction covers RPI whole token rows.
+    // Before the first slab of a unit that holds a block missed this step, the warp
+    // waits (bounded, acquire) until the loaders have put the unit's misses in the pool.
+    int io_unit_ready = -1;
     const char* kbase = reinterpret_cast<const char*>(a.k_pages);
     const char* vbase = reinterpret_cast<const char*>(a.v_pages);
     const int cp_c = lane % SS::CPR, cp_r = lane / SS::CPR;
@@ -313,6 +380,16 @@ __device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* 
     auto issue_slab = [&](int s, int st) {
         const int k = s >> spi_shift;                                  // item within the range
         const int t0 = (s & spi_mask) * kSlabTokens;                  // first token in the item
+        if constexpr (IO) {
+            const int su = (i_begin + k) / ipu;
+            if (su != io_unit_ready && (blk_host[k * bpi + (t0 >> bs_shift)] >= 0 ||
+                                        blk_host[k * bpi + ((t0 + kSlabTokens - 1) >> bs_shift)] >= 0)) {
+                if (!wait_flag_bounded(a.io_flags + su, flag_value, handoff_wait_limit(a.err)))
+                    raise_error(a.err, SPARSE_ATTN_ERR_TIMEOUT);
+                __syncwarp();
+                io_unit_ready = su;
+            }
+        }
         const size_t head_rows = a.slot_C > 0 ? 0 : size_t(((i_begin + k) / ipu) % a.Hkv) * a.bs;
         const uint32_t kd = ring + uint32_t(st) * SS::SLAB_BYTES + uint32_t(cp_c >> 3) * SS::HALF_BYTES;
         const uint32_t vd = kd + SS::TENSOR_BYTES;
@@ -495,13 +572,13 @@ __device__ __forceinline__ void decode_mma_items(const DecodeArgs& a, uint32_t* 
 
 
 // One CTA's share of a decode launch: range blockIdx.x of a.ranges (none beyond).
-template <int D, int G, bool QSPLIT>
+template <int D, int G, bool QSPLIT, bool IO = false>
 __device__ __forceinline__ void decode_mma_body(const DecodeArgs& a, uint32_t* ready, uint32_t flag_value)
 {
     if (int(blockIdx.x) >= a.ranges) return;
     const int i_begin = int((long long)a.total_items * blockIdx.x / a.ranges);
     const int i_end = int((long long)a.total_items * (blockIdx.x + 1) / a.ranges);
-    decode_mma_items<D, G, QSPLIT>(a, ready, flag_value, i_begin, i_end);
+    decode_mma_items<D, G, QSPLIT, IO>(a, ready, flag_value, i_begin, i_end);
 }
 
 // Item ranges of a bf16 decode launch (one per CTA).  By default one per SM (more when

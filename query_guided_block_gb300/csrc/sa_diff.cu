@@ -26,6 +26,7 @@ struct DiffArgs {
     int32_t* counts;
     uint32_t* err;
     int units, stride, C, nb, step;
+    int32_t* sel_slot;   // optional [units, stride]: each selected block's slot after the step
 };
 
 __device__ __forceinline__ bool find_sorted(const int* a, int n, int x, int* pos)
@@ -177,6 +178,21 @@ __global__ void __launch_bounds__(kDiffWarps * 32) diff_kernel(DiffArgs a)
     }
     for (int i = lane; i < ns; i += 32)
         if (hit_slot[i] >= 0) a.slot_last_use[size_t(u) * C + hit_slot[i]] = a.step;
+    if (a.sel_slot != nullptr) {
+        // the slot map of the step: a hit keeps its slot; the r-th miss (selection order)
+        // takes the r-th placement above
+        int run = 0;
+        for (int base = 0; base < ns; base += 32) {
+            const int i = base + lane;
+            const bool miss = i < ns && hit_slot[i] < 0;
+            const uint32_t bal = __ballot_sync(kFullMask, miss);
+            if (i < ns) {
+                const int r = run + __popc(bal & lanemask_lt());
+                a.sel_slot[row + i] = miss ? (r < n_free ? freel[r] : victim[r - n_free]) : hit_slot[i];
+            }
+            run += __popc(bal);
+        }
+    }
     if (lane == 0) {
         cnt[0] = n_hit;
         cnt[1] = n_miss;
@@ -194,13 +210,13 @@ cudaError_t launch_diff(const Geometry& g, int step, const int32_t* sel_ids,
                         int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
                         int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
                         int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, uint32_t* err,
-                        cudaStream_t s)
+                        cudaStream_t s, int32_t* sel_slot)
 {
     const int units = g.units();
     if (units == 0) return cudaSuccess;
     DiffArgs a{sel_ids, sel_count, prev_ids, prev_count, slot_block, slot_last_use,
                hit_ids, miss_ids, miss_slot, evict_ids, evict_slot, new_ids, dropped_ids,
-               counts, err, units, g.sel_stride, cache_slots, g.nb, step};
+               counts, err, units, g.sel_stride, cache_slots, g.nb, step, sel_slot};
     const size_t smem = size_t(kDiffWarps) * (3 * size_t(g.sel_stride) + 5 * size_t(cache_slots)) * sizeof(int);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(diff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -102,11 +102,21 @@ cudaError_t launch_select(const Geometry& g, const WorkspaceLayout& L, char* ws,
                           const int32_t* reserve_ids, int32_t* sel_ids, int32_t* sel_count,
                           cudaStream_t s, uint32_t* ready = nullptr);   // publish ready[u] per unit
 
+// Slot-pool decode reading the step's misses from the host store in the same pass.
+struct SlotIo {
+    const void* host_k;          // [num_pages, Hkv, bs, D], device-readable
+    const void* host_v;
+    const int32_t* miss_ids;     // [units, sel_stride], ascending per unit
+    const int32_t* miss_slot;    // [units, sel_stride]: the pool slot of each miss
+    const int32_t* counts;       // [units, 5]: misses at [1]
+};
+
 cudaError_t launch_decode(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
                           const void* k_pages, const void* v_pages, const int32_t* block_table,
                           const int32_t* sel_ids, const int32_t* sel_count, float* out,
                           const int32_t* sel_slot, int slot_C, cudaStream_t s,
-                          uint32_t* ready = nullptr);   // bf16 K/V only: wait per unit on ready[]
+                          uint32_t* ready = nullptr,    // bf16 K/V only: wait per unit on ready[]
+                          const SlotIo* io = nullptr);  // bf16 K/V, slot mode only
 // Multi-query attention (sa_decode_mq.cu): Q query vectors per sequence, one selection.
 int mq_row_tiles(int Q, int G);
 cudaError_t launch_decode_mq(const Geometry& g, const WorkspaceLayout& L, char* ws, const void* q,
@@ -144,6 +154,6 @@ cudaError_t launch_diff(const Geometry& g, int step, const int32_t* sel_ids,
                         int32_t* slot_last_use, int32_t* hit_ids, int32_t* miss_ids,
                         int32_t* miss_slot, int32_t* evict_ids, int32_t* evict_slot,
                         int32_t* new_ids, int32_t* dropped_ids, int32_t* counts, uint32_t* err,
-                        cudaStream_t s);
+                        cudaStream_t s, int32_t* sel_slot = nullptr);   // also the slot map
 
 }  // namespace sa

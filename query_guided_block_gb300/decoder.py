@@ -122,15 +122,20 @@ class SlotCache:
         self.counts = torch.zeros(u, 5, dtype=torch.int32, device=dev)
 
     def diff(self, step: int, sel_ids: Optional[torch.Tensor] = None,
-             sel_count: Optional[torch.Tensor] = None, stream=None):
+             sel_count: Optional[torch.Tensor] = None, stream=None, sel_slot: Optional[torch.Tensor] = None):
+        """The step's diff; with `sel_slot` also its slot map, in the same launch."""
         d = self.decoder
         ids = d.sel_ids if sel_ids is None else sel_ids
         cnt = d.sel_count if sel_count is None else sel_count
         L = self.lists
-        B.sparse_attn_diff(d.p, step, ids, cnt, self.prev_ids, self.prev_count, self.cache_slots,
-                           self.slot_block, self.slot_last_use, L["hit_ids"], L["miss_ids"],
-                           L["miss_slot"], L["evict_ids"], L["evict_slot"], L["new_ids"],
-                           L["dropped_ids"], self.counts, d.ws, stream)
+        args = (d.p, step, ids, cnt, self.prev_ids, self.prev_count, self.cache_slots,
+                self.slot_block, self.slot_last_use, L["hit_ids"], L["miss_ids"],
+                L["miss_slot"], L["evict_ids"], L["evict_slot"], L["new_ids"],
+                L["dropped_ids"], self.counts)
+        if sel_slot is None:
+            B.sparse_attn_diff(*args, d.ws, stream)
+        else:
+            B.sparse_attn_diff_slots(*args, sel_slot, d.ws, stream)
 
     def advance(self, sel_ids: Optional[torch.Tensor] = None,
                 sel_count: Optional[torch.Tensor] = None):
@@ -143,7 +148,9 @@ class SlotCache:
 class SlotPool:
     """Per-unit slot pool of K/V page tiles fed from a host-resident page-first store:
     after the diff of a step, ``load_misses`` brings the misses in (one launch),
-    ``slot_map`` finds each selected block's slot and ``decode`` attends through it."""
+    ``slot_map`` finds each selected block's slot and ``decode`` attends through it;
+    ``decode_io`` does the miss loads and the attention in one pass (after
+    ``slot_map``), so that the transfer overlaps the attention over resident blocks."""
 
     def __init__(self, cache: SlotCache):
         d = cache.decoder
@@ -174,3 +181,10 @@ class SlotPool:
         B.sparse_attn_decode_slots(d.p, q, self.pool_k, self.pool_v, c.cache_slots, d.sel_ids,
                                    self.sel_slot, d.sel_count, d.out if out is None else out, d.ws,
                                    stream)
+
+    def decode_io(self, q, host_k_pages, host_v_pages, block_table, out=None, stream=None):
+        c, d = self.cache, self.cache.decoder
+        B.sparse_attn_decode_slots_io(d.p, q, self.pool_k, self.pool_v, c.cache_slots, d.sel_ids,
+                                      self.sel_slot, d.sel_count, host_k_pages, host_v_pages, block_table,
+                                      c.lists["miss_ids"], c.lists["miss_slot"], c.counts,
+                                      d.out if out is None else out, d.ws, stream)

@@ -133,3 +133,85 @@ def test_unregistered_host_store_is_rejected():
         B._ptr(cache.lists["miss_slot"]), B._ptr(cache.counts), w.cache_slots,
         B._ptr(pool.pool_k), B._ptr(pool.pool_v), B._ptr(dec.ws), dec.ws_bytes, None)
     assert rc == B.INVALID_ARG
+
+
+def _check_same_pool_and_output(w, pool_a, pool_b, out_a, out_b, counts, t):
+    """The pools end equal; outputs are the same bits for units without misses (same
+    order) and equal up to fp32 rounding of the reordered sum for the others (the fused
+    pass attends to a unit's missed blocks last)."""
+    assert torch.equal(pool_a.pool_k, pool_b.pool_k) and torch.equal(pool_a.pool_v, pool_b.pool_v), f"step {t}"
+    g = w.num_q_heads // w.num_kv_heads
+    oa = out_a.reshape(w.units, g, -1)
+    ob = out_b.reshape(w.units, g, -1)
+    clean = counts[:, 1] == 0
+    assert torch.equal(oa[clean], ob[clean]), f"step {t}: a unit without misses changed"
+    assert torch.allclose(oa, ob, rtol=1e-5, atol=1e-6), f"step {t}: {float((oa - ob).abs().max())}"
+
+
+@pytest.mark.parametrize("store", ["pinned", "device"])
+def test_fused_miss_load_equals_load_then_decode(store):
+    """sparse_attn_decode_slots_io (misses loaded in the decode's own launch) against
+    load_misses + decode_slots over drifting steps, ragged last block included."""
+    w = _small()
+    inp = make_inputs(w, "cuda")
+    if store == "pinned":
+        hk, hv = inp["k_pages"].cpu().pin_memory(), inp["v_pages"].cpu().pin_memory()
+    else:
+        hk, hv = inp["k_pages"], inp["v_pages"]
+    p = B.params_for(w)
+    runs = []
+    for _ in range(2):
+        dec = SparseDecoder(p)
+        dec.build_meta(inp["k_pages"], inp["block_table"])
+        cache = SlotCache(dec, w.cache_slots)
+        runs.append((dec, cache, SlotPool(cache)))
+    (da, ca, pa), (db, cb, pb) = runs
+    misses = 0
+    for t in range(w.steps):
+        q = inp["q"][t]
+        for dec, cache, pool in runs:   # run b: the diff writes the slot map itself
+            dec.select(q)
+            cache.diff(t, sel_slot=pool.sel_slot if pool is pb else None)
+        pa.load_misses(hk, hv, inp["block_table"])
+        pa.slot_map()
+        pa.decode(q)
+        pb.decode_io(q, hk, hv, inp["block_table"])
+        torch.cuda.synchronize()
+        assert da.device_error() == 0 and db.device_error() == 0
+        assert torch.equal(ca.counts, cb.counts)
+        assert torch.equal(pa.sel_slot, pb.sel_slot), f"step {t}: the diff's slot map differs"
+        misses += int(cb.counts[:, 1].sum())
+        _check_same_pool_and_output(w, pa, pb, da.out, db.out, cb.counts, t)
+        for _, cache, _ in runs:
+            cache.advance()
+    assert misses > 0
+
+
+def test_fused_miss_load_full_size():
+    """lru_64k at full size, 3 steps from pinned memory: the fused pass against the
+    two-launch path on every output and every slot."""
+    w = scaled(WORKLOADS["lru_64k"], steps=3, name="lru_64k")
+    inp = make_inputs(w, "cuda")
+    hk, hv = inp["k_pages"].cpu().pin_memory(), inp["v_pages"].cpu().pin_memory()
+    p = B.params_for(w)
+    runs = []
+    for _ in range(2):
+        dec = SparseDecoder(p)
+        dec.build_meta(inp["k_pages"], inp["block_table"])
+        cache = SlotCache(dec, w.cache_slots)
+        runs.append((dec, cache, SlotPool(cache)))
+    (da, ca, pa), (db, cb, pb) = runs
+    for t in range(w.steps):
+        q = inp["q"][t]
+        for dec, cache, pool in runs:
+            dec.select(q)
+            cache.diff(t, sel_slot=pool.sel_slot if pool is pb else None)
+        pa.load_misses(hk, hv, inp["block_table"])
+        pa.slot_map()
+        pa.decode(q)
+        pb.decode_io(q, hk, hv, inp["block_table"])
+        torch.cuda.synchronize()
+        assert da.device_error() == 0 and db.device_error() == 0
+        _check_same_pool_and_output(w, pa, pb, da.out, db.out, cb.counts, t)
+        for _, cache, _ in runs:
+            cache.advance()
