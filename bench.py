@@ -529,6 +529,9 @@ def run_gpu_arm(args):
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
+        # this rank's per-step distribution (the value above is the mean, max over ranks)
+        "ms_per_step_p50": statistics.median(step_ms),
+        "ms_per_step_p90": sorted(step_ms)[int(0.9 * (len(step_ms) - 1))],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,

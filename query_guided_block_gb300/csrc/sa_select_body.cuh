@@ -37,6 +37,7 @@ struct SelectArgs {
     int n_cand;              // candidate slots per unit = groups * group_rows
     int groups, group_rows;  // candidate slots come in groups of contiguous rows
     int chunks_per_group, chunks_per_unit, total_chunks;
+    int unit_ranges;         // warp-slab select: CTA c streams unit c's chunks (no more units than CTAs)
     int stages;
     // selection
     int k;
@@ -652,8 +653,13 @@ __device__ __forceinline__ uint32_t select_body_warps(const SelectArgs& a, uint3
     const int d0 = sub * EPL;
     const char* hi_src = reinterpret_cast<const char*>(KIND == KIND_QUEST ? a.kmax : (const void*)a.kmean);
     const char* lo_src = reinterpret_cast<const char*>(a.kmin);
-    const int c_begin = int((long long)a.total_chunks * blockIdx.x / gridDim.x);
-    const int c_end = int((long long)a.total_chunks * (blockIdx.x + 1) / gridDim.x);
+    // CTA c's chunks: an equal share, or with unit_ranges all of unit c's (so each CTA
+    // completes exactly one unit)
+    const int n_units_all = a.chunks_per_unit > 0 ? a.total_chunks / a.chunks_per_unit : 0;
+    const int c_begin = a.unit_ranges ? min(int(blockIdx.x), n_units_all) * a.chunks_per_unit
+                                      : int((long long)a.total_chunks * blockIdx.x / gridDim.x);
+    const int c_end = a.unit_ranges ? min(int(blockIdx.x) + 1, n_units_all) * a.chunks_per_unit
+                                    : int((long long)a.total_chunks * (blockIdx.x + 1) / gridDim.x);
     const int n_mine = c_end - c_begin > warp ? (c_end - c_begin - warp + kSelWarps - 1) / kSelWarps : 0;
     const uint32_t ring = smem_u32(smem) + uint32_t(warp) * (S * kSlabSelBytes);
 

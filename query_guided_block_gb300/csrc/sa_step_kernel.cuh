@@ -171,6 +171,9 @@ cudaError_t launch_step_impl(const Geometry& g, const WorkspaceLayout& L, char* 
     if (mean) set_slab_chunking<KIND_MEAN, false, D>(sa_args, units);
     else set_slab_chunking<KIND_QUEST, true, D>(sa_args, units);
     DecodeArgs da = decode_args(g, L, ws, q, k_pages, v_pages, block_table, sel_ids, sel_count, out, nullptr, 0);
+    // with whole-unit decode ranges every CTA up to the unit count streams one unit,
+    // ranks it and decodes it
+    sa_args.unit_ranges = da.ranges == da.units ? 1 : 0;
     uint32_t* ready = reinterpret_cast<uint32_t*>(ws + L.ready);
     uint32_t* queue = reinterpret_cast<uint32_t*>(ws + L.queue);
 
