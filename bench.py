@@ -4,11 +4,18 @@
 One step = one pass of the hot path over one batch of decode queries:
 select (score every block from its metadata + top-k + window) and decode (exact
 softmax attention over the selected blocks), plus the diff/LRU step for the
-multi-step workload.  Inputs are resident in HBM when the timed region starts;
-the L2 is flushed before every timed step, outside the step's events: a buffer of
-twice the L2 size is written and then read back, so the L2 holds only clean lines of
-unrelated data (a write alone would leave the L2 full of dirty lines, and the timed
-step would pay for writing them back).  Each kernel is bracketed by CUDA events on the launching stream.
+multi-step workload.  Inputs are resident in HBM when the timed region starts.
+
+Headline (stateless workloads): the K steps run back to back between one pair of
+CUDA events on the launching stream, alternating between two independent instances
+of the workload (another seed, separate buffers).  Each step touches several times
+the L2's capacity and the step before it touched only the other instance, so no step
+finds its inputs in the L2.  Beside it, each step is also timed between its own
+events with the L2 flushed before it (a buffer of twice the L2 size written and then
+read back, so the L2 holds only clean lines of unrelated data); that time carries
+the event pair's own cost (~2 us on a GB300) and gives the per-step distribution and
+the per-kernel breakdown.  The slot-cache workload carries state from step to step
+and is timed per step, flushed, only.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
@@ -354,12 +361,58 @@ def run_gpu_arm(args):
         raise RuntimeError("device error during warm-up")
 
     K = args.steps
+    # Headline timing (stateless workloads): the K steps back to back between one pair of
+    # events, alternating between two independent instances of the workload (another
+    # seed, separate buffers).  A step touches several times the L2's capacity and the
+    # step before it touched only the other instance, so no step finds its inputs in
+    # the L2, and no flush or event runs between the steps.  The slot-cache workloads
+    # carry state from step to step and are timed per step with the L2 flushed instead.
+    block = not cache
+    inst = []
+    if block:
+        inp2 = make_inputs(dataclasses.replace(w, seed=w.seed + 1), dev)
+        dec2 = SparseDecoder(p, dev)
+        dec2.build_meta(inp2["k_pages"], inp2["block_table"])
+        q2_all = inp2["q"] if (inp2["q"].dim() == 4 and not multi_q) else inp2["q"].unsqueeze(0)
+        inst = [(dec, q_static, kp, vp, bt, reserve),
+                (dec2, q2_all[0].clone(), inp2["k_pages"], inp2["v_pages"], inp2["block_table"],
+                 inp2.get("reserve_ids"))]
+        del inp2, q2_all
+
+    def inst_step(j):
+        d, q_, k_, v_, b_, r_ = inst[j]
+        if use_step:
+            d.step_fused(q_, k_, v_, b_, r_)
+        else:
+            d.select(q_, r_)
+            d.decode(q_, k_, v_, b_)
+
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     sampler = ClockSampler(dev.index) if (rank == 0 or world == 1) else None
     time.sleep(0.2 if sampler else 0)
+    block_ms_local = None
+    if block:
+        for i in range(max(args.warmup, 4)):
+            inst_step(i & 1)
+        torch.cuda.synchronize()
+        if dec.device_error() != 0 or inst[1][0].device_error() != 0:
+            raise RuntimeError("device error during the second instance's warm-up")
+        blk0, blk1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start = time.time()
+        blk0.record(stream)
+        for i in range(K):
+            inst_step(i & 1)
+        blk1.record(stream)
+        torch.cuda.synchronize()
+        block_ms_local = blk0.elapsed_time(blk1)
+    # per-step timing: each step between its own events, the L2 flushed before it
+    # (the headline for the slot-cache workloads; the per-step distribution otherwise)
     barrier(world)
     torch.cuda.synchronize()
-    t_start = time.time()
+    if not block:
+        t_start = time.time()
     for i in range(K):
         flush.zero_()
         q = q_all[(args.warmup + i) % q_all.shape[0]] if cache else q_static
@@ -397,7 +450,7 @@ def run_gpu_arm(args):
     clocks = sampler.summary(t_start, t_end) if sampler else None
     if sampler:
         sampler.stop()
-    flags = dec.device_error()
+    flags = dec.device_error() | (inst[1][0].device_error() if block else 0)
     if flags:
         raise RuntimeError(f"device error flags 0x{flags:x}")
 
@@ -420,7 +473,8 @@ def run_gpu_arm(args):
     else:
         sel_ms = [e[0].elapsed_time(e[1]) for e in ev]
         dec_ms = [e[2].elapsed_time(e[3]) if io else e[1].elapsed_time(e[2]) for e in ev]
-    total_ms_local = sum(step_ms)
+    flushed_ms_per_step = aggregate_max(sum(step_ms), world, dev) / K
+    total_ms_local = block_ms_local if block else sum(step_ms)
     total_ms = aggregate_max(total_ms_local, world, dev)
     queries = w.batch * w.num_q_heads * max(1, w.num_queries)
     value = world * queries * K / (total_ms / 1e3)
@@ -452,8 +506,10 @@ def run_gpu_arm(args):
                         "launches_per_step": 1}
     step_bytes = nbytes["select"] + nbytes["decode"]
     if use_step:
-        st_avg = statistics.mean(fused_ms)
-        kern["step"] = {"ms": st_avg, "bytes": step_bytes, "gbs": step_bytes / st_avg / 1e6,
+        st_flushed = statistics.mean(fused_ms)
+        st_avg = ms_per_step if block else st_flushed
+        kern["step"] = {"ms": st_avg, "ms_per_step_events_flushed": st_flushed,
+                        "bytes": step_bytes, "gbs": step_bytes / st_avg / 1e6,
                         "launches_per_step": step_launches,
                         "note": "sparse_attn_step: " + ("one cooperative launch (select phase, then decode "
                                 "phase waiting per unit)" if step_launches == 1 else
@@ -461,7 +517,7 @@ def run_gpu_arm(args):
         kern["select"]["note"] = kern["decode"]["note"] = "separate call, timed after the timed region"
     dominant = "step" if use_step else ("select" if sel_avg >= dec_avg else "decode")
     dk = kern[dominant]
-    step_gbs = step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9
+    step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     traffic = recorded_traffic(dominant, w.name, "decode_mq" if (multi_q and dominant == "decode") else "")
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dk["gbs"] / peak, "traffic": traffic,
@@ -474,32 +530,61 @@ def run_gpu_arm(args):
     q_dev = torch.empty_like(q_static)
     res_host = reserve.cpu().pin_memory() if reserve is not None else None
     res_dev = torch.empty_like(reserve) if reserve is not None else None
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    torch.cuda.synchronize()
-    for i in range(K):
-        flush.zero_()
-        a, b = e2e_ev[i]
-        a.record(stream)
-        q_dev.copy_(q_host, non_blocking=True)
-        if reserve is not None:
-            res_dev.copy_(res_host, non_blocking=True)
-        if use_step:
-            dec.step_fused(q_dev, kp, vp, bt, res_dev if reserve is not None else None)
+    if block:
+        # the K steps back to back, alternating instances as in the headline; every step
+        # uploads its instance's queries and reads its output back
+        hosts = [(q_host, q_dev, res_host, res_dev, out_host)]
+        d1, q1, _, _, _, r1 = inst[1]
+        hosts.append((q1.cpu().pin_memory(), torch.empty_like(q1),
+                      r1.cpu().pin_memory() if r1 is not None else None,
+                      torch.empty_like(r1) if r1 is not None else None,
+                      torch.empty(d1.out.shape, dtype=d1.out.dtype).pin_memory()))
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ea.record(stream)
+        for i in range(K):
+            j = i & 1
+            qh, qd, rh, rd, oh = hosts[j]
+            d_, _, k_, v_, b_, _ = inst[j]
+            qd.copy_(qh, non_blocking=True)
+            if rh is not None:
+                rd.copy_(rh, non_blocking=True)
+            if use_step:
+                d_.step_fused(qd, k_, v_, b_, rd)
+            else:
+                d_.select(qd, rd)
+                d_.decode(qd, k_, v_, b_)
+            oh.copy_(d_.out, non_blocking=True)
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = aggregate_max(ea.elapsed_time(eb), world, dev)
+    else:
+        e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            a, b = e2e_ev[i]
+            a.record(stream)
+            q_dev.copy_(q_host, non_blocking=True)
+            if reserve is not None:
+                res_dev.copy_(res_host, non_blocking=True)
+            if use_step:
+                dec.step_fused(q_dev, kp, vp, bt, res_dev if reserve is not None else None)
+                out_host.copy_(dec.out, non_blocking=True)
+                b.record(stream)
+                continue
+            dec.select(q_dev, res_dev if reserve is not None else None)
+            if io:
+                io_phase()
+                io_decode(q_dev)
+                cache.advance()
+                step_counter[0] += 1
+            else:
+                dec.decode(q_dev, kp, vp, bt)
             out_host.copy_(dec.out, non_blocking=True)
             b.record(stream)
-            continue
-        dec.select(q_dev, res_dev if reserve is not None else None)
-        if io:
-            io_phase()
-            io_decode(q_dev)
-            cache.advance()
-            step_counter[0] += 1
-        else:
-            dec.decode(q_dev, kp, vp, bt)
-        out_host.copy_(dec.out, non_blocking=True)
-        b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = aggregate_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
+        torch.cuda.synchronize()
+        e2e_ms = aggregate_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
     e2e = {"value": world * queries * K / (e2e_ms / 1e3), "unit": "queries/s",
            "h2d_bytes_per_step": q_host.numel() * q_host.element_size() +
                                  (res_host.numel() * 4 if res_host is not None else 0),
@@ -515,6 +600,7 @@ def run_gpu_arm(args):
     if args.other_workloads and args.workload == DEFAULT_WORKLOAD and not args.batch and not io:
         del inp, dec, cache
         kp = vp = bt = q_all = q_static = None
+        inst = hosts = None
         torch.cuda.empty_cache()
         other = {}
         for name in OTHER_WORKLOADS:
@@ -529,9 +615,12 @@ def run_gpu_arm(args):
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
-        # this rank's per-step distribution (the value above is the mean, max over ranks)
-        "ms_per_step_p50": statistics.median(step_ms),
-        "ms_per_step_p90": sorted(step_ms)[int(0.9 * (len(step_ms) - 1))],
+        # each step between its own events with the L2 flushed before it (mean max over
+        # ranks; median and 90th percentile of this rank): each such step also carries
+        # the event pair's own ~2 us
+        "ms_per_step_events_flushed": flushed_ms_per_step,
+        "ms_per_step_events_flushed_p50": statistics.median(step_ms),
+        "ms_per_step_events_flushed_p90": sorted(step_ms)[int(0.9 * (len(step_ms) - 1))],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -542,15 +631,22 @@ def run_gpu_arm(args):
                    "block_size": w.block_size, "topk_blocks": w.topk,
                    "window_tokens": w.window_tokens, "two_level": w.two_level,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"flushed before every step ({flush.numel() >> 20} MB written then read back, "
-                         "outside the step events)",
+                   "l2": ("inputs larger than L2: two independent instances of the workload alternate, "
+                          f"each step touches {step_bytes / 2**20:.0f} MB against a {l2 >> 20} MB L2, and the step "
+                          "before it touched only the other instance"
+                          if block else
+                          f"flushed before every step ({flush.numel() >> 20} MB written then read back, "
+                          "outside the step events)"),
                    "step": (f"sparse_attn_step ({step_launches} launch{'es' if step_launches > 1 else ''})"
                             if use_step else
                             ("sparse_attn_select + diff + load_misses + slot_map + decode_slots" if serial_io else
                              "sparse_attn_select + diff_slots + decode_slots_io (misses loaded in the decode's "
                              "launch)")
                             if io else "sparse_attn_select + sparse_attn_decode"),
-                   "timing": "CUDA events per call on the launching stream"},
+                   "timing": ("CUDA events on the launching stream around the K steps back to back (value, "
+                              "ms_per_step, e2e); per call around each step with the L2 flushed before it "
+                              "(ms_per_step_events_flushed*, kernels)"
+                              if block else "CUDA events per call on the launching stream")},
         "hbm_gbs": step_gbs,
         "hbm_frac_of_measured": step_gbs / peak,
         "hbm_frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS,
@@ -579,10 +675,12 @@ OTHER_WORKLOADS = ("mha_32k", "two_level_256k", "lru_64k")
 
 
 def measure_other_workload(name, dev, steps, warmup, flush, peak):
-    """One more workload timed the way the headline is (L2 flushed before every step,
-    CUDA events around the step on the launching stream): the step a user calls
+    """One more workload timed the way the headline is: the step a user calls
     (sparse_attn_step where it covers the problem, else select + decode), plus the
-    diff against the LRU slot cache for the multi-step workload."""
+    diff against the LRU slot cache for the multi-step workload.  Stateless workloads:
+    the steps back to back between one pair of events, alternating between two
+    independent instances; the slot-cache workload: CUDA events around each step with
+    the L2 flushed before it.  The per-step flushed time is reported for both."""
     from query_guided_block_gb300 import binding as Bn
     from query_guided_block_gb300.decoder import SlotCache, SparseDecoder
     from query_guided_block_gb300.workloads import WORKLOADS, make_inputs
@@ -599,47 +697,72 @@ def measure_other_workload(name, dev, steps, warmup, flush, peak):
     use_step = launches > 0
     stream = torch.cuda.current_stream()
     counter = [0]
+    block = not cache
+    insts = [(dec, q_all, kp, vp, bt)]
+    if block:
+        inp2 = make_inputs(dataclasses.replace(w, seed=w.seed + 1), dev)
+        dec2 = SparseDecoder(p, dev)
+        dec2.build_meta(inp2["k_pages"], inp2["block_table"])
+        q2 = inp2["q"] if inp2["q"].dim() == 4 else inp2["q"].unsqueeze(0)
+        insts.append((dec2, q2, inp2["k_pages"], inp2["v_pages"], inp2["block_table"]))
+        del inp2, q2
 
-    def one_step(q):
+    def one_step(i, j=0):
+        d, qa, k_, v_, b_ = insts[j]
+        q = qa[i % qa.shape[0]]
         if use_step:
-            dec.step_fused(q, kp, vp, bt)
+            d.step_fused(q, k_, v_, b_)
         else:
-            dec.select(q)
-            dec.decode(q, kp, vp, bt)
+            d.select(q)
+            d.decode(q, k_, v_, b_)
         if cache:
             cache.diff(counter[0])
             cache.advance()
         counter[0] += 1
 
     for i in range(warmup):
-        one_step(q_all[i % q_all.shape[0]])
+        one_step(i, i % len(insts))
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i, (a, b) in enumerate(ev):
         flush.zero_()
         a.record(stream)
-        one_step(q_all[(warmup + i) % q_all.shape[0]])
+        one_step(warmup + i)
         b.record(stream)
     torch.cuda.synchronize()
-    flags = dec.device_error()
+    ms_flushed = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms = ms_flushed
+    if block:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            one_step(warmup + i, i & 1)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+    flags = 0
+    for d_, *_ in insts:
+        flags |= d_.device_error()
     if flags:
         raise RuntimeError(f"{name}: device error flags 0x{flags:x}")
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     nbytes = algorithmic_bytes(w, dec.sel_count, dec.sel_ids)
     step_bytes = nbytes["select"] + nbytes["decode"]
     gbs = step_bytes / ms / 1e6
     per_step = (f"sparse_attn_step ({launches} launch{'es' if launches > 1 else ''})" if use_step
                 else "sparse_attn_select + sparse_attn_decode") + (" + sparse_attn_diff" if cache else "")
-    out = {"ms_per_step": ms, "value": w.batch * w.num_q_heads / (ms / 1e3), "unit": "queries/s",
+    out = {"ms_per_step": ms, "ms_per_step_events_flushed": ms_flushed,
+           "value": w.batch * w.num_q_heads / (ms / 1e3), "unit": "queries/s",
            "steps": steps, "warmup": warmup, "step": per_step, "step_bytes": step_bytes,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak},
            "config": {"batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                       "head_dim": w.head_dim, "context": w.n_tokens, "block_size": w.block_size,
                       "topk_blocks": w.topk, "window_tokens": w.window_tokens, "two_level": w.two_level,
-                      "cache_slots": w.cache_slots},
+                      "cache_slots": w.cache_slots,
+                      "timing": ("steps back to back, two instances alternating (inputs larger than L2)" if block
+                                 else "per step, L2 flushed before each")},
            "gpu_launches": (launches if use_step else 1 + select_launches(w)) * steps +
                            (steps if cache else 0)}
-    del inp, dec, cache
+    del inp, dec, cache, insts
     torch.cuda.empty_cache()
     return out
 
