@@ -532,29 +532,53 @@ def run_gpu_arm(args):
     res_dev = torch.empty_like(reserve) if reserve is not None else None
     if block:
         # the K steps back to back, alternating instances as in the headline; every step
-        # uploads its instance's queries and reads its output back
+        # uploads its instance's queries from pinned host memory and reads its output
+        # back.  Uploads and downloads run on streams of their own, ordered by events:
+        # step i waits for its upload and for the download of the step before it on the
+        # same instance (which last wrote that output); the upload for step i waits for
+        # that earlier step to finish reading the queries.  So step i's copies overlap
+        # the neighbouring steps, and the region ends after the last download.
         hosts = [(q_host, q_dev, res_host, res_dev, out_host)]
         d1, q1, _, _, _, r1 = inst[1]
         hosts.append((q1.cpu().pin_memory(), torch.empty_like(q1),
                       r1.cpu().pin_memory() if r1 is not None else None,
                       torch.empty_like(r1) if r1 is not None else None,
                       torch.empty(d1.out.shape, dtype=d1.out.dtype).pin_memory()))
+        up_s, down_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        stepped = [torch.cuda.Event() for _ in range(2)]
+        downloaded = [torch.cuda.Event() for _ in range(2)]
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         ea.record(stream)
+        up_s.wait_event(ea)
+        down_s.wait_event(ea)
         for i in range(K):
             j = i & 1
             qh, qd, rh, rd, oh = hosts[j]
             d_, _, k_, v_, b_, _ = inst[j]
-            qd.copy_(qh, non_blocking=True)
-            if rh is not None:
-                rd.copy_(rh, non_blocking=True)
+            with torch.cuda.stream(up_s):
+                if i >= 2:
+                    up_s.wait_event(stepped[j])
+                qd.copy_(qh, non_blocking=True)
+                if rh is not None:
+                    rd.copy_(rh, non_blocking=True)
+                uploaded[j].record(up_s)
+            stream.wait_event(uploaded[j])
+            if i >= 2:
+                stream.wait_event(downloaded[j])
             if use_step:
                 d_.step_fused(qd, k_, v_, b_, rd)
             else:
                 d_.select(qd, rd)
                 d_.decode(qd, k_, v_, b_)
-            oh.copy_(d_.out, non_blocking=True)
+            stepped[j].record(stream)
+            with torch.cuda.stream(down_s):
+                down_s.wait_event(stepped[j])
+                oh.copy_(d_.out, non_blocking=True)
+                downloaded[j].record(down_s)
+        stream.wait_event(downloaded[0])
+        stream.wait_event(downloaded[1])
         eb.record(stream)
         torch.cuda.synchronize()
         e2e_ms = aggregate_max(ea.elapsed_time(eb), world, dev)
